@@ -1,0 +1,547 @@
+#!/usr/bin/env python
+"""Throughput of the FP8 fine-grained-scaled GEMM path on GB300.
+
+Default workload (one step): the dense NT prefill-like shapes, M=4096 and
+(N, K) in {(2112,7168), (24576,1536), (7168,16384), (4096,7168), (7168,2048)}.
+Per shape a step quantises the FP32 activations A (1x128 groups, packed UE8M0
+scales) and runs D = A @ B.T and D2 = C + A @ B.T.  The weights B are
+quantised (128x128 blocks) once at setup.  Inputs are seeded N(0, 1); the
+per-step working set (~1.6 GB) is larger than L2.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead, on a bounded row sample of the same workload.  Other workloads
+(`--workload decode|contiguous|masked|small`) print their own line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "FP8 TFLOPS (and % of GB300 FP8 peak / HBM roofline) per shape at 1 GPU"
+FP8_OVER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor throughput (4.5 : 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="prefill", choices=["prefill", "decode", "contiguous", "masked", "small"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--profile-steps", type=int, default=0,
+                   help="run this many untimed steps and exit (for an external profiler)")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------- ranks
+
+
+class Ranks:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")  # timing barrier / max only, no data-path traffic
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [line.strip().split(", ") for line in self.file if line.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- workloads
+
+
+def prefill_setup(dg, workloads, dev):
+    shapes = []
+    for cfg in workloads.PREFILL:
+        m, n, k = cfg["m"], cfg["n"], cfg["k"]
+        w = workloads.dense(m, n, k, cfg["seed"], with_c=True)
+        a = w.a.to(dev)
+        qb, sfb = dg.quantize_fp8(w.b.to(dev), 128)
+        qa = torch.empty(m, k, dtype=torch.float8_e4m3fn, device=dev)
+        sfa = torch.empty(dg.sf_packed_shape(m, k), dtype=torch.int32, device=dev)
+        shapes.append(dict(m=m, n=n, k=k, a=a, qa=qa, sfa=sfa, qb=qb, sfb=sfb, c=w.c.to(dev),
+                           d=torch.empty(m, n, dtype=torch.bfloat16, device=dev),
+                           d2=torch.empty(m, n, dtype=torch.bfloat16, device=dev),
+                           host=w))
+    return shapes
+
+
+def prefill_step(dg, shapes, events=None):
+    """One step; if `events` is a list, appends (start, end, flops) per GEMM."""
+    for s in shapes:
+        dg.quantize_fp8(s["a"], 1, out=(s["qa"], s["sfa"]))
+        for c, d in ((None, s["d"]), (s["c"], s["d2"])):
+            if events is not None:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            dg.fp8_gemm_nt(s["qa"], s["sfa"], s["qb"], s["sfb"], d=d, c=c)
+            if events is not None:
+                e1.record()
+                events.append((e0, e1, 2.0 * s["m"] * s["n"] * s["k"], s))
+
+
+def step_flops(shapes):
+    return sum(2 * 2.0 * s["m"] * s["n"] * s["k"] for s in shapes)
+
+
+def algorithmic_bytes_gemm(m, n, k, with_c):
+    kb = k // 128
+    return (m * k + n * k + m * ((kb + 3) // 4) * 4 + n * ((kb + 3) // 4) * 4 + 2 * m * n +
+            (2 * m * n if with_c else 0))
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+
+def oracle_sample(workloads, rows_per_shape, seed=0):
+    """Bounded sample of the prefill workload for the CPU oracle: per shape,
+    `rows_per_shape` rows of A (quantised 1x128 by the oracle) against the
+    oracle-quantised B, computing D and D2 = C + D for those rows."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    items = []
+    for cfg in workloads.PREFILL:
+        m, n, k = cfg["m"], cfg["n"], cfg["k"]
+        w = workloads.dense(m, n, k, cfg["seed"], with_c=True)
+        qb, _, sb = oracle.quantize(w.b.numpy(), 128)
+        rows = np.sort(rng.choice(m, size=rows_per_shape, replace=False))
+        a_rows = np.ascontiguousarray(w.a.numpy()[rows])
+        c_rows = np.ascontiguousarray(w.c[torch.from_numpy(rows)].view(torch.int16).numpy().view(np.uint16))
+        items.append(dict(n=n, k=k, a=a_rows, c=c_rows, qb=qb, sb=sb))
+    return items
+
+
+def oracle_run(items):
+    import oracle
+    flops = 0.0
+    for it in items:
+        qa, _, sa = oracle.quantize(it["a"], 1)
+        idx = np.arange(qa.shape[0], dtype=np.int64)
+        oracle.gemm_nt_rows(qa, sa, it["qb"], it["sb"], idx)
+        oracle.gemm_nt_rows(qa, sa, it["qb"], it["sb"], idx, it["c"])
+        flops += 2 * 2.0 * qa.shape[0] * it["qb"].shape[0] * it["k"]
+    return flops
+
+
+def cpu_baseline(workloads, rows_per_shape=16):
+    import oracle
+    items = oracle_sample(workloads, rows_per_shape)
+    t0 = time.perf_counter()
+    flops = oracle_run(items)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.get_threads(),
+            "kind": "oracle",
+            "sample": "%d rows of A per prefill shape (quantise + D and C + D rows), FP64, %.1f s" %
+                      (rows_per_shape, dt)}
+
+
+def run_reference(args, ranks):
+    from moe_grouped_gemm_fp8_gb300 import workloads
+    import oracle
+    if ranks.rank != 0:
+        return 0
+    rows = 4
+    items = oracle_sample(workloads, rows)
+    for _ in range(args.warmup):
+        oracle_run(items)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += oracle_run(items)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = "%d rows of A per prefill shape per step (quantise + D and C + D rows), FP64" % rows
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "dense NT prefill-like M=4096, (N,K) in %s, with and without C; CPU oracle row sample" %
+                   workloads.PREFILL_NK},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.get_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- main arm
+
+
+def run_prefill(args, ranks, dg, workloads, dev):
+    shapes = prefill_setup(dg, workloads, dev)
+    if args.profile_steps:
+        for _ in range(args.profile_steps):
+            prefill_step(dg, shapes)
+        torch.cuda.synchronize()
+        return None
+    for _ in range(max(3, args.warmup)):
+        prefill_step(dg, shapes)
+    torch.cuda.synchronize()
+    st, word = dg.get_device_error()
+    if st != 0:
+        raise RuntimeError("device error after warm-up: 0x%x" % word)
+
+    # device-timed region: inputs resident in HBM
+    events = []
+    clocks = ClockSampler(torch.cuda.current_device())
+    ranks.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        prefill_step(dg, shapes, events)
+    t1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ranks.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    ms_max = ranks.max(ms)
+    flops_step = step_flops(shapes)
+    value = ranks.sum(flops_step) / (ms_max * 1e-3) / 1e12
+
+    gemm_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in events]
+    gemm_flops = [f for _, _, f, _ in events]
+    achieved = sum(gemm_flops) / (sum(gemm_ms) * 1e-3) / 1e12
+    per_shape = []
+    for i, s in enumerate(shapes):
+        for j, with_c in enumerate((False, True)):
+            ts = [gemm_ms[q] for q in range(2 * i + j, len(events), 2 * len(shapes))]
+            t = statistics.median(ts)
+            f = 2.0 * s["m"] * s["n"] * s["k"]
+            byt = algorithmic_bytes_gemm(s["m"], s["n"], s["k"], with_c)
+            per_shape.append({"m": s["m"], "n": s["n"], "k": s["k"], "c": with_c, "us": t * 1e3,
+                              "tflops": f / (t * 1e-3) / 1e12, "gbs": byt / (t * 1e-3) / 1e9})
+
+    st, word = dg.get_device_error()
+    if st != 0:
+        raise RuntimeError("device error in timed region: 0x%x" % word)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_prefill_e2e(args, ranks, dg, shapes, dev)
+    ws = sum(s["a"].numel() * 4 + s["qa"].numel() + s["qb"].numel() + 3 * 2 * s["m"] * s["n"] for s in shapes)
+    return dict(value=value, ms=ms_max, achieved=achieved, per_shape=per_shape, clocks=clk, e2e=e2e,
+                launches=args.steps * len(shapes) * 3, flops_step=flops_step, working_set_gb=ws / 1e9)
+
+
+def run_prefill_e2e(args, ranks, dg, shapes, dev):
+    host = []
+    h2d = d2h = 0
+    for s in shapes:
+        hb = {"a": s["host"].a.pin_memory(), "c": s["host"].c.pin_memory(),
+              "qb": s["qb"].cpu().pin_memory(), "sfb": s["sfb"].cpu().pin_memory(),
+              "d": torch.empty(s["m"], s["n"], dtype=torch.bfloat16).pin_memory(),
+              "d2": torch.empty(s["m"], s["n"], dtype=torch.bfloat16).pin_memory()}
+        dv = {k: torch.empty_like(v, device=dev) for k, v in hb.items() if k in ("a", "c", "qb", "sfb")}
+        host.append((hb, dv))
+        h2d += sum(hb[k].numel() * hb[k].element_size() for k in ("a", "c", "qb", "sfb"))
+        d2h += 2 * s["m"] * s["n"] * 2
+
+    def step():
+        for s, (hb, dv) in zip(shapes, host):
+            for k in ("a", "c", "qb", "sfb"):
+                dv[k].copy_(hb[k], non_blocking=True)
+            dg.quantize_fp8(dv["a"], 1, out=(s["qa"], s["sfa"]))
+            dg.fp8_gemm_nt(s["qa"], s["sfa"], dv["qb"], dv["sfb"], d=s["d"])
+            dg.fp8_gemm_nt(s["qa"], s["sfa"], dv["qb"], dv["sfb"], d=s["d2"], c=dv["c"])
+            hb["d"].copy_(s["d"], non_blocking=True)
+            hb["d2"].copy_(s["d2"], non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    ranks.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    dt = ranks.max((time.perf_counter() - t0) / args.steps)
+    return {"value": ranks.sum(step_flops(shapes)) / dt / 1e12, "unit": "TFLOPS",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+
+# --------------------------------------------------------------------------- other workloads
+
+
+def _flush_l2(buf):
+    buf.add_(1)  # touches more bytes than L2 holds
+
+
+def _time_gemm(fn, iters, flush):
+    """Median device time (ms) of fn() over iters launches, L2 flushed before each."""
+    ts = []
+    for _ in range(iters):
+        _flush_l2(flush)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
+    """GEMM-only timing of the decode, contiguous, masked or small workloads,
+    with L2 flushed before every launch (B of the decode shapes fits in L2)."""
+    flush = torch.zeros(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    cases = []
+    if args.workload in ("decode", "small"):
+        cfgs = workloads.DECODE if args.workload == "decode" else [workloads.SMALL]
+        for cfg in cfgs:
+            m, n, k = cfg["m"], cfg["n"], cfg["k"]
+            w = workloads.dense(m, n, k, cfg["seed"])
+            qa, sfa = dg.quantize_fp8(w.a.to(dev), 1)
+            qb, sfb = dg.quantize_fp8(w.b.to(dev), 128)
+            d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+            fn = (lambda qa=qa, sfa=sfa, qb=qb, sfb=sfb, d=d: dg.fp8_gemm_nt(qa, sfa, qb, sfb, d=d))
+            cases.append(dict(name="dense m=%d n=%d k=%d" % (m, n, k), fn=fn, flops=2.0 * m * n * k,
+                              bytes=algorithmic_bytes_gemm(m, n, k, False)))
+    elif args.workload == "contiguous":
+        cfg = workloads.CONTIG
+        w = workloads.contiguous(cfg["num_groups"], cfg["n"], cfg["k"], cfg["seed"])
+        qa, sfa = dg.quantize_fp8(w.a.to(dev), 1)
+        qb, sfb = dg.quantize_fp8(w.b.to(dev), 128)
+        mi = w.m_indices.to(dev)
+        d = torch.empty(w.a.shape[0], cfg["n"], dtype=torch.bfloat16, device=dev)
+        valid = int(w.counts.sum())
+        n, k, G = cfg["n"], cfg["k"], cfg["num_groups"]
+        byt = valid * k + G * n * k + 2 * valid * n + valid * k // 128 + G * n * k // 128 // 32
+        cases.append(dict(name="contiguous G=%d valid_rows=%d padded_rows=%d n=%d k=%d" %
+                          (G, valid, w.a.shape[0], n, k),
+                          fn=lambda: dg.m_grouped_fp8_gemm_nt_contiguous(qa, sfa, qb, sfb, mi, d=d),
+                          flops=2.0 * valid * n * k, bytes=byt))
+    elif args.workload == "masked":
+        cfg = workloads.MASKED
+        G, cap, n, k = cfg["num_groups"], cfg["cap"], cfg["n"], cfg["k"]
+        w = workloads.masked(G, cap, n, k, cfg["seed"])
+        qa, sfa = dg.quantize_fp8(w.a.to(dev), 1)
+        qb, sfb = dg.quantize_fp8(w.b.to(dev), 128)
+        mm = w.masked_m.to(dev)
+        d = torch.empty(G, cap, n, dtype=torch.bfloat16, device=dev)
+        valid = int(w.masked_m.sum())
+        used = int((w.masked_m > 0).sum())
+        byt = valid * k + used * n * k + 2 * valid * n + valid * k // 128 + used * n * (k // 512) * 4
+        exp_m = int(w.masked_m.float().mean())
+        cases.append(dict(name="masked G=%d cap=%d valid_rows=%d n=%d k=%d" % (G, cap, valid, n, k),
+                          fn=lambda: dg.m_grouped_fp8_gemm_nt_masked(qa, sfa, qb, sfb, mm, exp_m, d=d),
+                          flops=2.0 * valid * n * k, bytes=byt))
+    for c in cases:
+        for _ in range(max(3, args.warmup)):
+            c["fn"]()
+    torch.cuda.synchronize()
+    st, word = dg.get_device_error()
+    if st != 0:
+        raise RuntimeError("device error: 0x%x" % word)
+    if args.profile_steps:
+        for _ in range(args.profile_steps):
+            for c in cases:
+                c["fn"]()
+        torch.cuda.synchronize()
+        return None
+    clocks = ClockSampler(torch.cuda.current_device())
+    ranks.barrier()
+    clocks.start()
+    res = []
+    for c in cases:
+        t = _time_gemm(c["fn"], args.steps, flush)
+        res.append({"case": c["name"], "us": t * 1e3, "tflops": c["flops"] / (t * 1e-3) / 1e12,
+                    "gbs": c["bytes"] / (t * 1e-3) / 1e9,
+                    "frac_fp8_peak": c["flops"] / (t * 1e-3) / 1e12 / fp8_peak,
+                    "frac_hbm": c["bytes"] / (t * 1e-3) / 1e9 / hbm})
+    clk = clocks.stop()
+    ranks.barrier()
+    tot_t = ranks.max(sum(r["us"] for r in res) * 1e-6)
+    tot_f = ranks.sum(sum(c["flops"] for c in cases))
+    tot_b = sum(c["bytes"] for c in cases)
+    hbm_bound = args.workload in ("decode", "masked")
+    achieved = (tot_b / tot_t / 1e9) if hbm_bound else (sum(c["flops"] for c in cases) / tot_t / 1e12)
+    peak = hbm if hbm_bound else fp8_peak
+    line = {
+        "metric": METRIC, "value": tot_f / tot_t / 1e12, "unit": "TFLOPS", "n_gpus": ranks.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "l2": "flushed (512 MB write) before every launch"},
+        "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s" if hbm_bound else "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": peak_src},
+        "gpu_launches": len(cases) * args.steps,
+        "cases": res, "impl": "ours",
+    }
+    if clk:
+        line["clocks"] = clk
+    return line
+
+
+
+def main():
+    args = parse_args()
+    ranks = Ranks()
+    if args.impl == "reference":
+        rc = run_reference(args, ranks)
+        ranks.close()
+        return rc
+    import moe_grouped_gemm_fp8_gb300 as dg
+    from moe_grouped_gemm_fp8_gb300 import workloads
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(ranks.local)
+    dev = torch.device("cuda", ranks.local)
+    peaks, peak_src = load_peaks()
+
+    if args.workload != "prefill":
+        line = run_other(args, ranks, dg, workloads, dev, peaks, peak_src)
+        if ranks.rank == 0 and line:
+            print(json.dumps(line), flush=True)
+        ranks.close()
+        return 0
+
+    res = run_prefill(args, ranks, dg, workloads, dev)
+    if res is None:
+        ranks.close()
+        return 0
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    line = {
+        "metric": METRIC, "value": res["value"], "unit": "TFLOPS", "n_gpus": ranks.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+        "data": "synthetic",
+        "config": {"workload": "dense NT prefill-like M=4096, (N,K) in %s; per step: quantise A "
+                               "(1x128, packed UE8M0), D = A@B.T and D2 = C + A@B.T per shape; B "
+                               "quantised (128x128) once at setup" % (workloads.PREFILL_NK,),
+                   "l2": "inputs larger than L2 (per-step working set %.2f GB)" % res["working_set_gb"],
+                   "replicas": ranks.world},
+        "roofline": {"bound": "tensor", "achieved": res["achieved"], "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": res["achieved"] / fp8_peak, "traffic": None,
+                     "kernel": "fp8_gemm_kernel (all GEMM launches of the timed region)",
+                     "peak_source": "%s bf16 burst %.1f TFLOP/s x %.1f nominal FP8:BF16 ratio" %
+                                    (peak_src, peaks["bf16_tflops"], FP8_OVER_BF16)},
+        "gpu_launches": res["launches"],
+        "shapes": res["per_shape"],
+        "impl": "ours",
+    }
+    if res["clocks"]:
+        line["clocks"] = res["clocks"]
+    if res["e2e"]:
+        line["e2e"] = res["e2e"]
+    if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(workloads)
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+    ranks.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,207 @@
+/*
+ * dg.h - C ABI of libdg.so: FP8 GEMM with fine-grained scaling for NVIDIA
+ * GB300 (sm_103a), in the dense NT form and the two M-grouped MoE layouts.
+ *
+ * Operation (all GEMM entry points):   D = C + A @ B.T
+ *   "DeepGEMM: kernels GEMM FP8 limpos e eficientes por meio de scaling
+ *   granular" (pt.news.hada.io), section "Interface GEMM e restrições de
+ *   layout": the naming convention D = C + A @ B with NT as the reference
+ *   layout, fp8_gemm_nt computing D = C + A @ B.T.
+ *   A is E4M3 [M, K] with one scale per 1x128 row group, B is E4M3 [N, K]
+ *   (K-major, i.e. row-major [N, K]) with one scale per 128x128 block,
+ *   accumulation is FP32 and D (and the optional C) is BF16.
+ *
+ * Scale factors.  The GEMMs take the packed UE8M0 layout the same section
+ * gives for SM100: four 8-bit exponents per 32-bit word, transposed
+ * ("MN-major") and TMA-aligned:
+ *   sf[j, r] (int32, [ceil(K/512), align(MN, 4)]) holds in byte t (least
+ *   significant first) the biased exponent e + 127 of K block 4j + t for
+ *   row r; the scale is 2^e.  For B the 128x128 block exponent is repeated on
+ *   each of the block's 128 rows.  Rows in [MN, align(MN, 4)) and bytes past
+ *   the last K block are ignored.  Grouped tensors add a leading group
+ *   dimension: [G, ceil(K/512), align(MN, 4)].
+ *   dg_transform_sf converts plain FP32 scales (the SM90 format of the same
+ *   section) into this layout; dg_quantize_fp8 writes either format.
+ *
+ * Common conventions.
+ *   - Every pointer argument that names tensor data is a DEVICE pointer on
+ *     the current CUDA device unless stated otherwise; `stream` is a
+ *     cudaStream_t (NULL = legacy default stream).  The caller owns all memory
+ *     and the stream.  The library never allocates device memory, never
+ *     synchronises the stream (except dg_get_device_error) and keeps no
+ *     pointer after a call returns.  Work is enqueued asynchronously.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     failed check returns its status and enqueues nothing.  Checks: non-null
+ *     pointers for non-empty tensors, K % 128 == 0, 16-byte aligned data
+ *     pointers and row strides, N % 8 == 0 (16-byte BF16 output rows), sizes
+ *     within the 32-bit coordinate range of TMA, a device of compute
+ *     capability 10.3.  An empty problem (M, N, m_sum or num_groups equal to
+ *     0) is a no-op returning DG_OK.
+ *   - Kernel launch failures return DG_ERR_CUDA.  Conditions found on the
+ *     device (a bounded wait that ran out, a group index out of range, a scale
+ *     that is not a power of two) never trap: the kernel records the first
+ *     such condition in a device error word and completes; read it with
+ *     dg_get_device_error.
+ *   - Entry points may be called from several host threads; calls on the
+ *     same stream execute in order.
+ */
+#ifndef DG_H_
+#define DG_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dg_status {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum value */
+  DG_ERR_ALIGNMENT = 2,         /* K % 128, N % 8, pointer or stride alignment */
+  DG_ERR_UNSUPPORTED_ARCH = 3,  /* current device is not compute capability 10.3 */
+  DG_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
+  DG_ERR_DEVICE_TIMEOUT = 5,    /* device: a pipeline wait exceeded its limit */
+  DG_ERR_DEVICE_BAD_INDEX = 6,  /* device: m_indices >= num_groups, masked_m outside [0, max_m],
+                                   or a contiguous 128-row block mixing experts */
+  DG_ERR_TOO_LARGE = 7,         /* a size beyond the supported range */
+  DG_ERR_DEVICE_BAD_SCALE = 8   /* device: an FP32 scale that is not a positive power of two */
+} dg_status;
+
+typedef enum dg_sf_format {
+  DG_SF_FP32 = 0,         /* float, [G, ceil(MN/block_rows), K/128], K blocks innermost */
+  DG_SF_UE8M0_PACKED = 1  /* int32, [G, ceil(K/512), align(MN, 4)], the layout described above */
+} dg_sf_format;
+
+/* ------------------------------------------------------------------------ */
+/* GEMMs                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Dense NT:  D[m, n] = C[m, n] + sum_k A[m, k] * B[n, k]  (dequantised).
+ *   a    E4M3 [m, k], row stride lda elements (lda >= k, lda % 16 == 0)
+ *   sfa  packed UE8M0 [ceil(k/512), align(m, 4)]  (1x128 row groups of A)
+ *   b    E4M3 [n, k], row stride ldb (ldb >= k, ldb % 16 == 0)
+ *   sfb  packed UE8M0 [ceil(k/512), align(n, 4)]  (128x128 blocks of B, per row)
+ *   c    BF16 [m, n], row stride ldc (ldc % 8 == 0), or NULL for C = 0;
+ *        c may equal d (in-place accumulate) when ldc == ldd
+ *   d    BF16 [m, n], row stride ldd (ldd >= n, ldd % 8 == 0)
+ * Cited: "DeepGEMM: kernels GEMM FP8 limpos e eficientes por meio de scaling
+ * granular", sections "Interface GEMM e restrições de layout" and "GEMM denso
+ * e grouped" (fp8_gemm_{nt, nn, tn, tt}; NT implemented here). */
+dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
+
+/* M-grouped, contiguous layout.  The token rows of all experts are
+ * concatenated along M, each expert's segment padded to a multiple of 128 rows
+ * (dg_get_mk_alignment_for_contiguous_layout); N and K are shared.
+ *   a          E4M3 [m_sum, k] (contiguous rows), m_sum % 128 == 0
+ *   sfa        packed UE8M0 [ceil(k/512), align(m_sum, 4)]
+ *   b          E4M3 [num_groups, n, k] (contiguous)
+ *   sfb        packed UE8M0 [num_groups, ceil(k/512), align(n, 4)]
+ *   d          BF16 [m_sum, n] (contiguous)
+ *   m_indices  int32 [m_sum] on the device: the expert of each row, -1 for a
+ *              padding row.  Row r of D is written iff m_indices[r] >= 0; other
+ *              rows are left untouched.  Each 128-row block must hold rows of
+ *              one expert followed only by -1 rows; a block whose first row
+ *              is -1 is skipped.  Violations (index >= num_groups, a second
+ *              expert inside a block) leave those rows unwritten and set
+ *              DG_ERR_DEVICE_BAD_INDEX.
+ * m_indices is never read on the host.
+ * Cited: same page, section "GEMM denso e grouped" (contiguous layout:
+ * M-axis grouping, fixed N and K, segments aligned to the GEMM M block). */
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b,
+                                              const int32_t* sfb, void* d,
+                                              const int32_t* m_indices, int64_t m_sum, int64_t n,
+                                              int64_t k, int32_t num_groups, void* stream);
+
+/* M-grouped, masked layout (decode under CUDA graphs: the host does not know
+ * the per-expert token counts).
+ *   a         E4M3 [num_groups, max_m, k] (contiguous)
+ *   sfa       packed UE8M0 [num_groups, ceil(k/512), align(max_m, 4)]
+ *   b         E4M3 [num_groups, n, k]
+ *   sfb       packed UE8M0 [num_groups, ceil(k/512), align(n, 4)]
+ *   d         BF16 [num_groups, max_m, n]
+ *   masked_m  int32 [num_groups] on the device: rows [0, masked_m[g]) of
+ *             group g are computed and written; rows at or beyond it are left
+ *             untouched (their A rows are never used).  Values outside
+ *             [0, max_m] are clamped and set DG_ERR_DEVICE_BAD_INDEX.
+ *   expected_m  host hint of the typical masked_m (tile selection only);
+ *               0 = unknown.  Never affects results.
+ * num_groups <= 1024.  masked_m is never read on the host, so the call can
+ * be captured in a CUDA graph.
+ * Cited: same page, section "GEMM denso e grouped" (masked grouped GEMM,
+ * m_grouped_fp8_gemm_nt_masked: with a mask tensor the kernel computes only
+ * the valid region). */
+dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b,
+                                          const int32_t* sfb, void* d, const int32_t* masked_m,
+                                          int32_t num_groups, int64_t max_m, int64_t n, int64_t k,
+                                          int64_t expected_m, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Quantisation and scale layout                                             */
+/* ------------------------------------------------------------------------ */
+
+/* FP32 -> E4M3 with fine-grained power-of-two scales.
+ *   x   float [groups, rows, cols] (contiguous), cols % 128 == 0
+ *   q   E4M3 [groups, rows, cols] (contiguous)
+ *   sf  block_rows == 1:   one scale per 1x128 row group (activations)
+ *       block_rows == 128: one scale per 128x128 block (weights; a partial
+ *                          last block covers the rows that exist)
+ *       sf_format DG_SF_FP32: float [groups, ceil(rows/block_rows), cols/128]
+ *       sf_format DG_SF_UE8M0_PACKED: int32 [groups, ceil(cols/512), align(rows, 4)]
+ *       (rows in the alignment padding and unused bytes are written as 0).
+ * Scale rule: s = 2^e, e the smallest integer with 448 * 2^e >= amax of the
+ * group (e clamped to [-127, 127]; an all-zero group gets e = 0), then
+ * q = E4M3(x / s), rounding to nearest even and saturating at +-448.
+ * Cited: same page, section "Interface GEMM e restrições de layout" (casting
+ * to FP8 is left to the user; the library offers simple utilities). */
+dg_status dg_quantize_fp8(const float* x, void* q, void* sf, int64_t groups, int64_t rows,
+                          int64_t cols, int32_t block_rows, int32_t sf_format, void* stream);
+
+/* FP32 scales -> packed UE8M0 layout.
+ *   sf      float [groups, ceil(mn/block_rows), ceil(k/128)]
+ *   packed  int32 [groups, ceil(k/512), align(mn, 4)]
+ * Each scale must be a positive power of two (2^-127 .. 2^127).  Any other
+ * value is rounded up to the next power of two (non-positive or non-finite
+ * values become 1.0) and DG_ERR_DEVICE_BAD_SCALE is recorded.
+ * Cited: same page, section "Utilitários e variáveis de ambiente"
+ * (transform_sf_into_required_layout). */
+dg_status dg_transform_sf(const float* sf, int32_t* packed, int64_t groups, int64_t mn, int64_t k,
+                          int32_t block_rows, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Utilities (same page, section "Utilitários e variáveis de ambiente")      */
+/* ------------------------------------------------------------------------ */
+
+/* x rounded up so that x * element_size is a multiple of 16 bytes. */
+int64_t dg_get_tma_aligned_size(int64_t x, int32_t element_size);
+
+/* Row alignment of each expert segment in the contiguous layout: 128. */
+int32_t dg_get_mk_alignment_for_contiguous_layout(void);
+
+/* Upper bound on the SMs the persistent GEMM grid uses; 0 = all SMs of the
+ * device.  Process-wide; returns DG_ERR_INVALID_ARG for n < 0. */
+dg_status dg_set_num_sms(int32_t n);
+int32_t dg_get_num_sms(void);
+
+/* Limit of every bounded wait inside the kernels, in nanoseconds (default
+ * 2e9).  Process-wide; applies to launches made after the call. */
+dg_status dg_set_wait_timeout_ns(uint64_t ns);
+
+/* Synchronises `stream`, then reads and clears the device error words of the
+ * current device.  Returns DG_OK or the first recorded DG_ERR_DEVICE_* code.
+ * If detail is not NULL it receives the raw word (code in bits 0-7, the
+ * recording site in bits 8-23, block index in bits 32-63).  Debug/test use. */
+dg_status dg_get_device_error(void* stream, uint64_t* detail);
+
+/* Static description of a status code. */
+const char* dg_status_string(dg_status s);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t dg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H_ */

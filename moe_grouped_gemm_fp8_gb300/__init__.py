@@ -1,0 +1,24 @@
+"""FP8 GEMM with fine-grained scaling for NVIDIA GB300 (sm_103a).
+
+D = C + A @ B.T with E4M3 operands, 1x128 / 128x128 power-of-two scales,
+FP32 accumulation and BF16 output, in the dense NT form and the two
+M-grouped MoE layouts (contiguous, masked).  The kernels live in libdg.so
+(C ABI: include/dg.h); this package is a thin torch binding over it.
+"""
+from .api import (  # noqa: F401
+    DGError,
+    fp8_gemm_nt,
+    get_device_error,
+    get_mk_alignment_for_contiguous_layout,
+    get_num_sms,
+    get_tma_aligned_size,
+    m_grouped_fp8_gemm_nt_contiguous,
+    m_grouped_fp8_gemm_nt_masked,
+    quantize_fp8,
+    set_num_sms,
+    set_wait_timeout_ns,
+    sf_packed_shape,
+    transform_sf_into_required_layout,
+)
+
+__version__ = "0.1.0"

@@ -1,0 +1,232 @@
+"""Torch-facing wrappers of the C ABI in include/dg.h.
+
+Argument marshalling only: dtype/device/shape checks, output allocation by
+torch, ``data_ptr()`` and the current CUDA stream.  Every step of the
+computation runs in libdg.so's kernels; there is no fallback.
+
+Naming follows "DeepGEMM: kernels GEMM FP8 limpos e eficientes por meio de
+scaling granular" (pt.news.hada.io), sections "Interface GEMM e restrições de
+layout", "GEMM denso e grouped" and "Utilitários e variáveis de ambiente".
+"""
+import ctypes as C
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+FP8_DTYPES = (torch.float8_e4m3fn, torch.uint8)
+
+
+class DGError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s failed: %s (%s)" % (what, _lib.status_name(status),
+                                                 _lib.lib().dg_status_string(status).decode()))
+        self.status = int(status)
+
+
+def _check(status: int, what: str) -> None:
+    if status != _lib.DG_OK:
+        raise DGError(status, what)
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtypes, ndim: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype not in dtypes:
+        raise TypeError("%s: dtype %s not in %s" % (name, t.dtype, dtypes))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dim() != ndim:
+        raise ValueError("%s must have %d dims, got %s" % (name, ndim, tuple(t.shape)))
+
+
+def get_tma_aligned_size(x: int, element_size: int) -> int:
+    return int(_lib.lib().dg_get_tma_aligned_size(int(x), int(element_size)))
+
+
+def get_mk_alignment_for_contiguous_layout() -> int:
+    return int(_lib.lib().dg_get_mk_alignment_for_contiguous_layout())
+
+
+def set_num_sms(n: int) -> None:
+    _check(_lib.lib().dg_set_num_sms(int(n)), "dg_set_num_sms")
+
+
+def get_num_sms() -> int:
+    return int(_lib.lib().dg_get_num_sms())
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _check(_lib.lib().dg_set_wait_timeout_ns(int(ns)), "dg_set_wait_timeout_ns")
+
+
+def get_device_error(stream=None) -> Tuple[int, int]:
+    """Synchronises the stream; returns (status, raw word) and clears the word."""
+    detail = C.c_uint64(0)
+    st = _lib.lib().dg_get_device_error(_stream(stream), C.byref(detail))
+    return int(st), int(detail.value)
+
+
+def sf_packed_shape(mn: int, k: int, groups: Optional[int] = None):
+    kp = (k // 128 + 3) // 4
+    shape = (kp, get_tma_aligned_size(mn, 4))
+    return shape if groups is None else (groups,) + shape
+
+
+def quantize_fp8(x: torch.Tensor, block_rows: int, packed: bool = True, out=None, stream=None):
+    """FP32 [rows, cols] or [G, rows, cols] -> (E4M3 codes, scales).
+
+    block_rows=1: 1x128 row groups (activations); 128: 128x128 blocks
+    (weights).  packed=True gives the int32 UE8M0 layout the GEMMs take;
+    packed=False FP32 scales [G?, ceil(rows/block_rows), cols/128].
+    out=(q, sf) writes into preallocated tensors of those shapes."""
+    if x.dim() not in (2, 3):
+        raise ValueError("x must be [rows, cols] or [groups, rows, cols]")
+    _need(x, "x", (torch.float32,), x.dim())
+    x = x.contiguous()
+    grouped = x.dim() == 3
+    groups = x.shape[0] if grouped else 1
+    rows, cols = x.shape[-2], x.shape[-1]
+    if packed:
+        sf_shape = sf_packed_shape(rows, cols, groups if grouped else None)
+        sf_dtype = torch.int32
+    else:
+        sf_shape = ((groups,) if grouped else ()) + ((rows + block_rows - 1) // block_rows, cols // 128)
+        sf_dtype = torch.float32
+    if out is None:
+        q = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+        sf = torch.empty(sf_shape, dtype=sf_dtype, device=x.device)
+    else:
+        q, sf = out
+        _need(q, "q", FP8_DTYPES, x.dim())
+        _need(sf, "sf", (sf_dtype,), len(sf_shape))
+        if tuple(q.shape) != tuple(x.shape) or tuple(sf.shape) != tuple(sf_shape) or \
+                not q.is_contiguous() or not sf.is_contiguous():
+            raise ValueError("out tensors must be contiguous %s / %s" % (tuple(x.shape), sf_shape))
+    st = _lib.lib().dg_quantize_fp8(_ptr(x), _ptr(q), _ptr(sf), groups, rows, cols, int(block_rows),
+                                    _lib.DG_SF_UE8M0_PACKED if packed else _lib.DG_SF_FP32,
+                                    _stream(stream))
+    _check(st, "dg_quantize_fp8")
+    return q, sf
+
+
+def transform_sf_into_required_layout(sf: torch.Tensor, mn: int, k: int, block_rows: int,
+                                      stream=None) -> torch.Tensor:
+    """FP32 scales [G?, ceil(mn/block_rows), ceil(k/128)] -> packed UE8M0
+    int32 [G?, ceil(k/512), align(mn, 4)]."""
+    _need(sf, "sf", (torch.float32,), sf.dim())
+    grouped = sf.dim() == 3
+    groups = sf.shape[0] if grouped else 1
+    sf = sf.contiguous()
+    out = torch.empty(sf_packed_shape(mn, k, groups if grouped else None), dtype=torch.int32,
+                      device=sf.device)
+    st = _lib.lib().dg_transform_sf(_ptr(sf), _ptr(out), groups, int(mn), int(k), int(block_rows),
+                                    _stream(stream))
+    _check(st, "dg_transform_sf")
+    return out
+
+
+def fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,
+                d: Optional[torch.Tensor] = None, c: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """D = C + A @ B.T with A [M,K], B [N,K] E4M3 and packed UE8M0 scales."""
+    _need(a, "a", FP8_DTYPES, 2)
+    _need(b, "b", FP8_DTYPES, 2)
+    _need(sfa, "sfa", (torch.int32,), 2)
+    _need(sfb, "sfb", (torch.int32,), 2)
+    m, k = a.shape
+    n = b.shape[0]
+    if b.shape[1] != k:
+        raise ValueError("K mismatch: a %s, b %s" % (tuple(a.shape), tuple(b.shape)))
+    if tuple(sfa.shape) != sf_packed_shape(m, k) or tuple(sfb.shape) != sf_packed_shape(n, k):
+        raise ValueError("scale shapes %s / %s, expected %s / %s" % (
+            tuple(sfa.shape), tuple(sfb.shape), sf_packed_shape(m, k), sf_packed_shape(n, k)))
+    if a.stride(1) != 1 or b.stride(1) != 1 or not sfa.is_contiguous() or not sfb.is_contiguous():
+        raise ValueError("a and b need unit stride along K; scales must be contiguous")
+    if d is None:
+        d = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _need(d, "d", (torch.bfloat16,), 2)
+    if tuple(d.shape) != (m, n) or d.stride(1) != 1:
+        raise ValueError("d must be [M, N] with unit column stride")
+    if c is not None:
+        _need(c, "c", (torch.bfloat16,), 2)
+        if tuple(c.shape) != (m, n) or c.stride(1) != 1:
+            raise ValueError("c must be [M, N] with unit column stride")
+    st = _lib.lib().dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                   m, n, k, a.stride(0), b.stride(0),
+                                   c.stride(0) if c is not None else 0, d.stride(0), _stream(stream))
+    _check(st, "dg_fp8_gemm_nt")
+    return d
+
+
+def m_grouped_fp8_gemm_nt_contiguous(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor,
+                                     sfb: torch.Tensor, m_indices: torch.Tensor,
+                                     d: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Rows of A [m_sum,K] routed to experts B [G,N,K] by m_indices (-1 = padding)."""
+    _need(a, "a", FP8_DTYPES, 2)
+    _need(b, "b", FP8_DTYPES, 3)
+    _need(sfa, "sfa", (torch.int32,), 2)
+    _need(sfb, "sfb", (torch.int32,), 3)
+    _need(m_indices, "m_indices", (torch.int32,), 1)
+    m_sum, k = a.shape
+    g, n, kb = b.shape
+    if kb != k or m_indices.numel() != m_sum:
+        raise ValueError("shape mismatch")
+    if tuple(sfa.shape) != sf_packed_shape(m_sum, k) or tuple(sfb.shape) != sf_packed_shape(n, k, g):
+        raise ValueError("scale shapes do not match the packed layout")
+    for t, name in ((a, "a"), (b, "b"), (sfa, "sfa"), (sfb, "sfb"), (m_indices, "m_indices")):
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if d is None:
+        d = torch.empty((m_sum, n), dtype=torch.bfloat16, device=a.device)
+    _need(d, "d", (torch.bfloat16,), 2)
+    if tuple(d.shape) != (m_sum, n) or not d.is_contiguous():
+        raise ValueError("d must be contiguous [m_sum, N]")
+    st = _lib.lib().dg_m_grouped_fp8_gemm_nt_contiguous(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(m_indices), m_sum, n, k, g,
+        _stream(stream))
+    _check(st, "dg_m_grouped_fp8_gemm_nt_contiguous")
+    return d
+
+
+def m_grouped_fp8_gemm_nt_masked(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor,
+                                 sfb: torch.Tensor, masked_m: torch.Tensor, expected_m: int = 0,
+                                 d: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """A [G,max_m,K] x B [G,N,K]; rows >= masked_m[g] are left untouched."""
+    _need(a, "a", FP8_DTYPES, 3)
+    _need(b, "b", FP8_DTYPES, 3)
+    _need(sfa, "sfa", (torch.int32,), 3)
+    _need(sfb, "sfb", (torch.int32,), 3)
+    _need(masked_m, "masked_m", (torch.int32,), 1)
+    g, max_m, k = a.shape
+    gb, n, kb = b.shape
+    if gb != g or kb != k or masked_m.numel() != g:
+        raise ValueError("shape mismatch")
+    if tuple(sfa.shape) != sf_packed_shape(max_m, k, g) or tuple(sfb.shape) != sf_packed_shape(n, k, g):
+        raise ValueError("scale shapes do not match the packed layout")
+    for t, name in ((a, "a"), (b, "b"), (sfa, "sfa"), (sfb, "sfb"), (masked_m, "masked_m")):
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if d is None:
+        d = torch.empty((g, max_m, n), dtype=torch.bfloat16, device=a.device)
+    _need(d, "d", (torch.bfloat16,), 3)
+    if tuple(d.shape) != (g, max_m, n) or not d.is_contiguous():
+        raise ValueError("d must be contiguous [G, max_m, N]")
+    st = _lib.lib().dg_m_grouped_fp8_gemm_nt_masked(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), g, max_m, n, k,
+        int(expected_m), _stream(stream))
+    _check(st, "dg_m_grouped_fp8_gemm_nt_masked")
+    return d

@@ -1,0 +1,71 @@
+// Declarations shared by the translation units of libdg.so (not part of the
+// public C ABI, which is include/dg.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dg.h"
+
+namespace dg {
+
+constexpr int kBlockM = 128;  // rows of an output tile (UMMA M)
+constexpr int kBlockK = 128;  // K extent of one scale block / pipeline stage
+constexpr int kMaxMaskedGroups = 1024;
+
+enum GemmMode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+
+// Sites recorded with device errors (bits 8-23 of the error word).
+enum ErrorSite : uint32_t {
+  kSiteProducerEmpty = 1,
+  kSiteMmaTmemEmpty = 2,
+  kSiteMmaFull = 3,
+  kSiteEpilogueTmemFull = 4,
+  kSiteDrain = 5,
+  kSiteProducerDrain = 6,
+  kSiteContiguousIndex = 16,
+  kSiteMaskedCount = 17,
+  kSiteTransformScale = 32,
+};
+
+struct GemmArgs {
+  const __nv_bfloat16* c;  // nullable
+  __nv_bfloat16* d;
+  int64_t ldc, ldd;        // elements
+  const int32_t* m_indices;
+  const int32_t* masked_m;
+  int32_t m;               // dense M, contiguous m_sum, masked max_m
+  int32_t n, k;
+  int32_t num_groups;
+  int32_t m_blocks;        // ceil(m / 128)
+  int32_t n_blocks;
+  int32_t k_blocks;
+  int32_t band;            // raster band height in M blocks
+  uint64_t timeout_ns;
+};
+
+struct GemmConfig {
+  int block_n;
+  int stages;
+  int grid;
+  size_t smem_bytes;
+};
+
+// gemm.cu
+int gemm_max_stages(int block_n);
+size_t gemm_smem_bytes(int block_n, int stages, int mode);
+cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& sfa, const CUtensorMap& sfb, const GemmArgs& args,
+                        int grid, cudaStream_t stream);
+cudaError_t gemm_fetch_error(unsigned long long* word);  // reads and clears
+
+// quant.cu
+cudaError_t quantize_launch(const float* x, void* q, void* sf, int64_t groups, int64_t rows,
+                            int64_t cols, int block_rows, int sf_format, cudaStream_t stream);
+cudaError_t transform_sf_launch(const float* sf, int32_t* packed, int64_t groups, int64_t mn,
+                                int64_t k, int block_rows, cudaStream_t stream);
+cudaError_t quant_fetch_error(unsigned long long* word);  // reads and clears
+
+}  // namespace dg

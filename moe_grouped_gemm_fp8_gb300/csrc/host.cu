@@ -1,0 +1,419 @@
+// Host side of the C ABI declared in include/dg.h: argument checks, TMA
+// descriptor encoding, tile configuration and launches.  No device memory is
+// allocated and no stream is synchronised here (except dg_get_device_error).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "dg_internal.h"
+
+namespace dg {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxCoord = (int64_t)1 << 31;  // TMA coordinates are 32-bit signed
+
+std::atomic<int32_t> g_num_sms_limit{0};
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+struct DeviceInfo {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int cc_major = 0, cc_minor = 0, sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool env_flag(const char* name) {
+  const char* v = getenv(name);
+  return v && *v && strcmp(v, "0") != 0;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return (v && *v) ? atoi(v) : dflt;
+}
+
+dg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
+
+// Current device must be compute capability 10.3; reports its SM count.
+dg_status current_device(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return DG_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DG_ERR_CUDA;
+  DeviceInfo& d = g_devices[dev];
+  std::call_once(d.once, [&] {
+    d.err = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (d.err == cudaSuccess)
+      d.err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (d.err != cudaSuccess) return DG_ERR_CUDA;
+  if (d.cc_major != 10 || d.cc_minor != 3) return DG_ERR_UNSUPPORTED_ARCH;
+  int limit = g_num_sms_limit.load();
+  *sms = (limit > 0 && limit < d.sms) ? limit : d.sms;
+  return DG_OK;
+}
+
+dg_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? DG_OK : DG_ERR_CUDA;
+}
+
+// Encodes a tiled TMA descriptor.  dims/box innermost first; strides (bytes)
+// for dims 1..rank-1.
+dg_status encode(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle) {
+  uint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, dtype, (cuuint32_t)rank, const_cast<void*>(base),
+                        reinterpret_cast<const cuuint64_t*>(dims),
+                        reinterpret_cast<const cuuint64_t*>(strides),
+                        reinterpret_cast<const cuuint32_t*>(box),
+                        reinterpret_cast<const cuuint32_t*>(elem_strides),
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DG_OK : DG_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int64_t align4(int64_t x) { return (x + 3) / 4 * 4; }
+
+// Operand descriptors shared by the three GEMM forms.
+struct Operands {
+  CUtensorMap a, b, sfa, sfb;
+};
+
+dg_status encode_b_side(Operands& o, const void* b, const int32_t* sfb, int64_t groups,
+                        int64_t n, int64_t k, int64_t ldb, int block_n) {
+  const int64_t kp = (k / kBlockK + 3) / 4;
+  const int64_t n_pad = align4(n);
+  {
+    uint64_t dims[3] = {(uint64_t)k, (uint64_t)n, (uint64_t)groups};
+    uint64_t strides[2] = {(uint64_t)ldb, (uint64_t)(n * ldb)};
+    uint32_t box[3] = {(uint32_t)kBlockK, (uint32_t)block_n, 1};
+    dg_status s = encode(&o.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != DG_OK) return s;
+  }
+  {
+    uint64_t dims[3] = {(uint64_t)n_pad, (uint64_t)kp, (uint64_t)groups};
+    uint64_t strides[2] = {(uint64_t)(n_pad * 4), (uint64_t)(kp * n_pad * 4)};
+    uint32_t box[3] = {(uint32_t)block_n, 1, 1};
+    return encode(&o.sfb, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, sfb, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+}
+
+dg_status encode_a_2d(Operands& o, const void* a, const int32_t* sfa, int64_t m, int64_t k,
+                      int64_t lda) {
+  const int64_t kp = (k / kBlockK + 3) / 4;
+  const int64_t m_pad = align4(m);
+  {
+    uint64_t dims[2] = {(uint64_t)k, (uint64_t)m};
+    uint64_t strides[1] = {(uint64_t)lda};
+    uint32_t box[2] = {(uint32_t)kBlockK, (uint32_t)kBlockM};
+    dg_status s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != DG_OK) return s;
+  }
+  {
+    uint64_t dims[2] = {(uint64_t)m_pad, (uint64_t)kp};
+    uint64_t strides[1] = {(uint64_t)(m_pad * 4)};
+    uint32_t box[2] = {(uint32_t)kBlockM, 1};
+    return encode(&o.sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+}
+
+dg_status encode_a_3d(Operands& o, const void* a, const int32_t* sfa, int64_t groups,
+                      int64_t max_m, int64_t k) {
+  const int64_t kp = (k / kBlockK + 3) / 4;
+  const int64_t m_pad = align4(max_m);
+  {
+    uint64_t dims[3] = {(uint64_t)k, (uint64_t)max_m, (uint64_t)groups};
+    uint64_t strides[2] = {(uint64_t)k, (uint64_t)(max_m * k)};
+    uint32_t box[3] = {(uint32_t)kBlockK, (uint32_t)kBlockM, 1};
+    dg_status s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != DG_OK) return s;
+  }
+  {
+    uint64_t dims[3] = {(uint64_t)m_pad, (uint64_t)kp, (uint64_t)groups};
+    uint64_t strides[2] = {(uint64_t)(m_pad * 4), (uint64_t)(kp * m_pad * 4)};
+    uint32_t box[3] = {(uint32_t)kBlockM, 1, 1};
+    return encode(&o.sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, sfa, dims, strides, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+}
+
+// Tile width along N.  256-wide tiles halve the shared-memory traffic per MMA
+// but leave SMs idle when there are too few tiles; DG_BLOCK_N forces a choice.
+int choose_block_n(int64_t m_blocks_est, int64_t n, int sms) {
+  const int forced = env_int("DG_BLOCK_N", 0);
+  if (forced == 128 || forced == 256) return forced;
+  const int64_t tiles256 = m_blocks_est * ((n + 255) / 256);
+  return (n >= 1024 && tiles256 >= 2 * sms) ? 256 : 128;
+}
+
+void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_n,
+                  int grid, int band) {
+  if (!env_flag("DG_PRINT_CONFIGS")) return;
+  fprintf(stderr, "dg: %s m=%lld n=%lld k=%lld groups=%d block_m=128 block_n=%d stages=%d grid=%d band=%d\n",
+          what, (long long)m, (long long)n, (long long)k, groups, block_n,
+          gemm_max_stages(block_n), grid, band);
+}
+
+dg_status check_common_k_n(int64_t n, int64_t k) {
+  if (n < 0 || k < 0) return DG_ERR_INVALID_ARG;
+  if (k == 0) return DG_ERR_INVALID_ARG;
+  if (k % kBlockK != 0) return DG_ERR_ALIGNMENT;
+  if (n % 8 != 0) return DG_ERR_ALIGNMENT;
+  if (k >= kMaxCoord || n >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  return DG_OK;
+}
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
+  if (m < 0) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (m == 0 || n == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d) return DG_ERR_INVALID_ARG;
+  if (lda < k || ldb < k || ldd < n || (c && ldc < n)) return DG_ERR_INVALID_ARG;
+  if (lda % 16 || ldb % 16 || ldd % 8 || (c && ldc % 8)) return DG_ERR_ALIGNMENT;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) ||
+      (c && !aligned16(c)))
+    return DG_ERR_ALIGNMENT;
+  if (m >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  int sms = 0;
+  if ((s = current_device(&sms)) != DG_OK) return s;
+  if ((s = get_encoder()) != DG_OK) return s;
+
+  GemmArgs args = {};
+  args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
+  const int block_n = choose_block_n(args.m_blocks, n, sms);
+  Operands o;
+  if ((s = encode_a_2d(o, a, sfa, m, k, lda)) != DG_OK) return s;
+  if ((s = encode_b_side(o, b, sfb, 1, n, k, ldb, block_n)) != DG_OK) return s;
+  args.c = static_cast<const __nv_bfloat16*>(c);
+  args.d = static_cast<__nv_bfloat16*>(d);
+  args.ldc = c ? ldc : 0;
+  args.ldd = ldd;
+  args.m = (int32_t)m;
+  args.n = (int32_t)n;
+  args.k = (int32_t)k;
+  args.num_groups = 1;
+  args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
+  args.k_blocks = (int32_t)(k / kBlockK);
+  args.band = env_int("DG_RASTER_BAND", 16);
+  if (args.band < 1) args.band = 1;
+  args.timeout_ns = g_timeout_ns.load();
+  const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
+  if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  print_config("fp8_gemm_nt", m, n, k, 1, block_n, grid, args.band);
+  return from_cuda(gemm_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, args, grid,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b,
+                                              const int32_t* sfb, void* d,
+                                              const int32_t* m_indices, int64_t m_sum, int64_t n,
+                                              int64_t k, int32_t num_groups, void* stream) {
+  if (m_sum < 0 || num_groups < 0) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (m_sum == 0 || n == 0 || num_groups == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d || !m_indices) return DG_ERR_INVALID_ARG;
+  if (m_sum % kBlockM != 0) return DG_ERR_ALIGNMENT;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d))
+    return DG_ERR_ALIGNMENT;
+  if (m_sum >= kMaxCoord || (int64_t)num_groups * n >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  int sms = 0;
+  if ((s = current_device(&sms)) != DG_OK) return s;
+  if ((s = get_encoder()) != DG_OK) return s;
+
+  GemmArgs args = {};
+  args.m_blocks = (int32_t)(m_sum / kBlockM);
+  const int block_n = choose_block_n(args.m_blocks, n, sms);
+  Operands o;
+  if ((s = encode_a_2d(o, a, sfa, m_sum, k, k)) != DG_OK) return s;
+  if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n)) != DG_OK) return s;
+  args.d = static_cast<__nv_bfloat16*>(d);
+  args.ldd = n;
+  args.m_indices = m_indices;
+  args.m = (int32_t)m_sum;
+  args.n = (int32_t)n;
+  args.k = (int32_t)k;
+  args.num_groups = num_groups;
+  args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
+  args.k_blocks = (int32_t)(k / kBlockK);
+  args.band = env_int("DG_RASTER_BAND", 16);
+  if (args.band < 1) args.band = 1;
+  args.timeout_ns = g_timeout_ns.load();
+  const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
+  if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  print_config("m_grouped_fp8_gemm_nt_contiguous", m_sum, n, k, num_groups, block_n, grid, args.band);
+  return from_cuda(gemm_launch(kContiguous, block_n, o.a, o.b, o.sfa, o.sfb, args, grid,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b,
+                                          const int32_t* sfb, void* d, const int32_t* masked_m,
+                                          int32_t num_groups, int64_t max_m, int64_t n, int64_t k,
+                                          int64_t expected_m, void* stream) {
+  if (max_m < 0 || num_groups < 0 || expected_m < 0) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (max_m == 0 || n == 0 || num_groups == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d || !masked_m) return DG_ERR_INVALID_ARG;
+  if (num_groups > kMaxMaskedGroups) return DG_ERR_TOO_LARGE;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d))
+    return DG_ERR_ALIGNMENT;
+  if (max_m >= kMaxCoord || (int64_t)num_groups * max_m >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  int sms = 0;
+  if ((s = current_device(&sms)) != DG_OK) return s;
+  if ((s = get_encoder()) != DG_OK) return s;
+
+  GemmArgs args = {};
+  args.m_blocks = (int32_t)((max_m + kBlockM - 1) / kBlockM);
+  const int64_t m_est = expected_m > 0 ? (expected_m + kBlockM - 1) / kBlockM : args.m_blocks;
+  const int block_n = choose_block_n(m_est * num_groups, n, sms);
+  Operands o;
+  if ((s = encode_a_3d(o, a, sfa, num_groups, max_m, k)) != DG_OK) return s;
+  if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n)) != DG_OK) return s;
+  args.d = static_cast<__nv_bfloat16*>(d);
+  args.ldd = n;
+  args.masked_m = masked_m;
+  args.m = (int32_t)max_m;
+  args.n = (int32_t)n;
+  args.k = (int32_t)k;
+  args.num_groups = num_groups;
+  args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
+  args.k_blocks = (int32_t)(k / kBlockK);
+  args.band = 1;
+  args.timeout_ns = g_timeout_ns.load();
+  if ((int64_t)num_groups * args.m_blocks * args.n_blocks >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  print_config("m_grouped_fp8_gemm_nt_masked", max_m, n, k, num_groups, block_n, sms, 0);
+  return from_cuda(gemm_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, args, sms,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_quantize_fp8(const float* x, void* q, void* sf, int64_t groups, int64_t rows,
+                          int64_t cols, int32_t block_rows, int32_t sf_format, void* stream) {
+  if (groups < 0 || rows < 0 || cols < 0) return DG_ERR_INVALID_ARG;
+  if (block_rows != 1 && block_rows != 128) return DG_ERR_INVALID_ARG;
+  if (sf_format != DG_SF_FP32 && sf_format != DG_SF_UE8M0_PACKED) return DG_ERR_INVALID_ARG;
+  if (cols % kBlockK != 0) return DG_ERR_ALIGNMENT;
+  if (groups == 0 || rows == 0 || cols == 0) return DG_OK;
+  if (!x || !q || !sf) return DG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return DG_ERR_ALIGNMENT;
+  if (groups * rows >= kMaxCoord * 16 || cols >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  int sms = 0;
+  dg_status s = current_device(&sms);
+  if (s != DG_OK) return s;
+  return from_cuda(quantize_launch(x, q, sf, groups, rows, cols, block_rows, sf_format,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_transform_sf(const float* sf, int32_t* packed, int64_t groups, int64_t mn, int64_t k,
+                          int32_t block_rows, void* stream) {
+  if (groups < 0 || mn < 0 || k < 0) return DG_ERR_INVALID_ARG;
+  if (block_rows != 1 && block_rows != 128) return DG_ERR_INVALID_ARG;
+  if (groups == 0 || mn == 0 || k == 0) return DG_OK;
+  if (!sf || !packed) return DG_ERR_INVALID_ARG;
+  if (!aligned16(packed) || (reinterpret_cast<uintptr_t>(sf) & 3u)) return DG_ERR_ALIGNMENT;
+  if (groups * align4(mn) * ((k + 511) / 512) >= kMaxCoord * 64) return DG_ERR_TOO_LARGE;
+  int sms = 0;
+  dg_status s = current_device(&sms);
+  if (s != DG_OK) return s;
+  return from_cuda(transform_sf_launch(sf, packed, groups, mn, k, block_rows,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int64_t dg_get_tma_aligned_size(int64_t x, int32_t element_size) {
+  if (x < 0 || element_size <= 0 || 16 % element_size != 0) return -1;
+  const int64_t unit = 16 / element_size;
+  return (x + unit - 1) / unit * unit;
+}
+
+int32_t dg_get_mk_alignment_for_contiguous_layout(void) { return kBlockM; }
+
+dg_status dg_set_num_sms(int32_t n) {
+  if (n < 0) return DG_ERR_INVALID_ARG;
+  g_num_sms_limit.store(n);
+  return DG_OK;
+}
+
+int32_t dg_get_num_sms(void) {
+  const int32_t limit = g_num_sms_limit.load();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return limit;
+  int sms = 0;
+  if (current_device(&sms) != DG_OK) return limit;
+  return sms;
+}
+
+dg_status dg_set_wait_timeout_ns(uint64_t ns) {
+  if (ns == 0) return DG_ERR_INVALID_ARG;
+  g_timeout_ns.store(ns);
+  return DG_OK;
+}
+
+dg_status dg_get_device_error(void* stream, uint64_t* detail) {
+  if (detail) *detail = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DG_ERR_CUDA;
+  unsigned long long g = 0, q = 0;
+  if (gemm_fetch_error(&g) != cudaSuccess) return DG_ERR_CUDA;
+  if (quant_fetch_error(&q) != cudaSuccess) return DG_ERR_CUDA;
+  const unsigned long long w = g ? g : q;
+  if (detail) *detail = w;
+  return w ? static_cast<dg_status>(w & 0xFFu) : DG_OK;
+}
+
+const char* dg_status_string(dg_status s) {
+  switch (s) {
+    case DG_OK: return "ok";
+    case DG_ERR_INVALID_ARG: return "invalid argument";
+    case DG_ERR_ALIGNMENT: return "alignment or divisibility requirement not met";
+    case DG_ERR_UNSUPPORTED_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+    case DG_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case DG_ERR_DEVICE_TIMEOUT: return "device: a pipeline wait exceeded its time limit";
+    case DG_ERR_DEVICE_BAD_INDEX: return "device: group index or masked count out of range";
+    case DG_ERR_TOO_LARGE: return "size beyond the supported range";
+    case DG_ERR_DEVICE_BAD_SCALE: return "device: scale is not a positive power of two";
+  }
+  return "unknown status";
+}
+
+int32_t dg_version(void) { return 100; }
+
+}  // extern "C"

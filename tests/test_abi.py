@@ -1,0 +1,94 @@
+"""CPU-only checks of libdg.so: it loads, exports every function include/dg.h
+declares, and rejects bad arguments on the host before touching the device."""
+import ctypes as C
+
+import pytest
+
+from moe_grouped_gemm_fp8_gb300 import _lib
+
+DG_OK, INVALID, ALIGN, TOO_LARGE = 0, 1, 2, 7
+
+
+@pytest.fixture(scope="module")
+def L():
+    from moe_grouped_gemm_fp8_gb300 import build
+    build.build()
+    return _lib.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = _lib.header_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in _lib.SIGNATURES, "binding lacks a signature for %s" % n
+
+
+def test_pure_host_utilities(L):
+    assert L.dg_get_tma_aligned_size(4097, 4) == 4100
+    assert L.dg_get_tma_aligned_size(4096, 4) == 4096
+    assert L.dg_get_tma_aligned_size(1, 1) == 16
+    assert L.dg_get_tma_aligned_size(5, 2) == 8
+    assert L.dg_get_tma_aligned_size(5, 3) == -1
+    assert L.dg_get_mk_alignment_for_contiguous_layout() == 128
+    assert L.dg_version() >= 100
+    for s in range(9):
+        assert L.dg_status_string(s)
+    assert L.dg_set_num_sms(-1) == INVALID
+    assert L.dg_set_wait_timeout_ns(0) == INVALID
+
+
+P = C.c_void_p(0x1000)  # a 16-byte aligned fake pointer: never dereferenced on these paths
+
+
+def gemm(L, **kw):
+    a = dict(a=P, sfa=P, b=P, sfb=P, c=None, d=P, m=128, n=256, k=512, lda=512, ldb=512,
+             ldc=0, ldd=256, stream=None)
+    a.update(kw)
+    return L.dg_fp8_gemm_nt(a["a"], a["sfa"], a["b"], a["sfb"], a["c"], a["d"], a["m"], a["n"],
+                            a["k"], a["lda"], a["ldb"], a["ldc"], a["ldd"], a["stream"])
+
+
+def test_dense_host_checks(L):
+    assert gemm(L, k=100, lda=112, ldb=112) == ALIGN          # K % 128
+    assert gemm(L, n=260, ldd=260) == ALIGN                   # N % 8
+    assert gemm(L, k=0) == INVALID
+    assert gemm(L, m=-1) == INVALID
+    assert gemm(L, m=0) == DG_OK                              # empty problem: no-op
+    assert gemm(L, n=0, ldd=0) == DG_OK
+    assert gemm(L, a=None) == INVALID
+    assert gemm(L, d=None) == INVALID
+    assert gemm(L, lda=256) == INVALID                        # lda < K
+    assert gemm(L, lda=520) == ALIGN                          # lda % 16
+    assert gemm(L, a=C.c_void_p(0x1008)) == ALIGN             # 16-byte pointer alignment
+    assert gemm(L, c=P, ldc=100) == INVALID                   # ldc < N
+    assert gemm(L, m=1 << 31) == TOO_LARGE
+
+
+def test_grouped_host_checks(L):
+    cont = L.dg_m_grouped_fp8_gemm_nt_contiguous
+    assert cont(P, P, P, P, P, P, 130, 256, 512, 4, None) == ALIGN      # m_sum % 128
+    assert cont(P, P, P, P, P, None, 128, 256, 512, 4, None) == INVALID  # m_indices
+    assert cont(P, P, P, P, P, P, 0, 256, 512, 4, None) == DG_OK
+    assert cont(P, P, P, P, P, P, 128, 256, 512, 0, None) == DG_OK
+    assert cont(P, P, P, P, P, P, 128, 256, 500, 4, None) == ALIGN
+    masked = L.dg_m_grouped_fp8_gemm_nt_masked
+    assert masked(P, P, P, P, P, P, 1025, 256, 256, 512, 0, None) == TOO_LARGE
+    assert masked(P, P, P, P, P, None, 4, 256, 256, 512, 0, None) == INVALID
+    assert masked(P, P, P, P, P, P, 4, 0, 256, 512, 0, None) == DG_OK
+    assert masked(P, P, P, P, P, P, 4, 256, 250, 512, 0, None) == ALIGN
+    assert masked(P, P, P, P, P, P, 4, 256, 256, 512, -1, None) == INVALID
+
+
+def test_quantize_and_transform_host_checks(L):
+    q = L.dg_quantize_fp8
+    assert q(P, P, P, 1, 10, 130, 1, 1, None) == ALIGN
+    assert q(P, P, P, 1, 10, 128, 2, 1, None) == INVALID
+    assert q(P, P, P, 1, 10, 128, 1, 7, None) == INVALID
+    assert q(P, P, P, 0, 10, 128, 1, 1, None) == DG_OK
+    assert q(None, P, P, 1, 10, 128, 1, 1, None) == INVALID
+    t = L.dg_transform_sf
+    assert t(P, P, 1, 10, 128, 3, None) == INVALID
+    assert t(P, None, 1, 10, 128, 1, None) == INVALID
+    assert t(P, C.c_void_p(0x1004), 1, 10, 128, 1, None) == ALIGN
+    assert t(P, P, 0, 10, 128, 1, None) == DG_OK

@@ -1,0 +1,240 @@
+"""GPU parity of the GEMMs against the oracle on small and ragged shapes:
+bit-exact where the FP32 accumulation is exact, within the stated tolerance
+otherwise; rows and columns the kernel must not write are compared bit for bit
+against a sentinel fill."""
+import os
+from contextlib import contextmanager
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_grouped_gemm_fp8_gb300 as dg
+from moe_grouped_gemm_fp8_gb300 import workloads
+import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+_INT_CODE = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48, -1: 0xB8, -2: 0xC0, -3: 0xC4, -4: 0xC8}
+
+
+@contextmanager
+def block_n(bn):
+    old = os.environ.get("DG_BLOCK_N")
+    if bn:
+        os.environ["DG_BLOCK_N"] = str(bn)
+    else:
+        os.environ.pop("DG_BLOCK_N", None)
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("DG_BLOCK_N", None)
+        else:
+            os.environ["DG_BLOCK_N"] = old
+
+
+def _int_operand(rng, rows, cols):
+    v = rng.integers(-4, 5, size=(rows, cols))
+    return np.vectorize(_INT_CODE.get)(v).astype(np.uint8)
+
+
+def _no_device_error():
+    st, word = dg.get_device_error()
+    assert st == 0, "device error word 0x%x" % word
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(200, 264, 384), (128, 512, 1024), (5, 8, 128)])
+def test_dense_exact_small_integers(bn, M, N, K):
+    """Integer operands with power-of-two scales: every FP32 partial sum is
+    exact, so D must equal the BF16 rounding of the oracle bit for bit."""
+    rng = np.random.default_rng(M + N + K)
+    qa, qb = _int_operand(rng, M, K), _int_operand(rng, N, K)
+    ea = rng.integers(-2, 3, size=(M, K // 128))
+    eb = rng.integers(-2, 3, size=((N + 127) // 128, K // 128))
+    sa, sb = np.ldexp(1.0, ea), np.ldexp(1.0, eb)
+    want = oracle.bf16_rne(oracle.gemm_nt(qa, sa, qb, sb))
+    with block_n(bn):
+        d = dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1),
+                           P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    got = P.bf16_bits(d)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, "first mismatches (row, col): %s" % bad[:8].tolist()
+    _no_device_error()
+
+
+def test_dense_identity_b_is_exact():
+    K = 256
+    x = torch.randn(300, K, generator=torch.Generator().manual_seed(3))
+    qa, _, sa = P.quantize(x, 1)
+    qb = np.where(np.eye(K, dtype=bool), 0x38, 0x00).astype(np.uint8)
+    sb = np.ones((2, 2))
+    want = oracle.bf16_rne(oracle.gemm_nt(qa, sa, qb, sb))
+    d = dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, 300, K, 1), P.dev_codes(qb),
+                       P.dev_packed_sf(sb, K, K, 128))
+    assert np.array_equal(P.bf16_bits(d), want)
+
+
+def test_small_config_dense_128x256x512():
+    w = workloads.dense(**workloads.SMALL)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    o = oracle.gemm_nt(qa, sa, qb, sb)
+    d = dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, 128, 512, 1), P.dev_codes(qb),
+                       P.dev_packed_sf(sb, 256, 512, 128))
+    P.assert_close(P.bf16_to_f64(d), o, "dense 128x256x512")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("with_c", [False, True])
+@pytest.mark.parametrize("M,N,K", [(1, 8, 128), (100, 136, 640), (300, 392, 384), (129, 264, 1024), (257, 520, 256)])
+def test_dense_ragged(bn, with_c, M, N, K):
+    w = workloads.dense(M, N, K, seed=M * 7 + N + K, with_c=with_c)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    cb = P.bf16_bits(w.c) if with_c else None
+    o = oracle.gemm_nt(qa, sa, qb, sb, cb)
+    # D lives inside a wider sentinel-filled buffer: columns past N must stay untouched
+    ldd = N + 24
+    buf = P.sentinel_like((M, ldd))
+    d = buf[:, :N]
+    c = w.c.cuda() if with_c else None
+    with block_n(bn):
+        dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb),
+                       P.dev_packed_sf(sb, N, K, 128), d=d, c=c)
+    P.assert_close(P.bf16_to_f64(d), o, "dense %dx%dx%d" % (M, N, K))
+    assert (P.bf16_bits(buf[:, N:]) == P.SENTINEL_BITS).all()
+    _no_device_error()
+
+
+def test_dense_c_aliases_d():
+    M, N, K = 192, 256, 512
+    w = workloads.dense(M, N, K, seed=5, with_c=True)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    ref = dg.fp8_gemm_nt(*args, c=w.c.cuda())
+    inplace = w.c.cuda().clone()
+    dg.fp8_gemm_nt(*args, d=inplace, c=inplace)
+    assert torch.equal(inplace.view(torch.int16), ref.view(torch.int16))
+
+
+def _contig_setup(G, N, K, counts, seed):
+    w = workloads.contiguous(G, N, K, seed=seed, counts=counts)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    m_sum = w.a.shape[0]
+    dev = (P.dev_codes(qa), P.dev_packed_sf(sa, m_sum, K, 1), P.dev_codes(qb),
+           P.dev_packed_sf(sb, N, K, 128))
+    return w, (qa, sa, qb, sb), dev
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_contiguous_routing_and_values(bn):
+    G, N, K = 4, 264, 384
+    w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [100, 0, 250, 128], seed=77)
+    mi = w.m_indices.numpy()
+    o, written = oracle.gemm_contiguous(qa, sa, qb, sb, mi)
+    d = P.sentinel_like((mi.size, N))
+    with block_n(bn):
+        dg.m_grouped_fp8_gemm_nt_contiguous(*dev, w.m_indices.cuda(), d=d)
+    bits = P.bf16_bits(d)
+    wr = written.astype(bool)
+    assert np.array_equal(wr, mi >= 0)
+    assert (bits[~wr] == P.SENTINEL_BITS).all(), "padding rows were written"
+    P.assert_close(P.bf16_to_f64(d)[wr], o[wr], "contiguous")
+    _no_device_error()
+
+
+def test_contiguous_single_group_equals_dense():
+    G, N, K = 1, 256, 512
+    w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [384], seed=78)
+    d = dg.m_grouped_fp8_gemm_nt_contiguous(*dev, w.m_indices.cuda())
+    dd = dg.fp8_gemm_nt(dev[0], dev[1], dev[2][0], dev[3][0])
+    assert torch.equal(d.view(torch.int16), dd.view(torch.int16))
+
+
+def test_contiguous_bad_index_is_flagged_not_written():
+    G, N, K = 2, 128, 256
+    w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [128, 200], seed=79)
+    mi = w.m_indices.clone()
+    mi[128 + 5] = 7          # an expert id >= G inside expert 1's block
+    mi[128 * 2] = 9          # a whole block tagged with an expert id >= G
+    d = P.sentinel_like((mi.numel(), N))
+    dg.get_device_error()
+    dg.m_grouped_fp8_gemm_nt_contiguous(*dev, mi.cuda(), d=d)
+    st, word = dg.get_device_error()
+    assert st == 6, "expected DG_ERR_DEVICE_BAD_INDEX, got %d (0x%x)" % (st, word)
+    bits = P.bf16_bits(d)
+    assert (bits[128 + 5] == P.SENTINEL_BITS).all()
+    assert (bits[256:384] == P.SENTINEL_BITS).all()
+    o, _ = oracle.gemm_contiguous(qa, sa, qb, sb, w.m_indices.numpy())
+    P.assert_close(P.bf16_to_f64(d)[:128], o[:128], "block 0 unaffected")
+
+
+def _masked_setup(G, cap, N, K, mm, seed):
+    w = workloads.masked(G, cap, N, K, seed=seed, masked_m=mm)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    dev = (P.dev_codes(qa), P.dev_packed_sf(sa, cap, K, 1), P.dev_codes(qb),
+           P.dev_packed_sf(sb, N, K, 128))
+    return w, (qa, sa, qb, sb), dev
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("cap", [200, 256, 64])
+def test_masked_rows_and_values(bn, cap):
+    G, N, K = 4, 272, 256
+    mm = [0, cap, 77 % (cap + 1), min(129, cap)]
+    w, (qa, sa, qb, sb), dev = _masked_setup(G, cap, N, K, mm, seed=cap)
+    o, written = oracle.gemm_masked(qa, sa, qb, sb, np.array(mm, np.int32))
+    d = P.sentinel_like((G, cap, N))
+    with block_n(bn):
+        dg.m_grouped_fp8_gemm_nt_masked(*dev, w.masked_m.cuda(), expected_m=64, d=d)
+    bits = P.bf16_bits(d)
+    wr = written.astype(bool)
+    assert (bits[~wr] == P.SENTINEL_BITS).all(), "rows past masked_m were written"
+    P.assert_close(P.bf16_to_f64(d)[wr], o[wr], "masked")
+    _no_device_error()
+
+
+def test_masked_count_out_of_range_is_clamped_and_flagged():
+    G, cap, N, K = 2, 128, 128, 256
+    w, (qa, sa, qb, sb), dev = _masked_setup(G, cap, N, K, [cap, 3], seed=5)
+    mm = torch.tensor([cap + 50, -4], dtype=torch.int32)
+    d = P.sentinel_like((G, cap, N))
+    dg.get_device_error()
+    dg.m_grouped_fp8_gemm_nt_masked(*dev, mm.cuda(), d=d)
+    st, _ = dg.get_device_error()
+    assert st == 6
+    bits = P.bf16_bits(d)
+    assert (bits[1] == P.SENTINEL_BITS).all()
+    o, _ = oracle.gemm_masked(qa, sa, qb, sb, np.array([cap, 0], np.int32))
+    P.assert_close(P.bf16_to_f64(d)[0], o[0], "clamped group 0")
+
+
+def test_masked_all_zero_writes_nothing():
+    G, cap, N, K = 3, 128, 128, 128
+    w, _, dev = _masked_setup(G, cap, N, K, [0, 0, 0], seed=6)
+    d = P.sentinel_like((G, cap, N))
+    dg.m_grouped_fp8_gemm_nt_masked(*dev, w.masked_m.cuda(), d=d)
+    assert (P.bf16_bits(d) == P.SENTINEL_BITS).all()
+    _no_device_error()
+
+
+def test_num_sms_limit_does_not_change_results():
+    M, N, K = 512, 1024, 512
+    w = workloads.dense(M, N, K, seed=9)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    full = dg.fp8_gemm_nt(*args)
+    dg.set_num_sms(7)
+    try:
+        few = dg.fp8_gemm_nt(*args)
+    finally:
+        dg.set_num_sms(0)
+    assert torch.equal(full.view(torch.int16), few.view(torch.int16))
