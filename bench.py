@@ -44,6 +44,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-steps", type=int, default=0,
                    help="run this many untimed steps and exit (for an external profiler)")
+    p.add_argument("--shape", type=int, default=-1,
+                   help="prefill: restrict the step to this (N, K) index (profiling of one shape)")
     return p.parse_args()
 
 
@@ -151,9 +153,11 @@ class ClockSampler:
 # --------------------------------------------------------------------------- workloads
 
 
-def prefill_setup(dg, workloads, dev):
+def prefill_setup(dg, workloads, dev, only=-1):
     shapes = []
-    for cfg in workloads.PREFILL:
+    for i, cfg in enumerate(workloads.PREFILL):
+        if only >= 0 and i != only:
+            continue
         m, n, k = cfg["m"], cfg["n"], cfg["k"]
         w = workloads.dense(m, n, k, cfg["seed"], with_c=True)
         a = w.a.to(dev)
@@ -272,7 +276,7 @@ def run_reference(args, ranks):
 
 
 def run_prefill(args, ranks, dg, workloads, dev):
-    shapes = prefill_setup(dg, workloads, dev)
+    shapes = prefill_setup(dg, workloads, dev, args.shape)
     if args.profile_steps:
         for _ in range(args.profile_steps):
             prefill_step(dg, shapes)

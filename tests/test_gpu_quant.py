@@ -68,5 +68,6 @@ def test_transform_sf_flags_non_power_of_two():
     got = dg.transform_sf_into_required_layout(sf, 4, 256, 1).cpu().numpy().view(np.uint32)
     st, word = dg.get_device_error()
     assert st == 8 and (word & 0xFF) == 8  # DG_ERR_DEVICE_BAD_SCALE
-    assert ((got[0, 2] >> 8) & 0xFF) == 127 + 2  # 3.0 rounded up to 4.0
-    assert (got[0, 0] & 0xFFFF) == 0x7F7F
+    assert got.shape == (1, 1, 4)
+    assert ((got[0, 0, 2] >> 8) & 0xFF) == 127 + 2  # 3.0 rounded up to 4.0
+    assert (got[0, 0, 0] & 0xFFFF) == 0x7F7F
