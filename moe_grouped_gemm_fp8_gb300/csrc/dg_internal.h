@@ -25,6 +25,8 @@ enum ErrorSite : uint32_t {
   kSiteEpilogueTmemFull = 4,
   kSiteDrain = 5,
   kSiteProducerDrain = 6,
+  kSiteScaleFull = 7,
+  kSiteMmaScaleReady = 8,
   kSiteContiguousIndex = 16,
   kSiteMaskedCount = 17,
   kSiteTransformScale = 32,
@@ -44,22 +46,28 @@ struct GemmArgs {
   int32_t k_blocks;
   int32_t band;            // raster band height in M blocks
   uint64_t timeout_ns;
+  unsigned long long* err; // device error word
 };
 
-struct GemmConfig {
-  int block_n;
-  int stages;
-  int grid;
-  size_t smem_bytes;
-};
-
-// gemm.cu
-int gemm_max_stages(int block_n);
-size_t gemm_smem_bytes(int block_n, int stages, int mode);
+// gemm.cu: dispatch over the tile widths compiled in gemm_bn*.cu
+int gemm_stages(int block_n);
+bool gemm_block_n_supported(int block_n);
 cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
-                        const CUtensorMap& sfa, const CUtensorMap& sfb, const GemmArgs& args,
+                        const CUtensorMap& sfa, const CUtensorMap& sfb, GemmArgs args,
                         int grid, cudaStream_t stream);
 cudaError_t gemm_fetch_error(unsigned long long* word);  // reads and clears
+
+// gemm_bn*.cu: one tile width each (compiled in parallel)
+#define DG_DECLARE_GEMM_BN(BN)                                                                  \
+  cudaError_t gemm_launch_bn##BN(int mode, const CUtensorMap& a, const CUtensorMap& b,          \
+                                 const CUtensorMap& sfa, const CUtensorMap& sfb,                \
+                                 const GemmArgs& args, int grid, cudaStream_t stream);          \
+  int gemm_stages_bn##BN();
+DG_DECLARE_GEMM_BN(128)
+DG_DECLARE_GEMM_BN(192)
+DG_DECLARE_GEMM_BN(224)
+DG_DECLARE_GEMM_BN(256)
+#undef DG_DECLARE_GEMM_BN
 
 // quant.cu
 cudaError_t quantize_launch(const float* x, void* q, void* sf, int64_t groups, int64_t rows,

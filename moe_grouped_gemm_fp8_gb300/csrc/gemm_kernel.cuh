@@ -1,0 +1,562 @@
+// FP8 GEMM with fine-grained scaling on sm_103a: D = C + A @ B.T, dense and
+// M-grouped (contiguous / masked).  Kernel template; each tile width BN is
+// instantiated in its own translation unit (gemm_bn*.cu).
+//
+// Operation and layouts: "DeepGEMM: kernels GEMM FP8 limpos e eficientes por
+// meio de scaling granular" (pt.news.hada.io), sections "Interface GEMM e
+// restrições de layout" and "GEMM denso e grouped".  The Hopper design the
+// pages sketch (warp specialisation overlapping TMA data movement, tensor-core
+// MMA and CUDA-core promotion; launch report on feifmx.com, Feb 2025) is
+// re-done for Blackwell: the per-128-K scales are applied by the tensor core
+// itself (tcgen05 block-scaled MMA with UE8M0 scales held in TMEM) and the
+// FP32 accumulator lives in TMEM, so no CUDA-core promotion is needed.
+//
+// One persistent CTA per SM, 7 warps:
+//   warp 0      TMA producer (one lane): A tile [128 x 128] and B tile
+//               [BN x 128] (E4M3, 128-byte swizzle) per 128-wide K block into
+//               an S-stage ring; on every fourth K block also the packed
+//               scale words (one 32-bit word = the UE8M0 scales of four K
+//               blocks) of A's 128 rows and B's BN rows into a scale buffer.
+//   warp 1      MMA issuer (one lane, kept free of any other work): per
+//               fourth K block copies the scale words into TMEM
+//               (tcgen05.cp 32x128b.warpx4); per K block issues four
+//               128 x BN x 32 block-scaled MMAs, the instruction descriptor
+//               selecting the byte of the current K block; commits the stage
+//               back to the producer.  Also owns the TMEM allocation.
+//   warp 2      scale-layout warp: turns the TMA-loaded scale words (M-major
+//               row order) into the 32-row x 16-byte chunks tcgen05.cp reads
+//               (row r of a 128-row group at byte 16 (r % 32) + 4 (r / 32)).
+//   warps 3-6   epilogue: tcgen05.ld of the accumulator (one 32-lane TMEM
+//               quarter each), + C, round to BF16, predicated 16-byte stores
+//               of the rows the grouped layouts allow.
+// The accumulator is double-buffered in TMEM when 2 x BN columns leave room
+// for the scales, so the epilogue of one tile overlaps the next tile's MMAs.
+// Every mbarrier wait is bounded; on expiry the kernel records an error,
+// drains its in-flight copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dg_device.cuh"
+
+namespace dg {
+
+constexpr int kGemmThreads = 224;
+constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_103
+
+template <int BN>
+struct GemmLayout {
+  static constexpr int kSfbChunks = (BN + 127) / 128;  // 128-row chunks of B scales
+  static constexpr int kBytesA = kBlockM * kBlockK;
+  static constexpr int kBytesB = BN * kBlockK;
+  static constexpr int kOffB = kBytesA;
+  static constexpr int kStageBytes = (kBytesA + kBytesB + 1023) / 1024 * 1024;
+  // scale buffer: TMA-loaded words of A (128) and B (BN), then the same words
+  // in tcgen05.cp order
+  static constexpr int kRawA = 0;
+  static constexpr int kRawB = 512;
+  static constexpr int kCpA = kRawB + kSfbChunks * 512;
+  static constexpr int kCpB = kCpA + 512;
+  static constexpr int kSfBufBytes = kCpB + kSfbChunks * 512;
+  static constexpr uint32_t kTxAB = kBytesA + kBytesB;
+  static constexpr uint32_t kTxSF = 128 * 4 + BN * 4;
+  static constexpr int kSfCols = 4 + 4 * kSfbChunks;  // TMEM columns of one scale slot
+};
+
+static constexpr size_t gemm_ctrl_bytes(int stages, int mode) {
+  return (size_t)8 * (4 * stages + 5) + 16 +
+         (mode == kMasked ? (size_t)4 * (2 * kMaxMaskedGroups + 1) : 0);
+}
+
+// Scale buffers and TMEM scale slots are indexed by a running count of scale
+// packs modulo STAGES: a pack's buffer is reused only after the producer has
+// waited for the stage released STAGES uses later, by which point the copy
+// and every MMA that read the old pack have completed.  Each slot has its own
+// pair of barriers (scale words landed / scale words laid out) whose phases
+// advance once per pack, so every waiter sees every phase in order.
+template <int BN, int STAGES>
+struct GemmPlan {
+  using L = GemmLayout<BN>;
+  static constexpr int kNumAcc = (2 * BN + STAGES * L::kSfCols <= 512) ? 2 : 1;
+  static constexpr int kSfBase = kNumAcc * BN;
+  static_assert(kSfBase + STAGES * L::kSfCols <= 512, "TMEM over-subscribed");
+  static constexpr size_t smem_bytes(int mode) {
+    return (size_t)STAGES * L::kStageBytes + (size_t)STAGES * L::kSfBufBytes + 1024 +
+           gemm_ctrl_bytes(STAGES, mode);
+  }
+};
+
+struct Tile {
+  int g, mb, nb;
+};
+
+// Maps a linear tile index to (group, M block, N block).  Dense and
+// contiguous tiles are rastered in bands of `band` M blocks: inside a band the
+// M block varies fastest, so a wave of CTAs shares a few B column blocks and
+// one band of A.  Masked tiles are enumerated group by group (M block
+// fastest) from a prefix table built at kernel start.
+template <int MODE>
+struct Scheduler {
+  const GemmArgs* args;
+  const int* tile_start;   // masked: [G + 1]
+  const int* group_valid;  // masked: [G]
+  int total;
+  int cursor;              // masked: current group (tile indices only increase)
+
+  __device__ bool get(int t, Tile& tile) {
+    if (MODE == kMasked) {
+      while (t >= tile_start[cursor + 1]) ++cursor;
+      const int local = t - tile_start[cursor];
+      const int mbs = (group_valid[cursor] + kBlockM - 1) / kBlockM;
+      tile.g = cursor;
+      tile.mb = local % mbs;
+      tile.nb = local / mbs;
+      return true;
+    }
+    const int per_band = args->band * args->n_blocks;
+    const int b = t / per_band;
+    const int rem = t - b * per_band;
+    const int rows = min(args->band, args->m_blocks - b * args->band);
+    tile.nb = rem / rows;
+    tile.mb = b * args->band + rem % rows;
+    tile.g = 0;
+    if (MODE == kContiguous) {
+      const int g = __ldg(args->m_indices + (int64_t)tile.mb * kBlockM);
+      if (g < 0) return false;
+      if (g >= args->num_groups) {
+        record_error(args->err, DG_ERR_DEVICE_BAD_INDEX, kSiteContiguousIndex);
+        return false;
+      }
+      tile.g = g;
+    }
+    return true;
+  }
+};
+
+// Waits until the phase with `parity` of `bar` has completed, ignoring the
+// abort flag (used to drain in-flight work before exit), bounded in time.
+static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                               unsigned long long* err, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 63u) == 0 && (global_timer_ns() - t0 > timeout_ns || it >= (1u << 30))) {
+      record_error(err, DG_ERR_DEVICE_TIMEOUT, site);
+      return;
+    }
+  }
+}
+
+// Single-thread wait: one try first (the usual case), the bounded loop only
+// when the phase is not complete yet.
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         uint64_t timeout_ns, unsigned long long* err,
+                                         uint32_t site) {
+  return mbar_try_wait(bar, parity) ||
+         wait_bounded(bar, parity, abort_flag, timeout_ns, err, site);
+}
+
+// Whole-warp wait: lane 0 waits, the result is broadcast, and the warp
+// reconverges (so the other lanes observe what lane 0 acquired).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t timeout_ns, unsigned long long* err,
+                                          uint32_t site) {
+  const int lane = threadIdx.x & 31;
+  int ok = 0;
+  if (lane == 0) ok = wait_one(bar, parity, abort_flag, timeout_ns, err, site) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Stores 32 accumulator columns of one row (+ C), 16 bytes at a time, the
+// columns at or past n skipped (n % 8 == 0).
+__device__ __forceinline__ void store_row_chunk(const uint32_t (&r)[32], __nv_bfloat16* dp,
+                                                const __nv_bfloat16* cp, int cols_left) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    if (8 * p < cols_left) {
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(r[8 * p + i]);
+      if (cp) {
+        const uint4 cv = *reinterpret_cast<const uint4*>(cp + 8 * p);
+        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          f[2 * i] += __uint_as_float(cw[i] << 16);
+          f[2 * i + 1] += __uint_as_float(cw[i] & 0xFFFF0000u);
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(f[0], f[1]);
+      o.y = pack_bf16x2(f[2], f[3]);
+      o.z = pack_bf16x2(f[4], f[5]);
+      o.w = pack_bf16x2(f[6], f[7]);
+      *reinterpret_cast<uint4*>(dp + 8 * p) = o;
+    }
+  }
+}
+
+template <int BN, int STAGES, int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                    const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_sfa,
+                    const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
+  using L = GemmLayout<BN>;
+  using P = GemmPlan<BN, STAGES>;
+  constexpr int NUM_ACC = P::kNumAcc;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  uint8_t* sfbuf = smem + STAGES * L::kStageBytes;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sfbuf + STAGES * L::kSfBufBytes);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  auto sffull = [&](int p) { return smem_u32(bars + 2 * STAGES + p); };
+  auto sfready = [&](int p) { return smem_u32(bars + 3 * STAGES + p); };
+  auto tfull = [&](int a) { return smem_u32(bars + 4 * STAGES + a); };
+  auto tempty = [&](int a) { return smem_u32(bars + 4 * STAGES + 2 + a); };
+  const uint32_t drain = smem_u32(bars + 4 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
+  int* group_valid = tile_start + (kMaxMaskedGroups + 1);
+  unsigned long long* const err = args.err;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+      mbar_init(sffull(s), 1);
+      mbar_init(sfready(s), 1);
+    }
+    for (int a = 0; a < NUM_ACC; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+    tma_prefetch_desc(&tm_sfa);
+    tma_prefetch_desc(&tm_sfb);
+  }
+  if (MODE == kMasked && warp == 2) {
+    for (int g = lane; g < args.num_groups; g += 32) {
+      const int v = __ldg(args.masked_m + g);
+      const int c = v < 0 ? 0 : (v > args.m ? args.m : v);
+      if (c != v) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteMaskedCount);
+      group_valid[g] = c;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      int acc = 0;
+      for (int g = 0; g < args.num_groups; ++g) {
+        tile_start[g] = acc;
+        acc += (group_valid[g] + kBlockM - 1) / kBlockM * args.n_blocks;
+      }
+      tile_start[args.num_groups] = acc;
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  Scheduler<MODE> sched;
+  sched.args = &args;
+  sched.tile_start = tile_start;
+  sched.group_valid = group_valid;
+  sched.cursor = 0;
+  sched.total = MODE == kMasked ? tile_start[args.num_groups] : args.m_blocks * args.n_blocks;
+  const uint64_t tmo = args.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pack = 0;
+      uint32_t issued = 0, issued_parity = 0;        // stages: last fill's phase parity
+      uint32_t sf_issued = 0, sf_issued_parity = 0;  // scale slots
+      bool ok = true;
+      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+        Tile tile;
+        if (!sched.get(t, tile)) continue;
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!wait_one(empty(stage), phase ^ 1u, abort_flag, tmo, err, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sb = smem_u32(smem + stage * L::kStageBytes);
+          const uint32_t fb = full(stage);
+          mbar_arrive_expect_tx(fb, L::kTxAB);
+          const int kx = kb * kBlockK, my = tile.mb * kBlockM;
+          if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
+          else tma_load_2d(sb, &tm_a, fb, kx, my);
+          tma_load_3d(sb + L::kOffB, &tm_b, fb, kx, tile.nb * BN, tile.g);
+          if ((kb & 3) == 0) {
+            // The slot is free: its previous pack was laid out before the MMAs
+            // of a stage use this thread has since seen released.
+            const int slot = (int)(pack % STAGES);
+            const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
+            const uint32_t sfb = sffull(slot);
+            const uint32_t sf_phase = (pack / STAGES) & 1u;
+            mbar_arrive_expect_tx(sfb, L::kTxSF);
+            const int kp = kb >> 2;
+            if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, sfb, my, kp, tile.g);
+            else tma_load_2d(buf + L::kRawA, &tm_sfa, sfb, my, kp);
+            tma_load_3d(buf + L::kRawB, &tm_sfb, sfb, tile.nb * BN, kp, tile.g);
+            sf_issued |= 1u << slot;
+            sf_issued_parity = (sf_issued_parity & ~(1u << slot)) | (sf_phase << slot);
+            ++pack;
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every copy this thread issued has landed before smem is released.
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued & (1u << s))
+          wait_drain(full(s), (issued_parity >> s) & 1u, tmo, err, kSiteProducerDrain);
+        if (sf_issued & (1u << s))
+          wait_drain(sffull(s), (sf_issued_parity >> s) & 1u, tmo, err, kSiteProducerDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc0 = idesc_mxf8_e4m3(kBlockM, BN, 0, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pack = 0;
+      uint32_t sf_tmem = tmem_base + (uint32_t)P::kSfBase;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+        Tile tile;
+        if (!sched.get(t, tile)) continue;
+        if (!wait_one(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, err, kSiteMmaTmemEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < args.k_blocks; ++kb) {
+          if (!wait_one(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + stage * L::kStageBytes;
+          if ((kb & 3) == 0) {
+            const int slot = (int)(pack % STAGES);
+            if (!wait_one(sfready(slot), (pack / STAGES) & 1u, abort_flag, tmo, err,
+                          kSiteMmaScaleReady)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint8_t* buf = sfbuf + slot * L::kSfBufBytes;
+            sf_tmem = tmem_base + (uint32_t)(P::kSfBase + slot * L::kSfCols);
+            tc_cp_32x128b_warpx4(sf_tmem, smem_desc_sf_chunk(smem_u32(buf + L::kCpA)));
+#pragma unroll
+            for (int c = 0; c < L::kSfbChunks; ++c)
+              tc_cp_32x128b_warpx4(sf_tmem + 4 + 4 * c,
+                                   smem_desc_sf_chunk(smem_u32(buf + L::kCpB + c * 512)));
+            ++pack;
+          }
+          const uint32_t sel = (uint32_t)(kb & 3);
+          const uint32_t idesc = idesc0 | (sel << 4) | (sel << 29);
+          const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(st));
+          const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(st + L::kOffB));
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tc_mma_mxf8(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
+                        (kb | j) != 0 ? 1u : 0u);
+          tc_commit(empty(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull(acc));
+        if (++acc == NUM_ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Drain: all MMAs and TMEM copies issued here complete before TMEM is freed.
+      tc_commit(drain);
+      wait_drain(drain, 0, tmo, err, kSiteDrain);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ scale layout
+    // Visits every pack in order (never skipping a phase of a slot barrier).
+    uint32_t pack = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+      Tile tile;
+      if (!sched.get(t, tile)) continue;
+      for (int kb = 0; kb < args.k_blocks; kb += 4) {
+        const int slot = (int)(pack % STAGES);
+        if (!warp_wait(sffull(slot), (pack / STAGES) & 1u, abort_flag, tmo, err, kSiteScaleFull)) {
+          ok = false;
+          break;
+        }
+        uint8_t* buf = sfbuf + slot * L::kSfBufBytes;
+        {
+          const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawA);
+          const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
+          *reinterpret_cast<uint4*>(buf + L::kCpA + lane * 16) = v;
+        }
+#pragma unroll
+        for (int c = 0; c < L::kSfbChunks; ++c) {
+          const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawB + c * 512);
+          const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
+          *reinterpret_cast<uint4*>(buf + L::kCpB + c * 512 + lane * 16) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfready(slot));
+        ++pack;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
+      Tile tile;
+      if (!sched.get(t, tile)) continue;
+      if (!warp_wait(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
+      tc_fence_after();
+      const int row = tile.mb * kBlockM + row_in_tile;
+      bool row_ok;
+      int64_t out_row;
+      if (MODE == kDense) {
+        row_ok = row < args.m;
+        out_row = row;
+      } else if (MODE == kContiguous) {
+        const int gi = row < args.m ? __ldg(args.m_indices + row) : -1;
+        row_ok = gi == tile.g;
+        if (gi >= 0 && gi != tile.g) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteContiguousIndex);
+        out_row = row;
+      } else {
+        row_ok = row < group_valid[tile.g];
+        out_row = (int64_t)tile.g * args.m + row;
+      }
+      const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
+      const int col_base = tile.nb * BN;
+      __nv_bfloat16* drow = args.d + out_row * args.ldd;
+      const __nv_bfloat16* crow = args.c ? args.c + out_row * args.ldc : nullptr;
+      constexpr int NCH = BN / 32;
+      uint32_t ra[32], rb[32];
+      tc_ld_32x32b_x32(taddr, ra);
+      tc_wait_ld_regs(ra);
+#pragma unroll
+      for (int ch = 0; ch < NCH; ch += 2) {
+        if (ch + 1 < NCH) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
+        {
+          const int col0 = col_base + ch * 32;
+          if (row_ok && col0 < args.n)
+            store_row_chunk(ra, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
+        }
+        if (ch + 1 < NCH) {
+          tc_wait_ld_regs(rb);
+          if (ch + 2 < NCH) tc_ld_32x32b_x32(taddr + (ch + 2) * 32, ra);
+          const int col0 = col_base + (ch + 1) * 32;
+          if (row_ok && col0 < args.n)
+            store_row_chunk(rb, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
+          if (ch + 2 < NCH) tc_wait_ld_regs(ra);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+      if (++acc == NUM_ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int BN, int STAGES, int MODE>
+static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
+                                    const CUtensorMap& sfa, const CUtensorMap& sfb,
+                                    const GemmArgs& args, int grid, cudaStream_t stream) {
+  static_assert(GemmPlan<BN, STAGES>::smem_bytes(kMasked) <= (size_t)kSmemLimit,
+                "shared memory over the per-CTA limit");
+  auto kern = fp8_gemm_kernel<BN, STAGES, MODE>;
+  const size_t smem = GemmPlan<BN, STAGES>::smem_bytes(MODE);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, sfa, sfb, args);
+}
+
+template <int BN, int STAGES>
+static cudaError_t gemm_launch_modes(int mode, const CUtensorMap& a, const CUtensorMap& b,
+                                     const CUtensorMap& sfa, const CUtensorMap& sfb,
+                                     const GemmArgs& args, int grid, cudaStream_t stream) {
+  switch (mode) {
+    case kDense: return gemm_launch_impl<BN, STAGES, kDense>(a, b, sfa, sfb, args, grid, stream);
+    case kContiguous: return gemm_launch_impl<BN, STAGES, kContiguous>(a, b, sfa, sfb, args, grid, stream);
+    case kMasked: return gemm_launch_impl<BN, STAGES, kMasked>(a, b, sfa, sfb, args, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dg
+
+// Defines the launch entry of one tile width (one translation unit each).
+#define DG_DEFINE_GEMM_BN(BN, STAGES)                                                        \
+  namespace dg {                                                                           \
+  cudaError_t gemm_launch_bn##BN(int mode, const CUtensorMap& a, const CUtensorMap& b,     \
+                                 const CUtensorMap& sfa, const CUtensorMap& sfb,           \
+                                 const GemmArgs& args, int grid, cudaStream_t stream) {    \
+    return gemm_launch_modes<BN, STAGES>(mode, a, b, sfa, sfb, args, grid, stream);        \
+  }                                                                                        \
+  int gemm_stages_bn##BN() { return STAGES; }                                              \
+  }

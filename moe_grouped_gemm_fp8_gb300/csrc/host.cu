@@ -165,13 +165,30 @@ dg_status encode_a_3d(Operands& o, const void* a, const int32_t* sfa, int64_t gr
   }
 }
 
-// Tile width along N.  256-wide tiles halve the shared-memory traffic per MMA
-// but leave SMs idle when there are too few tiles; DG_BLOCK_N forces a choice.
-int choose_block_n(int64_t m_blocks_est, int64_t n, int sms) {
+// Tile width along N.  Wider tiles cut the shared-memory and L2 traffic per
+// MMA and amortise the fixed cost of each MMA instruction; narrower tiles
+// leave fewer SMs idle in the last wave and, below 256 columns, keep two
+// accumulators in TMEM so the epilogue overlaps the next tile.  The estimate
+// is waves x (K blocks + epilogue cost) x columns / relative throughput;
+// DG_BLOCK_N forces a width.
+int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int sms) {
   const int forced = env_int("DG_BLOCK_N", 0);
-  if (forced == 128 || forced == 256) return forced;
-  const int64_t tiles256 = m_blocks_est * ((n + 255) / 256);
-  return (n >= 1024 && tiles256 >= 2 * sms) ? 256 : 128;
+  if (gemm_block_n_supported(forced)) return forced;
+  static const int widths[4] = {128, 192, 224, 256};
+  static const double rate[4] = {1.0, 1.35, 1.5, 1.6};      // per-column MMA throughput
+  static const double epi_blocks[4] = {0.5, 0.5, 0.5, 6.0};  // non-overlapped epilogue
+  int best = 128;
+  double best_cost = 1e300;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t tiles = m_blocks * ((n + widths[i] - 1) / widths[i]);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double cost = (double)waves * ((double)k_blocks + epi_blocks[i]) * widths[i] / rate[i];
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = widths[i];
+    }
+  }
+  return best;
 }
 
 void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_n,
@@ -179,7 +196,7 @@ void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups,
   if (!env_flag("DG_PRINT_CONFIGS")) return;
   fprintf(stderr, "dg: %s m=%lld n=%lld k=%lld groups=%d block_m=128 block_n=%d stages=%d grid=%d band=%d\n",
           what, (long long)m, (long long)n, (long long)k, groups, block_n,
-          gemm_max_stages(block_n), grid, band);
+          gemm_stages(block_n), grid, band);
 }
 
 dg_status check_common_k_n(int64_t n, int64_t k) {
@@ -218,7 +235,7 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
-  const int block_n = choose_block_n(args.m_blocks, n, sms);
+  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms);
   Operands o;
   if ((s = encode_a_2d(o, a, sfa, m, k, lda)) != DG_OK) return s;
   if ((s = encode_b_side(o, b, sfb, 1, n, k, ldb, block_n)) != DG_OK) return s;
@@ -262,7 +279,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)(m_sum / kBlockM);
-  const int block_n = choose_block_n(args.m_blocks, n, sms);
+  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms);
   Operands o;
   if ((s = encode_a_2d(o, a, sfa, m_sum, k, k)) != DG_OK) return s;
   if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n)) != DG_OK) return s;
@@ -306,7 +323,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   GemmArgs args = {};
   args.m_blocks = (int32_t)((max_m + kBlockM - 1) / kBlockM);
   const int64_t m_est = expected_m > 0 ? (expected_m + kBlockM - 1) / kBlockM : args.m_blocks;
-  const int block_n = choose_block_n(m_est * num_groups, n, sms);
+  const int block_n = choose_block_n(m_est * num_groups, n, k / kBlockK, sms);
   Operands o;
   if ((s = encode_a_3d(o, a, sfa, num_groups, max_m, k)) != DG_OK) return s;
   if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n)) != DG_OK) return s;

@@ -45,7 +45,7 @@ def _no_device_error():
     assert st == 0, "device error word 0x%x" % word
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("bn", [128, 192, 224, 256])
 @pytest.mark.parametrize("M,N,K", [(200, 264, 384), (128, 512, 1024), (5, 8, 128)])
 def test_dense_exact_small_integers(bn, M, N, K):
     """Integer operands with power-of-two scales: every FP32 partial sum is
@@ -88,7 +88,7 @@ def test_small_config_dense_128x256x512():
     _no_device_error()
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("bn", [128, 192, 224, 256])
 @pytest.mark.parametrize("with_c", [False, True])
 @pytest.mark.parametrize("M,N,K", [(1, 8, 128), (100, 136, 640), (300, 392, 384), (129, 264, 1024), (257, 520, 256)])
 def test_dense_ragged(bn, with_c, M, N, K):
@@ -132,7 +132,7 @@ def _contig_setup(G, N, K, counts, seed):
     return w, (qa, sa, qb, sb), dev
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("bn", [128, 192, 224, 256])
 def test_contiguous_routing_and_values(bn):
     G, N, K = 4, 264, 384
     w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [100, 0, 250, 128], seed=77)
@@ -184,7 +184,7 @@ def _masked_setup(G, cap, N, K, mm, seed):
     return w, (qa, sa, qb, sb), dev
 
 
-@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("bn", [128, 192, 224, 256])
 @pytest.mark.parametrize("cap", [200, 256, 64])
 def test_masked_rows_and_values(bn, cap):
     G, N, K = 4, 272, 256
@@ -238,3 +238,25 @@ def test_num_sms_limit_does_not_change_results():
     finally:
         dg.set_num_sms(0)
     assert torch.equal(full.view(torch.int16), few.view(torch.int16))
+
+
+@pytest.mark.parametrize("K", [128, 640, 1536])
+def test_scale_ring_with_many_short_tiles(K):
+    """Few SMs, many tiles per CTA and K-block counts that are not multiples of
+    four: the scale buffers and TMEM scale slots cycle through every slot."""
+    M, N = 1024, 2048
+    w = workloads.dense(M, N, K, seed=K)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    rows = np.arange(0, M, 37)
+    o = oracle.gemm_nt_rows(qa, sa, qb, sb, rows)
+    for bn in (128, 192, 224, 256):
+        dg.set_num_sms(3)
+        try:
+            with block_n(bn):
+                d = dg.fp8_gemm_nt(*args)
+        finally:
+            dg.set_num_sms(0)
+        P.assert_close(P.bf16_to_f64(d)[rows], o, "K=%d bn=%d" % (K, bn))
+    _no_device_error()

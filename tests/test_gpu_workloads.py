@@ -121,3 +121,35 @@ def test_masked_moe_config():
     assert written.all()
     got = P.bf16_to_f64(d.view(G * cap, n)[torch.from_numpy(rows).cuda()])
     P.assert_close(got, o, "masked config")
+
+
+@pytest.mark.parametrize("counts", ["uniform128", "seeded"])
+def test_masked_moe_every_tile_width_full_grid(counts):
+    """The masked MoE shape at every tile width on all SMs: many CTAs with
+    several tiles each and 5- and 6-stage pipelines, the setting in which a
+    waiter that skips phases of a stage barrier would read stale scales."""
+    import os
+    cfg = workloads.MASKED
+    G, cap, n, k = cfg["num_groups"], cfg["cap"], cfg["n"], cfg["k"]
+    w = workloads.masked(G, cap, n, k, cfg["seed"], masked_m=[128] * G if counts == "uniform128" else None)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    mm = w.masked_m.numpy()
+    rows = np.array(sorted({g * cap + r for g in range(G) for r in range(0, mm[g], 29)} |
+                           {g * cap + mm[g] - 1 for g in range(G) if mm[g]}), dtype=np.int64)
+    o, _ = oracle.gemm_masked(qa, sa, qb, sb, mm, rows=rows)
+    dev = (P.dev_codes(qa), P.dev_packed_sf(sa, cap, k, 1), P.dev_codes(qb), P.dev_packed_sf(sb, n, k, 128))
+    old = os.environ.get("DG_BLOCK_N")
+    try:
+        for bn in ("128", "192", "224", "256"):
+            os.environ["DG_BLOCK_N"] = bn
+            d = P.sentinel_like((G, cap, n))
+            dg.m_grouped_fp8_gemm_nt_masked(*dev, w.masked_m.cuda(), d=d)
+            _no_device_error()
+            got = P.bf16_to_f64(d.view(G * cap, n)[torch.from_numpy(rows).cuda()])
+            P.assert_close(got, o, "masked bn=%s" % bn)
+    finally:
+        if old is None:
+            os.environ.pop("DG_BLOCK_N", None)
+        else:
+            os.environ["DG_BLOCK_N"] = old
