@@ -36,7 +36,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="prefill", choices=["prefill", "decode", "contiguous", "masked", "small"])
@@ -113,7 +113,7 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -282,19 +282,25 @@ def run_prefill(args, ranks, dg, workloads, dev):
             prefill_step(dg, shapes)
         torch.cuda.synchronize()
         return None
-    for _ in range(max(3, args.warmup)):
-        prefill_step(dg, shapes)
-    torch.cuda.synchronize()
+    # clocks are sampled from the first warm-up step to the end of the timed
+    # region (the sampler needs a few hundred ms to start reporting)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t_warm = time.perf_counter()
+    while True:
+        for _ in range(max(3, args.warmup)):
+            prefill_step(dg, shapes)
+        torch.cuda.synchronize()
+        if time.perf_counter() - t_warm > 0.5:
+            break
     st, word = dg.get_device_error()
     if st != 0:
         raise RuntimeError("device error after warm-up: 0x%x" % word)
 
     # device-timed region: inputs resident in HBM
     events = []
-    clocks = ClockSampler(torch.cuda.current_device())
     ranks.barrier()
     torch.cuda.synchronize()
-    clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record()
