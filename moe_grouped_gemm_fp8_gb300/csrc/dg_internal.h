@@ -27,6 +27,7 @@ enum ErrorSite : uint32_t {
   kSiteProducerDrain = 6,
   kSiteScaleFull = 7,
   kSiteMmaScaleReady = 8,
+  kSiteScaleEmpty = 9,
   kSiteContiguousIndex = 16,
   kSiteMaskedCount = 17,
   kSiteTransformScale = 32,

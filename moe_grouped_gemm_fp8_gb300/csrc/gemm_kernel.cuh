@@ -14,18 +14,19 @@
 // One persistent CTA per SM, 7 warps:
 //   warp 0      TMA producer (one lane): A tile [128 x 128] and B tile
 //               [BN x 128] (E4M3, 128-byte swizzle) per 128-wide K block into
-//               an S-stage ring; on every fourth K block also the packed
-//               scale words (one 32-bit word = the UE8M0 scales of four K
-//               blocks) of A's 128 rows and B's BN rows into a scale buffer.
+//               an S-stage ring.
 //   warp 1      MMA issuer (one lane, kept free of any other work): per
 //               fourth K block copies the scale words into TMEM
 //               (tcgen05.cp 32x128b.warpx4); per K block issues four
 //               128 x BN x 32 block-scaled MMAs, the instruction descriptor
 //               selecting the byte of the current K block; commits the stage
 //               back to the producer.  Also owns the TMEM allocation.
-//   warp 2      scale-layout warp: turns the TMA-loaded scale words (M-major
-//               row order) into the 32-row x 16-byte chunks tcgen05.cp reads
-//               (row r of a 128-row group at byte 16 (r % 32) + 4 (r / 32)).
+//   warp 2      scale warp: loads the packed scale words (one 32-bit word =
+//               the UE8M0 scales of four K blocks) of A's 128 rows and B's BN
+//               rows by TMA, up to three packs ahead of use, into a ring of
+//               kSfSlots buffers, and turns them (M-major row order) into the
+//               32-row x 16-byte chunks tcgen05.cp reads (row r of a 128-row
+//               group at byte 16 (r % 32) + 4 (r / 32)).
 //   warps 3-6   epilogue: tcgen05.ld of the accumulator (one 32-lane TMEM
 //               quarter each), + C, round to BF16, predicated 16-byte stores
 //               of the rows the grouped layouts allow.
@@ -66,25 +67,27 @@ struct GemmLayout {
   static constexpr int kSfCols = 4 + 4 * kSfbChunks;  // TMEM columns of one scale slot
 };
 
+constexpr int kSfSlots = 4;      // scale buffers / TMEM scale slots
+constexpr int kSfLookahead = 3;  // packs loaded ahead of the one being laid out
+
 static constexpr size_t gemm_ctrl_bytes(int stages, int mode) {
-  return (size_t)8 * (4 * stages + 5) + 16 +
+  return (size_t)8 * (2 * stages + 3 * kSfSlots + 5) + 16 +
          (mode == kMasked ? (size_t)4 * (2 * kMaxMaskedGroups + 1) : 0);
 }
 
 // Scale buffers and TMEM scale slots are indexed by a running count of scale
-// packs modulo STAGES: a pack's buffer is reused only after the producer has
-// waited for the stage released STAGES uses later, by which point the copy
-// and every MMA that read the old pack have completed.  Each slot has its own
-// pair of barriers (scale words landed / scale words laid out) whose phases
-// advance once per pack, so every waiter sees every phase in order.
+// packs modulo kSfSlots.  Each slot has three barriers whose phases advance
+// once per pack - words landed (TMA), words laid out (scale warp), slot free
+// (tcgen05.commit after the pack's last MMA) - and every waiter visits every
+// pack in order, so no wait ever skips a phase.
 template <int BN, int STAGES>
 struct GemmPlan {
   using L = GemmLayout<BN>;
-  static constexpr int kNumAcc = (2 * BN + STAGES * L::kSfCols <= 512) ? 2 : 1;
+  static constexpr int kNumAcc = (2 * BN + kSfSlots * L::kSfCols <= 512) ? 2 : 1;
   static constexpr int kSfBase = kNumAcc * BN;
-  static_assert(kSfBase + STAGES * L::kSfCols <= 512, "TMEM over-subscribed");
+  static_assert(kSfBase + kSfSlots * L::kSfCols <= 512, "TMEM over-subscribed");
   static constexpr size_t smem_bytes(int mode) {
-    return (size_t)STAGES * L::kStageBytes + (size_t)STAGES * L::kSfBufBytes + 1024 +
+    return (size_t)STAGES * L::kStageBytes + (size_t)kSfSlots * L::kSfBufBytes + 1024 +
            gemm_ctrl_bytes(STAGES, mode);
   }
 };
@@ -133,6 +136,37 @@ struct Scheduler {
       tile.g = g;
     }
     return true;
+  }
+};
+
+// Walks the scale packs (tile, K block / 4) of this CTA in the order the MMA
+// consumes them, skipping the tiles the scheduler skips.
+template <int MODE>
+struct PackCursor {
+  Scheduler<MODE> s;
+  int t, stride, kb, k_blocks;
+  Tile tile;
+  bool done;
+
+  __device__ void init(const Scheduler<MODE>& sch, int first, int stride_, int kbs) {
+    s = sch;
+    stride = stride_;
+    k_blocks = kbs;
+    t = first - stride_;
+    next_tile();
+  }
+  __device__ void next_tile() {
+    done = true;
+    for (t += stride; t < s.total; t += stride)
+      if (s.get(t, tile)) {
+        done = false;
+        kb = 0;
+        return;
+      }
+  }
+  __device__ void advance() {
+    kb += 4;
+    if (kb >= k_blocks) next_tile();
   }
 };
 
@@ -225,15 +259,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sfbuf + STAGES * L::kSfBufBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sfbuf + kSfSlots * L::kSfBufBytes);
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto sffull = [&](int p) { return smem_u32(bars + 2 * STAGES + p); };
-  auto sfready = [&](int p) { return smem_u32(bars + 3 * STAGES + p); };
-  auto tfull = [&](int a) { return smem_u32(bars + 4 * STAGES + a); };
-  auto tempty = [&](int a) { return smem_u32(bars + 4 * STAGES + 2 + a); };
-  const uint32_t drain = smem_u32(bars + 4 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * STAGES + 5);
+  auto sfready = [&](int p) { return smem_u32(bars + 2 * STAGES + kSfSlots + p); };
+  auto sfempty = [&](int p) { return smem_u32(bars + 2 * STAGES + 2 * kSfSlots + p); };
+  constexpr int kB0 = 2 * STAGES + 3 * kSfSlots;
+  auto tfull = [&](int a) { return smem_u32(bars + kB0 + a); };
+  auto tempty = [&](int a) { return smem_u32(bars + kB0 + 2 + a); };
+  const uint32_t drain = smem_u32(bars + kB0 + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kB0 + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
   int* group_valid = tile_start + (kMaxMaskedGroups + 1);
@@ -243,8 +279,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
-      mbar_init(sffull(s), 1);
-      mbar_init(sfready(s), 1);
+    }
+    for (int p = 0; p < kSfSlots; ++p) {
+      mbar_init(sffull(p), 1);
+      mbar_init(sfready(p), 1);
+      mbar_init(sfempty(p), 1);
     }
     for (int a = 0; a < NUM_ACC; ++a) {
       mbar_init(tfull(a), 1);
@@ -297,9 +336,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t pack = 0;
-      uint32_t issued = 0, issued_parity = 0;        // stages: last fill's phase parity
-      uint32_t sf_issued = 0, sf_issued_parity = 0;  // scale slots
+      uint32_t issued = 0, issued_parity = 0;  // stages: last fill's phase parity
       bool ok = true;
       for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
         Tile tile;
@@ -316,22 +353,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
           else tma_load_2d(sb, &tm_a, fb, kx, my);
           tma_load_3d(sb + L::kOffB, &tm_b, fb, kx, tile.nb * BN, tile.g);
-          if ((kb & 3) == 0) {
-            // The slot is free: its previous pack was laid out before the MMAs
-            // of a stage use this thread has since seen released.
-            const int slot = (int)(pack % STAGES);
-            const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
-            const uint32_t sfb = sffull(slot);
-            const uint32_t sf_phase = (pack / STAGES) & 1u;
-            mbar_arrive_expect_tx(sfb, L::kTxSF);
-            const int kp = kb >> 2;
-            if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, sfb, my, kp, tile.g);
-            else tma_load_2d(buf + L::kRawA, &tm_sfa, sfb, my, kp);
-            tma_load_3d(buf + L::kRawB, &tm_sfb, sfb, tile.nb * BN, kp, tile.g);
-            sf_issued |= 1u << slot;
-            sf_issued_parity = (sf_issued_parity & ~(1u << slot)) | (sf_phase << slot);
-            ++pack;
-          }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -341,12 +362,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       // Drain: every copy this thread issued has landed before smem is released.
-      for (int s = 0; s < STAGES; ++s) {
+      for (int s = 0; s < STAGES; ++s)
         if (issued & (1u << s))
           wait_drain(full(s), (issued_parity >> s) & 1u, tmo, err, kSiteProducerDrain);
-        if (sf_issued & (1u << s))
-          wait_drain(sffull(s), (sf_issued_parity >> s) & 1u, tmo, err, kSiteProducerDrain);
-      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -375,9 +393,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           uint8_t* st = smem + stage * L::kStageBytes;
+          const int slot = (int)(pack % kSfSlots);
           if ((kb & 3) == 0) {
-            const int slot = (int)(pack % STAGES);
-            if (!wait_one(sfready(slot), (pack / STAGES) & 1u, abort_flag, tmo, err,
+            if (!wait_one(sfready(slot), (pack / kSfSlots) & 1u, abort_flag, tmo, err,
                           kSiteMmaScaleReady)) {
               ok = false;
               break;
@@ -390,7 +408,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int c = 0; c < L::kSfbChunks; ++c)
               tc_cp_32x128b_warpx4(sf_tmem + 4 + 4 * c,
                                    smem_desc_sf_chunk(smem_u32(buf + L::kCpB + c * 512)));
-            ++pack;
           }
           const uint32_t sel = (uint32_t)(kb & 3);
           const uint32_t idesc = idesc0 | (sel << 4) | (sel << 29);
@@ -401,6 +418,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_mma_mxf8(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
                         (kb | j) != 0 ? 1u : 0u);
           tc_commit(empty(stage));
+          if ((kb & 3) == 3 || kb == args.k_blocks - 1) {
+            tc_commit(sfempty(slot));  // the pack's buffer and TMEM slot are free
+            ++pack;
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -419,37 +440,68 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ------------------------------------------------------------ scale layout
-    // Visits every pack in order (never skipping a phase of a slot barrier).
-    uint32_t pack = 0;
+    // ------------------------------------------------------------ scale warp
+    // Two cursors walk the same sequence of packs (tile, K block / 4): one
+    // loads up to kSfLookahead packs ahead, the other lays them out in order.
+    PackCursor<MODE> ld, lay;
+    ld.init(sched, blockIdx.x, gridDim.x, args.k_blocks);
+    lay.init(sched, blockIdx.x, gridDim.x, args.k_blocks);
+    uint32_t n_loaded = 0, n_laid = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
-      Tile tile;
-      if (!sched.get(t, tile)) continue;
-      for (int kb = 0; kb < args.k_blocks; kb += 4) {
-        const int slot = (int)(pack % STAGES);
-        if (!warp_wait(sffull(slot), (pack / STAGES) & 1u, abort_flag, tmo, err, kSiteScaleFull)) {
+    while (!lay.done && ok) {
+      while (!ld.done && n_loaded < n_laid + kSfLookahead) {
+        const int slot = (int)(n_loaded % kSfSlots);
+        int go = 1;
+        if (lane == 0) {
+          go = wait_one(sfempty(slot), ((n_loaded / kSfSlots) & 1u) ^ 1u, abort_flag, tmo, err,
+                        kSiteScaleEmpty) ? 1 : 0;
+          if (go) {
+            const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
+            const uint32_t bar = sffull(slot);
+            const int my = ld.tile.mb * kBlockM, kp = ld.kb >> 2;
+            mbar_arrive_expect_tx(bar, L::kTxSF);
+            if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
+            else tma_load_2d(buf + L::kRawA, &tm_sfa, bar, my, kp);
+            tma_load_3d(buf + L::kRawB, &tm_sfb, bar, ld.tile.nb * BN, kp, ld.tile.g);
+          }
+        }
+        go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) {
           ok = false;
           break;
         }
-        uint8_t* buf = sfbuf + slot * L::kSfBufBytes;
-        {
-          const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawA);
-          const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
-          *reinterpret_cast<uint4*>(buf + L::kCpA + lane * 16) = v;
-        }
-#pragma unroll
-        for (int c = 0; c < L::kSfbChunks; ++c) {
-          const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawB + c * 512);
-          const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
-          *reinterpret_cast<uint4*>(buf + L::kCpB + c * 512 + lane * 16) = v;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sfready(slot));
-        ++pack;
+        ++n_loaded;
+        ld.advance();
       }
+      if (!ok) break;
+      const int slot = (int)(n_laid % kSfSlots);
+      if (!warp_wait(sffull(slot), (n_laid / kSfSlots) & 1u, abort_flag, tmo, err, kSiteScaleFull)) {
+        ok = false;
+        break;
+      }
+      uint8_t* buf = sfbuf + slot * L::kSfBufBytes;
+      {
+        const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawA);
+        const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
+        *reinterpret_cast<uint4*>(buf + L::kCpA + lane * 16) = v;
+      }
+#pragma unroll
+      for (int c = 0; c < L::kSfbChunks; ++c) {
+        const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawB + c * 512);
+        const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
+        *reinterpret_cast<uint4*>(buf + L::kCpB + c * 512 + lane * 16) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfready(slot));
+      ++n_laid;
+      lay.advance();
     }
+    // Drain: scale loads issued but not laid out (abort path) land before exit.
+    if (lane == 0)
+      for (uint32_t q = n_laid; q < n_loaded; ++q)
+        wait_drain(sffull((int)(q % kSfSlots)), (q / kSfSlots) & 1u, tmo, err, kSiteProducerDrain);
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
