@@ -127,7 +127,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
  *             [0, max_m] are clamped and set DG_ERR_DEVICE_BAD_INDEX.
  *   expected_m  host hint of the typical masked_m (tile selection only);
  *               0 = unknown.  Never affects results.
- * num_groups <= 1024.  masked_m is never read on the host, so the call can
+ * num_groups <= 512.  masked_m is never read on the host, so the call can
  * be captured in a CUDA graph.
  * Cited: same page, section "GEMM denso e grouped" (masked grouped GEMM,
  * m_grouped_fp8_gemm_nt_masked: with a mask tensor the kernel computes only

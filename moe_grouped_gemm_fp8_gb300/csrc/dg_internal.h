@@ -13,7 +13,7 @@ namespace dg {
 
 constexpr int kBlockM = 128;  // rows of an output tile (UMMA M)
 constexpr int kBlockK = 128;  // K extent of one scale block / pipeline stage
-constexpr int kMaxMaskedGroups = 1024;
+constexpr int kMaxMaskedGroups = 512;
 
 enum GemmMode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
 
@@ -54,15 +54,16 @@ struct GemmArgs {
 int gemm_stages(int block_n);
 bool gemm_block_n_supported(int block_n);
 cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
-                        const CUtensorMap& sfa, const CUtensorMap& sfb, GemmArgs args,
-                        int grid, cudaStream_t stream);
+                        const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
+                        GemmArgs args, int grid, cudaStream_t stream);
 cudaError_t gemm_fetch_error(unsigned long long* word);  // reads and clears
 
 // gemm_bn*.cu: one tile width each (compiled in parallel)
 #define DG_DECLARE_GEMM_BN(BN)                                                                  \
   cudaError_t gemm_launch_bn##BN(int mode, const CUtensorMap& a, const CUtensorMap& b,          \
                                  const CUtensorMap& sfa, const CUtensorMap& sfb,                \
-                                 const GemmArgs& args, int grid, cudaStream_t stream);          \
+                                 const CUtensorMap& d, const GemmArgs& args, int grid,          \
+                                 cudaStream_t stream);                                          \
   int gemm_stages_bn##BN();
 DG_DECLARE_GEMM_BN(128)
 DG_DECLARE_GEMM_BN(192)

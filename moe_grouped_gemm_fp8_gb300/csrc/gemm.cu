@@ -20,8 +20,8 @@ int gemm_stages(int block_n) {
 bool gemm_block_n_supported(int block_n) { return gemm_stages(block_n) > 0; }
 
 cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
-                        const CUtensorMap& sfa, const CUtensorMap& sfb, GemmArgs args, int grid,
-                        cudaStream_t stream) {
+                        const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
+                        GemmArgs args, int grid, cudaStream_t stream) {
   // Host code must pass the device address of the error word, not the
   // host-side shadow the symbol name denotes here.
   void* err = nullptr;
@@ -29,10 +29,10 @@ cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUten
   if (e != cudaSuccess) return e;
   args.err = static_cast<unsigned long long*>(err);
   switch (block_n) {
-    case 128: return gemm_launch_bn128(mode, a, b, sfa, sfb, args, grid, stream);
-    case 192: return gemm_launch_bn192(mode, a, b, sfa, sfb, args, grid, stream);
-    case 224: return gemm_launch_bn224(mode, a, b, sfa, sfb, args, grid, stream);
-    case 256: return gemm_launch_bn256(mode, a, b, sfa, sfb, args, grid, stream);
+    case 128: return gemm_launch_bn128(mode, a, b, sfa, sfb, d, args, grid, stream);
+    case 192: return gemm_launch_bn192(mode, a, b, sfa, sfb, d, args, grid, stream);
+    case 224: return gemm_launch_bn224(mode, a, b, sfa, sfb, d, args, grid, stream);
+    case 256: return gemm_launch_bn256(mode, a, b, sfa, sfb, d, args, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

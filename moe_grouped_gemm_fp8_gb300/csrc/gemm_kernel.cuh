@@ -28,8 +28,14 @@
 //               32-row x 16-byte chunks tcgen05.cp reads (row r of a 128-row
 //               group at byte 16 (r % 32) + 4 (r / 32)).
 //   warps 3-6   epilogue: tcgen05.ld of the accumulator (one 32-lane TMEM
-//               quarter each), + C, round to BF16, predicated 16-byte stores
-//               of the rows the grouped layouts allow.
+//               quarter each, 32 columns at a time, the next chunk loading
+//               while the current one is converted), + C, round to BF16.  A
+//               32 x 32 chunk is staged in shared memory (64-byte swizzle,
+//               conflict-free for one row per thread) and written by a TMA
+//               store; C arrives through coalesced loads staged the same way.
+//               Quarters of grouped tiles with rows that must stay untouched
+//               use row-predicated 16-byte stores instead.  TMEM is released
+//               as soon as the last chunk is in registers.
 // The accumulator is double-buffered in TMEM when 2 x BN columns leave room
 // for the scales, so the epilogue of one tile overlaps the next tile's MMAs.
 // Every mbarrier wait is bounded; on expiry the kernel records an error,
@@ -68,6 +74,8 @@ struct GemmLayout {
 };
 
 constexpr int kSfSlots = 4;      // scale buffers / TMEM scale slots
+constexpr int kEpiBuf = 32 * 32 * 2;  // one 32 x 32 BF16 staging chunk
+constexpr int kEpiBytes = 4 * 2 * kEpiBuf;  // 4 epilogue warps x 2 buffers
 constexpr int kSfLookahead = 3;  // packs loaded ahead of the one being laid out
 
 static constexpr size_t gemm_ctrl_bytes(int stages, int mode) {
@@ -87,8 +95,8 @@ struct GemmPlan {
   static constexpr int kSfBase = kNumAcc * BN;
   static_assert(kSfBase + kSfSlots * L::kSfCols <= 512, "TMEM over-subscribed");
   static constexpr size_t smem_bytes(int mode) {
-    return (size_t)STAGES * L::kStageBytes + (size_t)kSfSlots * L::kSfBufBytes + 1024 +
-           gemm_ctrl_bytes(STAGES, mode);
+    return (size_t)STAGES * L::kStageBytes + (size_t)kSfSlots * L::kSfBufBytes + kEpiBytes +
+           1024 + gemm_ctrl_bytes(STAGES, mode);
   }
 };
 
@@ -246,7 +254,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
-                    const __grid_constant__ CUtensorMap tm_sfb, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tm_sfb,
+                    const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
   using L = GemmLayout<BN>;
   using P = GemmPlan<BN, STAGES>;
   constexpr int NUM_ACC = P::kNumAcc;
@@ -259,7 +268,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sfbuf + kSfSlots * L::kSfBufBytes);
+  uint8_t* epi_smem = sfbuf + kSfSlots * L::kSfBufBytes;  // 1024-aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + kEpiBytes);
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto sffull = [&](int p) { return smem_u32(bars + 2 * STAGES + p); };
@@ -296,6 +306,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_sfa);
     tma_prefetch_desc(&tm_sfb);
+    tma_prefetch_desc(&tm_d);
   }
   if (MODE == kMasked && warp == 2) {
     for (int g = lane; g < args.num_groups; g += 32) {
@@ -505,7 +516,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
-    const int row_in_tile = quarter * 32 + lane;
+    uint8_t* ebuf = epi_smem + (warp - 3) * 2 * kEpiBuf;
+    // 64-byte swizzle of a 32 x 32 BF16 chunk: 16-byte piece j of row r sits at
+    // r * 64 + 16 * (j ^ ((r >> 1) & 3)) (the layout of CU_TENSOR_MAP_SWIZZLE_64B)
+    const uint32_t my_row_off = (uint32_t)lane * 64u;
+    const uint32_t my_swz = ((uint32_t)lane >> 1) & 3u;
+    uint32_t nchunk = 0;  // chunks staged so far (buffer = nchunk & 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
@@ -513,54 +529,105 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!sched.get(t, tile)) continue;
       if (!warp_wait(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
       tc_fence_after();
-      const int row = tile.mb * kBlockM + row_in_tile;
+      const int row0 = tile.mb * kBlockM + quarter * 32;
+      const int row = row0 + lane;
       bool row_ok;
-      int64_t out_row;
+      int64_t out_row0;
       if (MODE == kDense) {
         row_ok = row < args.m;
-        out_row = row;
+        out_row0 = row0;
       } else if (MODE == kContiguous) {
         const int gi = row < args.m ? __ldg(args.m_indices + row) : -1;
         row_ok = gi == tile.g;
         if (gi >= 0 && gi != tile.g) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteContiguousIndex);
-        out_row = row;
+        out_row0 = row0;
       } else {
         row_ok = row < group_valid[tile.g];
-        out_row = (int64_t)tile.g * args.m + row;
+        out_row0 = (int64_t)tile.g * args.m + row0;
       }
+      // The TMA store clips at M and N, so dense quarters always use it; a
+      // grouped quarter uses it only when every one of its rows is written.
+      const bool use_tma = (MODE == kDense) ? true : (__all_sync(0xffffffffu, row_ok) != 0);
+      __nv_bfloat16* drow = args.d + (out_row0 + lane) * args.ldd;
+      const __nv_bfloat16* crow = args.c ? args.c + (out_row0 + lane) * args.ldc : nullptr;
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
-      const int col_base = tile.nb * BN;
-      __nv_bfloat16* drow = args.d + out_row * args.ldd;
-      const __nv_bfloat16* crow = args.c ? args.c + out_row * args.ldc : nullptr;
       constexpr int NCH = BN / 32;
       uint32_t ra[32], rb[32];
       tc_ld_32x32b_x32(taddr, ra);
-      tc_wait_ld_regs(ra);
 #pragma unroll
-      for (int ch = 0; ch < NCH; ch += 2) {
-        if (ch + 1 < NCH) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, rb);
-        {
-          const int col0 = col_base + ch * 32;
-          if (row_ok && col0 < args.n)
-            store_row_chunk(ra, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
-        }
+      for (int ch = 0; ch < NCH; ++ch) {
+        uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
+        uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
+        tc_wait_ld_regs(cur);
         if (ch + 1 < NCH) {
-          tc_wait_ld_regs(rb);
-          if (ch + 2 < NCH) tc_ld_32x32b_x32(taddr + (ch + 2) * 32, ra);
-          const int col0 = col_base + (ch + 1) * 32;
-          if (row_ok && col0 < args.n)
-            store_row_chunk(rb, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
-          if (ch + 2 < NCH) tc_wait_ld_regs(ra);
+          tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
+        } else {
+          // every column of this accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty(acc));
+        }
+        const int col0 = tile.nb * BN + ch * 32;
+        if (col0 >= args.n) continue;
+        if (use_tma) {
+          uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
+          const uint32_t sbuf = smem_u32(buf);
+          if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+          __syncwarp();
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
+          if (args.c) {
+            // coalesced: lane l fetches 16 bytes of rows l/4 + 8i, piece l % 4
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i, pc = lane & 3;
+              const int gcol = col0 + pc * 8;
+              uint4 v = make_uint4(0u, 0u, 0u, 0u);
+              if (gcol < args.n && (MODE != kDense || row0 + r < args.m))
+                v = __ldg(reinterpret_cast<const uint4*>(args.c + (out_row0 + r) * args.ldc + gcol));
+              *reinterpret_cast<uint4*>(buf + r * 64 + 16 * (pc ^ ((r >> 1) & 3))) = v;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 cv = *reinterpret_cast<const uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz));
+              const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                f[8 * j + 2 * i] += __uint_as_float(cw[i] << 16);
+                f[8 * j + 2 * i + 1] += __uint_as_float(cw[i] & 0xFFFF0000u);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 o;
+            o.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
+            o.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
+            o.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
+            o.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+            *reinterpret_cast<uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz)) = o;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_d, sbuf, col0, (int32_t)out_row0);
+            bulk_commit_group();
+          }
+          ++nchunk;
+        } else if (row_ok) {
+          store_row_chunk(cur, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(acc));
       if (++acc == NUM_ACC) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
+    // every TMA store issued here has completed before the CTA exits
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   __syncthreads();
@@ -573,7 +640,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int BN, int STAGES, int MODE>
 static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
                                     const CUtensorMap& sfa, const CUtensorMap& sfb,
-                                    const GemmArgs& args, int grid, cudaStream_t stream) {
+                                    const CUtensorMap& d, const GemmArgs& args, int grid,
+                                    cudaStream_t stream) {
   static_assert(GemmPlan<BN, STAGES>::smem_bytes(kMasked) <= (size_t)kSmemLimit,
                 "shared memory over the per-CTA limit");
   auto kern = fp8_gemm_kernel<BN, STAGES, MODE>;
@@ -585,17 +653,18 @@ static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, sfa, sfb, args);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, sfa, sfb, d, args);
 }
 
 template <int BN, int STAGES>
 static cudaError_t gemm_launch_modes(int mode, const CUtensorMap& a, const CUtensorMap& b,
                                      const CUtensorMap& sfa, const CUtensorMap& sfb,
-                                     const GemmArgs& args, int grid, cudaStream_t stream) {
+                                     const CUtensorMap& d, const GemmArgs& args, int grid,
+                                     cudaStream_t stream) {
   switch (mode) {
-    case kDense: return gemm_launch_impl<BN, STAGES, kDense>(a, b, sfa, sfb, args, grid, stream);
-    case kContiguous: return gemm_launch_impl<BN, STAGES, kContiguous>(a, b, sfa, sfb, args, grid, stream);
-    case kMasked: return gemm_launch_impl<BN, STAGES, kMasked>(a, b, sfa, sfb, args, grid, stream);
+    case kDense: return gemm_launch_impl<BN, STAGES, kDense>(a, b, sfa, sfb, d, args, grid, stream);
+    case kContiguous: return gemm_launch_impl<BN, STAGES, kContiguous>(a, b, sfa, sfb, d, args, grid, stream);
+    case kMasked: return gemm_launch_impl<BN, STAGES, kMasked>(a, b, sfa, sfb, d, args, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -607,8 +676,9 @@ static cudaError_t gemm_launch_modes(int mode, const CUtensorMap& a, const CUten
   namespace dg {                                                                           \
   cudaError_t gemm_launch_bn##BN(int mode, const CUtensorMap& a, const CUtensorMap& b,     \
                                  const CUtensorMap& sfa, const CUtensorMap& sfb,           \
-                                 const GemmArgs& args, int grid, cudaStream_t stream) {    \
-    return gemm_launch_modes<BN, STAGES>(mode, a, b, sfa, sfb, args, grid, stream);        \
+                                 const CUtensorMap& d, const GemmArgs& args, int grid,     \
+                                 cudaStream_t stream) {                                    \
+    return gemm_launch_modes<BN, STAGES>(mode, a, b, sfa, sfb, d, args, grid, stream);     \
   }                                                                                        \
   int gemm_stages_bn##BN() { return STAGES; }                                              \
   }

@@ -99,8 +99,18 @@ int64_t align4(int64_t x) { return (x + 3) / 4 * 4; }
 
 // Operand descriptors shared by the three GEMM forms.
 struct Operands {
-  CUtensorMap a, b, sfa, sfb;
+  CUtensorMap a, b, sfa, sfb, d;
 };
+
+// D as a 2-D BF16 tensor [rows, n] with row stride ldd (elements); 32 x 32
+// boxes with the 64-byte swizzle the epilogue stages in.
+dg_status encode_d(Operands& o, void* d, int64_t rows, int64_t n, int64_t ldd) {
+  uint64_t dims[2] = {(uint64_t)n, (uint64_t)rows};
+  uint64_t strides[1] = {(uint64_t)(ldd * 2)};
+  uint32_t box[2] = {32, 32};
+  return encode(&o.d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_64B);
+}
 
 dg_status encode_b_side(Operands& o, const void* b, const int32_t* sfb, int64_t groups,
                         int64_t n, int64_t k, int64_t ldb, int block_n) {
@@ -171,12 +181,13 @@ dg_status encode_a_3d(Operands& o, const void* a, const int32_t* sfa, int64_t gr
 // accumulators in TMEM so the epilogue overlaps the next tile.  The estimate
 // is waves x (K blocks + epilogue cost) x columns / relative throughput;
 // DG_BLOCK_N forces a width.
-int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int sms) {
+int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int sms, bool with_c) {
   const int forced = env_int("DG_BLOCK_N", 0);
   if (gemm_block_n_supported(forced)) return forced;
   static const int widths[4] = {128, 192, 224, 256};
-  static const double rate[4] = {1.0, 1.35, 1.5, 1.6};      // per-column MMA throughput
-  static const double epi_blocks[4] = {0.5, 0.5, 0.5, 6.0};  // non-overlapped epilogue
+  static const double rate[4] = {1.0, 1.35, 1.5, 1.6};  // per-column MMA throughput
+  // epilogue not overlapped with MMAs (only the single-accumulator width)
+  const double epi_blocks[4] = {0.5, 0.5, 0.5, with_c ? 12.0 : 6.0};
   int best = 128;
   double best_cost = 1e300;
   for (int i = 0; i < 4; ++i) {
@@ -235,10 +246,11 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
-  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms);
+  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, c != nullptr);
   Operands o;
   if ((s = encode_a_2d(o, a, sfa, m, k, lda)) != DG_OK) return s;
   if ((s = encode_b_side(o, b, sfb, 1, n, k, ldb, block_n)) != DG_OK) return s;
+  if ((s = encode_d(o, d, m, n, ldd)) != DG_OK) return s;
   args.c = static_cast<const __nv_bfloat16*>(c);
   args.d = static_cast<__nv_bfloat16*>(d);
   args.ldc = c ? ldc : 0;
@@ -256,7 +268,7 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
   print_config("fp8_gemm_nt", m, n, k, 1, block_n, grid, args.band);
-  return from_cuda(gemm_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, args, grid,
+  return from_cuda(gemm_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                static_cast<cudaStream_t>(stream)));
 }
 
@@ -279,10 +291,11 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)(m_sum / kBlockM);
-  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms);
+  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, false);
   Operands o;
   if ((s = encode_a_2d(o, a, sfa, m_sum, k, k)) != DG_OK) return s;
   if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n)) != DG_OK) return s;
+  if ((s = encode_d(o, d, m_sum, n, n)) != DG_OK) return s;
   args.d = static_cast<__nv_bfloat16*>(d);
   args.ldd = n;
   args.m_indices = m_indices;
@@ -299,7 +312,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
   print_config("m_grouped_fp8_gemm_nt_contiguous", m_sum, n, k, num_groups, block_n, grid, args.band);
-  return from_cuda(gemm_launch(kContiguous, block_n, o.a, o.b, o.sfa, o.sfb, args, grid,
+  return from_cuda(gemm_launch(kContiguous, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                static_cast<cudaStream_t>(stream)));
 }
 
@@ -323,10 +336,11 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   GemmArgs args = {};
   args.m_blocks = (int32_t)((max_m + kBlockM - 1) / kBlockM);
   const int64_t m_est = expected_m > 0 ? (expected_m + kBlockM - 1) / kBlockM : args.m_blocks;
-  const int block_n = choose_block_n(m_est * num_groups, n, k / kBlockK, sms);
+  const int block_n = choose_block_n(m_est * num_groups, n, k / kBlockK, sms, false);
   Operands o;
   if ((s = encode_a_3d(o, a, sfa, num_groups, max_m, k)) != DG_OK) return s;
   if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n)) != DG_OK) return s;
+  if ((s = encode_d(o, d, (int64_t)num_groups * max_m, n, n)) != DG_OK) return s;
   args.d = static_cast<__nv_bfloat16*>(d);
   args.ldd = n;
   args.masked_m = masked_m;
@@ -340,7 +354,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   args.timeout_ns = g_timeout_ns.load();
   if ((int64_t)num_groups * args.m_blocks * args.n_blocks >= kMaxCoord) return DG_ERR_TOO_LARGE;
   print_config("m_grouped_fp8_gemm_nt_masked", max_m, n, k, num_groups, block_n, sms, 0);
-  return from_cuda(gemm_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, args, sms,
+  return from_cuda(gemm_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, sms,
                                static_cast<cudaStream_t>(stream)));
 }
 

@@ -73,7 +73,7 @@ def test_grouped_host_checks(L):
     assert cont(P, P, P, P, P, P, 128, 256, 512, 0, None) == DG_OK
     assert cont(P, P, P, P, P, P, 128, 256, 500, 4, None) == ALIGN
     masked = L.dg_m_grouped_fp8_gemm_nt_masked
-    assert masked(P, P, P, P, P, P, 1025, 256, 256, 512, 0, None) == TOO_LARGE
+    assert masked(P, P, P, P, P, P, 513, 256, 256, 512, 0, None) == TOO_LARGE
     assert masked(P, P, P, P, P, None, 4, 256, 256, 512, 0, None) == INVALID
     assert masked(P, P, P, P, P, P, 4, 0, 256, 512, 0, None) == DG_OK
     assert masked(P, P, P, P, P, P, 4, 256, 250, 512, 0, None) == ALIGN
