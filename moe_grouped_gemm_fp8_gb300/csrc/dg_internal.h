@@ -50,9 +50,15 @@ struct GemmArgs {
   unsigned long long* err; // device error word
 };
 
-// gemm.cu: dispatch over the tile widths compiled in gemm_bn*.cu
+// gemm.cu: dispatch over the tile widths compiled in gemm_bn*.cu (single CTA)
+// and gemm2_bn*.cu (CTA pairs, 256-row tiles)
 int gemm_stages(int block_n);
 bool gemm_block_n_supported(int block_n);
+bool gemm2_block_n_supported(int block_n);
+int gemm2_max_clusters(int mode, int block_n);  // per device, cached
+cudaError_t gemm2_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                         const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
+                         GemmArgs args, int clusters, cudaStream_t stream);
 cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                         GemmArgs args, int grid, cudaStream_t stream);
@@ -65,6 +71,16 @@ cudaError_t gemm_fetch_error(unsigned long long* word);  // reads and clears
                                  const CUtensorMap& d, const GemmArgs& args, int grid,          \
                                  cudaStream_t stream);                                          \
   int gemm_stages_bn##BN();
+#define DG_DECLARE_GEMM2_BN(BN)                                                                 \
+  cudaError_t gemm2_launch_bn##BN(int mode, const CUtensorMap& a, const CUtensorMap& b,         \
+                                  const CUtensorMap& sfa, const CUtensorMap& sfb,               \
+                                  const CUtensorMap& d, const GemmArgs& args, int clusters,     \
+                                  cudaStream_t stream);                                         \
+  int gemm2_max_clusters_bn##BN(int mode);
+DG_DECLARE_GEMM2_BN(192)
+DG_DECLARE_GEMM2_BN(224)
+DG_DECLARE_GEMM2_BN(256)
+#undef DG_DECLARE_GEMM2_BN
 DG_DECLARE_GEMM_BN(128)
 DG_DECLARE_GEMM_BN(192)
 DG_DECLARE_GEMM_BN(224)

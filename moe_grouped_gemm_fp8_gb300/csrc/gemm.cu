@@ -37,6 +37,45 @@ cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUten
   return cudaErrorInvalidValue;
 }
 
+bool gemm2_block_n_supported(int block_n) {
+  return block_n == 192 || block_n == 224 || block_n == 256;
+}
+
+int gemm2_max_clusters(int mode, int block_n) {
+  // cached per (device, mode, width); the occupancy query is host-side only
+  static int cache[64][3][3];
+  static bool filled[64][3][3];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int wi = block_n == 192 ? 0 : (block_n == 224 ? 1 : 2);
+  if (!filled[dev][mode][wi]) {
+    int n = 0;
+    switch (block_n) {
+      case 192: n = gemm2_max_clusters_bn192(mode); break;
+      case 224: n = gemm2_max_clusters_bn224(mode); break;
+      case 256: n = gemm2_max_clusters_bn256(mode); break;
+    }
+    cache[dev][mode][wi] = n;
+    filled[dev][mode][wi] = true;
+  }
+  return cache[dev][mode][wi];
+}
+
+cudaError_t gemm2_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                         const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
+                         GemmArgs args, int clusters, cudaStream_t stream) {
+  void* err = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&err, g_gemm_err);
+  if (e != cudaSuccess) return e;
+  args.err = static_cast<unsigned long long*>(err);
+  switch (block_n) {
+    case 192: return gemm2_launch_bn192(mode, a, b, sfa, sfb, d, args, clusters, stream);
+    case 224: return gemm2_launch_bn224(mode, a, b, sfa, sfb, d, args, clusters, stream);
+    case 256: return gemm2_launch_bn256(mode, a, b, sfa, sfb, d, args, clusters, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t gemm_fetch_error(unsigned long long* word) {
   cudaError_t e = cudaMemcpyFromSymbol(word, g_gemm_err, sizeof(*word));
   if (e != cudaSuccess) return e;

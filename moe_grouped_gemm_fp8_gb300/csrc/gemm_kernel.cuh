@@ -149,14 +149,14 @@ struct Scheduler {
 
 // Walks the scale packs (tile, K block / 4) of this CTA in the order the MMA
 // consumes them, skipping the tiles the scheduler skips.
-template <int MODE>
+template <class Sched>
 struct PackCursor {
-  Scheduler<MODE> s;
+  Sched s;
   int t, stride, kb, k_blocks;
   Tile tile;
   bool done;
 
-  __device__ void init(const Scheduler<MODE>& sch, int first, int stride_, int kbs) {
+  __device__ void init(const Sched& sch, int first, int stride_, int kbs) {
     s = sch;
     stride = stride_;
     k_blocks = kbs;
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ scale warp
     // Two cursors walk the same sequence of packs (tile, K block / 4): one
     // loads up to kSfLookahead packs ahead, the other lays them out in order.
-    PackCursor<MODE> ld, lay;
+    PackCursor<Scheduler<MODE>> ld, lay;
     ld.init(sched, blockIdx.x, gridDim.x, args.k_blocks);
     lay.init(sched, blockIdx.x, gridDim.x, args.k_blocks);
     uint32_t n_loaded = 0, n_laid = 0;

@@ -112,14 +112,16 @@ dg_status encode_d(Operands& o, void* d, int64_t rows, int64_t n, int64_t ldd) {
                 CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// B tiles of `b_rows` rows (block_n, or half of it on a CTA pair) and the
+// scale words of `block_n` rows.
 dg_status encode_b_side(Operands& o, const void* b, const int32_t* sfb, int64_t groups,
-                        int64_t n, int64_t k, int64_t ldb, int block_n) {
+                        int64_t n, int64_t k, int64_t ldb, int block_n, int b_rows) {
   const int64_t kp = (k / kBlockK + 3) / 4;
   const int64_t n_pad = align4(n);
   {
     uint64_t dims[3] = {(uint64_t)k, (uint64_t)n, (uint64_t)groups};
     uint64_t strides[2] = {(uint64_t)ldb, (uint64_t)(n * ldb)};
-    uint32_t box[3] = {(uint32_t)kBlockK, (uint32_t)block_n, 1};
+    uint32_t box[3] = {(uint32_t)kBlockK, (uint32_t)b_rows, 1};
     dg_status s = encode(&o.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != DG_OK) return s;
@@ -181,16 +183,20 @@ dg_status encode_a_3d(Operands& o, const void* a, const int32_t* sfa, int64_t gr
 // accumulators in TMEM so the epilogue overlaps the next tile.  The estimate
 // is waves x (K blocks + epilogue cost) x columns / relative throughput;
 // DG_BLOCK_N forces a width.
-int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int sms, bool with_c) {
+// m_blocks counts output-tile rows (128 rows, or 256 on a CTA pair) and
+// `slots` the tiles that run at once (SMs, or co-resident pairs).
+int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, bool with_c,
+                   bool pair) {
   const int forced = env_int("DG_BLOCK_N", 0);
-  if (gemm_block_n_supported(forced)) return forced;
+  if (pair ? gemm2_block_n_supported(forced) : gemm_block_n_supported(forced)) return forced;
   static const int widths[4] = {128, 192, 224, 256};
   static const double rate[4] = {1.0, 1.35, 1.5, 1.6};  // per-column MMA throughput
   // epilogue not overlapped with MMAs (only the single-accumulator width)
   const double epi_blocks[4] = {0.5, 0.5, 0.5, with_c ? 12.0 : 6.0};
-  int best = 128;
+  const int sms = slots > 0 ? slots : 1;
+  int best = pair ? 256 : 128;
   double best_cost = 1e300;
-  for (int i = 0; i < 4; ++i) {
+  for (int i = pair ? 1 : 0; i < 4; ++i) {
     const int64_t tiles = m_blocks * ((n + widths[i] - 1) / widths[i]);
     const int64_t waves = (tiles + sms - 1) / sms;
     const double cost = (double)waves * ((double)k_blocks + epi_blocks[i]) * widths[i] / rate[i];
@@ -246,10 +252,26 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
-  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, c != nullptr);
+  // CTA pairs (256-row tiles) unless the problem has a single 128-row block
+  // or DG_CTA_PAIR=0; DG_CTA_PAIR=1 forces them.
+  const int pair_env = env_int("DG_CTA_PAIR", -1);
+  const bool pair = sms >= 2 && (pair_env == 1 || (pair_env != 0 && args.m_blocks >= 2 &&
+                                                    env_int("DG_BLOCK_N", 0) != 128));
+  const int64_t p_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
+  int block_n, clusters = 0;
+  if (pair) {
+    block_n = choose_block_n(p_blocks, n, k / kBlockK, sms / 2, c != nullptr, true);
+    clusters = gemm2_max_clusters(kDense, block_n);
+    const int limit = sms / 2;
+    if (clusters > limit) clusters = limit;
+    if (clusters <= 0) return DG_ERR_CUDA;
+  } else {
+    block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, c != nullptr, false);
+  }
   Operands o;
   if ((s = encode_a_2d(o, a, sfa, m, k, lda)) != DG_OK) return s;
-  if ((s = encode_b_side(o, b, sfb, 1, n, k, ldb, block_n)) != DG_OK) return s;
+  if ((s = encode_b_side(o, b, sfb, 1, n, k, ldb, block_n, pair ? block_n / 2 : block_n)) != DG_OK)
+    return s;
   if ((s = encode_d(o, d, m, n, ldd)) != DG_OK) return s;
   args.c = static_cast<const __nv_bfloat16*>(c);
   args.d = static_cast<__nv_bfloat16*>(d);
@@ -261,11 +283,17 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   args.num_groups = 1;
   args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
   args.k_blocks = (int32_t)(k / kBlockK);
-  args.band = env_int("DG_RASTER_BAND", 16);
+  args.band = env_int("DG_RASTER_BAND", 16) / (pair ? 2 : 1);
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
-  const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
+  const int64_t tiles = (pair ? p_blocks : (int64_t)args.m_blocks) * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  if (pair) {
+    if (tiles < clusters) clusters = (int)tiles;
+    print_config("fp8_gemm_nt (cta pair)", m, n, k, 1, block_n, 2 * clusters, args.band);
+    return from_cuda(gemm2_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
+                                  static_cast<cudaStream_t>(stream)));
+  }
   const int grid = (int)(tiles < sms ? tiles : sms);
   print_config("fp8_gemm_nt", m, n, k, 1, block_n, grid, args.band);
   return from_cuda(gemm_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
@@ -291,10 +319,10 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)(m_sum / kBlockM);
-  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, false);
+  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, false, false);
   Operands o;
   if ((s = encode_a_2d(o, a, sfa, m_sum, k, k)) != DG_OK) return s;
-  if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n)) != DG_OK) return s;
+  if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n, block_n)) != DG_OK) return s;
   if ((s = encode_d(o, d, m_sum, n, n)) != DG_OK) return s;
   args.d = static_cast<__nv_bfloat16*>(d);
   args.ldd = n;
@@ -335,11 +363,27 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)((max_m + kBlockM - 1) / kBlockM);
-  const int64_t m_est = expected_m > 0 ? (expected_m + kBlockM - 1) / kBlockM : args.m_blocks;
-  const int block_n = choose_block_n(m_est * num_groups, n, k / kBlockK, sms, false);
+  // CTA pairs when a group can span two 128-row blocks (DG_CTA_PAIR as above)
+  const int pair_env = env_int("DG_CTA_PAIR", -1);
+  const bool pair = sms >= 2 && (pair_env == 1 || (pair_env != 0 && max_m > kBlockM &&
+                                                    env_int("DG_BLOCK_N", 0) != 128));
+  const int64_t m_est = expected_m > 0 ? expected_m : max_m;
+  int block_n, grid_units;
+  if (pair) {
+    block_n = choose_block_n(((m_est + 2 * kBlockM - 1) / (2 * kBlockM)) * num_groups, n,
+                             k / kBlockK, sms / 2, false, true);
+    grid_units = gemm2_max_clusters(kMasked, block_n);
+    if (grid_units > sms / 2) grid_units = sms / 2;
+    if (grid_units <= 0) return DG_ERR_CUDA;
+  } else {
+    block_n = choose_block_n(((m_est + kBlockM - 1) / kBlockM) * num_groups, n, k / kBlockK, sms,
+                             false, false);
+    grid_units = sms;
+  }
   Operands o;
   if ((s = encode_a_3d(o, a, sfa, num_groups, max_m, k)) != DG_OK) return s;
-  if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n)) != DG_OK) return s;
+  if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n, pair ? block_n / 2 : block_n)) != DG_OK)
+    return s;
   if ((s = encode_d(o, d, (int64_t)num_groups * max_m, n, n)) != DG_OK) return s;
   args.d = static_cast<__nv_bfloat16*>(d);
   args.ldd = n;
@@ -353,8 +397,14 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
   if ((int64_t)num_groups * args.m_blocks * args.n_blocks >= kMaxCoord) return DG_ERR_TOO_LARGE;
-  print_config("m_grouped_fp8_gemm_nt_masked", max_m, n, k, num_groups, block_n, sms, 0);
-  return from_cuda(gemm_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, sms,
+  if (pair) {
+    print_config("m_grouped_fp8_gemm_nt_masked (cta pair)", max_m, n, k, num_groups, block_n,
+                 2 * grid_units, 0);
+    return from_cuda(gemm2_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid_units,
+                                  static_cast<cudaStream_t>(stream)));
+  }
+  print_config("m_grouped_fp8_gemm_nt_masked", max_m, n, k, num_groups, block_n, grid_units, 0);
+  return from_cuda(gemm_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid_units,
                                static_cast<cudaStream_t>(stream)));
 }
 

@@ -19,20 +19,31 @@ pytestmark = pytest.mark.gpu
 _INT_CODE = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48, -1: 0xB8, -2: 0xC0, -3: 0xC4, -4: 0xC8}
 
 
+# (CTA pair, tile width): single-CTA 128-row tiles at every width, and
+# 256-row tiles on 2-CTA clusters at the widths they support
+CONFIGS = [(0, 128), (0, 192), (0, 224), (0, 256), (1, 192), (1, 224), (1, 256)]
+CONFIG_IDS = ["%s%d" % ("pair" if p else "cta", b) for p, b in CONFIGS]
+
+
 @contextmanager
-def block_n(bn):
-    old = os.environ.get("DG_BLOCK_N")
+def tile_config(cfg):
+    pair, bn = cfg if isinstance(cfg, tuple) else (None, cfg)
+    old = {k: os.environ.get(k) for k in ("DG_BLOCK_N", "DG_CTA_PAIR")}
     if bn:
         os.environ["DG_BLOCK_N"] = str(bn)
-    else:
-        os.environ.pop("DG_BLOCK_N", None)
+    if pair is not None:
+        os.environ["DG_CTA_PAIR"] = str(pair)
     try:
         yield
     finally:
-        if old is None:
-            os.environ.pop("DG_BLOCK_N", None)
-        else:
-            os.environ["DG_BLOCK_N"] = old
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+block_n = tile_config
 
 
 def _int_operand(rng, rows, cols):
@@ -45,7 +56,7 @@ def _no_device_error():
     assert st == 0, "device error word 0x%x" % word
 
 
-@pytest.mark.parametrize("bn", [128, 192, 224, 256])
+@pytest.mark.parametrize("bn", CONFIGS, ids=CONFIG_IDS)
 @pytest.mark.parametrize("M,N,K", [(200, 264, 384), (128, 512, 1024), (5, 8, 128)])
 def test_dense_exact_small_integers(bn, M, N, K):
     """Integer operands with power-of-two scales: every FP32 partial sum is
@@ -88,7 +99,7 @@ def test_small_config_dense_128x256x512():
     _no_device_error()
 
 
-@pytest.mark.parametrize("bn", [128, 192, 224, 256])
+@pytest.mark.parametrize("bn", CONFIGS, ids=CONFIG_IDS)
 @pytest.mark.parametrize("with_c", [False, True])
 @pytest.mark.parametrize("M,N,K", [(1, 8, 128), (100, 136, 640), (300, 392, 384), (129, 264, 1024), (257, 520, 256)])
 def test_dense_ragged(bn, with_c, M, N, K):
@@ -132,7 +143,7 @@ def _contig_setup(G, N, K, counts, seed):
     return w, (qa, sa, qb, sb), dev
 
 
-@pytest.mark.parametrize("bn", [128, 192, 224, 256])
+@pytest.mark.parametrize("bn", CONFIGS, ids=CONFIG_IDS)
 def test_contiguous_routing_and_values(bn):
     G, N, K = 4, 264, 384
     w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [100, 0, 250, 128], seed=77)
@@ -184,7 +195,7 @@ def _masked_setup(G, cap, N, K, mm, seed):
     return w, (qa, sa, qb, sb), dev
 
 
-@pytest.mark.parametrize("bn", [128, 192, 224, 256])
+@pytest.mark.parametrize("bn", CONFIGS, ids=CONFIG_IDS)
 @pytest.mark.parametrize("cap", [200, 256, 64])
 def test_masked_rows_and_values(bn, cap):
     G, N, K = 4, 272, 256
@@ -251,12 +262,12 @@ def test_scale_ring_with_many_short_tiles(K):
     args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
     rows = np.arange(0, M, 37)
     o = oracle.gemm_nt_rows(qa, sa, qb, sb, rows)
-    for bn in (128, 192, 224, 256):
-        dg.set_num_sms(3)
+    for bn in CONFIGS:
+        dg.set_num_sms(6)
         try:
             with block_n(bn):
                 d = dg.fp8_gemm_nt(*args)
         finally:
             dg.set_num_sms(0)
-        P.assert_close(P.bf16_to_f64(d)[rows], o, "K=%d bn=%d" % (K, bn))
+        P.assert_close(P.bf16_to_f64(d)[rows], o, "K=%d cfg=%s" % (K, bn))
     _no_device_error()

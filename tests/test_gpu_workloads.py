@@ -139,17 +139,22 @@ def test_masked_moe_every_tile_width_full_grid(counts):
                            {g * cap + mm[g] - 1 for g in range(G) if mm[g]}), dtype=np.int64)
     o, _ = oracle.gemm_masked(qa, sa, qb, sb, mm, rows=rows)
     dev = (P.dev_codes(qa), P.dev_packed_sf(sa, cap, k, 1), P.dev_codes(qb), P.dev_packed_sf(sb, n, k, 128))
-    old = os.environ.get("DG_BLOCK_N")
+    old = {k: os.environ.get(k) for k in ("DG_BLOCK_N", "DG_CTA_PAIR")}
     try:
-        for bn in ("128", "192", "224", "256"):
-            os.environ["DG_BLOCK_N"] = bn
+        for pair, bn in ((0, 128), (0, 192), (0, 224), (0, 256), (1, 192), (1, 224), (1, 256)):
+            os.environ["DG_BLOCK_N"] = str(bn)
+            os.environ["DG_CTA_PAIR"] = str(pair)
             d = P.sentinel_like((G, cap, n))
             dg.m_grouped_fp8_gemm_nt_masked(*dev, w.masked_m.cuda(), d=d)
             _no_device_error()
+            bits = P.bf16_bits(d)
+            for g in range(G):
+                assert (bits[g, mm[g]:] == P.SENTINEL_BITS).all(), "pair=%d bn=%d g=%d" % (pair, bn, g)
             got = P.bf16_to_f64(d.view(G * cap, n)[torch.from_numpy(rows).cuda()])
-            P.assert_close(got, o, "masked bn=%s" % bn)
+            P.assert_close(got, o, "masked pair=%d bn=%d" % (pair, bn))
     finally:
-        if old is None:
-            os.environ.pop("DG_BLOCK_N", None)
-        else:
-            os.environ["DG_BLOCK_N"] = old
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
