@@ -192,7 +192,7 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
   static const int widths[4] = {128, 192, 224, 256};
   static const double rate[4] = {1.0, 1.35, 1.5, 1.6};  // per-column MMA throughput
   // epilogue not overlapped with MMAs (only the single-accumulator width)
-  const double epi_blocks[4] = {0.5, 0.5, 0.5, with_c ? 12.0 : 6.0};
+  const double epi_blocks[4] = {0.5, 0.5, 0.5, with_c ? 10.0 : 4.0};
   const int sms = slots > 0 ? slots : 1;
   int best = pair ? 256 : 128;
   double best_cost = 1e300;
@@ -209,11 +209,11 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
 }
 
 void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_n,
-                  int grid, int band) {
+                  int grid, int band, bool pair = false) {
   if (!env_flag("DG_PRINT_CONFIGS")) return;
-  fprintf(stderr, "dg: %s m=%lld n=%lld k=%lld groups=%d block_m=128 block_n=%d stages=%d grid=%d band=%d\n",
-          what, (long long)m, (long long)n, (long long)k, groups, block_n,
-          gemm_stages(block_n), grid, band);
+  fprintf(stderr, "dg: %s m=%lld n=%lld k=%lld groups=%d block_m=%d block_n=%d stages=%d grid=%d band=%d\n",
+          what, (long long)m, (long long)n, (long long)k, groups, pair ? 256 : 128, block_n,
+          pair ? 6 : gemm_stages(block_n), grid, band);
 }
 
 dg_status check_common_k_n(int64_t n, int64_t k) {
@@ -252,11 +252,9 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
-  // CTA pairs (256-row tiles) unless the problem has a single 128-row block
-  // or DG_CTA_PAIR=0; DG_CTA_PAIR=1 forces them.
-  const int pair_env = env_int("DG_CTA_PAIR", -1);
-  const bool pair = sms >= 2 && (pair_env == 1 || (pair_env != 0 && args.m_blocks >= 2 &&
-                                                    env_int("DG_BLOCK_N", 0) != 128));
+  // CTA pairs (256-row tiles) only on request (DG_CTA_PAIR=1): on the
+  // measured shapes they match, not beat, single-CTA tiles.
+  const bool pair = sms >= 2 && args.m_blocks >= 2 && env_int("DG_CTA_PAIR", 0) == 1;
   const int64_t p_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
   int block_n, clusters = 0;
   if (pair) {
@@ -290,7 +288,7 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   if (pair) {
     if (tiles < clusters) clusters = (int)tiles;
-    print_config("fp8_gemm_nt (cta pair)", m, n, k, 1, block_n, 2 * clusters, args.band);
+    print_config("fp8_gemm_nt (cta pair)", m, n, k, 1, block_n, 2 * clusters, args.band, true);
     return from_cuda(gemm2_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
                                   static_cast<cudaStream_t>(stream)));
   }
@@ -363,10 +361,9 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)((max_m + kBlockM - 1) / kBlockM);
-  // CTA pairs when a group can span two 128-row blocks (DG_CTA_PAIR as above)
-  const int pair_env = env_int("DG_CTA_PAIR", -1);
-  const bool pair = sms >= 2 && (pair_env == 1 || (pair_env != 0 && max_m > kBlockM &&
-                                                    env_int("DG_BLOCK_N", 0) != 128));
+  // CTA pairs only on request (DG_CTA_PAIR=1); with few valid rows per group
+  // the peer's half of the tile is mostly empty.
+  const bool pair = sms >= 2 && max_m > kBlockM && env_int("DG_CTA_PAIR", 0) == 1;
   const int64_t m_est = expected_m > 0 ? expected_m : max_m;
   int block_n, grid_units;
   if (pair) {
@@ -399,7 +396,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   if ((int64_t)num_groups * args.m_blocks * args.n_blocks >= kMaxCoord) return DG_ERR_TOO_LARGE;
   if (pair) {
     print_config("m_grouped_fp8_gemm_nt_masked (cta pair)", max_m, n, k, num_groups, block_n,
-                 2 * grid_units, 0);
+                 2 * grid_units, 0, true);
     return from_cuda(gemm2_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid_units,
                                   static_cast<cudaStream_t>(stream)));
   }
