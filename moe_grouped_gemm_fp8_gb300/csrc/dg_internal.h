@@ -28,6 +28,8 @@ enum ErrorSite : uint32_t {
   kSiteScaleFull = 7,
   kSiteMmaScaleReady = 8,
   kSiteScaleEmpty = 9,
+  kSiteSplitFree = 10,
+  kSiteSplitFull = 11,
   kSiteContiguousIndex = 16,
   kSiteMaskedCount = 17,
   kSiteTransformScale = 32,
@@ -81,6 +83,12 @@ DG_DECLARE_GEMM2_BN(192)
 DG_DECLARE_GEMM2_BN(224)
 DG_DECLARE_GEMM2_BN(256)
 #undef DG_DECLARE_GEMM2_BN
+// gemm_splitk.cu: dense split-K over 2 or 4 CTAs, 128-column tiles
+cudaError_t gemm_splitk_launch(int ksplit, const CUtensorMap& a, const CUtensorMap& b,
+                               const CUtensorMap& sfa, const CUtensorMap& sfb,
+                               const CUtensorMap& d, GemmArgs args, int clusters,
+                               cudaStream_t stream);
+int gemm_splitk_max_clusters(int ksplit);
 DG_DECLARE_GEMM_BN(128)
 DG_DECLARE_GEMM_BN(192)
 DG_DECLARE_GEMM_BN(224)

@@ -7,6 +7,25 @@ namespace dg {
 
 __device__ unsigned long long g_gemm_err = 0ull;
 
+// Device address of the error word on the current device.  Host code must
+// pass this address, not the host-side shadow the symbol name denotes here;
+// looked up once per device.
+static cudaError_t error_word_address(unsigned long long** out) {
+  static unsigned long long* addr[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_gemm_err);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<unsigned long long*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
 int gemm_stages(int block_n) {
   switch (block_n) {
     case 128: return gemm_stages_bn128();
@@ -22,12 +41,10 @@ bool gemm_block_n_supported(int block_n) { return gemm_stages(block_n) > 0; }
 cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                         GemmArgs args, int grid, cudaStream_t stream) {
-  // Host code must pass the device address of the error word, not the
-  // host-side shadow the symbol name denotes here.
-  void* err = nullptr;
-  cudaError_t e = cudaGetSymbolAddress(&err, g_gemm_err);
+  unsigned long long* err = nullptr;
+  cudaError_t e = error_word_address(&err);
   if (e != cudaSuccess) return e;
-  args.err = static_cast<unsigned long long*>(err);
+  args.err = err;
   switch (block_n) {
     case 128: return gemm_launch_bn128(mode, a, b, sfa, sfb, d, args, grid, stream);
     case 192: return gemm_launch_bn192(mode, a, b, sfa, sfb, d, args, grid, stream);
@@ -64,10 +81,10 @@ int gemm2_max_clusters(int mode, int block_n) {
 cudaError_t gemm2_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                          const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                          GemmArgs args, int clusters, cudaStream_t stream) {
-  void* err = nullptr;
-  cudaError_t e = cudaGetSymbolAddress(&err, g_gemm_err);
+  unsigned long long* err = nullptr;
+  cudaError_t e = error_word_address(&err);
   if (e != cudaSuccess) return e;
-  args.err = static_cast<unsigned long long*>(err);
+  args.err = err;
   switch (block_n) {
     case 192: return gemm2_launch_bn192(mode, a, b, sfa, sfb, d, args, clusters, stream);
     case 224: return gemm2_launch_bn224(mode, a, b, sfa, sfb, d, args, clusters, stream);

@@ -311,8 +311,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale warp (both CTAs)
     PackCursor<PairScheduler<MODE>> ld, lay;
-    ld.init(sched, cluster_id, num_clusters, args.k_blocks);
-    lay.init(sched, cluster_id, num_clusters, args.k_blocks);
+    ld.init(sched, cluster_id, num_clusters, 0, args.k_blocks);
+    lay.init(sched, cluster_id, num_clusters, 0, args.k_blocks);
     uint32_t n_loaded = 0, n_laid = 0;
     bool ok = true;
     while (!lay.done && ok) {
@@ -502,7 +502,7 @@ static cudaError_t gemm2_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
                 "shared memory over the per-CTA limit");
   auto kern = fp8_gemm_pair_kernel<BN, STAGES, MODE>;
   const size_t smem = Gemm2Plan<BN, STAGES>::smem_bytes(MODE);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_once<KernelTag<BN, STAGES, MODE, 1, 2>>(kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -525,9 +525,7 @@ template <int BN, int STAGES, int MODE>
 static int gemm2_max_clusters() {
   auto kern = fp8_gemm_pair_kernel<BN, STAGES, MODE>;
   const size_t smem = Gemm2Plan<BN, STAGES>::smem_bytes(MODE);
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return 0;
+  if (set_smem_once<KernelTag<BN, STAGES, MODE, 1, 2>>(kern, smem) != cudaSuccess) return 0;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;

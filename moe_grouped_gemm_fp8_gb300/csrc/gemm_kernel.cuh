@@ -38,6 +38,15 @@
 //               as soon as the last chunk is in registers.
 // The accumulator is double-buffered in TMEM when 2 x BN columns leave room
 // for the scales, so the epilogue of one tile overlaps the next tile's MMAs.
+//
+// Split-K (KSPLIT = 2 or 4, dense only, for problems with fewer output tiles
+// than SMs): a cluster of KSPLIT CTAs shares each output tile, CTA r taking a
+// slice of the K blocks aligned to scale packs.  Quarter q (32 rows) of the
+// tile belongs to CTA q % KSPLIT: every other CTA writes its FP32 partial of
+// that quarter into the owner's shared memory (distributed shared memory)
+// and arrives on the owner's barrier; the owner adds the partials in rank
+// order - the same order whatever the timing, so results are deterministic -
+// adds C, rounds to BF16 and stores.  No global scratch memory is used.
 // Every mbarrier wait is bounded; on expiry the kernel records an error,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #pragma once
@@ -79,7 +88,7 @@ constexpr int kEpiBytes = 4 * 2 * kEpiBuf;  // 4 epilogue warps x 2 buffers
 constexpr int kSfLookahead = 3;  // packs loaded ahead of the one being laid out
 
 static constexpr size_t gemm_ctrl_bytes(int stages, int mode) {
-  return (size_t)8 * (2 * stages + 3 * kSfSlots + 5) + 16 +
+  return (size_t)8 * (2 * stages + 3 * kSfSlots + 5 + 8) + 16 +
          (mode == kMasked ? (size_t)4 * (2 * kMaxMaskedGroups + 1) : 0);
 }
 
@@ -88,15 +97,21 @@ static constexpr size_t gemm_ctrl_bytes(int stages, int mode) {
 // once per pack - words landed (TMA), words laid out (scale warp), slot free
 // (tcgen05.commit after the pack's last MMA) - and every waiter visits every
 // pack in order, so no wait ever skips a phase.
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KSPLIT = 1>
 struct GemmPlan {
   using L = GemmLayout<BN>;
   static constexpr int kNumAcc = (2 * BN + kSfSlots * L::kSfCols <= 512) ? 2 : 1;
   static constexpr int kSfBase = kNumAcc * BN;
   static_assert(kSfBase + kSfSlots * L::kSfCols <= 512, "TMEM over-subscribed");
+  static_assert(KSPLIT == 1 || KSPLIT == 2 || KSPLIT == 4, "split-K over 1, 2 or 4 CTAs");
+  // split-K receive buffers: per owned quarter and per other CTA, 32 rows of
+  // BN FP32 partial sums, rows padded by 16 bytes (conflict-free row access)
+  static constexpr int kRecvRow = BN * 4 + 16;
+  static constexpr int kRecvSlot = 32 * kRecvRow;
+  static constexpr int kRecvBytes = KSPLIT > 1 ? (4 / KSPLIT) * (KSPLIT - 1) * kRecvSlot : 0;
   static constexpr size_t smem_bytes(int mode) {
     return (size_t)STAGES * L::kStageBytes + (size_t)kSfSlots * L::kSfBufBytes + kEpiBytes +
-           1024 + gemm_ctrl_bytes(STAGES, mode);
+           (size_t)kRecvBytes + 1024 + gemm_ctrl_bytes(STAGES, mode);
   }
 };
 
@@ -156,10 +171,14 @@ struct PackCursor {
   Tile tile;
   bool done;
 
-  __device__ void init(const Sched& sch, int first, int stride_, int kbs) {
+  int kb_begin;
+
+  // Packs of K blocks [kb0, kb1) of every tile (kb0 a multiple of 4).
+  __device__ void init(const Sched& sch, int first, int stride_, int kb0, int kb1) {
     s = sch;
     stride = stride_;
-    k_blocks = kbs;
+    kb_begin = kb0;
+    k_blocks = kb1;
     t = first - stride_;
     next_tile();
   }
@@ -168,7 +187,7 @@ struct PackCursor {
     for (t += stride; t < s.total; t += stride)
       if (s.get(t, tile)) {
         done = false;
-        kb = 0;
+        kb = kb_begin;
         return;
       }
   }
@@ -215,6 +234,20 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok != 0;
 }
 
+// Whole-warp wait with cluster-scope acquire (barriers other CTAs arrive on).
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, uint64_t timeout_ns,
+                                                  unsigned long long* err, uint32_t site) {
+  const int lane = threadIdx.x & 31;
+  int ok = 0;
+  if (lane == 0)
+    ok = (mbar_try_wait_cluster(bar, parity) ||
+          wait_bounded_cluster(bar, parity, abort_flag, timeout_ns, err, site)) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -249,7 +282,57 @@ __device__ __forceinline__ void store_row_chunk(const uint32_t (&r)[32], __nv_bf
   }
 }
 
-template <int BN, int STAGES, int MODE>
+// One 32 x 32 output chunk of a warp's quarter: + C (coalesced loads staged
+// through `buf`), round to BF16, write into `buf` with the 64-byte swizzle and
+// TMA-store it at (col0, out_row0).  `buf` must be free (its previous store
+// has finished reading it).  Rows past m are skipped for C when dense_rows.
+__device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
+                                               const CUtensorMap* tm_d, const GemmArgs& args,
+                                               int col0, int64_t out_row0, int row0,
+                                               bool dense_rows, int lane) {
+  const uint32_t my_row_off = (uint32_t)lane * 64u;
+  const uint32_t my_swz = ((uint32_t)lane >> 1) & 3u;
+  if (args.c) {
+    // coalesced: lane l fetches 16 bytes of rows l/4 + 8i, piece l % 4
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (lane >> 2) + 8 * i, pc = lane & 3;
+      const int gcol = col0 + pc * 8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (gcol < args.n && (!dense_rows || row0 + r < args.m))
+        v = __ldg(reinterpret_cast<const uint4*>(args.c + (out_row0 + r) * args.ldc + gcol));
+      *reinterpret_cast<uint4*>(buf + r * 64 + 16 * (pc ^ ((r >> 1) & 3))) = v;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 cv = *reinterpret_cast<const uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz));
+      const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[8 * j + 2 * i] += __uint_as_float(cw[i] << 16);
+        f[8 * j + 2 * i + 1] += __uint_as_float(cw[i] & 0xFFFF0000u);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 o;
+    o.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
+    o.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
+    o.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
+    o.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
+    *reinterpret_cast<uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz)) = o;
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm_d, smem_u32(buf), col0, (int32_t)out_row0);
+    bulk_commit_group();
+  }
+}
+
+template <int BN, int STAGES, int MODE, int KSPLIT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
@@ -257,8 +340,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
   using L = GemmLayout<BN>;
-  using P = GemmPlan<BN, STAGES>;
+  using P = GemmPlan<BN, STAGES, KSPLIT>;
   constexpr int NUM_ACC = P::kNumAcc;
+  static_assert(KSPLIT == 1 || MODE == kDense, "split-K is for the dense form");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -269,7 +353,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int lane = threadIdx.x & 31;
 
   uint8_t* epi_smem = sfbuf + kSfSlots * L::kSfBufBytes;  // 1024-aligned
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + kEpiBytes);
+  uint8_t* recv = epi_smem + kEpiBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(recv + P::kRecvBytes);
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
   auto sffull = [&](int p) { return smem_u32(bars + 2 * STAGES + p); };
@@ -279,7 +364,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto tfull = [&](int a) { return smem_u32(bars + kB0 + a); };
   auto tempty = [&](int a) { return smem_u32(bars + kB0 + 2 + a); };
   const uint32_t drain = smem_u32(bars + kB0 + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kB0 + 5);
+  auto recv_full = [&](int q) { return smem_u32(bars + kB0 + 5 + q); };  // owner side
+  auto recv_free = [&](int q) { return smem_u32(bars + kB0 + 9 + q); };  // sender side
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kB0 + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
   int* group_valid = tile_start + (kMaxMaskedGroups + 1);
@@ -300,6 +387,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(tempty(a), 4);
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(recv_full(q), KSPLIT > 1 ? KSPLIT - 1 : 1);
+      mbar_init(recv_free(q), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_a);
@@ -331,8 +422,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_before();
   }
   __syncthreads();
+  if (KSPLIT > 1) cluster_sync_all();  // every CTA's barriers exist before remote arrivals
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
+  // tile loop of this CTA (of this cluster, with split-K) and its K slice
+  const uint32_t krank = KSPLIT > 1 ? cluster_ctarank() : 0u;
+  const int first_tile = (int)blockIdx.x / KSPLIT;
+  const int tile_stride = (int)gridDim.x / KSPLIT;
+  const int kb_per = ((args.k_blocks + KSPLIT - 1) / KSPLIT + 3) / 4 * 4;
+  const int kb_begin = KSPLIT > 1 ? min(args.k_blocks, (int)krank * kb_per) : 0;
+  const int kb_end = KSPLIT > 1 ? min(args.k_blocks, kb_begin + kb_per) : args.k_blocks;
 
   Scheduler<MODE> sched;
   sched.args = &args;
@@ -349,10 +449,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // stages: last fill's phase parity
       bool ok = true;
-      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+      for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
         Tile tile;
         if (!sched.get(t, tile)) continue;
-        for (int kb = 0; kb < args.k_blocks; ++kb) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_one(empty(stage), phase ^ 1u, abort_flag, tmo, err, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -389,7 +489,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < sched.total && ok; t += gridDim.x) {
+      for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
         Tile tile;
         if (!sched.get(t, tile)) continue;
         if (!wait_one(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, err, kSiteMmaTmemEmpty)) {
@@ -398,7 +498,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < args.k_blocks; ++kb) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_one(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull)) {
             ok = false;
             break;
@@ -427,9 +527,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             tc_mma_mxf8(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
-                        (kb | j) != 0 ? 1u : 0u);
+                        (kb != kb_begin || j != 0) ? 1u : 0u);
           tc_commit(empty(stage));
-          if ((kb & 3) == 3 || kb == args.k_blocks - 1) {
+          if ((kb & 3) == 3 || kb == kb_end - 1) {
             tc_commit(sfempty(slot));  // the pack's buffer and TMEM slot are free
             ++pack;
           }
@@ -455,8 +555,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Two cursors walk the same sequence of packs (tile, K block / 4): one
     // loads up to kSfLookahead packs ahead, the other lays them out in order.
     PackCursor<Scheduler<MODE>> ld, lay;
-    ld.init(sched, blockIdx.x, gridDim.x, args.k_blocks);
-    lay.init(sched, blockIdx.x, gridDim.x, args.k_blocks);
+    ld.init(sched, first_tile, tile_stride, kb_begin, kb_end);
+    lay.init(sched, first_tile, tile_stride, kb_begin, kb_end);
     uint32_t n_loaded = 0, n_laid = 0;
     bool ok = true;
     while (!lay.done && ok) {
@@ -516,15 +616,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
+    // staging: 16-byte piece j of chunk row r at r * 64 + 16 * (j ^ ((r >> 1) & 3)),
+    // the layout of CU_TENSOR_MAP_SWIZZLE_64B
     uint8_t* ebuf = epi_smem + (warp - 3) * 2 * kEpiBuf;
-    // 64-byte swizzle of a 32 x 32 BF16 chunk: 16-byte piece j of row r sits at
-    // r * 64 + 16 * (j ^ ((r >> 1) & 3)) (the layout of CU_TENSOR_MAP_SWIZZLE_64B)
-    const uint32_t my_row_off = (uint32_t)lane * 64u;
-    const uint32_t my_swz = ((uint32_t)lane >> 1) & 3u;
     uint32_t nchunk = 0;  // chunks staged so far (buffer = nchunk & 1)
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < sched.total; t += gridDim.x) {
+    uint32_t tile_iter = 0;  // split-K barrier phases
+    for (int t = first_tile; t < sched.total; t += tile_stride, ++tile_iter) {
       Tile tile;
       if (!sched.get(t, tile)) continue;
       if (!warp_wait(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
@@ -552,6 +651,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const __nv_bfloat16* crow = args.c ? args.c + (out_row0 + lane) * args.ldc : nullptr;
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
       constexpr int NCH = BN / 32;
+      // split-K roles for this quarter
+      const int owner = KSPLIT > 1 ? quarter % KSPLIT : 0;
+      const bool sender = KSPLIT > 1 && (int)krank != owner;
+      const uint32_t kpar = tile_iter & 1u;
+      uint32_t send_base = 0;
+      if (KSPLIT > 1) {
+        bool ok2;
+        if (sender) {
+          ok2 = warp_wait_cluster(recv_free(quarter), kpar ^ 1u, abort_flag, tmo, err,
+                                  kSiteSplitFree);
+          const int sslot = (int)krank < owner ? (int)krank : (int)krank - 1;
+          send_base = mapa_shared(smem_u32(recv + ((quarter / KSPLIT) * (KSPLIT - 1) + sslot) *
+                                                      P::kRecvSlot + lane * P::kRecvRow),
+                                  (uint32_t)owner);
+        } else {
+          ok2 = warp_wait_cluster(recv_full(quarter), kpar, abort_flag, tmo, err, kSiteSplitFull);
+        }
+        if (!ok2) break;
+      }
       uint32_t ra[32], rb[32];
       tc_ld_32x32b_x32(taddr, ra);
 #pragma unroll
@@ -567,57 +685,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty(acc));
         }
+        if (sender) {
+          // this CTA's FP32 partial of the chunk into the owner's shared memory
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_cluster_v4(send_base + ch * 128 + j * 16, cur[4 * j], cur[4 * j + 1],
+                                 cur[4 * j + 2], cur[4 * j + 3]);
+          continue;
+        }
         const int col0 = tile.nb * BN + ch * 32;
         if (col0 >= args.n) continue;
         if (use_tma) {
           uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
-          const uint32_t sbuf = smem_u32(buf);
           if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
           __syncwarp();
           float f[32];
+          if (KSPLIT > 1) {
+            // partials added in CTA-rank order: the same result whatever the timing
 #pragma unroll
-          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
-          if (args.c) {
-            // coalesced: lane l fetches 16 bytes of rows l/4 + 8i, piece l % 4
+            for (int i = 0; i < 32; ++i) f[i] = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = (lane >> 2) + 8 * i, pc = lane & 3;
-              const int gcol = col0 + pc * 8;
-              uint4 v = make_uint4(0u, 0u, 0u, 0u);
-              if (gcol < args.n && (MODE != kDense || row0 + r < args.m))
-                v = __ldg(reinterpret_cast<const uint4*>(args.c + (out_row0 + r) * args.ldc + gcol));
-              *reinterpret_cast<uint4*>(buf + r * 64 + 16 * (pc ^ ((r >> 1) & 3))) = v;
-            }
-            __syncwarp();
+            for (int rr = 0; rr < KSPLIT; ++rr) {
+              if (rr == (int)krank) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 cv = *reinterpret_cast<const uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz));
-              const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+                for (int i = 0; i < 32; ++i) f[i] += __uint_as_float(cur[i]);
+              } else {
+                const int sslot = rr < (int)krank ? rr : rr - 1;
+                const uint8_t* src = recv + ((quarter / KSPLIT) * (KSPLIT - 1) + sslot) * P::kRecvSlot +
+                                     lane * P::kRecvRow + ch * 128;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                f[8 * j + 2 * i] += __uint_as_float(cw[i] << 16);
-                f[8 * j + 2 * i + 1] += __uint_as_float(cw[i] & 0xFFFF0000u);
+                for (int j = 0; j < 8; ++j) {
+                  const float4 v = *reinterpret_cast<const float4*>(src + j * 16);
+                  f[4 * j] += v.x;
+                  f[4 * j + 1] += v.y;
+                  f[4 * j + 2] += v.z;
+                  f[4 * j + 3] += v.w;
+                }
               }
             }
-          }
+          } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4 o;
-            o.x = pack_bf16x2(f[8 * j + 0], f[8 * j + 1]);
-            o.y = pack_bf16x2(f[8 * j + 2], f[8 * j + 3]);
-            o.z = pack_bf16x2(f[8 * j + 4], f[8 * j + 5]);
-            o.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
-            *reinterpret_cast<uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz)) = o;
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tm_d, sbuf, col0, (int32_t)out_row0);
-            bulk_commit_group();
-          }
+          emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, MODE == kDense, lane);
           ++nchunk;
         } else if (row_ok) {
           store_row_chunk(cur, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
+        }
+      }
+      if (KSPLIT > 1) {
+        __syncwarp();
+        if (lane == 0) {
+          if (sender) {
+            mbar_arrive_cluster(mapa_shared(recv_full(quarter), (uint32_t)owner));
+          } else {
+            for (int rr = 0; rr < KSPLIT; ++rr)
+              if (rr != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)rr));
+          }
         }
       }
       if (++acc == NUM_ACC) {
@@ -631,29 +755,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncthreads();
+  if (KSPLIT > 1) cluster_sync_all();  // no CTA leaves while others may still reach its memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
 }
 
-template <int BN, int STAGES, int MODE>
+// Raises the kernel's dynamic shared-memory limit once per device (host-side
+// setup kept out of the launch path, e.g. of a CUDA-graph capture).  `Tag`
+// makes one set of flags per kernel instantiation (kernels share a signature).
+template <int BN, int STAGES, int MODE, int KSPLIT, int CTAS>
+struct KernelTag {};
+
+template <class Tag, class Kern>
+static cudaError_t set_smem_once(Kern kern, size_t smem) {
+  static bool done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
+template <int BN, int STAGES, int MODE, int KSPLIT = 1>
 static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
                                     const CUtensorMap& sfa, const CUtensorMap& sfb,
                                     const CUtensorMap& d, const GemmArgs& args, int grid,
                                     cudaStream_t stream) {
-  static_assert(GemmPlan<BN, STAGES>::smem_bytes(kMasked) <= (size_t)kSmemLimit,
+  static_assert(GemmPlan<BN, STAGES, KSPLIT>::smem_bytes(MODE) <= (size_t)kSmemLimit,
                 "shared memory over the per-CTA limit");
-  auto kern = fp8_gemm_kernel<BN, STAGES, MODE>;
-  const size_t smem = GemmPlan<BN, STAGES>::smem_bytes(MODE);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT>;
+  const size_t smem = GemmPlan<BN, STAGES, KSPLIT>::smem_bytes(MODE);
+  cudaError_t e = set_smem_once<KernelTag<BN, STAGES, MODE, KSPLIT, 1>>(kern, smem);
   if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = KSPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = KSPLIT > 1 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, a, b, sfa, sfb, d, args);
+}
+
+// Largest number of co-resident KSPLIT-CTA clusters of a split-K configuration.
+template <int BN, int STAGES, int KSPLIT>
+static int gemm_splitk_max_clusters_impl() {
+  auto kern = fp8_gemm_kernel<BN, STAGES, kDense, KSPLIT>;
+  const size_t smem = GemmPlan<BN, STAGES, KSPLIT>::smem_bytes(kDense);
+  if (set_smem_once<KernelTag<BN, STAGES, kDense, KSPLIT, 1>>(kern, smem) != cudaSuccess) return 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = KSPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(KSPLIT, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  return n;
 }
 
 template <int BN, int STAGES>

@@ -252,6 +252,52 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
+  // Split-K over a cluster of 2 or 4 CTAs when 128-column tiles would leave
+  // most SMs idle (decode-sized M); DG_SPLIT_K = 1, 2 or 4 forces a factor.
+  // Every CTA's K slice (a multiple of 4 K blocks) must be non-empty.
+  int ksplit = 1;
+  {
+    const int64_t kb = k / kBlockK;
+    const int64_t tiles128 = (int64_t)args.m_blocks * ((n + 127) / 128);
+    const int forced = env_int("DG_SPLIT_K", 0);
+    if (forced == 1 || forced == 2 || forced == 4) ksplit = forced;
+    else if (tiles128 * 4 <= sms && kb >= 16) ksplit = 4;
+    else if (tiles128 * 2 <= sms && kb >= 8) ksplit = 2;
+    while (ksplit > 1) {
+      const int64_t per = ((kb + ksplit - 1) / ksplit + 3) / 4 * 4;
+      if ((ksplit - 1) * per < kb) break;
+      ksplit /= 2;
+    }
+  }
+  if (ksplit > 1) {
+    const int block_n = 128;
+    Operands o;
+    if ((s = encode_a_2d(o, a, sfa, m, k, lda)) != DG_OK) return s;
+    if ((s = encode_b_side(o, b, sfb, 1, n, k, ldb, block_n, block_n)) != DG_OK) return s;
+    if ((s = encode_d(o, d, m, n, ldd)) != DG_OK) return s;
+    args.c = static_cast<const __nv_bfloat16*>(c);
+    args.d = static_cast<__nv_bfloat16*>(d);
+    args.ldc = c ? ldc : 0;
+    args.ldd = ldd;
+    args.m = (int32_t)m;
+    args.n = (int32_t)n;
+    args.k = (int32_t)k;
+    args.num_groups = 1;
+    args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
+    args.k_blocks = (int32_t)(k / kBlockK);
+    args.band = env_int("DG_RASTER_BAND", 16);
+    if (args.band < 1) args.band = 1;
+    args.timeout_ns = g_timeout_ns.load();
+    const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
+    int clusters = gemm_splitk_max_clusters(ksplit);
+    if (clusters > sms / ksplit) clusters = sms / ksplit;
+    if (tiles < clusters) clusters = (int)tiles;
+    if (clusters <= 0) return DG_ERR_CUDA;
+    print_config(ksplit == 2 ? "fp8_gemm_nt (split-K 2)" : "fp8_gemm_nt (split-K 4)", m, n, k, 1,
+                 block_n, ksplit * clusters, args.band);
+    return from_cuda(gemm_splitk_launch(ksplit, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
+                                        static_cast<cudaStream_t>(stream)));
+  }
   // CTA pairs (256-row tiles) only on request (DG_CTA_PAIR=1): on the
   // measured shapes they match, not beat, single-CTA tiles.
   const bool pair = sms >= 2 && args.m_blocks >= 2 && env_int("DG_CTA_PAIR", 0) == 1;

@@ -271,3 +271,57 @@ def test_scale_ring_with_many_short_tiles(K):
             dg.set_num_sms(0)
         P.assert_close(P.bf16_to_f64(d)[rows], o, "K=%d cfg=%s" % (K, bn))
     _no_device_error()
+
+
+@contextmanager
+def split_k(ks):
+    old = os.environ.get("DG_SPLIT_K")
+    os.environ["DG_SPLIT_K"] = str(ks)
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("DG_SPLIT_K", None)
+        else:
+            os.environ["DG_SPLIT_K"] = old
+
+
+@pytest.mark.parametrize("ks", [2, 4])
+@pytest.mark.parametrize("with_c", [False, True])
+@pytest.mark.parametrize("M,N,K", [(64, 264, 2048), (128, 136, 4096), (200, 512, 2560), (1, 8, 1024), (300, 392, 1536)])
+def test_dense_split_k(ks, with_c, M, N, K):
+    """K split over a cluster of CTAs, partial sums reduced through
+    distributed shared memory; rows/columns past the problem stay untouched."""
+    w = workloads.dense(M, N, K, seed=M + N + K + ks, with_c=with_c)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    cb = P.bf16_bits(w.c) if with_c else None
+    o = oracle.gemm_nt(qa, sa, qb, sb, cb)
+    buf = P.sentinel_like((M, N + 24))
+    d = buf[:, :N]
+    with split_k(ks):
+        dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb),
+                       P.dev_packed_sf(sb, N, K, 128), d=d, c=w.c.cuda() if with_c else None)
+    P.assert_close(P.bf16_to_f64(d), o, "split-K %d %dx%dx%d" % (ks, M, N, K))
+    assert (P.bf16_bits(buf[:, N:]) == P.SENTINEL_BITS).all()
+    _no_device_error()
+
+
+@pytest.mark.parametrize("ks", [2, 4])
+def test_dense_split_k_exact_and_deterministic(ks):
+    """Exact integer products: the rank-ordered reduction must give the BF16
+    rounding of the oracle bit for bit, and the same bits on every run."""
+    rng = np.random.default_rng(17 + ks)
+    M, N, K = 96, 392, 4096
+    qa, qb = _int_operand(rng, M, K), _int_operand(rng, N, K)
+    ea = rng.integers(-2, 3, size=(M, K // 128))
+    eb = rng.integers(-2, 3, size=((N + 127) // 128, K // 128))
+    sa, sb = np.ldexp(1.0, ea), np.ldexp(1.0, eb)
+    want = oracle.bf16_rne(oracle.gemm_nt(qa, sa, qb, sb))
+    args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    with split_k(ks):
+        first = P.bf16_bits(dg.fp8_gemm_nt(*args))
+        again = P.bf16_bits(dg.fp8_gemm_nt(*args))
+    assert np.array_equal(first, want)
+    assert np.array_equal(first, again)
+    _no_device_error()
