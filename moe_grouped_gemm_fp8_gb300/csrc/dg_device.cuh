@@ -62,17 +62,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete yet
+// is suspended for at most HINT_NS nanoseconds before the test is repeated
+// (HINT_NS = 0: the form without a hint, whose suspend limit is left to the
+// hardware).  Measured on the single-CTA pipeline, a 32 ns limit shortens the
+// producer / MMA hand-offs.
+template <uint32_t HINT_NS>
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity) {
+  if (HINT_NS == 0) return mbar_try_wait(bar, parity);
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(HINT_NS)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // (returns false) when the shared abort flag is raised by another role, or
 // after `timeout_ns`, or after a fixed iteration cap; in the two last cases
 // it records DG_ERR_DEVICE_TIMEOUT with `site` and raises the abort flag.
+template <uint32_t HINT_NS = 0>
 static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t timeout_ns, unsigned long long* err,
                                           uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_hint<HINT_NS>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint<HINT_NS>(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > timeout_ns || it >= (1u << 30)) {

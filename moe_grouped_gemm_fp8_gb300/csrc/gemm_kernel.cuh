@@ -212,23 +212,28 @@ static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, ui
   }
 }
 
+// Suspend-time hint of the single-CTA kernel's waits (see mbar_try_wait_hint).
+constexpr uint32_t kSuspendHintNs = 32;
+
 // Single-thread wait: one try first (the usual case), the bounded loop only
 // when the phase is not complete yet.
+template <uint32_t HINT_NS = 0>
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          uint64_t timeout_ns, unsigned long long* err,
                                          uint32_t site) {
-  return mbar_try_wait(bar, parity) ||
-         wait_bounded(bar, parity, abort_flag, timeout_ns, err, site);
+  return mbar_try_wait_hint<HINT_NS>(bar, parity) ||
+         wait_bounded<HINT_NS>(bar, parity, abort_flag, timeout_ns, err, site);
 }
 
 // Whole-warp wait: lane 0 waits, the result is broadcast, and the warp
 // reconverges (so the other lanes observe what lane 0 acquired).
+template <uint32_t HINT_NS = 0>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t timeout_ns, unsigned long long* err,
                                           uint32_t site) {
   const int lane = threadIdx.x & 31;
   int ok = 0;
-  if (lane == 0) ok = wait_one(bar, parity, abort_flag, timeout_ns, err, site) ? 1 : 0;
+  if (lane == 0) ok = wait_one<HINT_NS>(bar, parity, abort_flag, timeout_ns, err, site) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
@@ -453,7 +458,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         Tile tile;
         if (!sched.get(t, tile)) continue;
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!wait_one(empty(stage), phase ^ 1u, abort_flag, tmo, err, kSiteProducerEmpty)) {
+          if (!wait_one<kSuspendHintNs>(empty(stage), phase ^ 1u, abort_flag, tmo, err, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
@@ -492,21 +497,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
         Tile tile;
         if (!sched.get(t, tile)) continue;
-        if (!wait_one(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, err, kSiteMmaTmemEmpty)) {
+        if (!wait_one<kSuspendHintNs>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, err, kSiteMmaTmemEmpty)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!wait_one(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull)) {
+          if (!wait_one<kSuspendHintNs>(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + stage * L::kStageBytes;
           const int slot = (int)(pack % kSfSlots);
           if ((kb & 3) == 0) {
-            if (!wait_one(sfready(slot), (pack / kSfSlots) & 1u, abort_flag, tmo, err,
+            if (!wait_one<kSuspendHintNs>(sfready(slot), (pack / kSfSlots) & 1u, abort_flag, tmo, err,
                           kSiteMmaScaleReady)) {
               ok = false;
               break;
@@ -564,7 +569,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int slot = (int)(n_loaded % kSfSlots);
         int go = 1;
         if (lane == 0) {
-          go = wait_one(sfempty(slot), ((n_loaded / kSfSlots) & 1u) ^ 1u, abort_flag, tmo, err,
+          go = wait_one<kSuspendHintNs>(sfempty(slot), ((n_loaded / kSfSlots) & 1u) ^ 1u, abort_flag, tmo, err,
                         kSiteScaleEmpty) ? 1 : 0;
           if (go) {
             const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
@@ -586,7 +591,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) break;
       const int slot = (int)(n_laid % kSfSlots);
-      if (!warp_wait(sffull(slot), (n_laid / kSfSlots) & 1u, abort_flag, tmo, err, kSiteScaleFull)) {
+      if (!warp_wait<kSuspendHintNs>(sffull(slot), (n_laid / kSfSlots) & 1u, abort_flag, tmo, err, kSiteScaleFull)) {
         ok = false;
         break;
       }
@@ -626,7 +631,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int t = first_tile; t < sched.total; t += tile_stride, ++tile_iter) {
       Tile tile;
       if (!sched.get(t, tile)) continue;
-      if (!warp_wait(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
+      if (!warp_wait<kSuspendHintNs>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
       tc_fence_after();
       const int row0 = tile.mb * kBlockM + quarter * 32;
       const int row = row0 + lane;

@@ -9,7 +9,9 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "dg_internal.h"
@@ -200,6 +202,33 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
     const int64_t tiles = m_blocks * ((n + widths[i] - 1) / widths[i]);
     const int64_t waves = (tiles + sms - 1) / sms;
     const double cost = (double)waves * ((double)k_blocks + epi_blocks[i]) * widths[i] / rate[i];
+    if (cost < best_cost * 0.999) {
+      best_cost = cost;
+      best = widths[i];
+    }
+  }
+  return best;
+}
+
+// Tile width for masked problems with few rows per group, which are bound by
+// streaming B from HBM rather than by the tensor cores.  A tile's time then
+// grows with its width (its share of B) plus a fixed part (A, scales, set-up);
+// the 256-column tile also pays for an epilogue that does not overlap the next
+// tile.  The host does not know the per-group counts (they stay on the
+// device), so the number of 128-row blocks is estimated from the expected
+// count per group: ceil(m / 128) is on average m / 128 + 1/2.
+int choose_block_n_masked_streaming(int64_t groups, int64_t expected_m, int64_t n, int slots) {
+  const int forced = env_int("DG_BLOCK_N", 0);
+  if (gemm_block_n_supported(forced)) return forced;
+  static const int widths[4] = {128, 192, 224, 256};
+  const double blocks = (double)groups * ((double)expected_m / kBlockM + 0.5);
+  const int sms = slots > 0 ? slots : 1;
+  int best = 224;
+  double best_cost = 1e300;
+  for (int i = 0; i < 4; ++i) {
+    const double tiles = std::ceil(blocks) * (double)((n + widths[i] - 1) / widths[i]);
+    const double waves = std::ceil(tiles / sms);
+    const double cost = waves * (widths[i] + 96.0 + (widths[i] == 256 ? 100.0 : 0.0));
     if (cost < best_cost * 0.999) {
       best_cost = cost;
       best = widths[i];
@@ -418,6 +447,10 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
     grid_units = gemm2_max_clusters(kMasked, block_n);
     if (grid_units > sms / 2) grid_units = sms / 2;
     if (grid_units <= 0) return DG_ERR_CUDA;
+  } else if (expected_m > 0 && expected_m <= 2 * kBlockM) {
+    block_n = choose_block_n_masked_streaming(num_groups, std::min<int64_t>(expected_m, max_m), n,
+                                              sms);
+    grid_units = sms;
   } else {
     block_n = choose_block_n(((m_est + kBlockM - 1) / kBlockM) * num_groups, n, k / kBlockK, sms,
                              false, false);
