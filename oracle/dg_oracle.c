@@ -1,6 +1,6 @@
 /*
  * CPU oracle for the fine-grained-scaled FP8 GEMM family (dense NT, M-grouped
- * contiguous, M-grouped masked).
+ * contiguous, M-grouped masked, K-grouped).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
  * this file; only the tests, the package's smoke check and the bench's
@@ -24,6 +24,9 @@
  *   - GEMM D = C + A @ B.T (NT): same page, same section.
  *   - Contiguous M-grouped layout and masked M-grouped layout: same page,
  *     section "GEMM denso e grouped".
+ *   - K-grouped (weight-gradient) layout, experts stacked along K: same page,
+ *     same section; the reading of its operand layout is stated beside
+ *     or_gemm_k_grouped below.
  *
  * Evaluation order of the GEMM: for each 128-wide K block the products of the
  * decoded codes are summed in FP64 (exact: every product is a multiple of
@@ -412,6 +415,130 @@ int or_gemm_masked(const uint8_t* qa, const double* sa, const uint8_t* qb, const
   grouped_ctx ctx = {qa, sa, qb, sb, group_of_row, num_groups, N, K, rows, o, written};
   parallel_for(rows ? nrows : total, grouped_range, &ctx);
   free(group_of_row);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* K-grouped layout (MoE weight gradients)                                    */
+/* ------------------------------------------------------------------------ */
+/* "DeepGEMM: kernels GEMM FP8 limpos e eficientes por meio de scaling
+ * granular" (pt.news.hada.io), section "GEMM denso e grouped": a grouped API
+ * along K for the weight backward of MoE models, M and N fixed, named
+ * k_grouped_fp8_gemm_tn_contiguous.  The page gives no more; the reading
+ * taken here: the experts' token rows are stacked along K (each expert's
+ * segment a multiple of 128 rows), A is stored [sum_k, M] and B [sum_k, N]
+ * ("TN": both with the reduction axis outermost), every 128-row block of one
+ * column carries one power-of-two scale (the same fine-grained grouping, along
+ * the reduction axis), and expert g produces
+ *   D[g] = C[g] + A_g^T B_g   (FP32 [M, N]).                                */
+
+typedef struct {
+  const float* x;
+  int64_t rows, cols;
+  uint8_t* q;
+  int32_t* sf_exp;   /* [rows/128, cols] */
+  double* sf_scale;  /* same shape, 2^e; may be NULL */
+} quant_cols_ctx;
+
+static void quant_cols_range(void* p, int64_t rb_begin, int64_t rb_end) {
+  quant_cols_ctx* c = (quant_cols_ctx*)p;
+  for (int64_t rb = rb_begin; rb < rb_end; ++rb) {
+    int64_t r0 = rb * OR_BLOCK_K;
+    for (int64_t j = 0; j < c->cols; ++j) {
+      double amax = 0.0;
+      for (int64_t r = r0; r < r0 + OR_BLOCK_K; ++r) {
+        double v = fabs((double)c->x[r * c->cols + j]);
+        if (v > amax) amax = v;
+      }
+      int e = or_scale_exponent(amax);
+      c->sf_exp[rb * c->cols + j] = e;
+      if (c->sf_scale) c->sf_scale[rb * c->cols + j] = ldexp(1.0, e);
+      for (int64_t r = r0; r < r0 + OR_BLOCK_K; ++r)
+        c->q[r * c->cols + j] = or_e4m3_encode(ldexp((double)c->x[r * c->cols + j], -e));
+    }
+  }
+}
+
+/* x: FP32 [rows, cols] row-major, rows % 128 == 0: one scale per 128 rows of
+ * each column (the reduction axis is the row axis).  Returns 0, or -1. */
+int or_quantize_cols(const float* x, int64_t rows, int64_t cols, uint8_t* q, int32_t* sf_exp,
+                     double* sf_scale) {
+  ensure_tables();
+  if (!x || !q || !sf_exp || rows < 0 || cols < 0 || rows % OR_BLOCK_K != 0) return -1;
+  quant_cols_ctx c = {x, rows, cols, q, sf_exp, sf_scale};
+  parallel_for(rows / OR_BLOCK_K, quant_cols_range, &c);
+  return 0;
+}
+
+typedef struct {
+  const uint8_t* qa; const double* sa;
+  const uint8_t* qb; const double* sb;
+  const int64_t* kb_start; /* [G + 1] first K block of each expert */
+  int64_t M, N;
+  const float* c;
+  const int64_t* rows;
+  double* o;
+} kgrouped_ctx;
+
+static void kgrouped_range(void* p, int64_t i0, int64_t i1) {
+  kgrouped_ctx* c = (kgrouped_ctx*)p;
+  double* inner = (double*)malloc((size_t)(c->N > 0 ? c->N : 1) * sizeof(double));
+  if (!inner) return;
+  for (int64_t i = i0; i < i1; ++i) {
+    int64_t flat = c->rows ? c->rows[i] : i; /* g * M + m */
+    int64_t g = flat / c->M, m = flat % c->M;
+    double* acc = c->o + i * c->N;
+    for (int64_t n = 0; n < c->N; ++n) acc[n] = c->c ? (double)c->c[flat * c->N + n] : 0.0;
+    for (int64_t kb = c->kb_start[g]; kb < c->kb_start[g + 1]; ++kb) {
+      for (int64_t n = 0; n < c->N; ++n) inner[n] = 0.0;
+      for (int64_t k = kb * OR_BLOCK_K; k < (kb + 1) * OR_BLOCK_K; ++k) {
+        double av = g_e4m3[c->qa[k * c->M + m]];
+        const uint8_t* brow = c->qb + k * c->N;
+        for (int64_t n = 0; n < c->N; ++n) inner[n] += av * g_e4m3[brow[n]];
+      }
+      double sam = c->sa[kb * c->M + m];
+      for (int64_t n = 0; n < c->N; ++n) acc[n] += inner[n] * sam * c->sb[kb * c->N + n];
+    }
+  }
+  free(inner);
+}
+
+/* K-grouped TN: qa [sum_k, M] codes, sa [sum_k/128, M] scales; qb [sum_k, N]
+ * codes, sb [sum_k/128, N] scales; ks [G] rows per expert (each >= 0 and a
+ * multiple of 128, summing to sum_k); c [G, M, N] FP32 or NULL.
+ * o [G, M, N] = C + per expert sum over its K blocks, in increasing K order,
+ * of (exact FP64 inner sum over the block) * sa * sb.  rows (optional) lists
+ * flat indices g * M + m; o is then [nrows, N].  Returns 0, or -1. */
+int or_gemm_k_grouped(const uint8_t* qa, const double* sa, const uint8_t* qb, const double* sb,
+                      const int32_t* ks, int64_t num_groups, int64_t M, int64_t N, int64_t sum_k,
+                      const float* c, const int64_t* rows, int64_t nrows, double* o) {
+  ensure_tables();
+  if (!qa || !sa || !qb || !sb || !ks || !o || num_groups < 0 || M < 0 || N < 0 || sum_k < 0 ||
+      sum_k % OR_BLOCK_K != 0)
+    return -1;
+  int64_t* kb_start = (int64_t*)malloc((size_t)(num_groups + 1) * sizeof(int64_t));
+  if (!kb_start) return -2;
+  kb_start[0] = 0;
+  for (int64_t g = 0; g < num_groups; ++g) {
+    if (ks[g] < 0 || ks[g] % OR_BLOCK_K != 0) {
+      free(kb_start);
+      return -1;
+    }
+    kb_start[g + 1] = kb_start[g] + ks[g] / OR_BLOCK_K;
+  }
+  if (kb_start[num_groups] * OR_BLOCK_K != sum_k) {
+    free(kb_start);
+    return -1;
+  }
+  if (rows)
+    for (int64_t i = 0; i < nrows; ++i)
+      if (rows[i] < 0 || rows[i] >= num_groups * M) {
+        free(kb_start);
+        return -1;
+      }
+  kgrouped_ctx ctx = {qa, sa, qb, sb, kb_start, M, N, c, rows, o};
+  parallel_for(rows ? nrows : num_groups * M, kgrouped_range, &ctx);
+  free(kb_start);
   return 0;
 }
 

@@ -44,6 +44,10 @@ def lib():
         L.or_gemm_contiguous.restype = C.c_int
         L.or_gemm_masked.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p, p]
         L.or_gemm_masked.restype = C.c_int
+        L.or_quantize_cols.argtypes = [p, i64, i64, p, p, p]
+        L.or_quantize_cols.restype = C.c_int
+        L.or_gemm_k_grouped.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, p, i64, p]
+        L.or_gemm_k_grouped.restype = C.c_int
         _LIB = L
     return _LIB
 
@@ -195,8 +199,52 @@ def gemm_masked(qa, sa, qb, sb, masked_m, rows=None):
     return o, w
 
 
+def quantize_cols(x):
+    """FP32 [rows, cols], rows % 128 == 0 -> (codes uint8 [rows, cols],
+    exponents int32 [rows/128, cols], scales float64 (2^e), same shape): one
+    scale per 128 rows of each column."""
+    x = _c(x, np.float32)
+    assert x.ndim == 2
+    rows, cols = x.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    e = np.empty((rows // 128, cols), dtype=np.int32)
+    s = np.empty((rows // 128, cols), dtype=np.float64)
+    rc = lib().or_quantize_cols(_ptr(x), rows, cols, _ptr(q), _ptr(e), _ptr(s))
+    if rc != 0:
+        raise ValueError("or_quantize_cols rejected its arguments (rc=%d)" % rc)
+    return q, e, s
+
+
+def pack_ue8m0_cols(sf_exp) -> np.ndarray:
+    """Column-wise exponents [kblocks, cols] -> packed int32
+    [ceil(kblocks/4), align(cols, 4)]: the same word layout as pack_ue8m0 with
+    one scale per row, the columns playing the rows (a transposition only)."""
+    e = _c(sf_exp, np.int32)
+    return pack_ue8m0(np.ascontiguousarray(e.T), e.shape[1], 1)
+
+
+def gemm_k_grouped(qa, sa, qb, sb, ks, c=None, rows=None) -> np.ndarray:
+    """o[g] = C[g] + A_g^T B_g in FP64.  qa [sum_k, M] codes, sa [sum_k/128, M];
+    qb [sum_k, N], sb [sum_k/128, N]; ks [G] rows per expert; c FP32 [G, M, N]
+    or None.  Returns [G, M, N], or [len(rows), N] for flat rows g * M + m."""
+    qa, qb = _c(qa, np.uint8), _c(qb, np.uint8)
+    sa, sb = _c(sa, np.float64), _c(sb, np.float64)
+    ks = _c(ks, np.int32)
+    sum_k, M = qa.shape
+    N = qb.shape[1]
+    G = ks.size
+    cc = None if c is None else _c(c, np.float32)
+    r = None if rows is None else _c(rows, np.int64)
+    o = np.empty((G, M, N) if r is None else (r.size, N), dtype=np.float64)
+    rc = lib().or_gemm_k_grouped(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), _ptr(ks), G, M, N, sum_k,
+                                 _ptr(cc), _ptr(r), 0 if r is None else r.size, _ptr(o))
+    if rc != 0:
+        raise ValueError("or_gemm_k_grouped rejected its arguments (rc=%d)" % rc)
+    return o
+
+
 __all__ = [
     "lib", "set_threads", "get_threads", "e4m3_table", "e4m3_encode", "e4m3_decode", "bf16_rne",
     "scale_exponent", "quantize", "pack_ue8m0", "gemm_nt", "gemm_nt_rows", "gemm_contiguous",
-    "gemm_masked",
+    "gemm_masked", "quantize_cols", "pack_ue8m0_cols", "gemm_k_grouped",
 ]

@@ -386,3 +386,108 @@ def test_bf16_rne_ties_to_even_from_double():
     assert oracle.bf16_rne([1.0 + 3 * 2.0 ** -8])[0] == 0x3F82
     # a double just above the midpoint rounds up (no double rounding through FP32)
     assert oracle.bf16_rne([1.0 + 2.0 ** -8 + 2.0 ** -40])[0] == 0x3F81
+
+
+# --------------------------------------------------------------------------- K-grouped (weight gradients)
+
+
+def test_quantize_cols_is_row_quantize_of_the_transpose():
+    # one scale per 128 rows of a column = the 1x128 row grouping of x.T
+    g = torch.Generator().manual_seed(21)
+    x = (torch.randn(384, 72, generator=g) * torch.logspace(-3, 3, 72)).numpy()
+    q, e, s = oracle.quantize_cols(x)
+    qt, et, st = oracle.quantize(np.ascontiguousarray(x.T), 1)
+    assert np.array_equal(q, qt.T) and np.array_equal(e, et.T) and np.array_equal(s, st.T)
+
+
+def test_pack_ue8m0_cols_hand_example():
+    e = np.array([[0, 1, -1], [2, 0, 0], [-3, 5, 1], [0, 0, 0], [7, -7, 2]], dtype=np.int32)  # [kb=5, cols=3]
+    p = oracle.pack_ue8m0_cols(e)
+    assert p.shape == (2, 4)
+    assert p[0, 0] == 127 | (129 << 8) | (124 << 16) | (127 << 24)
+    assert p[0, 1] == 128 | (127 << 8) | (132 << 16) | (127 << 24)
+    assert p[1, 0] == 134 and p[1, 1] == 120 and p[1, 2] == 129 and p[1, 3] == 0
+    assert np.all(p[:, 3] == 0)
+
+
+def _kg_small_ints(rng, sum_k, cols):
+    vals = rng.integers(-4, 5, size=(sum_k, cols))
+    codes = np.vectorize(lambda v: _INT_CODES[float(v)])(vals).astype(np.uint8)
+    return vals, codes
+
+
+def test_k_grouped_exact_small_integers_with_pow2_scales():
+    rng = np.random.default_rng(31)
+    ks = np.array([256, 0, 128, 384], dtype=np.int32)
+    sum_k, M, N = int(ks.sum()), 6, 10
+    av, qa = _kg_small_ints(rng, sum_k, M)
+    bv, qb = _kg_small_ints(rng, sum_k, N)
+    ea = rng.integers(-3, 4, size=(sum_k // 128, M))
+    eb = rng.integers(-3, 4, size=(sum_k // 128, N))
+    cv = rng.integers(-20, 20, size=(len(ks), M, N)).astype(np.float32)
+    o = oracle.gemm_k_grouped(qa, np.ldexp(1.0, ea), qb, np.ldexp(1.0, eb), ks, c=cv)
+    start = np.concatenate([[0], np.cumsum(ks)])
+    for g in range(len(ks)):
+        for m in range(M):
+            for n in range(N):
+                want = Fraction(int(cv[g, m, n]))
+                for k in range(start[g], start[g + 1]):
+                    want += Fraction(int(av[k, m]) * int(bv[k, n])) * Fraction(2) ** int(ea[k // 128, m] + eb[k // 128, n])
+                assert Fraction(o[g, m, n]) == want, (g, m, n)
+
+
+@pytest.mark.parametrize("ks", [[128], [256, 128], [0, 384, 0, 128]])
+def test_k_grouped_brute_force_tiny(ks):
+    ks = np.array(ks, dtype=np.int32)
+    sum_k, M, N = int(ks.sum()), 9, 24
+    g = torch.Generator().manual_seed(int(sum_k) + len(ks))
+    a = torch.randn(sum_k, M, generator=g).numpy()
+    b = torch.randn(sum_k, N, generator=g).numpy()
+    c = torch.randn(len(ks), M, N, generator=g).numpy()
+    qa, _, sa = oracle.quantize_cols(a)
+    qb, _, sb = oracle.quantize_cols(b)
+    o = oracle.gemm_k_grouped(qa, sa, qb, sb, ks, c=c)
+    # naive loop over independently dequantised FP64 matrices
+    A = _torch_decode(qa) * np.repeat(sa, 128, axis=0)
+    B = _torch_decode(qb) * np.repeat(sb, 128, axis=0)
+    start = np.concatenate([[0], np.cumsum(ks)])
+    for gi in range(len(ks)):
+        want = c[gi].astype(np.float64).copy()
+        for m in range(M):
+            for n in range(N):
+                s = want[m, n]
+                for k in range(start[gi], start[gi + 1]):
+                    s += A[k, m] * B[k, n]
+                want[m, n] = s
+        np.testing.assert_allclose(o[gi], want, rtol=1e-12, atol=1e-12)
+
+
+def test_k_grouped_split_of_a_group_is_additive_and_empty_group_is_c():
+    rng = np.random.default_rng(41)
+    sum_k, M, N = 512, 5, 8
+    _, qa = _kg_small_ints(rng, sum_k, M)
+    _, qb = _kg_small_ints(rng, sum_k, N)
+    sa = np.ldexp(1.0, rng.integers(-2, 3, size=(4, M)))
+    sb = np.ldexp(1.0, rng.integers(-2, 3, size=(4, N)))
+    whole = oracle.gemm_k_grouped(qa, sa, qb, sb, [512])
+    parts = oracle.gemm_k_grouped(qa, sa, qb, sb, [128, 384])
+    assert np.array_equal(whole[0], parts[0] + parts[1])
+    cv = rng.standard_normal((3, M, N)).astype(np.float32)
+    o = oracle.gemm_k_grouped(qa, sa, qb, sb, [0, 512, 0], c=cv)
+    assert np.array_equal(o[0], cv[0].astype(np.float64)) and np.array_equal(o[2], cv[2].astype(np.float64))
+    assert np.array_equal(o[1], whole[0] + cv[1].astype(np.float64))
+
+
+def test_k_grouped_rows_subset_and_argument_checks():
+    g = torch.Generator().manual_seed(43)
+    ks = np.array([128, 256], dtype=np.int32)
+    a = torch.randn(384, 16, generator=g).numpy(); b = torch.randn(384, 40, generator=g).numpy()
+    qa, _, sa = oracle.quantize_cols(a); qb, _, sb = oracle.quantize_cols(b)
+    full = oracle.gemm_k_grouped(qa, sa, qb, sb, ks)
+    rows = np.array([31, 0, 16, 17])
+    sub = oracle.gemm_k_grouped(qa, sa, qb, sb, ks, rows=rows)
+    assert np.array_equal(sub, full.reshape(-1, 40)[rows])
+    with pytest.raises(ValueError):
+        oracle.gemm_k_grouped(qa, sa, qb, sb, [128, 200])  # not a multiple of 128
+    with pytest.raises(ValueError):
+        oracle.gemm_k_grouped(qa, sa, qb, sb, [128, 128])  # does not cover sum_k
