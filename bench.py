@@ -40,7 +40,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="prefill", choices=["prefill", "decode", "contiguous", "masked", "small"])
+    p.add_argument("--workload", default="prefill",
+                   choices=["prefill", "decode", "contiguous", "masked", "kgrouped", "small"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-steps", type=int, default=0,
@@ -478,6 +479,21 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
                for t in rotate((qa, sfa, qb, sfb, mi, d), byt)]
         cases.append(dict(name="contiguous G=%d valid_rows=%d padded_rows=%d n=%d k=%d" %
                           (G, valid, w.a.shape[0], n, k), fns=fns, flops=2.0 * valid * n * k, bytes=byt))
+    elif args.workload == "kgrouped":
+        cfg = workloads.KGROUPED
+        w = workloads.k_grouped(cfg["num_groups"], cfg["m"], cfg["n"], cfg["seed"])
+        qa, sfa = dg.quantize_fp8_cols(w.a.to(dev))
+        qb, sfb = dg.quantize_fp8_cols(w.b.to(dev))
+        ks = w.ks.to(dev)
+        G, m, n = cfg["num_groups"], cfg["m"], cfg["n"]
+        d = torch.empty(G, m, n, dtype=torch.float32, device=dev)
+        valid = int(w.counts.sum())
+        sum_k = int(w.ks.sum())
+        byt = valid * (m + n) + 4 * G * m * n + (sum_k // 128) * (m + n)
+        fns = [(lambda t=t: dg.k_grouped_fp8_gemm_tn_contiguous(t[0], t[1], t[2], t[3], t[4], d=t[5]))
+               for t in rotate((qa, sfa, qb, sfb, ks, d), byt)]
+        cases.append(dict(name="k-grouped G=%d valid_k=%d padded_k=%d m=%d n=%d" % (G, valid, sum_k, m, n),
+                          fns=fns, flops=2.0 * valid * m * n, bytes=byt))
     elif args.workload == "masked":
         cfg = workloads.MASKED
         G, cap, n, k = cfg["num_groups"], cfg["cap"], cfg["n"], cfg["k"]

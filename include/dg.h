@@ -137,6 +137,35 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
                                           int32_t num_groups, int64_t max_m, int64_t n, int64_t k,
                                           int64_t expected_m, void* stream);
 
+/* K-grouped, contiguous layout ("TN"), for the weight gradients of MoE
+ * experts: the experts' token rows are stacked along K, M and N are shared.
+ * Expert g owns rows [off_g, off_g + ks[g]) of A and B (off_g = ks[0] + ... +
+ * ks[g-1]) and produces
+ *   D[g][m, n] = C[g][m, n] + sum_{k in expert g} A[k, m] * B[k, n]
+ * (dequantised, FP32 accumulation, FP32 output).
+ *   a    E4M3 [sum_k, m] (contiguous, M innermost), m % 16 == 0
+ *   sfa  packed UE8M0 [ceil(sum_k/512), align(m, 4)]: one scale per 128 rows
+ *        of each column of A (byte t of word (j, col) = e + 127 of K block 4j+t)
+ *   b    E4M3 [sum_k, n] (contiguous, N innermost), n % 16 == 0
+ *   sfb  packed UE8M0 [ceil(sum_k/512), align(n, 4)], the same per column of B
+ *   c    float [num_groups, m, n] or NULL for C = 0; may equal d
+ *   d    float [num_groups, m, n] (contiguous); every element is written
+ *   ks   int32 [num_groups] on the device: rows per expert, each a multiple
+ *        of 128 (dg_get_mk_alignment_for_contiguous_layout), summing to
+ *        sum_k.  An expert with 0 rows gets D[g] = C[g] (or 0).  A size that
+ *        is negative or not a multiple of 128 counts as 0, and rows past
+ *        sum_k are dropped; both set DG_ERR_DEVICE_BAD_INDEX.
+ * sum_k % 128 == 0; num_groups <= 512.  ks is never read on the host.
+ * Cited: same page, section "GEMM denso e grouped" (a grouped API along K for
+ * the weight backward of MoE, M and N fixed, k_grouped_fp8_gemm_tn_contiguous);
+ * the page does not give the operand layout or scale granularity: the
+ * reading above ("TN": both operands with the reduction axis outermost; the
+ * fine-grained 128-element scale groups taken along K) is this library's. */
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa, const void* b,
+                                              const int32_t* sfb, const float* c, float* d,
+                                              const int32_t* ks, int64_t m, int64_t n,
+                                              int64_t sum_k, int32_t num_groups, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Quantisation and scale layout                                             */
 /* ------------------------------------------------------------------------ */
@@ -157,6 +186,22 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
  * to FP8 is left to the user; the library offers simple utilities). */
 dg_status dg_quantize_fp8(const float* x, void* q, void* sf, int64_t groups, int64_t rows,
                           int64_t cols, int32_t block_rows, int32_t sf_format, void* stream);
+
+/* FP32 -> E4M3 with one power-of-two scale per 128 rows of each column, the
+ * grouping of operands whose reduction axis is the row axis (A and B of
+ * dg_k_grouped_fp8_gemm_tn_contiguous).
+ *   x   float [rows, cols] (contiguous), rows % 128 == 0, cols % 4 == 0
+ *   q   E4M3 [rows, cols] (contiguous)
+ *   sf  sf_format DG_SF_FP32: float [rows/128, cols]
+ *       sf_format DG_SF_UE8M0_PACKED: int32 [ceil(rows/512), align(cols, 4)],
+ *       byte t of word (j, col) = e + 127 of the 128-row block 4j+t (unused
+ *       bytes and padding columns are 0)
+ * Same scale rule and cast as dg_quantize_fp8.  Cited: same page, section
+ * "Interface GEMM e restrições de layout" (fine-grained scaling; casting is
+ * the user's job, the library offers utilities), applied along K for the
+ * K-grouped layout of section "GEMM denso e grouped". */
+dg_status dg_quantize_fp8_cols(const float* x, void* q, void* sf, int64_t rows, int64_t cols,
+                               int32_t sf_format, void* stream);
 
 /* FP32 scales -> packed UE8M0 layout.
  *   sf      float [groups, ceil(mn/block_rows), ceil(k/128)]

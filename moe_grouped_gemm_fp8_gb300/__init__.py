@@ -2,7 +2,8 @@
 
 D = C + A @ B.T with E4M3 operands, 1x128 / 128x128 power-of-two scales,
 FP32 accumulation and BF16 output, in the dense NT form and the two
-M-grouped MoE layouts (contiguous, masked).  The kernels live in libdg.so
+M-grouped MoE layouts (contiguous, masked); and the K-grouped layout of MoE
+weight gradients (FP32 output).  The kernels live in libdg.so
 (C ABI: include/dg.h); this package is a thin torch binding over it.
 """
 from .api import (  # noqa: F401
@@ -12,9 +13,11 @@ from .api import (  # noqa: F401
     get_mk_alignment_for_contiguous_layout,
     get_num_sms,
     get_tma_aligned_size,
+    k_grouped_fp8_gemm_tn_contiguous,
     m_grouped_fp8_gemm_nt_contiguous,
     m_grouped_fp8_gemm_nt_masked,
     quantize_fp8,
+    quantize_fp8_cols,
     set_num_sms,
     set_wait_timeout_ns,
     sf_packed_shape,

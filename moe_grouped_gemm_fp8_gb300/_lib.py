@@ -31,7 +31,9 @@ SIGNATURES = {
     "dg_fp8_gemm_nt": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
     "dg_m_grouped_fp8_gemm_nt_contiguous": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p]),
     "dg_m_grouped_fp8_gemm_nt_masked": (_st, [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _i64, _p]),
+    "dg_k_grouped_fp8_gemm_tn_contiguous": (_st, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p]),
     "dg_quantize_fp8": (_st, [_p, _p, _p, _i64, _i64, _i64, _i32, _i32, _p]),
+    "dg_quantize_fp8_cols": (_st, [_p, _p, _p, _i64, _i64, _i32, _p]),
     "dg_transform_sf": (_st, [_p, _p, _i64, _i64, _i64, _i32, _p]),
     "dg_get_tma_aligned_size": (_i64, [_i64, _i32]),
     "dg_get_mk_alignment_for_contiguous_layout": (_i32, []),

@@ -123,6 +123,35 @@ def quantize_fp8(x: torch.Tensor, block_rows: int, packed: bool = True, out=None
     return q, sf
 
 
+def quantize_fp8_cols(x: torch.Tensor, packed: bool = True, out=None, stream=None):
+    """FP32 [rows, cols] (rows % 128 == 0) -> (E4M3 codes, scales) with one
+    scale per 128 rows of each column, the grouping of the K-grouped GEMM's
+    operands.  packed=True gives int32 [ceil(rows/512), align(cols, 4)];
+    packed=False FP32 [rows/128, cols]."""
+    _need(x, "x", (torch.float32,), 2)
+    x = x.contiguous()
+    rows, cols = x.shape
+    if packed:
+        sf_shape, sf_dtype = sf_packed_shape(cols, rows), torch.int32
+    else:
+        sf_shape, sf_dtype = (rows // 128, cols), torch.float32
+    if out is None:
+        q = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+        sf = torch.empty(sf_shape, dtype=sf_dtype, device=x.device)
+    else:
+        q, sf = out
+        _need(q, "q", FP8_DTYPES, 2)
+        _need(sf, "sf", (sf_dtype,), 2)
+        if tuple(q.shape) != tuple(x.shape) or tuple(sf.shape) != tuple(sf_shape) or \
+                not q.is_contiguous() or not sf.is_contiguous():
+            raise ValueError("out tensors must be contiguous %s / %s" % (tuple(x.shape), sf_shape))
+    st = _lib.lib().dg_quantize_fp8_cols(_ptr(x), _ptr(q), _ptr(sf), rows, cols,
+                                         _lib.DG_SF_UE8M0_PACKED if packed else _lib.DG_SF_FP32,
+                                         _stream(stream))
+    _check(st, "dg_quantize_fp8_cols")
+    return q, sf
+
+
 def transform_sf_into_required_layout(sf: torch.Tensor, mn: int, k: int, block_rows: int,
                                       stream=None) -> torch.Tensor:
     """FP32 scales [G?, ceil(mn/block_rows), ceil(k/128)] -> packed UE8M0
@@ -199,6 +228,44 @@ def m_grouped_fp8_gemm_nt_contiguous(a: torch.Tensor, sfa: torch.Tensor, b: torc
         _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(m_indices), m_sum, n, k, g,
         _stream(stream))
     _check(st, "dg_m_grouped_fp8_gemm_nt_contiguous")
+    return d
+
+
+def k_grouped_fp8_gemm_tn_contiguous(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor,
+                                     sfb: torch.Tensor, ks: torch.Tensor,
+                                     d: Optional[torch.Tensor] = None,
+                                     c: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Experts stacked along K: A [sum_k, M], B [sum_k, N] (E4M3, M / N
+    innermost), ks [G] int32 on the device (rows per expert, multiples of
+    128).  D[g] = C[g] + A_g^T B_g, FP32 [G, M, N]."""
+    _need(a, "a", FP8_DTYPES, 2)
+    _need(b, "b", FP8_DTYPES, 2)
+    _need(sfa, "sfa", (torch.int32,), 2)
+    _need(sfb, "sfb", (torch.int32,), 2)
+    _need(ks, "ks", (torch.int32,), 1)
+    sum_k, m = a.shape
+    kb, n = b.shape
+    g = ks.numel()
+    if kb != sum_k:
+        raise ValueError("shape mismatch")
+    if tuple(sfa.shape) != sf_packed_shape(m, sum_k) or tuple(sfb.shape) != sf_packed_shape(n, sum_k):
+        raise ValueError("scale shapes do not match the packed layout")
+    for t, name in ((a, "a"), (b, "b"), (sfa, "sfa"), (sfb, "sfb"), (ks, "ks")):
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if d is None:
+        d = torch.empty((g, m, n), dtype=torch.float32, device=a.device)
+    _need(d, "d", (torch.float32,), 3)
+    if tuple(d.shape) != (g, m, n) or not d.is_contiguous():
+        raise ValueError("d must be contiguous [G, M, N]")
+    if c is not None:
+        _need(c, "c", (torch.float32,), 3)
+        if tuple(c.shape) != (g, m, n) or not c.is_contiguous():
+            raise ValueError("c must be contiguous [G, M, N]")
+    st = _lib.lib().dg_k_grouped_fp8_gemm_tn_contiguous(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d), _ptr(ks), m, n, sum_k, g,
+        _stream(stream))
+    _check(st, "dg_k_grouped_fp8_gemm_tn_contiguous")
     return d
 
 

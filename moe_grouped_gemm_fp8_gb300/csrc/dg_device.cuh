@@ -206,6 +206,18 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
   return smem_desc(saddr, 16, 1024, 2);
 }
 
+// MN-major operand tile with 128-byte swizzle, as written by TMA boxes of 128
+// bytes (along M or N) x 128 rows (along K): a swizzle atom is 8 K rows of
+// 128 bytes (1024 bytes, 8-row K groups 1024 bytes apart: SBO); atoms along
+// the MN dimension are 16 KB apart (LBO: the next 128-column box).  Checked
+// on the hardware with exact small-integer operands.
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr) {
+  return smem_desc(saddr, 16384, 1024, 2);
+}
+
+// Instruction-descriptor bits marking A and B as MN-major ("transposed").
+constexpr uint32_t kIdescMnMajorAB = (1u << 15) | (1u << 16);
+
 // 32 rows x 16 bytes, row r at byte 16 r, no swizzle (source of a
 // 32x128b tcgen05.cp).  Core matrices (8 rows x 16 B) are 128 bytes apart.
 __device__ __forceinline__ uint64_t smem_desc_sf_chunk(uint32_t saddr) {

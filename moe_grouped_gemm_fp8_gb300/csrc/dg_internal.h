@@ -15,7 +15,9 @@ constexpr int kBlockM = 128;  // rows of an output tile (UMMA M)
 constexpr int kBlockK = 128;  // K extent of one scale block / pipeline stage
 constexpr int kMaxMaskedGroups = 512;
 
-enum GemmMode : int { kDense = 0, kContiguous = 1, kMasked = 2 };
+// kKGrouped: experts stacked along K (weight gradients), MN-major operands,
+// FP32 output [G, M, N].
+enum GemmMode : int { kDense = 0, kContiguous = 1, kMasked = 2, kKGrouped = 3 };
 
 // Sites recorded with device errors (bits 8-23 of the error word).
 enum ErrorSite : uint32_t {
@@ -32,6 +34,7 @@ enum ErrorSite : uint32_t {
   kSiteSplitFull = 11,
   kSiteContiguousIndex = 16,
   kSiteMaskedCount = 17,
+  kSiteKGroupSize = 18,
   kSiteTransformScale = 32,
 };
 
@@ -50,6 +53,10 @@ struct GemmArgs {
   int32_t band;            // raster band height in M blocks
   uint64_t timeout_ns;
   unsigned long long* err; // device error word
+  // K-grouped form only
+  const int32_t* ks;       // rows per expert along K, [num_groups]
+  const float* c_f32;      // nullable, [num_groups, m, n]
+  float* d_f32;            // [num_groups, m, n]
 };
 
 // gemm.cu: dispatch over the tile widths compiled in gemm_bn*.cu (single CTA)
@@ -98,6 +105,8 @@ DG_DECLARE_GEMM_BN(256)
 // quant.cu
 cudaError_t quantize_launch(const float* x, void* q, void* sf, int64_t groups, int64_t rows,
                             int64_t cols, int block_rows, int sf_format, cudaStream_t stream);
+cudaError_t quantize_cols_launch(const float* x, void* q, void* sf, int64_t rows, int64_t cols,
+                                 int sf_format, cudaStream_t stream);
 cudaError_t transform_sf_launch(const float* sf, int32_t* packed, int64_t groups, int64_t mn,
                                 int64_t k, int block_rows, cudaStream_t stream);
 cudaError_t quant_fetch_error(unsigned long long* word);  // reads and clears

@@ -70,6 +70,11 @@ struct PairScheduler {
   int cursor;
   int p_blocks;  // dense: ceil(m / 256)
 
+  __device__ void k_range(const Tile&, int& kb0, int& kb1) const {
+    kb0 = 0;
+    kb1 = args->k_blocks;
+  }
+
   __device__ bool get(int t, Tile& tile) {
     if (MODE == kMasked) {
       while (t >= tile_start[cursor + 1]) ++cursor;
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                          const __grid_constant__ CUtensorMap tm_sfa,
                          const __grid_constant__ CUtensorMap tm_sfb,
                          const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
-  static_assert(MODE != kContiguous, "contiguous tiles are not paired");
+  static_assert(MODE == kDense || MODE == kMasked, "only dense and masked tiles are paired");
   using L = Gemm2Layout<BN>;
   using P = Gemm2Plan<BN, STAGES>;
   constexpr int NUM_ACC = P::kNumAcc;
@@ -311,8 +316,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale warp (both CTAs)
     PackCursor<PairScheduler<MODE>> ld, lay;
-    ld.init(sched, cluster_id, num_clusters, 0, args.k_blocks);
-    lay.init(sched, cluster_id, num_clusters, 0, args.k_blocks);
+    ld.init(sched, cluster_id, num_clusters);
+    lay.init(sched, cluster_id, num_clusters);
     uint32_t n_loaded = 0, n_laid = 0;
     bool ok = true;
     while (!lay.done && ok) {
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (go) {
             const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
             const uint32_t bar = sffull(slot);
-            const int my = (2 * ld.tile.mb + (int)rank) * kBlockM, kp = ld.kb >> 2;
+            const int my = (2 * ld.tile.mb + (int)rank) * kBlockM, kp = ld.kp;
             mbar_arrive_expect_tx(bar, L::kTxSF);
             if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
             else tma_load_2d(buf + L::kRawA, &tm_sfa, bar, my, kp);

@@ -89,7 +89,7 @@ constexpr int kSfLookahead = 3;  // packs loaded ahead of the one being laid out
 
 static constexpr size_t gemm_ctrl_bytes(int stages, int mode) {
   return (size_t)8 * (2 * stages + 3 * kSfSlots + 5 + 8) + 16 +
-         (mode == kMasked ? (size_t)4 * (2 * kMaxMaskedGroups + 1) : 0);
+         ((mode == kMasked || mode == kKGrouped) ? (size_t)4 * (2 * kMaxMaskedGroups + 1) : 0);
 }
 
 // Scale buffers and TMEM scale slots are indexed by a running count of scale
@@ -123,16 +123,42 @@ struct Tile {
 // contiguous tiles are rastered in bands of `band` M blocks: inside a band the
 // M block varies fastest, so a wave of CTAs shares a few B column blocks and
 // one band of A.  Masked tiles are enumerated group by group (M block
-// fastest) from a prefix table built at kernel start.
+// fastest) from a prefix table built at kernel start.  K-grouped tiles are
+// enumerated expert by expert, each expert's M x N tiles rastered like dense
+// ones.  k_range gives the K blocks a tile accumulates: this CTA's split-K
+// slice, or the expert's own K blocks for the K-grouped form.
 template <int MODE>
 struct Scheduler {
   const GemmArgs* args;
-  const int* tile_start;   // masked: [G + 1]
+  const int* tile_start;   // masked: [G + 1] first tile; K-grouped: [G + 1] first K block
   const int* group_valid;  // masked: [G]
   int total;
   int cursor;              // masked: current group (tile indices only increase)
+  int kb_lo, kb_hi;        // K blocks of every tile (not K-grouped)
+
+  __device__ void k_range(const Tile& tile, int& kb0, int& kb1) const {
+    if (MODE == kKGrouped) {
+      kb0 = tile_start[tile.g];
+      kb1 = tile_start[tile.g + 1];
+    } else {
+      kb0 = kb_lo;
+      kb1 = kb_hi;
+    }
+  }
 
   __device__ bool get(int t, Tile& tile) {
+    if (MODE == kKGrouped) {
+      const int per_group = args->m_blocks * args->n_blocks;
+      tile.g = t / per_group;
+      const int r = t - tile.g * per_group;
+      const int per_band = args->band * args->n_blocks;
+      const int b = r / per_band;
+      const int rem = r - b * per_band;
+      const int rows = min(args->band, args->m_blocks - b * args->band);
+      tile.nb = rem / rows;
+      tile.mb = b * args->band + rem % rows;
+      return true;
+    }
     if (MODE == kMasked) {
       while (t >= tile_start[cursor + 1]) ++cursor;
       const int local = t - tile_start[cursor];
@@ -163,22 +189,20 @@ struct Scheduler {
 };
 
 // Walks the scale packs (tile, K block / 4) of this CTA in the order the MMA
-// consumes them, skipping the tiles the scheduler skips.
+// consumes them, skipping the tiles the scheduler skips and tiles without K
+// blocks.  A tile's K blocks [kb0, kb1) touch the packs kb0 / 4 ..
+// (kb1 - 1) / 4; the MMA thread starts a pack at kb0 and at every K block
+// that is a multiple of 4, so both walk the same sequence.
 template <class Sched>
 struct PackCursor {
   Sched s;
-  int t, stride, kb, k_blocks;
+  int t, stride, kp, kp_end;
   Tile tile;
   bool done;
 
-  int kb_begin;
-
-  // Packs of K blocks [kb0, kb1) of every tile (kb0 a multiple of 4).
-  __device__ void init(const Sched& sch, int first, int stride_, int kb0, int kb1) {
+  __device__ void init(const Sched& sch, int first, int stride_) {
     s = sch;
     stride = stride_;
-    kb_begin = kb0;
-    k_blocks = kb1;
     t = first - stride_;
     next_tile();
   }
@@ -186,14 +210,17 @@ struct PackCursor {
     done = true;
     for (t += stride; t < s.total; t += stride)
       if (s.get(t, tile)) {
+        int kb0, kb1;
+        s.k_range(tile, kb0, kb1);
+        if (kb0 >= kb1) continue;
+        kp = kb0 >> 2;
+        kp_end = ((kb1 - 1) >> 2) + 1;
         done = false;
-        kb = kb_begin;
         return;
       }
   }
   __device__ void advance() {
-    kb += 4;
-    if (kb >= k_blocks) next_tile();
+    if (++kp >= kp_end) next_tile();
   }
 };
 
@@ -283,6 +310,33 @@ __device__ __forceinline__ void store_row_chunk(const uint32_t (&r)[32], __nv_bf
       o.z = pack_bf16x2(f[4], f[5]);
       o.w = pack_bf16x2(f[6], f[7]);
       *reinterpret_cast<uint4*>(dp + 8 * p) = o;
+    }
+  }
+}
+
+// Stores 32 FP32 accumulator columns of one row (+ FP32 C), 16 bytes at a
+// time, the columns at or past n skipped (n % 4 == 0).  `zero`: the tile had
+// no K blocks, so the result is C (or 0) and the accumulator is not read.
+__device__ __forceinline__ void store_row_chunk_f32(const uint32_t (&r)[32], float* dp,
+                                                    const float* cp, int cols_left, bool zero) {
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    if (4 * p < cols_left) {
+      float4 v = zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                      : make_float4(__uint_as_float(r[4 * p]), __uint_as_float(r[4 * p + 1]),
+                                    __uint_as_float(r[4 * p + 2]), __uint_as_float(r[4 * p + 3]));
+      if (cp) {
+        const float4 c = *reinterpret_cast<const float4*>(cp + 4 * p);
+        if (zero) {
+          v = c;
+        } else {
+          v.x += c.x;
+          v.y += c.y;
+          v.z += c.z;
+          v.w += c.w;
+        }
+      }
+      *reinterpret_cast<float4*>(dp + 4 * p) = v;
     }
   }
 }
@@ -421,6 +475,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tile_start[args.num_groups] = acc;
     }
   }
+  if (MODE == kKGrouped && warp == 2) {
+    // Experts' K blocks: sizes must be >= 0 and multiples of 128; a bad size
+    // counts as 0 and K blocks past the end of A and B are dropped, both
+    // flagged.
+    for (int g = lane; g < args.num_groups; g += 32) {
+      const int v = __ldg(args.ks + g);
+      const bool bad = v < 0 || (v % kBlockK) != 0;
+      if (bad) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteKGroupSize);
+      group_valid[g] = bad ? 0 : v / kBlockK;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      int acc = 0;
+      for (int g = 0; g < args.num_groups; ++g) {
+        tile_start[g] = acc;
+        int next = acc + group_valid[g];
+        if (next > args.k_blocks) {
+          record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteKGroupSize);
+          next = args.k_blocks;
+        }
+        acc = next;
+      }
+      tile_start[args.num_groups] = acc;
+    }
+  }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -444,7 +523,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   sched.tile_start = tile_start;
   sched.group_valid = group_valid;
   sched.cursor = 0;
-  sched.total = MODE == kMasked ? tile_start[args.num_groups] : args.m_blocks * args.n_blocks;
+  sched.kb_lo = kb_begin;
+  sched.kb_hi = kb_end;
+  sched.total = MODE == kMasked      ? tile_start[args.num_groups]
+                : MODE == kKGrouped ? args.num_groups * args.m_blocks * args.n_blocks
+                                    : args.m_blocks * args.n_blocks;
   const uint64_t tmo = args.timeout_ns;
 
   if (warp == 0) {
@@ -457,7 +540,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
         Tile tile;
         if (!sched.get(t, tile)) continue;
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
+        int kb0, kb1;
+        sched.k_range(tile, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_one<kSuspendHintNs>(empty(stage), phase ^ 1u, abort_flag, tmo, err, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -466,9 +551,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = full(stage);
           mbar_arrive_expect_tx(fb, L::kTxAB);
           const int kx = kb * kBlockK, my = tile.mb * kBlockM;
-          if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
-          else tma_load_2d(sb, &tm_a, fb, kx, my);
-          tma_load_3d(sb + L::kOffB, &tm_b, fb, kx, tile.nb * BN, tile.g);
+          if constexpr (MODE == kKGrouped) {
+            // MN-major tiles of A [sum_k, M] and B [sum_k, N]: 128 K rows of
+            // 128 bytes per box; B's 256-column tile is two boxes 16 KB apart
+            tma_load_2d(sb, &tm_a, fb, my, kx);
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_2d(sb + L::kOffB + h * 16384, &tm_b, fb, tile.nb * BN + h * 128, kx);
+          } else {
+            if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
+            else tma_load_2d(sb, &tm_a, fb, kx, my);
+            tma_load_3d(sb + L::kOffB, &tm_b, fb, kx, tile.nb * BN, tile.g);
+          }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -503,14 +597,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = kb_begin; kb < kb_end; ++kb) {
+        int kb0, kb1;
+        sched.k_range(tile, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_one<kSuspendHintNs>(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull)) {
             ok = false;
             break;
           }
           uint8_t* st = smem + stage * L::kStageBytes;
           const int slot = (int)(pack % kSfSlots);
-          if ((kb & 3) == 0) {
+          if (kb == kb0 || (kb & 3) == 0) {
             if (!wait_one<kSuspendHintNs>(sfready(slot), (pack / kSfSlots) & 1u, abort_flag, tmo, err,
                           kSiteMmaScaleReady)) {
               ok = false;
@@ -527,14 +623,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t sel = (uint32_t)(kb & 3);
           const uint32_t idesc = idesc0 | (sel << 4) | (sel << 29);
-          const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(st));
-          const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(st + L::kOffB));
+          if constexpr (MODE == kKGrouped) {
+            // MN-major operands: 8-row K groups 1024 bytes apart, 128-byte
+            // MN atoms 16 KB apart; a 32-deep K step is 4 groups (4096 bytes)
+            const uint64_t adesc = smem_desc_mnmajor_sw128(smem_u32(st));
+            const uint64_t bdesc = smem_desc_mnmajor_sw128(smem_u32(st + L::kOffB));
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tc_mma_mxf8(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
-                        (kb != kb_begin || j != 0) ? 1u : 0u);
+            for (int j = 0; j < 4; ++j)
+              tc_mma_mxf8(d_tmem, adesc + 256 * j, bdesc + 256 * j, idesc | kIdescMnMajorAB, sf_tmem,
+                          sf_tmem + 4, (kb != kb0 || j != 0) ? 1u : 0u);
+          } else {
+            const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(st));
+            const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(st + L::kOffB));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc_mma_mxf8(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
+                          (kb != kb0 || j != 0) ? 1u : 0u);
+          }
           tc_commit(empty(stage));
-          if ((kb & 3) == 3 || kb == kb_end - 1) {
+          if ((kb & 3) == 3 || kb == kb1 - 1) {
             tc_commit(sfempty(slot));  // the pack's buffer and TMEM slot are free
             ++pack;
           }
@@ -560,8 +667,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Two cursors walk the same sequence of packs (tile, K block / 4): one
     // loads up to kSfLookahead packs ahead, the other lays them out in order.
     PackCursor<Scheduler<MODE>> ld, lay;
-    ld.init(sched, first_tile, tile_stride, kb_begin, kb_end);
-    lay.init(sched, first_tile, tile_stride, kb_begin, kb_end);
+    ld.init(sched, first_tile, tile_stride);
+    lay.init(sched, first_tile, tile_stride);
     uint32_t n_loaded = 0, n_laid = 0;
     bool ok = true;
     while (!lay.done && ok) {
@@ -574,11 +681,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (go) {
             const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
             const uint32_t bar = sffull(slot);
-            const int my = ld.tile.mb * kBlockM, kp = ld.kb >> 2;
+            const int my = ld.tile.mb * kBlockM, kp = ld.kp;
             mbar_arrive_expect_tx(bar, L::kTxSF);
             if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
             else tma_load_2d(buf + L::kRawA, &tm_sfa, bar, my, kp);
-            tma_load_3d(buf + L::kRawB, &tm_sfb, bar, ld.tile.nb * BN, kp, ld.tile.g);
+            tma_load_3d(buf + L::kRawB, &tm_sfb, bar, ld.tile.nb * BN, kp,
+                        MODE == kKGrouped ? 0 : ld.tile.g);
           }
         }
         go = __shfl_sync(0xffffffffu, go, 0);
@@ -645,15 +753,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         row_ok = gi == tile.g;
         if (gi >= 0 && gi != tile.g) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteContiguousIndex);
         out_row0 = row0;
+      } else if (MODE == kKGrouped) {
+        row_ok = row < args.m;
+        out_row0 = (int64_t)tile.g * args.m + row0;
       } else {
         row_ok = row < group_valid[tile.g];
         out_row0 = (int64_t)tile.g * args.m + row0;
       }
       // The TMA store clips at M and N, so dense quarters always use it; a
       // grouped quarter uses it only when every one of its rows is written.
-      const bool use_tma = (MODE == kDense) ? true : (__all_sync(0xffffffffu, row_ok) != 0);
+      const bool use_tma = (MODE == kDense)      ? true
+                           : (MODE == kKGrouped) ? false
+                                                 : (__all_sync(0xffffffffu, row_ok) != 0);
       __nv_bfloat16* drow = args.d + (out_row0 + lane) * args.ldd;
       const __nv_bfloat16* crow = args.c ? args.c + (out_row0 + lane) * args.ldc : nullptr;
+      // K-grouped: FP32 rows of D[g] / C[g]; a tile without K blocks writes C (or 0)
+      float* drow32 = MODE == kKGrouped ? args.d_f32 + (out_row0 + lane) * args.n : nullptr;
+      const float* crow32 =
+          (MODE == kKGrouped && args.c_f32) ? args.c_f32 + (out_row0 + lane) * args.n : nullptr;
+      bool k_empty = false;
+      if (MODE == kKGrouped) {
+        int kb0, kb1;
+        sched.k_range(tile, kb0, kb1);
+        k_empty = kb0 >= kb1;
+      }
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
       constexpr int NCH = BN / 32;
       // split-K roles for this quarter
@@ -700,6 +823,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         const int col0 = tile.nb * BN + ch * 32;
         if (col0 >= args.n) continue;
+        if (MODE == kKGrouped) {
+          if (row_ok)
+            store_row_chunk_f32(cur, drow32 + col0, crow32 ? crow32 + col0 : nullptr, args.n - col0,
+                                k_empty);
+          continue;
+        }
         if (use_tma) {
           uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
           if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
@@ -842,6 +971,11 @@ static cudaError_t gemm_launch_modes(int mode, const CUtensorMap& a, const CUten
     case kDense: return gemm_launch_impl<BN, STAGES, kDense>(a, b, sfa, sfb, d, args, grid, stream);
     case kContiguous: return gemm_launch_impl<BN, STAGES, kContiguous>(a, b, sfa, sfb, d, args, grid, stream);
     case kMasked: return gemm_launch_impl<BN, STAGES, kMasked>(a, b, sfa, sfb, d, args, grid, stream);
+    case kKGrouped:
+      // MN-major B tiles are whole 128-column boxes
+      if constexpr (BN % 128 == 0)
+        return gemm_launch_impl<BN, STAGES, kKGrouped>(a, b, sfa, sfb, d, args, grid, stream);
+      return cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;
 }

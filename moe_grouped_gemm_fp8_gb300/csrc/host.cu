@@ -417,6 +417,105 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
                                static_cast<cudaStream_t>(stream)));
 }
 
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa, const void* b,
+                                              const int32_t* sfb, const float* c, float* d,
+                                              const int32_t* ks, int64_t m, int64_t n,
+                                              int64_t sum_k, int32_t num_groups, void* stream) {
+  if (m < 0 || n < 0 || sum_k < 0 || num_groups < 0) return DG_ERR_INVALID_ARG;
+  if (m % 16 != 0 || n % 16 != 0 || sum_k % kBlockK != 0) return DG_ERR_ALIGNMENT;
+  if (m == 0 || n == 0 || num_groups == 0) return DG_OK;
+  if (num_groups > kMaxMaskedGroups) return DG_ERR_TOO_LARGE;
+  if (!d || !ks) return DG_ERR_INVALID_ARG;
+  if (!aligned16(d) || (c && !aligned16(c))) return DG_ERR_ALIGNMENT;
+  if (m >= kMaxCoord || n >= kMaxCoord || sum_k >= kMaxCoord ||
+      (int64_t)num_groups * m >= kMaxCoord)
+    return DG_ERR_TOO_LARGE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t out_bytes = (size_t)num_groups * (size_t)m * (size_t)n * sizeof(float);
+  if (sum_k == 0) {
+    // every expert is empty: D = C (or 0)
+    if (c == d) return DG_OK;
+    return from_cuda(c ? cudaMemcpyAsync(d, c, out_bytes, cudaMemcpyDeviceToDevice, st)
+                       : cudaMemsetAsync(d, 0, out_bytes, st));
+  }
+  if (!a || !sfa || !b || !sfb) return DG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb)) return DG_ERR_ALIGNMENT;
+  dg_status s;
+  int sms = 0;
+  if ((s = current_device(&sms)) != DG_OK) return s;
+  if ((s = get_encoder()) != DG_OK) return s;
+
+  GemmArgs args = {};
+  args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
+  // 128 or 256 columns (whole MN-major boxes): the compute-bound estimate
+  // over the average K blocks per expert
+  const int64_t kb_avg = std::max<int64_t>(1, sum_k / kBlockK / num_groups);
+  int block_n = 256;
+  {
+    const int forced = env_int("DG_BLOCK_N", 0);
+    if (forced == 128 || forced == 256) {
+      block_n = forced;
+    } else {
+      double best = 1e300;
+      for (int w : {128, 256}) {
+        const int64_t tiles = (int64_t)num_groups * args.m_blocks * ((n + w - 1) / w);
+        const double waves = (double)((tiles + sms - 1) / sms);
+        const double cost = waves * ((double)kb_avg + (w == 256 ? 4.0 : 0.5)) * w / (w == 256 ? 1.6 : 1.0);
+        if (cost < best * 0.999) {
+          best = cost;
+          block_n = w;
+        }
+      }
+    }
+  }
+  Operands o;
+  {
+    const int64_t kp = (sum_k / kBlockK + 3) / 4;
+    uint64_t dims_a[2] = {(uint64_t)m, (uint64_t)sum_k};
+    uint64_t str_a[1] = {(uint64_t)m};
+    uint32_t box[2] = {128, (uint32_t)kBlockK};
+    if ((s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a, dims_a, str_a, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
+      return s;
+    uint64_t dims_b[2] = {(uint64_t)n, (uint64_t)sum_k};
+    uint64_t str_b[1] = {(uint64_t)n};
+    if ((s = encode(&o.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b, dims_b, str_b, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
+      return s;
+    const int64_t m_pad = align4(m), n_pad = align4(n);
+    uint64_t dims_sa[2] = {(uint64_t)m_pad, (uint64_t)kp};
+    uint64_t str_sa[1] = {(uint64_t)(m_pad * 4)};
+    uint32_t box_sa[2] = {(uint32_t)kBlockM, 1};
+    if ((s = encode(&o.sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa, dims_sa, str_sa, box_sa,
+                    CU_TENSOR_MAP_SWIZZLE_NONE)) != DG_OK)
+      return s;
+    uint64_t dims_sb[3] = {(uint64_t)n_pad, (uint64_t)kp, 1};
+    uint64_t str_sb[2] = {(uint64_t)(n_pad * 4), (uint64_t)(kp * n_pad * 4)};
+    uint32_t box_sb[3] = {(uint32_t)block_n, 1, 1};
+    if ((s = encode(&o.sfb, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, sfb, dims_sb, str_sb, box_sb,
+                    CU_TENSOR_MAP_SWIZZLE_NONE)) != DG_OK)
+      return s;
+    o.d = o.a;  // the output is written with plain stores; the slot is unused
+  }
+  args.c_f32 = c;
+  args.d_f32 = d;
+  args.ks = ks;
+  args.m = (int32_t)m;
+  args.n = (int32_t)n;
+  args.k = (int32_t)sum_k;
+  args.num_groups = num_groups;
+  args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
+  args.k_blocks = (int32_t)(sum_k / kBlockK);
+  args.band = env_int("DG_RASTER_BAND", 16);
+  if (args.band < 1) args.band = 1;
+  args.timeout_ns = g_timeout_ns.load();
+  const int64_t tiles = (int64_t)num_groups * args.m_blocks * args.n_blocks;
+  if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  print_config("k_grouped_fp8_gemm_tn_contiguous", m, n, sum_k, num_groups, block_n, grid, args.band);
+  return from_cuda(gemm_launch(kKGrouped, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid, st));
+}
+
 dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b,
                                           const int32_t* sfb, void* d, const int32_t* masked_m,
                                           int32_t num_groups, int64_t max_m, int64_t n, int64_t k,
@@ -499,6 +598,22 @@ dg_status dg_quantize_fp8(const float* x, void* q, void* sf, int64_t groups, int
   if (s != DG_OK) return s;
   return from_cuda(quantize_launch(x, q, sf, groups, rows, cols, block_rows, sf_format,
                                    static_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_quantize_fp8_cols(const float* x, void* q, void* sf, int64_t rows, int64_t cols,
+                               int32_t sf_format, void* stream) {
+  if (rows < 0 || cols < 0) return DG_ERR_INVALID_ARG;
+  if (sf_format != DG_SF_FP32 && sf_format != DG_SF_UE8M0_PACKED) return DG_ERR_INVALID_ARG;
+  if (rows % kBlockK != 0 || cols % 4 != 0) return DG_ERR_ALIGNMENT;
+  if (rows == 0 || cols == 0) return DG_OK;
+  if (!x || !q || !sf) return DG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return DG_ERR_ALIGNMENT;
+  if (rows >= kMaxCoord * 16 || cols >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  int sms = 0;
+  dg_status s = current_device(&sms);
+  if (s != DG_OK) return s;
+  return from_cuda(quantize_cols_launch(x, q, sf, rows, cols, sf_format,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 dg_status dg_transform_sf(const float* sf, int32_t* packed, int64_t groups, int64_t mn, int64_t k,

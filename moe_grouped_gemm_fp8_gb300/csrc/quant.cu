@@ -138,6 +138,58 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const float* __restri
   }
 }
 
+// One scale per 128 rows of each column (operands whose reduction axis is the
+// row axis: A and B of the K-grouped GEMM).  Thread i of a CTA handles 4
+// adjacent columns over 512 rows (four 128-row blocks = one packed word per
+// column); a warp reads 512 contiguous bytes per row.  Each block is read
+// twice, once for the column maxima and once to encode (the second read hits
+// L2).
+template <bool kPacked>
+__global__ void __launch_bounds__(128) quant_cols_kernel(const float* __restrict__ x,
+                                                         uint8_t* __restrict__ q,
+                                                         void* __restrict__ sf, int64_t rows,
+                                                         int64_t cols, int64_t cols_pad,
+                                                         int rblocks) {
+  const int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  const int j = blockIdx.y;  // 512-row pack
+  if (c >= cols_pad) return;
+  uint32_t word[4] = {0u, 0u, 0u, 0u};
+  if (c < cols) {
+    for (int t = 0; t < 4; ++t) {
+      const int rb = 4 * j + t;
+      if (rb >= rblocks) break;
+      const float* xb = x + (int64_t)rb * 128 * cols + c;
+      float4 amax = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < 128; ++r) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(xb + (int64_t)r * cols));
+        amax.x = fmaxf(amax.x, fabsf(v.x));
+        amax.y = fmaxf(amax.y, fabsf(v.y));
+        amax.z = fmaxf(amax.z, fabsf(v.z));
+        amax.w = fmaxf(amax.w, fabsf(v.w));
+      }
+      const int e0 = scale_exponent(amax.x), e1 = scale_exponent(amax.y);
+      const int e2 = scale_exponent(amax.z), e3 = scale_exponent(amax.w);
+      uint8_t* qb = q + (int64_t)rb * 128 * cols + c;
+      for (int r = 0; r < 128; ++r) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(xb + (int64_t)r * cols));
+        const uint32_t lo = cvt_e4m3x2(scale_down(v.x, e0), scale_down(v.y, e1));
+        const uint32_t hi = cvt_e4m3x2(scale_down(v.z, e2), scale_down(v.w, e3));
+        *reinterpret_cast<uint32_t*>(qb + (int64_t)r * cols) = lo | (hi << 16);
+      }
+      word[0] |= (uint32_t)(e0 + 127) << (8 * t);
+      word[1] |= (uint32_t)(e1 + 127) << (8 * t);
+      word[2] |= (uint32_t)(e2 + 127) << (8 * t);
+      word[3] |= (uint32_t)(e3 + 127) << (8 * t);
+      if (!kPacked)
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(sf) + (int64_t)rb * cols + c) =
+            make_float4(pow2f(e0), pow2f(e1), pow2f(e2), pow2f(e3));
+    }
+  }
+  if (kPacked)
+    *reinterpret_cast<uint4*>(reinterpret_cast<int32_t*>(sf) + (int64_t)j * cols_pad + c) =
+        make_uint4(word[0], word[1], word[2], word[3]);
+}
+
 // Exponent of a power-of-two FP32 scale.  Returns false (and the exponent of
 // the next power of two up, or 0 for a non-positive / non-finite value) when
 // s is not an exact power of two within 2^-127 .. 2^127.
@@ -211,6 +263,20 @@ cudaError_t quantize_launch(const float* x, void* q, void* sf, int64_t groups, i
     else
       quant_blocks_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(x, (uint8_t*)q, sf, groups, rows, align4(rows), cols, kblocks, kpacks, rblocks);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t quantize_cols_launch(const float* x, void* q, void* sf, int64_t rows, int64_t cols,
+                                 int sf_format, cudaStream_t stream) {
+  const int rblocks = (int)(rows / 128);
+  const int kpacks = (rblocks + 3) / 4;
+  const int64_t cols_pad = align4(cols);
+  const int64_t threads = cols_pad / 4;
+  const dim3 grid((unsigned)((threads + 127) / 128), (unsigned)kpacks);
+  if (sf_format == DG_SF_UE8M0_PACKED)
+    quant_cols_kernel<true><<<grid, 128, 0, stream>>>(x, (uint8_t*)q, sf, rows, cols, cols_pad, rblocks);
+  else
+    quant_cols_kernel<false><<<grid, 128, 0, stream>>>(x, (uint8_t*)q, sf, rows, cols, cols_pad, rblocks);
   return cudaGetLastError();
 }
 

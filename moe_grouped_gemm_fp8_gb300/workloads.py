@@ -18,7 +18,10 @@ por meio de scaling granular", section "GEMM denso e grouped"):
   padding rows zero in A and tagged -1 in ``m_indices``;
 * masked M-grouped: 16 experts of capacity 256, B [16, 7168, 2048];
   ``masked_m`` uniform in [0, 256]; every row of A is random (rows past
-  ``masked_m`` hold data the GEMM must ignore).
+  ``masked_m`` hold data the GEMM must ignore);
+* K-grouped (MoE weight gradients): 8 experts, M=4096, N=7168; per-expert
+  token counts uniform in [256, 8192], each padded to a multiple of 128 rows
+  along K, the padding rows zero in both operands.
 
 A, B and C entries are N(0, 1).
 """
@@ -107,6 +110,35 @@ def masked(num_groups: int, cap: int, n: int, k: int, seed: int,
     return Masked(a, b, mm)
 
 
+@dataclass
+class KGrouped:
+    a: torch.Tensor   # [sum_k, M] float32 (experts stacked along K), padding rows zero
+    b: torch.Tensor   # [sum_k, N] float32, padding rows zero
+    ks: torch.Tensor  # [G] int32 rows per expert incl. padding (multiples of 128)
+    counts: torch.Tensor  # [G] int64 real rows per expert
+
+
+def k_grouped(num_groups: int, m: int, n: int, seed: int, lo: int = 256, hi: int = 8192,
+              align: int = CONTIG_ALIGN, counts: Optional[list] = None) -> KGrouped:
+    g = _gen(seed)
+    if counts is None:
+        cnt = torch.randint(lo, hi + 1, (num_groups,), generator=g, dtype=torch.int64)
+    else:
+        cnt = torch.tensor(counts, dtype=torch.int64)
+    padded = (cnt + align - 1) // align * align
+    sum_k = int(padded.sum())
+    a = torch.zeros(sum_k, m, dtype=torch.float32)
+    b = torch.zeros(sum_k, n, dtype=torch.float32)
+    row = 0
+    for e in range(num_groups):
+        c_e = int(cnt[e])
+        if c_e:
+            a[row:row + c_e] = torch.randn(c_e, m, generator=g, dtype=torch.float32)
+            b[row:row + c_e] = torch.randn(c_e, n, generator=g, dtype=torch.float32)
+        row += int(padded[e])
+    return KGrouped(a, b, padded.to(torch.int32), cnt)
+
+
 # Named workloads with their seeds (one seed per shape, C drawn from seed+100).
 SMALL = dict(m=128, n=256, k=512, seed=0)
 PREFILL = [dict(m=4096, n=n, k=k, seed=1 + i) for i, (n, k) in enumerate(PREFILL_NK)]
@@ -114,3 +146,4 @@ DECODE = [dict(m=m, n=n, k=k, seed=(11 if m == 64 else 21) + i)
           for m in DECODE_M for i, (n, k) in enumerate(PREFILL_NK)]
 CONTIG = dict(num_groups=8, n=4096, k=7168, seed=31)
 MASKED = dict(num_groups=16, cap=256, n=7168, k=2048, seed=41)
+KGROUPED = dict(num_groups=8, m=4096, n=7168, seed=51)

@@ -92,3 +92,29 @@ def test_quantize_and_transform_host_checks(L):
     assert t(P, None, 1, 10, 128, 1, None) == INVALID
     assert t(P, C.c_void_p(0x1004), 1, 10, 128, 1, None) == ALIGN
     assert t(P, P, 0, 10, 128, 1, None) == DG_OK
+
+
+def test_k_grouped_host_checks(L):
+    kg = L.dg_k_grouped_fp8_gemm_tn_contiguous
+    # a, sfa, b, sfb, c, d, ks, m, n, sum_k, groups, stream
+    assert kg(P, P, P, P, None, P, P, 130, 256, 512, 4, None) == ALIGN     # m % 16
+    assert kg(P, P, P, P, None, P, P, 128, 250, 512, 4, None) == ALIGN     # n % 16
+    assert kg(P, P, P, P, None, P, P, 128, 256, 500, 4, None) == ALIGN     # sum_k % 128
+    assert kg(P, P, P, P, None, P, P, 0, 256, 512, 4, None) == DG_OK       # empty output
+    assert kg(P, P, P, P, None, P, P, 128, 256, 512, 0, None) == DG_OK
+    assert kg(P, P, P, P, None, P, P, 128, 256, 512, 513, None) == TOO_LARGE
+    assert kg(P, P, P, P, None, None, P, 128, 256, 512, 4, None) == INVALID  # d
+    assert kg(P, P, P, P, None, P, None, 128, 256, 512, 4, None) == INVALID  # ks
+    assert kg(None, P, P, P, None, P, P, 128, 256, 512, 4, None) == INVALID  # a with sum_k > 0
+    assert kg(P, P, P, P, None, C.c_void_p(0x1008), P, 128, 256, 512, 4, None) == ALIGN
+    assert kg(P, P, P, P, None, P, P, -16, 256, 512, 4, None) == INVALID
+
+
+def test_quantize_cols_host_checks(L):
+    qc = L.dg_quantize_fp8_cols
+    assert qc(P, P, P, 100, 16, 1, None) == ALIGN      # rows % 128
+    assert qc(P, P, P, 128, 18, 1, None) == ALIGN      # cols % 4
+    assert qc(P, P, P, 128, 16, 7, None) == INVALID    # format
+    assert qc(P, P, P, 0, 16, 1, None) == DG_OK
+    assert qc(None, P, P, 128, 16, 1, None) == INVALID
+    assert qc(P, C.c_void_p(0x1004), P, 128, 16, 1, None) == ALIGN
