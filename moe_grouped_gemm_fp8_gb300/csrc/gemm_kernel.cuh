@@ -341,6 +341,37 @@ __device__ __forceinline__ void store_row_chunk_f32(const uint32_t (&r)[32], flo
   }
 }
 
+// FP32 output: one 32 x 32 chunk of a warp's quarter as two 32 x 16 halves,
+// each written into a free staging buffer (64-byte rows, 16-byte piece j of
+// row r at r * 64 + 16 * (j ^ ((r >> 1) & 3)), the layout of
+// CU_TENSOR_MAP_SWIZZLE_64B) and TMA-stored at (col0 + 16 h, out_row0).  A
+// half that starts at or past n is skipped (n % 16 == 0).
+__device__ __forceinline__ void emit_chunk_tma_f32(const float (&f)[32], uint8_t* ebuf,
+                                                   uint32_t& nchunk, const CUtensorMap* tm_d,
+                                                   int col0, int n, int64_t out_row0, int lane) {
+  const uint32_t my_row_off = (uint32_t)lane * 64u;
+  const uint32_t my_swz = ((uint32_t)lane >> 1) & 3u;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (col0 + 16 * h >= n) break;
+    uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
+    if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<float4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz)) =
+          make_float4(f[16 * h + 4 * j], f[16 * h + 4 * j + 1], f[16 * h + 4 * j + 2],
+                      f[16 * h + 4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm_d, smem_u32(buf), col0 + 16 * h, (int32_t)out_row0);
+      bulk_commit_group();
+    }
+    ++nchunk;
+  }
+}
+
 // One 32 x 32 output chunk of a warp's quarter: + C (coalesced loads staged
 // through `buf`), round to BF16, write into `buf` with the 64-byte swizzle and
 // TMA-store it at (col0, out_row0).  `buf` must be free (its previous store
@@ -824,9 +855,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int col0 = tile.nb * BN + ch * 32;
         if (col0 >= args.n) continue;
         if (MODE == kKGrouped) {
-          if (row_ok)
+          // a quarter whose 32 rows all lie inside M goes through the TMA
+          // store; one that crosses M (into the next expert's rows) does not
+          if (row0 + 32 <= args.m) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = k_empty ? 0.0f : __uint_as_float(cur[i]);
+            if (crow32) {
+#pragma unroll
+              for (int p = 0; p < 8; ++p) {
+                if (col0 + 4 * p < args.n) {
+                  const float4 c4 = *reinterpret_cast<const float4*>(crow32 + col0 + 4 * p);
+                  f[4 * p] += c4.x;
+                  f[4 * p + 1] += c4.y;
+                  f[4 * p + 2] += c4.z;
+                  f[4 * p + 3] += c4.w;
+                }
+              }
+            }
+            emit_chunk_tma_f32(f, ebuf, nchunk, &tm_d, col0, args.n, out_row0, lane);
+          } else if (row_ok) {
             store_row_chunk_f32(cur, drow32 + col0, crow32 ? crow32 + col0 : nullptr, args.n - col0,
                                 k_empty);
+          }
           continue;
         }
         if (use_tma) {

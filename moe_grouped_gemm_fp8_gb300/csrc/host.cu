@@ -495,7 +495,14 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa,
     if ((s = encode(&o.sfb, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, sfb, dims_sb, str_sb, box_sb,
                     CU_TENSOR_MAP_SWIZZLE_NONE)) != DG_OK)
       return s;
-    o.d = o.a;  // the output is written with plain stores; the slot is unused
+    // FP32 D as a 2-D tensor [num_groups * m, n]: 16 x 32 boxes with the
+    // 64-byte swizzle the epilogue stages in
+    uint64_t dims_d[2] = {(uint64_t)n, (uint64_t)num_groups * (uint64_t)m};
+    uint64_t str_d[1] = {(uint64_t)(n * 4)};
+    uint32_t box_d[2] = {16, 32};
+    if ((s = encode(&o.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d, dims_d, str_d, box_d,
+                    CU_TENSOR_MAP_SWIZZLE_64B)) != DG_OK)
+      return s;
   }
   args.c_f32 = c;
   args.d_f32 = d;
