@@ -91,6 +91,28 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
                          const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
                          int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
 
+/* Dense GEMM in the other three operand layouts ("D = C + A @ B" with A
+ * logically [m, k] and B logically [k, n]; "n" = stored as is, "t" = stored
+ * transposed).  Scales, C, D, their layouts and all checks are as for
+ * dg_fp8_gemm_nt; only the storage of A and B differs:
+ *   nn:  a E4M3 [m, k] row stride lda >= k;  b E4M3 [k, n] row stride ldb >= n
+ *   tn:  a E4M3 [k, m] row stride lda >= m;  b E4M3 [k, n] row stride ldb >= n
+ *   tt:  a E4M3 [k, m] row stride lda >= m;  b E4M3 [n, k] row stride ldb >= k
+ * (lda, ldb % 16 == 0).  sfa is packed per row m, sfb per row n, exactly as
+ * for NT (the scale groups follow K whatever the storage).
+ * Cited: same page, section "GEMM denso e grouped" (fp8_gemm_{nt, nn, tn, tt})
+ * and section "Interface GEMM e restrições de layout" (the SM100 path supports
+ * the NT, TN, NN and TT memory layouts). */
+dg_status dg_fp8_gemm_nn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
+dg_status dg_fp8_gemm_tn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
+dg_status dg_fp8_gemm_tt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
+
 /* M-grouped, contiguous layout.  The token rows of all experts are
  * concatenated along M, each expert's segment padded to a multiple of 128 rows
  * (dg_get_mk_alignment_for_contiguous_layout); N and K are shared.

@@ -8,7 +8,10 @@ weight gradients (FP32 output).  The kernels live in libdg.so
 """
 from .api import (  # noqa: F401
     DGError,
+    fp8_gemm_nn,
     fp8_gemm_nt,
+    fp8_gemm_tn,
+    fp8_gemm_tt,
     get_device_error,
     get_mk_alignment_for_contiguous_layout,
     get_num_sms,

@@ -29,6 +29,9 @@ _st = C.c_int
 
 SIGNATURES = {
     "dg_fp8_gemm_nt": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
+    "dg_fp8_gemm_nn": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
+    "dg_fp8_gemm_tn": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
+    "dg_fp8_gemm_tt": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
     "dg_m_grouped_fp8_gemm_nt_contiguous": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p]),
     "dg_m_grouped_fp8_gemm_nt_masked": (_st, [_p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _i64, _p]),
     "dg_k_grouped_fp8_gemm_tn_contiguous": (_st, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i32, _p]),

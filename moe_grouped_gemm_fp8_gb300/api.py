@@ -201,6 +201,55 @@ def fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.
     return d
 
 
+def _dense_layout(layout: str, a, sfa, b, sfb, d, c, stream):
+    """Shared marshalling of fp8_gemm_{nn, tn, tt}: A is [M,K] ('n') or
+    [K,M] ('t'); B is [K,N] ('n') or [N,K] ('t')."""
+    _need(a, "a", FP8_DTYPES, 2)
+    _need(b, "b", FP8_DTYPES, 2)
+    _need(sfa, "sfa", (torch.int32,), 2)
+    _need(sfb, "sfb", (torch.int32,), 2)
+    a_t, b_t = layout[0] == "t", layout[1] == "t"
+    k, m = a.shape if a_t else a.shape[::-1]
+    n, kb = b.shape if b_t else b.shape[::-1]
+    if kb != k:
+        raise ValueError("K mismatch: a %s, b %s" % (tuple(a.shape), tuple(b.shape)))
+    if tuple(sfa.shape) != sf_packed_shape(m, k) or tuple(sfb.shape) != sf_packed_shape(n, k):
+        raise ValueError("scale shapes %s / %s, expected %s / %s" % (
+            tuple(sfa.shape), tuple(sfb.shape), sf_packed_shape(m, k), sf_packed_shape(n, k)))
+    if a.stride(1) != 1 or b.stride(1) != 1 or not sfa.is_contiguous() or not sfb.is_contiguous():
+        raise ValueError("a and b need a unit inner stride; scales must be contiguous")
+    if d is None:
+        d = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _need(d, "d", (torch.bfloat16,), 2)
+    if tuple(d.shape) != (m, n) or d.stride(1) != 1:
+        raise ValueError("d must be [M, N] with unit column stride")
+    if c is not None:
+        _need(c, "c", (torch.bfloat16,), 2)
+        if tuple(c.shape) != (m, n) or c.stride(1) != 1:
+            raise ValueError("c must be [M, N] with unit column stride")
+    fn = "dg_fp8_gemm_" + layout
+    st = getattr(_lib.lib(), fn)(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d), m, n, k,
+                                 a.stride(0), b.stride(0), c.stride(0) if c is not None else 0,
+                                 d.stride(0), _stream(stream))
+    _check(st, fn)
+    return d
+
+
+def fp8_gemm_nn(a, sfa, b, sfb, d=None, c=None, stream=None) -> torch.Tensor:
+    """D = C + A @ B with A [M,K] and B [K,N] (N innermost)."""
+    return _dense_layout("nn", a, sfa, b, sfb, d, c, stream)
+
+
+def fp8_gemm_tn(a, sfa, b, sfb, d=None, c=None, stream=None) -> torch.Tensor:
+    """D = C + A^T @ B with A stored [K,M] and B [K,N]."""
+    return _dense_layout("tn", a, sfa, b, sfb, d, c, stream)
+
+
+def fp8_gemm_tt(a, sfa, b, sfb, d=None, c=None, stream=None) -> torch.Tensor:
+    """D = C + A^T @ B^T with A stored [K,M] and B [N,K]."""
+    return _dense_layout("tt", a, sfa, b, sfb, d, c, stream)
+
+
 def m_grouped_fp8_gemm_nt_contiguous(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor,
                                      sfb: torch.Tensor, m_indices: torch.Tensor,
                                      d: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

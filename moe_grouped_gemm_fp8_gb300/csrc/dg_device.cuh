@@ -215,8 +215,9 @@ __device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr) {
   return smem_desc(saddr, 16384, 1024, 2);
 }
 
-// Instruction-descriptor bits marking A and B as MN-major ("transposed").
-constexpr uint32_t kIdescMnMajorAB = (1u << 15) | (1u << 16);
+// Instruction-descriptor bits marking A / B as MN-major ("transposed").
+constexpr uint32_t kIdescMnMajorA = 1u << 15;
+constexpr uint32_t kIdescMnMajorB = 1u << 16;
 
 // 32 rows x 16 bytes, row r at byte 16 r, no swizzle (source of a
 // 32x128b tcgen05.cp).  Core matrices (8 rows x 16 B) are 128 bytes apart.

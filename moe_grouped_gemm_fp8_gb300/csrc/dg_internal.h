@@ -16,8 +16,27 @@ constexpr int kBlockK = 128;  // K extent of one scale block / pipeline stage
 constexpr int kMaxMaskedGroups = 512;
 
 // kKGrouped: experts stacked along K (weight gradients), MN-major operands,
-// FP32 output [G, M, N].
-enum GemmMode : int { kDense = 0, kContiguous = 1, kMasked = 2, kKGrouped = 3 };
+// FP32 output [G, M, N].  kDense is the NT layout; kDenseNN / TN / TT are the
+// same dense GEMM with B, both, or A stored MN-major.
+enum GemmMode : int {
+  kDense = 0,
+  kContiguous = 1,
+  kMasked = 2,
+  kKGrouped = 3,
+  kDenseNN = 4,
+  kDenseTN = 5,
+  kDenseTT = 6,
+};
+__host__ __device__ constexpr bool is_dense_mode(int mode) {
+  return mode == kDense || mode == kDenseNN || mode == kDenseTN || mode == kDenseTT;
+}
+// A stored [K, M] (M innermost) / B stored [K, N] (N innermost)
+__host__ __device__ constexpr bool a_mn_major(int mode) {
+  return mode == kDenseTN || mode == kDenseTT || mode == kKGrouped;
+}
+__host__ __device__ constexpr bool b_mn_major(int mode) {
+  return mode == kDenseNN || mode == kDenseTN || mode == kKGrouped;
+}
 
 // Sites recorded with device errors (bits 8-23 of the error word).
 enum ErrorSite : uint32_t {

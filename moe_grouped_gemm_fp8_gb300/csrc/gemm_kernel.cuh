@@ -582,16 +582,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = full(stage);
           mbar_arrive_expect_tx(fb, L::kTxAB);
           const int kx = kb * kBlockK, my = tile.mb * kBlockM;
-          if constexpr (MODE == kKGrouped) {
-            // MN-major tiles of A [sum_k, M] and B [sum_k, N]: 128 K rows of
-            // 128 bytes per box; B's 256-column tile is two boxes 16 KB apart
-            tma_load_2d(sb, &tm_a, fb, my, kx);
+          // MN-major tiles ([K, M] / [K, N] storage): 128 K rows of 128 bytes
+          // per box; a 256-column B tile is two boxes 16 KB apart
+          if constexpr (a_mn_major(MODE)) tma_load_2d(sb, &tm_a, fb, my, kx);
+          else if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
+          else tma_load_2d(sb, &tm_a, fb, kx, my);
+          if constexpr (b_mn_major(MODE)) {
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h)
               tma_load_2d(sb + L::kOffB + h * 16384, &tm_b, fb, tile.nb * BN + h * 128, kx);
           } else {
-            if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
-            else tma_load_2d(sb, &tm_a, fb, kx, my);
             tma_load_3d(sb + L::kOffB, &tm_b, fb, kx, tile.nb * BN, tile.g);
           }
           issued |= 1u << stage;
@@ -654,23 +654,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t sel = (uint32_t)(kb & 3);
           const uint32_t idesc = idesc0 | (sel << 4) | (sel << 29);
-          if constexpr (MODE == kKGrouped) {
-            // MN-major operands: 8-row K groups 1024 bytes apart, 128-byte
-            // MN atoms 16 KB apart; a 32-deep K step is 4 groups (4096 bytes)
-            const uint64_t adesc = smem_desc_mnmajor_sw128(smem_u32(st));
-            const uint64_t bdesc = smem_desc_mnmajor_sw128(smem_u32(st + L::kOffB));
+          // K-major operands advance 32 bytes per 32-deep K step; MN-major
+          // ones 4 groups of 8 K rows (4096 bytes): descriptor units of 16 B
+          const uint64_t adesc = a_mn_major(MODE) ? smem_desc_mnmajor_sw128(smem_u32(st))
+                                                  : smem_desc_kmajor_sw128(smem_u32(st));
+          const uint64_t bdesc = b_mn_major(MODE) ? smem_desc_mnmajor_sw128(smem_u32(st + L::kOffB))
+                                                  : smem_desc_kmajor_sw128(smem_u32(st + L::kOffB));
+          constexpr uint32_t a_step = a_mn_major(MODE) ? 256u : 2u;
+          constexpr uint32_t b_step = b_mn_major(MODE) ? 256u : 2u;
+          constexpr uint32_t major_bits = (a_mn_major(MODE) ? kIdescMnMajorA : 0u) |
+                                          (b_mn_major(MODE) ? kIdescMnMajorB : 0u);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tc_mma_mxf8(d_tmem, adesc + 256 * j, bdesc + 256 * j, idesc | kIdescMnMajorAB, sf_tmem,
-                          sf_tmem + 4, (kb != kb0 || j != 0) ? 1u : 0u);
-          } else {
-            const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(st));
-            const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(st + L::kOffB));
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tc_mma_mxf8(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sf_tmem, sf_tmem + 4,
-                          (kb != kb0 || j != 0) ? 1u : 0u);
-          }
+          for (int j = 0; j < 4; ++j)
+            tc_mma_mxf8(d_tmem, adesc + a_step * j, bdesc + b_step * j, idesc | major_bits, sf_tmem,
+                        sf_tmem + 4, (kb != kb0 || j != 0) ? 1u : 0u);
           tc_commit(empty(stage));
           if ((kb & 3) == 3 || kb == kb1 - 1) {
             tc_commit(sfempty(slot));  // the pack's buffer and TMEM slot are free
@@ -776,7 +773,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row = row0 + lane;
       bool row_ok;
       int64_t out_row0;
-      if (MODE == kDense) {
+      if (is_dense_mode(MODE)) {
         row_ok = row < args.m;
         out_row0 = row0;
       } else if (MODE == kContiguous) {
@@ -793,7 +790,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // The TMA store clips at M and N, so dense quarters always use it; a
       // grouped quarter uses it only when every one of its rows is written.
-      const bool use_tma = (MODE == kDense)      ? true
+      const bool use_tma = is_dense_mode(MODE)   ? true
                            : (MODE == kKGrouped) ? false
                                                  : (__all_sync(0xffffffffu, row_ok) != 0);
       __nv_bfloat16* drow = args.d + (out_row0 + lane) * args.ldd;
@@ -912,7 +909,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
           }
-          emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, MODE == kDense, lane);
+          emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, is_dense_mode(MODE), lane);
           ++nchunk;
         } else if (row_ok) {
           store_row_chunk(cur, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
@@ -1022,10 +1019,23 @@ static cudaError_t gemm_launch_modes(int mode, const CUtensorMap& a, const CUten
     case kDense: return gemm_launch_impl<BN, STAGES, kDense>(a, b, sfa, sfb, d, args, grid, stream);
     case kContiguous: return gemm_launch_impl<BN, STAGES, kContiguous>(a, b, sfa, sfb, d, args, grid, stream);
     case kMasked: return gemm_launch_impl<BN, STAGES, kMasked>(a, b, sfa, sfb, d, args, grid, stream);
+    // MN-major B tiles are whole 128-column boxes; the other layouts are
+    // compiled at the widths 128 and 256 only
     case kKGrouped:
-      // MN-major B tiles are whole 128-column boxes
       if constexpr (BN % 128 == 0)
         return gemm_launch_impl<BN, STAGES, kKGrouped>(a, b, sfa, sfb, d, args, grid, stream);
+      return cudaErrorInvalidValue;
+    case kDenseNN:
+      if constexpr (BN % 128 == 0)
+        return gemm_launch_impl<BN, STAGES, kDenseNN>(a, b, sfa, sfb, d, args, grid, stream);
+      return cudaErrorInvalidValue;
+    case kDenseTN:
+      if constexpr (BN % 128 == 0)
+        return gemm_launch_impl<BN, STAGES, kDenseTN>(a, b, sfa, sfb, d, args, grid, stream);
+      return cudaErrorInvalidValue;
+    case kDenseTT:
+      if constexpr (BN % 128 == 0)
+        return gemm_launch_impl<BN, STAGES, kDenseTT>(a, b, sfa, sfb, d, args, grid, stream);
       return cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;

@@ -179,6 +179,47 @@ dg_status encode_a_3d(Operands& o, const void* a, const int32_t* sfa, int64_t gr
   }
 }
 
+// MN-major operand tiles ([K, MN] storage, MN innermost, row stride ld bytes):
+// boxes of 128 (MN) x 128 (K) with 128-byte swizzle.  The scale words are the
+// same as for the K-major forms.
+dg_status encode_a_mn(Operands& o, const void* a, const int32_t* sfa, int64_t m, int64_t k,
+                      int64_t lda) {
+  const int64_t kp = (k / kBlockK + 3) / 4;
+  const int64_t m_pad = align4(m);
+  {
+    uint64_t dims[2] = {(uint64_t)m, (uint64_t)k};
+    uint64_t strides[1] = {(uint64_t)lda};
+    uint32_t box[2] = {(uint32_t)kBlockM, (uint32_t)kBlockK};
+    dg_status s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != DG_OK) return s;
+  }
+  uint64_t dims[2] = {(uint64_t)m_pad, (uint64_t)kp};
+  uint64_t strides[1] = {(uint64_t)(m_pad * 4)};
+  uint32_t box[2] = {(uint32_t)kBlockM, 1};
+  return encode(&o.sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+dg_status encode_b_mn(Operands& o, const void* b, const int32_t* sfb, int64_t n, int64_t k,
+                      int64_t ldb, int block_n) {
+  const int64_t kp = (k / kBlockK + 3) / 4;
+  const int64_t n_pad = align4(n);
+  {
+    uint64_t dims[2] = {(uint64_t)n, (uint64_t)k};
+    uint64_t strides[1] = {(uint64_t)ldb};
+    uint32_t box[2] = {128, (uint32_t)kBlockK};
+    dg_status s = encode(&o.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != DG_OK) return s;
+  }
+  uint64_t dims[3] = {(uint64_t)n_pad, (uint64_t)kp, 1};
+  uint64_t strides[2] = {(uint64_t)(n_pad * 4), (uint64_t)(kp * n_pad * 4)};
+  uint32_t box[3] = {(uint32_t)block_n, 1, 1};
+  return encode(&o.sfb, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, sfb, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // Tile width along N.  Wider tiles cut the shared-memory and L2 traffic per
 // MMA and amortise the fixed cost of each MMA instruction; narrower tiles
 // leave fewer SMs idle in the last wave and, below 256 columns, keep two
@@ -187,10 +228,13 @@ dg_status encode_a_3d(Operands& o, const void* a, const int32_t* sfa, int64_t gr
 // DG_BLOCK_N forces a width.
 // m_blocks counts output-tile rows (128 rows, or 256 on a CTA pair) and
 // `slots` the tiles that run at once (SMs, or co-resident pairs).
+// whole_boxes: only the widths 128 and 256 (MN-major B tiles, other layouts).
 int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, bool with_c,
-                   bool pair) {
+                   bool pair, bool whole_boxes = false) {
   const int forced = env_int("DG_BLOCK_N", 0);
-  if (pair ? gemm2_block_n_supported(forced) : gemm_block_n_supported(forced)) return forced;
+  if (whole_boxes ? (forced == 128 || forced == 256)
+                  : (pair ? gemm2_block_n_supported(forced) : gemm_block_n_supported(forced)))
+    return forced;
   static const int widths[4] = {128, 192, 224, 256};
   static const double rate[4] = {1.0, 1.35, 1.5, 1.6};  // per-column MMA throughput
   // epilogue not overlapped with MMAs (only the single-accumulator width)
@@ -199,6 +243,7 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
   int best = pair ? 256 : 128;
   double best_cost = 1e300;
   for (int i = pair ? 1 : 0; i < 4; ++i) {
+    if (whole_boxes && widths[i] % 128 != 0) continue;
     const int64_t tiles = m_blocks * ((n + widths[i] - 1) / widths[i]);
     const int64_t waves = (tiles + sms - 1) / sms;
     const double cost = (double)waves * ((double)k_blocks + epi_blocks[i]) * widths[i] / rate[i];
@@ -261,15 +306,20 @@ using namespace dg;
 
 extern "C" {
 
-dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
-                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
-                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
+// Dense GEMM in one of the four operand layouts (mode kDense = NT, kDenseNN,
+// kDenseTN, kDenseTT).  Split-K and CTA pairs exist for NT only.
+static dg_status dense_gemm(int mode, const char* name, const void* a, const int32_t* sfa,
+                            const void* b, const int32_t* sfb, const void* c, void* d, int64_t m,
+                            int64_t n, int64_t k, int64_t lda, int64_t ldb, int64_t ldc,
+                            int64_t ldd, void* stream) {
   if (m < 0) return DG_ERR_INVALID_ARG;
   dg_status s = check_common_k_n(n, k);
   if (s != DG_OK) return s;
   if (m == 0 || n == 0) return DG_OK;
   if (!a || !sfa || !b || !sfb || !d) return DG_ERR_INVALID_ARG;
-  if (lda < k || ldb < k || ldd < n || (c && ldc < n)) return DG_ERR_INVALID_ARG;
+  if (lda < (a_mn_major(mode) ? m : k) || ldb < (b_mn_major(mode) ? n : k) || ldd < n ||
+      (c && ldc < n))
+    return DG_ERR_INVALID_ARG;
   if (lda % 16 || ldb % 16 || ldd % 8 || (c && ldc % 8)) return DG_ERR_ALIGNMENT;
   if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) ||
       (c && !aligned16(c)))
@@ -289,7 +339,8 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
     const int64_t kb = k / kBlockK;
     const int64_t tiles128 = (int64_t)args.m_blocks * ((n + 127) / 128);
     const int forced = env_int("DG_SPLIT_K", 0);
-    if (forced == 1 || forced == 2 || forced == 4) ksplit = forced;
+    if (mode != kDense) ksplit = 1;
+    else if (forced == 1 || forced == 2 || forced == 4) ksplit = forced;
     else if (tiles128 * 4 <= sms && kb >= 16) ksplit = 4;
     else if (tiles128 * 2 <= sms && kb >= 8) ksplit = 2;
     while (ksplit > 1) {
@@ -329,7 +380,8 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
   }
   // CTA pairs (256-row tiles) only on request (DG_CTA_PAIR=1): on the
   // measured shapes they match, not beat, single-CTA tiles.
-  const bool pair = sms >= 2 && args.m_blocks >= 2 && env_int("DG_CTA_PAIR", 0) == 1;
+  const bool pair = mode == kDense && sms >= 2 && args.m_blocks >= 2 &&
+                    env_int("DG_CTA_PAIR", 0) == 1;
   const int64_t p_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
   int block_n, clusters = 0;
   if (pair) {
@@ -339,12 +391,15 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
     if (clusters > limit) clusters = limit;
     if (clusters <= 0) return DG_ERR_CUDA;
   } else {
-    block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, c != nullptr, false);
+    block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, c != nullptr, false,
+                             mode != kDense);
   }
   Operands o;
-  if ((s = encode_a_2d(o, a, sfa, m, k, lda)) != DG_OK) return s;
-  if ((s = encode_b_side(o, b, sfb, 1, n, k, ldb, block_n, pair ? block_n / 2 : block_n)) != DG_OK)
-    return s;
+  s = a_mn_major(mode) ? encode_a_mn(o, a, sfa, m, k, lda) : encode_a_2d(o, a, sfa, m, k, lda);
+  if (s != DG_OK) return s;
+  s = b_mn_major(mode) ? encode_b_mn(o, b, sfb, n, k, ldb, block_n)
+                       : encode_b_side(o, b, sfb, 1, n, k, ldb, block_n, pair ? block_n / 2 : block_n);
+  if (s != DG_OK) return s;
   if ((s = encode_d(o, d, m, n, ldd)) != DG_OK) return s;
   args.c = static_cast<const __nv_bfloat16*>(c);
   args.d = static_cast<__nv_bfloat16*>(d);
@@ -368,9 +423,37 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
                                   static_cast<cudaStream_t>(stream)));
   }
   const int grid = (int)(tiles < sms ? tiles : sms);
-  print_config("fp8_gemm_nt", m, n, k, 1, block_n, grid, args.band);
-  return from_cuda(gemm_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
+  print_config(name, m, n, k, 1, block_n, grid, args.band);
+  return from_cuda(gemm_launch(mode, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                static_cast<cudaStream_t>(stream)));
+}
+
+dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
+  return dense_gemm(kDense, "fp8_gemm_nt", a, sfa, b, sfb, c, d, m, n, k, lda, ldb, ldc, ldd,
+                    stream);
+}
+
+dg_status dg_fp8_gemm_nn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
+  return dense_gemm(kDenseNN, "fp8_gemm_nn", a, sfa, b, sfb, c, d, m, n, k, lda, ldb, ldc, ldd,
+                    stream);
+}
+
+dg_status dg_fp8_gemm_tn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
+  return dense_gemm(kDenseTN, "fp8_gemm_tn", a, sfa, b, sfb, c, d, m, n, k, lda, ldb, ldc, ldd,
+                    stream);
+}
+
+dg_status dg_fp8_gemm_tt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                         const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                         int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
+  return dense_gemm(kDenseTT, "fp8_gemm_tt", a, sfa, b, sfb, c, d, m, n, k, lda, ldb, ldc, ldd,
+                    stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b,
@@ -469,32 +552,9 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa,
     }
   }
   Operands o;
+  if ((s = encode_a_mn(o, a, sfa, m, sum_k, m)) != DG_OK) return s;
+  if ((s = encode_b_mn(o, b, sfb, n, sum_k, n, block_n)) != DG_OK) return s;
   {
-    const int64_t kp = (sum_k / kBlockK + 3) / 4;
-    uint64_t dims_a[2] = {(uint64_t)m, (uint64_t)sum_k};
-    uint64_t str_a[1] = {(uint64_t)m};
-    uint32_t box[2] = {128, (uint32_t)kBlockK};
-    if ((s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a, dims_a, str_a, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
-      return s;
-    uint64_t dims_b[2] = {(uint64_t)n, (uint64_t)sum_k};
-    uint64_t str_b[1] = {(uint64_t)n};
-    if ((s = encode(&o.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b, dims_b, str_b, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
-      return s;
-    const int64_t m_pad = align4(m), n_pad = align4(n);
-    uint64_t dims_sa[2] = {(uint64_t)m_pad, (uint64_t)kp};
-    uint64_t str_sa[1] = {(uint64_t)(m_pad * 4)};
-    uint32_t box_sa[2] = {(uint32_t)kBlockM, 1};
-    if ((s = encode(&o.sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa, dims_sa, str_sa, box_sa,
-                    CU_TENSOR_MAP_SWIZZLE_NONE)) != DG_OK)
-      return s;
-    uint64_t dims_sb[3] = {(uint64_t)n_pad, (uint64_t)kp, 1};
-    uint64_t str_sb[2] = {(uint64_t)(n_pad * 4), (uint64_t)(kp * n_pad * 4)};
-    uint32_t box_sb[3] = {(uint32_t)block_n, 1, 1};
-    if ((s = encode(&o.sfb, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, sfb, dims_sb, str_sb, box_sb,
-                    CU_TENSOR_MAP_SWIZZLE_NONE)) != DG_OK)
-      return s;
     // FP32 D as a 2-D tensor [num_groups * m, n]: 16 x 32 boxes with the
     // 64-byte swizzle the epilogue stages in
     uint64_t dims_d[2] = {(uint64_t)n, (uint64_t)num_groups * (uint64_t)m};

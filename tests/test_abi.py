@@ -118,3 +118,16 @@ def test_quantize_cols_host_checks(L):
     assert qc(P, P, P, 0, 16, 1, None) == DG_OK
     assert qc(None, P, P, 128, 16, 1, None) == INVALID
     assert qc(P, C.c_void_p(0x1004), P, 128, 16, 1, None) == ALIGN
+
+
+def test_layout_host_checks(L):
+    for name, a_t, b_t in (("nn", False, False), ("tn", True, False), ("tt", True, True)):
+        fn = getattr(L, "dg_fp8_gemm_" + name)
+        # m=128, n=256, k=512: lda must cover M when A is stored [K, M], else K
+        lda_ok = 128 if a_t else 512
+        ldb_ok = 512 if b_t else 256
+        assert fn(P, P, P, P, None, P, 128, 256, 512, lda_ok - 16, ldb_ok, 0, 256, None) == INVALID
+        assert fn(P, P, P, P, None, P, 128, 256, 512, lda_ok, ldb_ok - 16, 0, 256, None) == INVALID
+        assert fn(P, P, P, P, None, P, 128, 256, 500, lda_ok, ldb_ok + 16, 0, 256, None) == ALIGN
+        assert fn(P, P, P, P, None, P, 0, 256, 512, lda_ok, ldb_ok, 0, 256, None) == DG_OK
+        assert fn(None, P, P, P, None, P, 128, 256, 512, lda_ok, ldb_ok, 0, 256, None) == INVALID
