@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--workload", default="prefill",
                    choices=["prefill", "decode", "contiguous", "masked", "kgrouped", "small"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--pdl", action="store_true",
+                   help="decode/masked/contiguous/kgrouped: launch with programmatic dependent launch")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-steps", type=int, default=0,
                    help="run this many untimed steps and exit (for an external profiler)")
@@ -444,6 +446,7 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
     HBM. A single launch after an L2 flush is timed too, as a second figure
     that includes the launch latency an isolated call pays."""
     flush = torch.zeros(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    dg.set_pdl(bool(args.pdl))
     hbm = peaks["hbm_gbs"]
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     cases = []
@@ -550,7 +553,7 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
         "data": "synthetic",
-        "config": {"workload": args.workload,
+        "config": {"workload": args.workload, "pdl": bool(args.pdl),
                    "l2": "inputs larger than L2: each case rotates over input copies totalling "
                          ">2.5x L2, launched back to back in a CUDA graph"},
         "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": achieved, "peak": peak,

@@ -251,6 +251,19 @@ int32_t dg_get_mk_alignment_for_contiguous_layout(void);
 dg_status dg_set_num_sms(int32_t n);
 int32_t dg_get_num_sms(void);
 
+/* Programmatic dependent launch (PDL), process-wide, off by default.  When on,
+ * every kernel of this library is launched with programmatic stream
+ * serialisation: it may start while the previous kernel on the stream is
+ * finishing, does its set-up (barriers, TMEM allocation, descriptor
+ * prefetch), then waits for that kernel's completion before reading global
+ * memory; and it lets the next kernel start its own set-up once its set-up is
+ * done.  Inside CUDA graphs the dependency becomes a programmatic edge.
+ * dg_set_pdl returns DG_ERR_INVALID_ARG for values other than 0 and 1.
+ * Cited: same page, section "Utilitários e variáveis de ambiente" (set_pdl /
+ * get_pdl). */
+dg_status dg_set_pdl(int32_t enable);
+int32_t dg_get_pdl(void);
+
 /* Limit of every bounded wait inside the kernels, in nanoseconds (default
  * 2e9).  Process-wide; applies to launches made after the call. */
 dg_status dg_set_wait_timeout_ns(uint64_t ns);

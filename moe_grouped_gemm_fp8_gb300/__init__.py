@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     get_device_error,
     get_mk_alignment_for_contiguous_layout,
     get_num_sms,
+    get_pdl,
     get_tma_aligned_size,
     k_grouped_fp8_gemm_tn_contiguous,
     m_grouped_fp8_gemm_nt_contiguous,
@@ -22,6 +23,7 @@ from .api import (  # noqa: F401
     quantize_fp8,
     quantize_fp8_cols,
     set_num_sms,
+    set_pdl,
     set_wait_timeout_ns,
     sf_packed_shape,
     transform_sf_into_required_layout,

@@ -42,6 +42,8 @@ SIGNATURES = {
     "dg_get_mk_alignment_for_contiguous_layout": (_i32, []),
     "dg_set_num_sms": (_st, [_i32]),
     "dg_get_num_sms": (_i32, []),
+    "dg_set_pdl": (_st, [_i32]),
+    "dg_get_pdl": (_i32, []),
     "dg_set_wait_timeout_ns": (_st, [C.c_uint64]),
     "dg_get_device_error": (_st, [_p, C.POINTER(C.c_uint64)]),
     "dg_status_string": (C.c_char_p, [_st]),

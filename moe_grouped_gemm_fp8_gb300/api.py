@@ -69,6 +69,15 @@ def get_num_sms() -> int:
     return int(_lib.lib().dg_get_num_sms())
 
 
+def set_pdl(enable: bool) -> None:
+    """Programmatic dependent launch for every kernel of the library."""
+    _check(_lib.lib().dg_set_pdl(1 if enable else 0), "dg_set_pdl")
+
+
+def get_pdl() -> bool:
+    return bool(_lib.lib().dg_get_pdl())
+
+
 def set_wait_timeout_ns(ns: int) -> None:
     _check(_lib.lib().dg_set_wait_timeout_ns(int(ns)), "dg_set_wait_timeout_ns")
 

@@ -104,6 +104,20 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
   }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Waits until the grids this launch depends on programmatically have completed
+// and their memory writes are visible.  Without such a dependency (PDL off, or
+// the previous work on the stream not launched by this library with PDL) it
+// returns at once.  Every thread that reads global memory another kernel may
+// have written executes it first.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the launches that depend on this grid start their own set-up (they
+// still wait for this grid's completion before reading its outputs).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- proxies
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

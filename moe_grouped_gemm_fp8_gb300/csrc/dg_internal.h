@@ -76,6 +76,7 @@ struct GemmArgs {
   const int32_t* ks;       // rows per expert along K, [num_groups]
   const float* c_f32;      // nullable, [num_groups, m, n]
   float* d_f32;            // [num_groups, m, n]
+  int32_t pdl;             // host side: launch with programmatic stream serialisation
 };
 
 // gemm.cu: dispatch over the tile widths compiled in gemm_bn*.cu (single CTA)
@@ -123,11 +124,12 @@ DG_DECLARE_GEMM_BN(256)
 
 // quant.cu
 cudaError_t quantize_launch(const float* x, void* q, void* sf, int64_t groups, int64_t rows,
-                            int64_t cols, int block_rows, int sf_format, cudaStream_t stream);
+                            int64_t cols, int block_rows, int sf_format, bool pdl,
+                            cudaStream_t stream);
 cudaError_t quantize_cols_launch(const float* x, void* q, void* sf, int64_t rows, int64_t cols,
-                                 int sf_format, cudaStream_t stream);
+                                 int sf_format, bool pdl, cudaStream_t stream);
 cudaError_t transform_sf_launch(const float* sf, int32_t* packed, int64_t groups, int64_t mn,
-                                int64_t k, int block_rows, cudaStream_t stream);
+                                int64_t k, int block_rows, bool pdl, cudaStream_t stream);
 cudaError_t quant_fetch_error(unsigned long long* word);  // reads and clears
 
 }  // namespace dg

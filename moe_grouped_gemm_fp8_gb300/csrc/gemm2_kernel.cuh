@@ -160,6 +160,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tm_sfb);
     tma_prefetch_desc(&tm_d);
   }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
+    tc_fence_before();
+  }
+  griddep_wait();  // see fp8_gemm_kernel
   if (MODE == kMasked && warp == 2) {
     for (int g = lane; g < args.num_groups; g += 32) {
       const int v = __ldg(args.masked_m + g);
@@ -177,15 +183,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tile_start[args.num_groups] = acc;
     }
   }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(tmem_slot), 512);
-    tmem_relinquish_pair();
-    tc_fence_before();
-  }
   __syncthreads();
   cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   PairScheduler<MODE> sched;
   sched.args = &args;
@@ -509,18 +511,20 @@ static cudaError_t gemm2_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
   const size_t smem = Gemm2Plan<BN, STAGES>::smem_bytes(MODE);
   cudaError_t e = set_smem_once<KernelTag<BN, STAGES, MODE, 1, 2>>(kern, smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = args.pdl ? 2 : 1;
   if (clusters <= 0) return cudaErrorInvalidValue;
   return cudaLaunchKernelEx(&cfg, kern, a, b, sfa, sfb, d, args);
 }

@@ -489,6 +489,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tm_sfb);
     tma_prefetch_desc(&tm_d);
   }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  // Set-up above overlaps the previous kernel's tail under PDL; from here on
+  // every thread may read what that kernel wrote.
+  griddep_wait();
   if (MODE == kMasked && warp == 2) {
     for (int g = lane; g < args.num_groups; g += 32) {
       const int v = __ldg(args.masked_m + g);
@@ -531,15 +539,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tile_start[args.num_groups] = acc;
     }
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-    tc_fence_before();
-  }
   __syncthreads();
   if (KSPLIT > 1) cluster_sync_all();  // every CTA's barriers exist before remote arrivals
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   // tile loop of this CTA (of this cluster, with split-K) and its K slice
   const uint32_t krank = KSPLIT > 1 ? cluster_ctarank() : 0u;
@@ -973,18 +977,27 @@ static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
   const size_t smem = GemmPlan<BN, STAGES, KSPLIT>::smem_bytes(MODE);
   cudaError_t e = set_smem_once<KernelTag<BN, STAGES, MODE, KSPLIT, 1>>(kern, smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = KSPLIT;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
+  if (KSPLIT > 1) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = KSPLIT;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
+  if (args.pdl) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = KSPLIT > 1 ? 1 : 0;
+  cfg.numAttrs = n_attr;
   return cudaLaunchKernelEx(&cfg, kern, a, b, sfa, sfb, d, args);
 }
 

@@ -24,6 +24,7 @@ constexpr int64_t kMaxCoord = (int64_t)1 << 31;  // TMA coordinates are 32-bit s
 
 std::atomic<int32_t> g_num_sms_limit{0};
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_pdl{0};
 
 struct DeviceInfo {
   std::once_flag once;
@@ -368,6 +369,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     args.band = env_int("DG_RASTER_BAND", 16);
     if (args.band < 1) args.band = 1;
     args.timeout_ns = g_timeout_ns.load();
+  args.pdl = g_pdl.load();
     const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
     int clusters = gemm_splitk_max_clusters(ksplit);
     if (clusters > sms / ksplit) clusters = sms / ksplit;
@@ -414,6 +416,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   args.band = env_int("DG_RASTER_BAND", 16) / (pair ? 2 : 1);
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
+  args.pdl = g_pdl.load();
   const int64_t tiles = (pair ? p_blocks : (int64_t)args.m_blocks) * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   if (pair) {
@@ -492,6 +495,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   args.band = env_int("DG_RASTER_BAND", 16);
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
+  args.pdl = g_pdl.load();
   const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
@@ -576,6 +580,7 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa,
   args.band = env_int("DG_RASTER_BAND", 16);
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
+  args.pdl = g_pdl.load();
   const int64_t tiles = (int64_t)num_groups * args.m_blocks * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
@@ -638,6 +643,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   args.k_blocks = (int32_t)(k / kBlockK);
   args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
+  args.pdl = g_pdl.load();
   if ((int64_t)num_groups * args.m_blocks * args.n_blocks >= kMaxCoord) return DG_ERR_TOO_LARGE;
   if (pair) {
     print_config("m_grouped_fp8_gemm_nt_masked (cta pair)", max_m, n, k, num_groups, block_n,
@@ -663,7 +669,7 @@ dg_status dg_quantize_fp8(const float* x, void* q, void* sf, int64_t groups, int
   int sms = 0;
   dg_status s = current_device(&sms);
   if (s != DG_OK) return s;
-  return from_cuda(quantize_launch(x, q, sf, groups, rows, cols, block_rows, sf_format,
+  return from_cuda(quantize_launch(x, q, sf, groups, rows, cols, block_rows, sf_format, g_pdl.load() != 0,
                                    static_cast<cudaStream_t>(stream)));
 }
 
@@ -679,7 +685,7 @@ dg_status dg_quantize_fp8_cols(const float* x, void* q, void* sf, int64_t rows, 
   int sms = 0;
   dg_status s = current_device(&sms);
   if (s != DG_OK) return s;
-  return from_cuda(quantize_cols_launch(x, q, sf, rows, cols, sf_format,
+  return from_cuda(quantize_cols_launch(x, q, sf, rows, cols, sf_format, g_pdl.load() != 0,
                                         static_cast<cudaStream_t>(stream)));
 }
 
@@ -694,7 +700,7 @@ dg_status dg_transform_sf(const float* sf, int32_t* packed, int64_t groups, int6
   int sms = 0;
   dg_status s = current_device(&sms);
   if (s != DG_OK) return s;
-  return from_cuda(transform_sf_launch(sf, packed, groups, mn, k, block_rows,
+  return from_cuda(transform_sf_launch(sf, packed, groups, mn, k, block_rows, g_pdl.load() != 0,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -720,6 +726,14 @@ int32_t dg_get_num_sms(void) {
   if (current_device(&sms) != DG_OK) return limit;
   return sms;
 }
+
+dg_status dg_set_pdl(int32_t enable) {
+  if (enable != 0 && enable != 1) return DG_ERR_INVALID_ARG;
+  g_pdl.store(enable);
+  return DG_OK;
+}
+
+int32_t dg_get_pdl(void) { return g_pdl.load(); }
 
 dg_status dg_set_wait_timeout_ns(uint64_t ns) {
   if (ns == 0) return DG_ERR_INVALID_ARG;

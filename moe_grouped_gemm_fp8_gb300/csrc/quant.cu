@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const float* __restrict
                                                          void* __restrict__ sf, int64_t groups,
                                                          int64_t rows, int64_t rows_out,
                                                          int64_t cols, int kblocks, int kpacks) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t w = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (w >= groups * rows_out * kpacks) return;
@@ -90,6 +92,8 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const float* __restri
                                                            int64_t cols, int kblocks, int kpacks,
                                                            int64_t rblocks) {
   __shared__ float red[8];
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t j = blockIdx.x % kpacks;
   const int64_t rb = (blockIdx.x / kpacks) % rblocks;
@@ -150,6 +154,8 @@ __global__ void __launch_bounds__(128) quant_cols_kernel(const float* __restrict
                                                          void* __restrict__ sf, int64_t rows,
                                                          int64_t cols, int64_t cols_pad,
                                                          int rblocks) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
   const int j = blockIdx.y;  // 512-row pack
   if (c >= cols_pad) return;
@@ -221,6 +227,8 @@ __global__ void __launch_bounds__(256) transform_sf_kernel(const float* __restri
                                                            int64_t mn_pad, int kblocks,
                                                            int kpacks, int block_rows,
                                                            int64_t mn_blocks) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= groups * kpacks * mn_pad) return;
   const int64_t r = idx % mn_pad;
@@ -242,8 +250,26 @@ __global__ void __launch_bounds__(256) transform_sf_kernel(const float* __restri
 
 static inline int64_t align4(int64_t x) { return (x + 3) / 4 * 4; }
 
+// Launches with programmatic stream serialisation when pdl is set.
+template <class Kern, class... Args>
+static cudaError_t launch(Kern kern, dim3 grid, unsigned threads, bool pdl, cudaStream_t stream,
+                          Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t quantize_launch(const float* x, void* q, void* sf, int64_t groups, int64_t rows,
-                            int64_t cols, int block_rows, int sf_format, cudaStream_t stream) {
+                            int64_t cols, int block_rows, int sf_format, bool pdl,
+                            cudaStream_t stream) {
   const int kblocks = (int)(cols / 128);
   const int kpacks = (kblocks + 3) / 4;
   const bool packed = sf_format == DG_SF_UE8M0_PACKED;
@@ -251,45 +277,38 @@ cudaError_t quantize_launch(const float* x, void* q, void* sf, int64_t groups, i
     const int64_t rows_out = packed ? align4(rows) : rows;
     const int64_t warps = groups * rows_out * kpacks;
     const int64_t blocks = (warps + 7) / 8;
-    if (packed)
-      quant_rows_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(x, (uint8_t*)q, sf, groups, rows, rows_out, cols, kblocks, kpacks);
-    else
-      quant_rows_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(x, (uint8_t*)q, sf, groups, rows, rows_out, cols, kblocks, kpacks);
+    return launch(packed ? quant_rows_kernel<true> : quant_rows_kernel<false>, dim3((unsigned)blocks),
+                  256, pdl, stream, x, (uint8_t*)q, sf, groups, rows, rows_out, cols, kblocks, kpacks);
   } else {
     const int64_t rblocks = (rows + 127) / 128;
     const int64_t blocks = groups * rblocks * kpacks;
-    if (packed)
-      quant_blocks_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(x, (uint8_t*)q, sf, groups, rows, align4(rows), cols, kblocks, kpacks, rblocks);
-    else
-      quant_blocks_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(x, (uint8_t*)q, sf, groups, rows, align4(rows), cols, kblocks, kpacks, rblocks);
+    return launch(packed ? quant_blocks_kernel<true> : quant_blocks_kernel<false>,
+                  dim3((unsigned)blocks), 256, pdl, stream, x, (uint8_t*)q, sf, groups, rows,
+                  align4(rows), cols, kblocks, kpacks, rblocks);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t quantize_cols_launch(const float* x, void* q, void* sf, int64_t rows, int64_t cols,
-                                 int sf_format, cudaStream_t stream) {
+                                 int sf_format, bool pdl, cudaStream_t stream) {
   const int rblocks = (int)(rows / 128);
   const int kpacks = (rblocks + 3) / 4;
   const int64_t cols_pad = align4(cols);
   const int64_t threads = cols_pad / 4;
   const dim3 grid((unsigned)((threads + 127) / 128), (unsigned)kpacks);
-  if (sf_format == DG_SF_UE8M0_PACKED)
-    quant_cols_kernel<true><<<grid, 128, 0, stream>>>(x, (uint8_t*)q, sf, rows, cols, cols_pad, rblocks);
-  else
-    quant_cols_kernel<false><<<grid, 128, 0, stream>>>(x, (uint8_t*)q, sf, rows, cols, cols_pad, rblocks);
-  return cudaGetLastError();
+  return launch(sf_format == DG_SF_UE8M0_PACKED ? quant_cols_kernel<true> : quant_cols_kernel<false>,
+                grid, 128, pdl, stream, x, (uint8_t*)q, sf, rows, cols, cols_pad, rblocks);
 }
 
 cudaError_t transform_sf_launch(const float* sf, int32_t* packed, int64_t groups, int64_t mn,
-                                int64_t k, int block_rows, cudaStream_t stream) {
+                                int64_t k, int block_rows, bool pdl, cudaStream_t stream) {
   const int kblocks = (int)((k + 127) / 128);
   const int kpacks = (kblocks + 3) / 4;
   const int64_t mn_pad = align4(mn);
   const int64_t mn_blocks = (mn + block_rows - 1) / block_rows;
   const int64_t total = groups * kpacks * mn_pad;
   const int64_t blocks = (total + 255) / 256;
-  transform_sf_kernel<<<(unsigned)blocks, 256, 0, stream>>>(sf, packed, groups, mn, mn_pad, kblocks, kpacks, block_rows, mn_blocks);
-  return cudaGetLastError();
+  return launch(transform_sf_kernel, dim3((unsigned)blocks), 256, pdl, stream, sf, packed, groups,
+                mn, mn_pad, kblocks, kpacks, block_rows, mn_blocks);
 }
 
 cudaError_t quant_fetch_error(unsigned long long* word) {

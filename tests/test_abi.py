@@ -131,3 +131,10 @@ def test_layout_host_checks(L):
         assert fn(P, P, P, P, None, P, 128, 256, 500, lda_ok, ldb_ok + 16, 0, 256, None) == ALIGN
         assert fn(P, P, P, P, None, P, 0, 256, 512, lda_ok, ldb_ok, 0, 256, None) == DG_OK
         assert fn(None, P, P, P, None, P, 128, 256, 512, lda_ok, ldb_ok, 0, 256, None) == INVALID
+
+
+def test_pdl_switch(L):
+    assert L.dg_get_pdl() == 0
+    assert L.dg_set_pdl(2) == INVALID
+    assert L.dg_set_pdl(1) == DG_OK and L.dg_get_pdl() == 1
+    assert L.dg_set_pdl(0) == DG_OK and L.dg_get_pdl() == 0
