@@ -586,6 +586,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fb = full(stage);
           mbar_arrive_expect_tx(fb, L::kTxAB);
           const int kx = kb * kBlockK, my = tile.mb * kBlockM;
+          if (args.debug_drop_load && blockIdx.x == 0 && t == first_tile &&
+              kb + 1 == args.debug_drop_load) {
+            // injected failure: the stage is armed but never filled
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           // MN-major tiles ([K, M] / [K, N] storage): 128 K rows of 128 bytes
           // per box; a 256-column B tile is two boxes 16 KB apart
           if constexpr (a_mn_major(MODE)) tma_load_2d(sb, &tm_a, fb, my, kx);

@@ -426,6 +426,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
                                   static_cast<cudaStream_t>(stream)));
   }
   const int grid = (int)(tiles < sms ? tiles : sms);
+  args.debug_drop_load = env_int("DG_DEBUG_DROP_LOAD", 0);
   print_config(name, m, n, k, 1, block_n, grid, args.band);
   return from_cuda(gemm_launch(mode, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                static_cast<cudaStream_t>(stream)));

@@ -1,0 +1,50 @@
+"""Failure detection on the GPU without a GPU fault: a test hook makes the
+producer of CTA 0 arm one pipeline stage without filling it, so the MMA
+issuer's bounded wait expires.  The launch must end by itself with
+DG_ERR_DEVICE_TIMEOUT recorded (read on the host), and the context must stay
+usable: the next launch is correct."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import moe_grouped_gemm_fp8_gb300 as dg
+import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+DG_ERR_DEVICE_TIMEOUT = 5
+# CTA 0's first expired wait may be the MMA issuer's wait for the unfilled
+# stage (3), the epilogue's wait for that tile's accumulator (4), the
+# producer's drain of the stage (6) or the MMA drain (5), whichever deadline
+# passes first
+SITES = {3, 4, 5, 6}
+
+
+def test_dropped_stage_times_out_and_context_survives():
+    M, N, K = 256, 256, 1024
+    g = torch.Generator().manual_seed(113)
+    a = torch.randn(M, K, generator=g); b = torch.randn(N, K, generator=g)
+    qa, _, sa = oracle.quantize(a.numpy(), 1)
+    qb, _, sb = oracle.quantize(b.numpy(), 128)
+    dev = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    assert dg.get_device_error()[0] == 0
+    dg.set_wait_timeout_ns(2_000_000)  # 2 ms
+    os.environ["DG_DEBUG_DROP_LOAD"] = "3"  # K block 2 of CTA 0's first tile
+    os.environ["DG_SPLIT_K"] = "1"  # the hook is in the single-CTA pipeline
+    try:
+        dg.fp8_gemm_nt(*dev)
+        st, word = dg.get_device_error()
+    finally:
+        os.environ.pop("DG_DEBUG_DROP_LOAD", None)
+        os.environ.pop("DG_SPLIT_K", None)
+        dg.set_wait_timeout_ns(2_000_000_000)
+    assert st == DG_ERR_DEVICE_TIMEOUT, (st, hex(word))
+    assert word & 0xFF == DG_ERR_DEVICE_TIMEOUT and (word >> 8) & 0xFFFF in SITES, hex(word)
+    assert (word >> 32) == 0  # recorded by CTA 0
+    # the context is intact: the same GEMM runs correctly (split-K path included)
+    d = dg.fp8_gemm_nt(*dev)
+    assert dg.get_device_error()[0] == 0
+    P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "after the injected timeout")
