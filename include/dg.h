@@ -91,6 +91,23 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
                          const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
                          int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
 
+/* Dense NT with arbitrary FP32 scales (no power-of-two requirement):
+ *   D[m, n] = C[m, n] + sum_kb (sum_{k in kb} A[m, k] B[n, k]) * sfa[kb][m] * sfb[n/128][kb]
+ *   sfa  float [ceil(k/128), align(m, 4)]: one scale per 1x128 group of A,
+ *        K-block-major ("transposed") and padded to 16 bytes per K block
+ *   sfb  float [ceil(n/128), k/128]: one scale per 128x128 block of B
+ *   a, b, c, d, strides and checks as dg_fp8_gemm_nt; sfa, sfb 4-byte aligned.
+ * The tensor core produces each 128-wide K block's FP32 partial sum in TMEM;
+ * it is scaled and accumulated in FP32 on the CUDA cores (two-level
+ * accumulation), so any finite scale is honoured exactly as the FP32
+ * product sfa * sfb.  128-column tiles.
+ * Cited: same page, section "Interface GEMM e restrições de layout" (FP32
+ * scale factors; LHS scales TMA-aligned and transposed); launch report on
+ * feifmx.com (Feb 2025), two-level accumulation with CUDA-core promotion. */
+dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b, const float* sfb,
+                                 const void* c, void* d, int64_t m, int64_t n, int64_t k,
+                                 int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
+
 /* Dense GEMM in the other three operand layouts ("D = C + A @ B" with A
  * logically [m, k] and B logically [k, n]; "n" = stored as is, "t" = stored
  * transposed).  Scales, C, D, their layouts and all checks are as for

@@ -10,6 +10,7 @@ from .api import (  # noqa: F401
     DGError,
     fp8_gemm_nn,
     fp8_gemm_nt,
+    fp8_gemm_nt_fp32_sf,
     fp8_gemm_tn,
     fp8_gemm_tt,
     get_device_error,

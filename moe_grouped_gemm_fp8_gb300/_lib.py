@@ -29,6 +29,7 @@ _st = C.c_int
 
 SIGNATURES = {
     "dg_fp8_gemm_nt": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
+    "dg_fp8_gemm_nt_fp32_sf": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
     "dg_fp8_gemm_nn": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
     "dg_fp8_gemm_tn": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
     "dg_fp8_gemm_tt": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),

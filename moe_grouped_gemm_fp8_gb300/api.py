@@ -210,6 +210,44 @@ def fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.
     return d
 
 
+def fp8_gemm_nt_fp32_sf(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,
+                        d: Optional[torch.Tensor] = None, c: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """D = C + A @ B.T with arbitrary FP32 scales: sfa float32 [ceil(K/128),
+    align(M, 4)] (one per 1x128 group of A, K-block-major), sfb float32
+    [ceil(N/128), K/128] (one per 128x128 block of B)."""
+    _need(a, "a", FP8_DTYPES, 2)
+    _need(b, "b", FP8_DTYPES, 2)
+    _need(sfa, "sfa", (torch.float32,), 2)
+    _need(sfb, "sfb", (torch.float32,), 2)
+    m, k = a.shape
+    n = b.shape[0]
+    if b.shape[1] != k:
+        raise ValueError("K mismatch: a %s, b %s" % (tuple(a.shape), tuple(b.shape)))
+    want_a = ((k + 127) // 128, get_tma_aligned_size(m, 4))
+    want_b = ((n + 127) // 128, k // 128)
+    if tuple(sfa.shape) != want_a or tuple(sfb.shape) != want_b:
+        raise ValueError("scale shapes %s / %s, expected %s / %s" % (
+            tuple(sfa.shape), tuple(sfb.shape), want_a, want_b))
+    if a.stride(1) != 1 or b.stride(1) != 1 or not sfa.is_contiguous() or not sfb.is_contiguous():
+        raise ValueError("a and b need unit stride along K; scales must be contiguous")
+    if d is None:
+        d = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _need(d, "d", (torch.bfloat16,), 2)
+    if tuple(d.shape) != (m, n) or d.stride(1) != 1:
+        raise ValueError("d must be [M, N] with unit column stride")
+    if c is not None:
+        _need(c, "c", (torch.bfloat16,), 2)
+        if tuple(c.shape) != (m, n) or c.stride(1) != 1:
+            raise ValueError("c must be [M, N] with unit column stride")
+    st = _lib.lib().dg_fp8_gemm_nt_fp32_sf(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                           m, n, k, a.stride(0), b.stride(0),
+                                           c.stride(0) if c is not None else 0, d.stride(0),
+                                           _stream(stream))
+    _check(st, "dg_fp8_gemm_nt_fp32_sf")
+    return d
+
+
 def _dense_layout(layout: str, a, sfa, b, sfb, d, c, stream):
     """Shared marshalling of fp8_gemm_{nn, tn, tt}: A is [M,K] ('n') or
     [K,M] ('t'); B is [K,N] ('n') or [N,K] ('t')."""

@@ -81,6 +81,10 @@ struct GemmArgs {
   // skips on its first tile, so that stage's barrier never completes and the
   // bounded waits must end the launch with DG_ERR_DEVICE_TIMEOUT; 0 = off.
   int32_t debug_drop_load;
+  // FP32-scale (promotion) form only
+  const float* sfa_f32;    // [ceil(k/128), sfa_ld]: per K block, one scale per row of A
+  const float* sfb_f32;    // [ceil(n/128), k/128]: one scale per 128 x 128 block of B
+  int32_t sfa_ld;          // align(m, 4)
 };
 
 // gemm.cu: dispatch over the tile widths compiled in gemm_bn*.cu (single CTA)
@@ -120,6 +124,9 @@ cudaError_t gemm_splitk_launch(int ksplit, const CUtensorMap& a, const CUtensorM
                                const CUtensorMap& d, GemmArgs args, int clusters,
                                cudaStream_t stream);
 int gemm_splitk_max_clusters(int ksplit);
+// gemm_promote.cu: arbitrary FP32 scales, partials promoted out of TMEM
+cudaError_t gemm_promote_launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
+                                const GemmArgs& args, int grid, cudaStream_t stream);
 DG_DECLARE_GEMM_BN(128)
 DG_DECLARE_GEMM_BN(192)
 DG_DECLARE_GEMM_BN(224)

@@ -439,6 +439,65 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
                     stream);
 }
 
+dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b, const float* sfb,
+                                 const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                                 int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
+  if (m < 0) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (m == 0 || n == 0) return DG_OK;
+  if (!a || !sfa || !b || !sfb || !d) return DG_ERR_INVALID_ARG;
+  if (lda < k || ldb < k || ldd < n || (c && ldc < n)) return DG_ERR_INVALID_ARG;
+  if (lda % 16 || ldb % 16 || ldd % 8 || (c && ldc % 8)) return DG_ERR_ALIGNMENT;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d) || (c && !aligned16(c)) ||
+      (reinterpret_cast<uintptr_t>(sfa) & 3u) || (reinterpret_cast<uintptr_t>(sfb) & 3u))
+    return DG_ERR_ALIGNMENT;
+  if (m >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  int sms = 0;
+  if ((s = current_device(&sms)) != DG_OK) return s;
+  if ((s = get_encoder()) != DG_OK) return s;
+  Operands o;
+  {
+    uint64_t dims_a[2] = {(uint64_t)k, (uint64_t)m};
+    uint64_t str_a[1] = {(uint64_t)lda};
+    uint32_t box[2] = {(uint32_t)kBlockK, (uint32_t)kBlockM};
+    if ((s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a, dims_a, str_a, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
+      return s;
+    uint64_t dims_b[3] = {(uint64_t)k, (uint64_t)n, 1};
+    uint64_t str_b[2] = {(uint64_t)ldb, (uint64_t)(n * ldb)};
+    uint32_t box_b[3] = {(uint32_t)kBlockK, 128, 1};
+    if ((s = encode(&o.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims_b, str_b, box_b,
+                    CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
+      return s;
+  }
+  if ((s = encode_d(o, d, m, n, ldd)) != DG_OK) return s;
+  GemmArgs args = {};
+  args.c = static_cast<const __nv_bfloat16*>(c);
+  args.d = static_cast<__nv_bfloat16*>(d);
+  args.ldc = c ? ldc : 0;
+  args.ldd = ldd;
+  args.m = (int32_t)m;
+  args.n = (int32_t)n;
+  args.k = (int32_t)k;
+  args.num_groups = 1;
+  args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
+  args.n_blocks = (int32_t)((n + 127) / 128);
+  args.k_blocks = (int32_t)(k / kBlockK);
+  args.band = env_int("DG_RASTER_BAND", 16);
+  if (args.band < 1) args.band = 1;
+  args.timeout_ns = g_timeout_ns.load();
+  args.pdl = g_pdl.load();
+  args.sfa_f32 = sfa;
+  args.sfb_f32 = sfb;
+  args.sfa_ld = (int32_t)align4(m);
+  const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
+  if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  print_config("fp8_gemm_nt_fp32_sf (promotion)", m, n, k, 1, 128, grid, args.band);
+  return from_cuda(gemm_promote_launch(o.a, o.b, o.d, args, grid, static_cast<cudaStream_t>(stream)));
+}
+
 dg_status dg_fp8_gemm_nn(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
                          const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
                          int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {

@@ -138,3 +138,12 @@ def test_pdl_switch(L):
     assert L.dg_set_pdl(2) == INVALID
     assert L.dg_set_pdl(1) == DG_OK and L.dg_get_pdl() == 1
     assert L.dg_set_pdl(0) == DG_OK and L.dg_get_pdl() == 0
+
+
+def test_fp32_scale_gemm_host_checks(L):
+    fn = L.dg_fp8_gemm_nt_fp32_sf
+    assert fn(P, P, P, P, None, P, 128, 256, 100, 112, 112, 0, 256, None) == ALIGN   # K % 128
+    assert fn(P, P, P, P, None, P, 0, 256, 512, 512, 512, 0, 256, None) == DG_OK
+    assert fn(P, None, P, P, None, P, 128, 256, 512, 512, 512, 0, 256, None) == INVALID
+    assert fn(P, C.c_void_p(0x1002), P, P, None, P, 128, 256, 512, 512, 512, 0, 256, None) == ALIGN
+    assert fn(P, P, P, P, None, P, 128, 256, 512, 256, 512, 0, 256, None) == INVALID  # lda < K
