@@ -358,15 +358,42 @@ def run_prefill_e2e(args, ranks, dg, shapes, dev):
         h2d += sum(hb[k].numel() * hb[k].element_size() for k in ("a", "c", "qb", "sfb"))
         d2h += 2 * s["m"] * s["n"] * 2
 
+    # Three streams: the host-to-device copies of shape i+1 and the
+    # device-to-host copies of shape i-1 run while shape i computes.  Events
+    # order every reuse of a device buffer across steps (a copy into an input
+    # waits for the previous step's kernels that read it; a GEMM writing D
+    # waits for the previous step's copy of D to the host).
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    n_sh = len(shapes)
+    used = [None] * n_sh     # compute done with shape i's inputs (previous step)
+    drained = [None] * n_sh  # D of shape i copied to the host (previous step)
+
     def step():
-        for s, (hb, dv) in zip(shapes, host):
-            for k in ("a", "c", "qb", "sfb"):
-                dv[k].copy_(hb[k], non_blocking=True)
+        for i, (s, (hb, dv)) in enumerate(zip(shapes, host)):
+            with torch.cuda.stream(s_in):
+                if used[i] is not None:
+                    s_in.wait_event(used[i])
+                for k in ("a", "c", "qb", "sfb"):
+                    dv[k].copy_(hb[k], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            comp.wait_event(ready)
+            if drained[i] is not None:
+                comp.wait_event(drained[i])
             dg.quantize_fp8(dv["a"], 1, out=(s["qa"], s["sfa"]))
             dg.fp8_gemm_nt(s["qa"], s["sfa"], dv["qb"], dv["sfb"], d=s["d"])
             dg.fp8_gemm_nt(s["qa"], s["sfa"], dv["qb"], dv["sfb"], d=s["d2"], c=dv["c"])
-            hb["d"].copy_(s["d"], non_blocking=True)
-            hb["d2"].copy_(s["d2"], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(comp)
+            used[i] = done
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                hb["d"].copy_(s["d"], non_blocking=True)
+                hb["d2"].copy_(s["d2"], non_blocking=True)
+                out = torch.cuda.Event()
+                out.record(s_out)
+            drained[i] = out
 
     for _ in range(2):
         step()
