@@ -41,7 +41,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="prefill",
-                   choices=["prefill", "decode", "contiguous", "masked", "kgrouped", "small"])
+                   choices=["prefill", "decode", "contiguous", "masked", "kgrouped", "fp32scales", "small"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--pdl", action="store_true",
                    help="decode/masked/contiguous/kgrouped: launch with programmatic dependent launch")
@@ -49,7 +49,7 @@ def parse_args():
     p.add_argument("--profile-steps", type=int, default=0,
                    help="run this many untimed steps and exit (for an external profiler)")
     p.add_argument("--shape", type=int, default=-1,
-                   help="prefill: restrict the step to this (N, K) index (profiling of one shape)")
+                   help="restrict the run to this shape index (profiling of one shape)")
     return p.parse_args()
 
 
@@ -509,6 +509,23 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
                for t in rotate((qa, sfa, qb, sfb, mi, d), byt)]
         cases.append(dict(name="contiguous G=%d valid_rows=%d padded_rows=%d n=%d k=%d" %
                           (G, valid, w.a.shape[0], n, k), fns=fns, flops=2.0 * valid * n * k, bytes=byt))
+    elif args.workload == "fp32scales":
+        # the prefill shapes through the FP32-scale (promotion) kernel; the
+        # scales are the quantiser's (powers of two), passed as FP32
+        for cfg in workloads.PREFILL:
+            m, n, k = cfg["m"], cfg["n"], cfg["k"]
+            w = workloads.dense(m, n, k, cfg["seed"])
+            qa, sa = dg.quantize_fp8(w.a.to(dev), 1, packed=False)
+            qb, sb = dg.quantize_fp8(w.b.to(dev), 128, packed=False)
+            fa = torch.zeros(k // 128, dg.get_tma_aligned_size(m, 4), dtype=torch.float32, device=dev)
+            fa[:, :m] = sa.t()
+            fb = sb.contiguous()
+            d = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+            byt = algorithmic_bytes_gemm(m, n, k, False)
+            fns = [(lambda t=t: dg.fp8_gemm_nt_fp32_sf(t[0], t[1], t[2], t[3], d=t[4]))
+                   for t in rotate((qa, fa, qb, fb, d), byt)]
+            cases.append(dict(name="fp32-scale dense m=%d n=%d k=%d" % (m, n, k), fns=fns,
+                              flops=2.0 * m * n * k, bytes=byt))
     elif args.workload == "kgrouped":
         cfg = workloads.KGROUPED
         w = workloads.k_grouped(cfg["num_groups"], cfg["m"], cfg["n"], cfg["seed"])
@@ -540,6 +557,8 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
                for t in rotate((qa, sfa, qb, sfb, mm, d), byt)]
         cases.append(dict(name="masked G=%d cap=%d valid_rows=%d n=%d k=%d" % (G, cap, valid, n, k),
                           fns=fns, flops=2.0 * valid * n * k, bytes=byt))
+    if args.shape >= 0:
+        cases = [cases[args.shape]]
     for c in cases:
         for _ in range(max(3, args.warmup)):
             for f in c["fns"]:

@@ -41,3 +41,58 @@ def test_masked_gemm_replays_with_new_counts():
         P.assert_close(P.bf16_to_f64(d)[wr], o[wr], "graph replay %s" % counts)
     st, word = dg.get_device_error()
     assert st == 0, hex(word)
+
+
+def _replay_matches_eager(fn, outs):
+    """fn() writes into the tensors `outs`; capture it once, zero the outputs,
+    replay, and require the results bit-identical to an eager call."""
+    fn()
+    torch.cuda.synchronize()
+    ref = [o.clone() for o in outs]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    for _ in range(2):
+        for o in outs:
+            o.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for o, r in zip(outs, ref):
+            assert torch.equal(o.view(torch.uint8), r.view(torch.uint8))
+    st, word = dg.get_device_error()
+    assert st == 0, hex(word)
+
+
+@pytest.mark.parametrize("split_k", ["1", "2"])
+def test_dense_quantise_and_gemm_capture(split_k, monkeypatch):
+    """Quantise + dense GEMM (single CTA, and the split-K cluster path) in one graph."""
+    monkeypatch.setenv("DG_SPLIT_K", split_k)
+    w = workloads.dense(64 if split_k == "2" else 512, 1024, 2048, seed=67)
+    a = w.a.cuda()
+    qb, sfb = dg.quantize_fp8(w.b.cuda(), 128)
+    qa = torch.empty(a.shape, dtype=torch.float8_e4m3fn, device="cuda")
+    sfa = torch.empty(dg.sf_packed_shape(a.shape[0], a.shape[1]), dtype=torch.int32, device="cuda")
+    d = torch.empty(a.shape[0], 1024, dtype=torch.bfloat16, device="cuda")
+
+    def fn():
+        dg.quantize_fp8(a, 1, out=(qa, sfa))
+        dg.fp8_gemm_nt(qa, sfa, qb, sfb, d=d)
+    _replay_matches_eager(fn, [d])
+
+
+def test_contiguous_and_k_grouped_capture():
+    cw = workloads.contiguous(3, 256, 512, seed=71, counts=[100, 0, 300])
+    qa, sfa = dg.quantize_fp8(cw.a.cuda(), 1)
+    qb, sfb = dg.quantize_fp8(cw.b.cuda(), 128)
+    mi = cw.m_indices.cuda()
+    d = torch.zeros(cw.a.shape[0], 256, dtype=torch.bfloat16, device="cuda")
+    kw = workloads.k_grouped(3, 128, 256, seed=73, counts=[200, 0, 64])
+    ka, ksa = dg.quantize_fp8_cols(kw.a.cuda())
+    kb, ksb = dg.quantize_fp8_cols(kw.b.cuda())
+    ks = kw.ks.cuda()
+    dk = torch.zeros(3, 128, 256, dtype=torch.float32, device="cuda")
+
+    def fn():
+        dg.m_grouped_fp8_gemm_nt_contiguous(qa, sfa, qb, sfb, mi, d=d)
+        dg.k_grouped_fp8_gemm_tn_contiguous(ka, ksa, kb, ksb, ks, d=dk)
+    _replay_matches_eager(fn, [d, dk])
