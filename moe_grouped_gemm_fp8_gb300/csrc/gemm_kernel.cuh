@@ -791,8 +791,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t nchunk = 0;  // chunks staged so far (buffer = nchunk & 1)
     int acc = 0;
     uint32_t acc_phase = 0;
-    uint32_t tile_iter = 0;  // split-K barrier phases
-    for (int t = first_tile; t < sched.total; t += tile_stride, ++tile_iter) {
+    uint32_t n_xchg = 0;  // split-K exchanges of this quarter so far (barrier phases)
+    for (int t = first_tile; t < sched.total; t += tile_stride) {
       Tile tile;
       if (!sched.get(t, tile)) continue;
       if (!warp_wait<kSuspendHintNs>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
@@ -833,12 +833,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         sched.k_range(tile, kb0, kb1);
         k_empty = kb0 >= kb1;
       }
+      // A quarter none of whose rows is written hands its accumulator back
+      // unread: no TMEM load, no exchange, no store.  For dense and K-grouped
+      // tiles the test (first row past M) is the same in every CTA of a
+      // split-K cluster, so all of them skip the same quarters.
+      const bool quarter_live = (is_dense_mode(MODE) || MODE == kKGrouped)
+                                    ? row0 < args.m
+                                    : __any_sync(0xffffffffu, row_ok) != 0;
+      if (!quarter_live) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(acc));
+        if (++acc == NUM_ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        continue;
+      }
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
       constexpr int NCH = BN / 32;
       // split-K roles for this quarter
       const int owner = KSPLIT > 1 ? quarter % KSPLIT : 0;
       const bool sender = KSPLIT > 1 && (int)krank != owner;
-      const uint32_t kpar = tile_iter & 1u;
+      const uint32_t kpar = n_xchg & 1u;
       uint32_t send_base = 0;
       if (KSPLIT > 1) {
         bool ok2;
@@ -953,6 +969,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               if (rr != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)rr));
           }
         }
+        ++n_xchg;
       }
       if (++acc == NUM_ACC) {
         acc = 0;
