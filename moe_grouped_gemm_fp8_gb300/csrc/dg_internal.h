@@ -70,6 +70,7 @@ struct GemmArgs {
   int32_t n_blocks;
   int32_t k_blocks;
   int32_t band;            // raster band height in M blocks
+  int32_t a_box_rows;      // rows of A per TMA box when M < 128 (dense), 0 = 128
   uint64_t timeout_ns;
   unsigned long long* err; // device error word
   // K-grouped form only

@@ -42,12 +42,15 @@
 //
 // Split-K (KSPLIT = 2 or 4, dense only, for problems with fewer output tiles
 // than SMs): a cluster of KSPLIT CTAs shares each output tile, CTA r taking a
-// slice of the K blocks aligned to scale packs.  Quarter q (32 rows) of the
-// tile belongs to CTA q % KSPLIT: every other CTA writes its FP32 partial of
-// that quarter into the owner's shared memory (distributed shared memory)
-// and arrives on the owner's barrier; the owner adds the partials in rank
-// order - the same order whatever the timing, so results are deterministic -
-// adds C, rounds to BF16 and stores.  No global scratch memory is used.
+// slice of ceil(K blocks / KSPLIT) K blocks (a slice may start inside a
+// scale pack; the pack is then loaded by both CTAs).  CTA r owns the r-th column
+// slice (BN / KSPLIT columns) of every 32-row quarter: each epilogue warp
+// writes the other slices of its FP32 partial into their owners' shared
+// memory (distributed shared memory) and arrives on their barriers, then adds
+// the partials of its own slice in rank order - the same order whatever the
+// timing, so results are deterministic - adds C, rounds to BF16 and stores.
+// All four epilogue warps of every CTA share the exchange and the stores.
+// No global scratch memory is used.
 // Every mbarrier wait is bounded; on expiry the kernel records an error,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #pragma once
@@ -105,11 +108,14 @@ struct GemmPlan {
   static constexpr int kSfBase = kNumAcc * BN;
   static_assert(kSfBase + kSfSlots * L::kSfCols <= 512, "TMEM over-subscribed");
   static_assert(KSPLIT == 1 || KSPLIT == 2 || KSPLIT == 4, "split-K over 1, 2 or 4 CTAs");
-  // split-K receive buffers: per owned quarter and per other CTA, 32 rows of
-  // BN FP32 partial sums, rows padded by 16 bytes (conflict-free row access)
-  static constexpr int kRecvRow = BN * 4 + 16;
-  static constexpr int kRecvSlot = 32 * kRecvRow;
-  static constexpr int kRecvBytes = KSPLIT > 1 ? (4 / KSPLIT) * (KSPLIT - 1) * kRecvSlot : 0;
+  // split-K: CTA r of a cluster owns columns [r, r + 1) * kSlice of every
+  // quarter.  Its receive buffer holds, per quarter and per other CTA, that
+  // CTA's FP32 partial of the slice: 32-column chunks of 32 rows, stored
+  // lane-interleaved (16-byte group j of row l at 512 j + 16 l) so that the
+  // remote stores and the owner's loads are both contiguous per warp.
+  static constexpr int kSlice = BN / KSPLIT;
+  static constexpr int kXSlot = 32 * kSlice * 4;
+  static constexpr int kRecvBytes = KSPLIT > 1 ? 4 * (KSPLIT - 1) * kXSlot : 0;
   static constexpr size_t smem_bytes(int mode) {
     return (size_t)STAGES * L::kStageBytes + (size_t)kSfSlots * L::kSfBufBytes + kEpiBytes +
            (size_t)kRecvBytes + 1024 + gemm_ctrl_bytes(STAGES, mode);
@@ -455,8 +461,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto tfull = [&](int a) { return smem_u32(bars + kB0 + a); };
   auto tempty = [&](int a) { return smem_u32(bars + kB0 + 2 + a); };
   const uint32_t drain = smem_u32(bars + kB0 + 4);
-  auto recv_full = [&](int q) { return smem_u32(bars + kB0 + 5 + q); };  // owner side
-  auto recv_free = [&](int q) { return smem_u32(bars + kB0 + 9 + q); };  // sender side
+  // split-K: quarter q's partials from the other CTAs have landed / every
+  // other CTA has consumed what this CTA sent it for quarter q
+  auto recv_full = [&](int q) { return smem_u32(bars + kB0 + 5 + q); };
+  auto recv_free = [&](int q) { return smem_u32(bars + kB0 + 9 + q); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kB0 + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
@@ -480,7 +488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) {
       mbar_init(recv_full(q), KSPLIT > 1 ? KSPLIT - 1 : 1);
-      mbar_init(recv_free(q), 1);
+      mbar_init(recv_free(q), KSPLIT > 1 ? KSPLIT - 1 : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -550,7 +558,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t krank = KSPLIT > 1 ? cluster_ctarank() : 0u;
   const int first_tile = (int)blockIdx.x / KSPLIT;
   const int tile_stride = (int)gridDim.x / KSPLIT;
-  const int kb_per = ((args.k_blocks + KSPLIT - 1) / KSPLIT + 3) / 4 * 4;
+  const int kb_per = (args.k_blocks + KSPLIT - 1) / KSPLIT;
   const int kb_begin = KSPLIT > 1 ? min(args.k_blocks, (int)krank * kb_per) : 0;
   const int kb_end = KSPLIT > 1 ? min(args.k_blocks, kb_begin + kb_per) : args.k_blocks;
 
@@ -568,6 +576,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // A single M block of fewer than 128 rows is loaded as a box of
+    // round_up(M, 8) rows: the rest of the A tile keeps stale bytes, which
+    // only reach accumulator rows that are never stored.
+    const uint32_t tx_ab = args.a_box_rows > 0 ? (uint32_t)(args.a_box_rows * kBlockK + L::kBytesB) : L::kTxAB;
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -585,7 +597,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t sb = smem_u32(smem + stage * L::kStageBytes);
           const uint32_t fb = full(stage);
-          mbar_arrive_expect_tx(fb, L::kTxAB);
+          mbar_arrive_expect_tx(fb, tx_ab);
           const int kx = kb * kBlockK, my = tile.mb * kBlockM;
           if (args.debug_drop_load && blockIdx.x == 0 && t == first_tile &&
               kb + 1 == args.debug_drop_load) {
@@ -851,24 +863,87 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
       constexpr int NCH = BN / 32;
-      // split-K roles for this quarter
-      const int owner = KSPLIT > 1 ? quarter % KSPLIT : 0;
-      const bool sender = KSPLIT > 1 && (int)krank != owner;
-      const uint32_t kpar = n_xchg & 1u;
-      uint32_t send_base = 0;
-      if (KSPLIT > 1) {
-        bool ok2;
-        if (sender) {
-          ok2 = warp_wait_cluster(recv_free(quarter), kpar ^ 1u, abort_flag, tmo, err,
-                                  kSiteSplitFree);
-          const int sslot = (int)krank < owner ? (int)krank : (int)krank - 1;
-          send_base = mapa_shared(smem_u32(recv + ((quarter / KSPLIT) * (KSPLIT - 1) + sslot) *
-                                                      P::kRecvSlot + lane * P::kRecvRow),
-                                  (uint32_t)owner);
-        } else {
-          ok2 = warp_wait_cluster(recv_full(quarter), kpar, abort_flag, tmo, err, kSiteSplitFull);
+      if constexpr (KSPLIT > 1) {
+        // Split-K exchange (dense tiles only).  Every CTA owns one column
+        // slice of this quarter: it sends the other slices of its partial to
+        // their owners, then adds the partials of its own slice in CTA-rank
+        // order (the same result whatever the timing) and stores them.
+        constexpr int SCH = P::kSlice / 32;  // chunks per slice
+        const uint32_t kpar = n_xchg & 1u;
+        const int ncol0 = tile.nb * BN;
+        // every owner has read what this warp sent it for the previous tile
+        if (n_xchg > 0 &&
+            !warp_wait_cluster(recv_free(quarter), kpar ^ 1u, abort_flag, tmo, err, kSiteSplitFree))
+          break;
+        for (int ch = 0; ch < NCH; ++ch) {
+          const int o = ch / SCH;
+          if (o == (int)krank || ncol0 + ch * 32 >= args.n) continue;
+          uint32_t v[32];
+          tc_ld_32x32b_x32(taddr + ch * 32, v);
+          tc_wait_ld_regs(v);
+          const int sslot = (int)krank < o ? (int)krank : (int)krank - 1;
+          const uint32_t dst = mapa_shared(
+              smem_u32(recv + (quarter * (KSPLIT - 1) + sslot) * P::kXSlot + (ch % SCH) * 4096 + lane * 16),
+              (uint32_t)o);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_cluster_v4(dst + j * 512, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
-        if (!ok2) break;
+        __syncwarp();
+        if (lane == 0)
+          for (int o = 0; o < KSPLIT; ++o)
+            if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_full(quarter), (uint32_t)o));
+        if (!warp_wait_cluster(recv_full(quarter), kpar, abort_flag, tmo, err, kSiteSplitFull)) break;
+#pragma unroll
+        for (int c = 0; c < SCH; ++c) {
+          const int ch = (int)krank * SCH + c;
+          const int col0 = ncol0 + ch * 32;
+          if (col0 >= args.n) break;
+          uint32_t v[32];
+          tc_ld_32x32b_x32(taddr + ch * 32, v);
+          tc_wait_ld_regs(v);
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = 0.0f;
+#pragma unroll
+          for (int rr = 0; rr < KSPLIT; ++rr) {
+            if (rr == (int)krank) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) f[i] += __uint_as_float(v[i]);
+            } else {
+              const int sslot = rr < (int)krank ? rr : rr - 1;
+              const uint8_t* src = recv + (quarter * (KSPLIT - 1) + sslot) * P::kXSlot + c * 4096 + lane * 16;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 w = *reinterpret_cast<const float4*>(src + j * 512);
+                f[4 * j] += w.x;
+                f[4 * j + 1] += w.y;
+                f[4 * j + 2] += w.z;
+                f[4 * j + 3] += w.w;
+              }
+            }
+          }
+          uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
+          if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+          __syncwarp();
+          emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, true, lane);
+          ++nchunk;
+        }
+        // all of this accumulator's columns have been read; the received
+        // partials have been consumed
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(tempty(acc));
+          for (int o = 0; o < KSPLIT; ++o)
+            if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)o));
+        }
+        ++n_xchg;
+        if (++acc == NUM_ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        continue;
       }
       uint32_t ra[32], rb[32];
       tc_ld_32x32b_x32(taddr, ra);
@@ -884,14 +959,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty(acc));
-        }
-        if (sender) {
-          // this CTA's FP32 partial of the chunk into the owner's shared memory
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_cluster_v4(send_base + ch * 128 + j * 16, cur[4 * j], cur[4 * j + 1],
-                                 cur[4 * j + 2], cur[4 * j + 3]);
-          continue;
         }
         const int col0 = tile.nb * BN + ch * 32;
         if (col0 >= args.n) continue;
@@ -926,58 +993,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
           __syncwarp();
           float f[32];
-          if (KSPLIT > 1) {
-            // partials added in CTA-rank order: the same result whatever the timing
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = 0.0f;
-#pragma unroll
-            for (int rr = 0; rr < KSPLIT; ++rr) {
-              if (rr == (int)krank) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) f[i] += __uint_as_float(cur[i]);
-              } else {
-                const int sslot = rr < (int)krank ? rr : rr - 1;
-                const uint8_t* src = recv + ((quarter / KSPLIT) * (KSPLIT - 1) + sslot) * P::kRecvSlot +
-                                     lane * P::kRecvRow + ch * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 v = *reinterpret_cast<const float4*>(src + j * 16);
-                  f[4 * j] += v.x;
-                  f[4 * j + 1] += v.y;
-                  f[4 * j + 2] += v.z;
-                  f[4 * j + 3] += v.w;
-                }
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
-          }
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
           emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, is_dense_mode(MODE), lane);
           ++nchunk;
         } else if (row_ok) {
           store_row_chunk(cur, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
         }
       }
-      if (KSPLIT > 1) {
-        __syncwarp();
-        if (lane == 0) {
-          if (sender) {
-            mbar_arrive_cluster(mapa_shared(recv_full(quarter), (uint32_t)owner));
-          } else {
-            for (int rr = 0; rr < KSPLIT; ++rr)
-              if (rr != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)rr));
-          }
-        }
-        ++n_xchg;
-      }
       if (++acc == NUM_ACC) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
-    // every TMA store issued here has completed before the CTA exits
-    if (lane == 0) bulk_wait_group<0>();
+    // every TMA store issued here has read its staging buffer before the CTA
+    // exits (the writes themselves complete before the grid does)
+    if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
   }
 

@@ -138,14 +138,15 @@ dg_status encode_b_side(Operands& o, const void* b, const int32_t* sfb, int64_t 
   }
 }
 
+// box_rows: rows per A box (kBlockM, or fewer for a single short M block).
 dg_status encode_a_2d(Operands& o, const void* a, const int32_t* sfa, int64_t m, int64_t k,
-                      int64_t lda) {
+                      int64_t lda, int box_rows = kBlockM) {
   const int64_t kp = (k / kBlockK + 3) / 4;
   const int64_t m_pad = align4(m);
   {
     uint64_t dims[2] = {(uint64_t)k, (uint64_t)m};
     uint64_t strides[1] = {(uint64_t)lda};
-    uint32_t box[2] = {(uint32_t)kBlockK, (uint32_t)kBlockM};
+    uint32_t box[2] = {(uint32_t)kBlockK, (uint32_t)box_rows};
     dg_status s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != DG_OK) return s;
@@ -334,7 +335,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
   // Split-K over a cluster of 2 or 4 CTAs when 128-column tiles would leave
   // most SMs idle (decode-sized M); DG_SPLIT_K = 1, 2 or 4 forces a factor.
-  // Every CTA's K slice (a multiple of 4 K blocks) must be non-empty.
+  // Every CTA's K slice (ceil(K blocks / factor) blocks) must be non-empty.
   int ksplit = 1;
   {
     const int64_t kb = k / kBlockK;
@@ -345,15 +346,19 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     else if (tiles128 * 4 <= sms && kb >= 16) ksplit = 4;
     else if (tiles128 * 2 <= sms && kb >= 8) ksplit = 2;
     while (ksplit > 1) {
-      const int64_t per = ((kb + ksplit - 1) / ksplit + 3) / 4 * 4;
+      const int64_t per = (kb + ksplit - 1) / ksplit;
       if ((ksplit - 1) * per < kb) break;
       ksplit /= 2;
     }
   }
+  // A single M block shorter than 128 rows loads only round_up(M, 8) rows of A
+  // per K block (dense NT; decode-sized M).
+  if (mode == kDense && m < kBlockM) args.a_box_rows = (int32_t)((m + 7) / 8 * 8);
   if (ksplit > 1) {
     const int block_n = 128;
     Operands o;
-    if ((s = encode_a_2d(o, a, sfa, m, k, lda)) != DG_OK) return s;
+    if ((s = encode_a_2d(o, a, sfa, m, k, lda, args.a_box_rows > 0 ? args.a_box_rows : kBlockM)) != DG_OK)
+      return s;
     if ((s = encode_b_side(o, b, sfb, 1, n, k, ldb, block_n, block_n)) != DG_OK) return s;
     if ((s = encode_d(o, d, m, n, ldd)) != DG_OK) return s;
     args.c = static_cast<const __nv_bfloat16*>(c);
@@ -397,7 +402,8 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
                              mode != kDense);
   }
   Operands o;
-  s = a_mn_major(mode) ? encode_a_mn(o, a, sfa, m, k, lda) : encode_a_2d(o, a, sfa, m, k, lda);
+  s = a_mn_major(mode) ? encode_a_mn(o, a, sfa, m, k, lda)
+                       : encode_a_2d(o, a, sfa, m, k, lda, args.a_box_rows > 0 ? args.a_box_rows : kBlockM);
   if (s != DG_OK) return s;
   s = b_mn_major(mode) ? encode_b_mn(o, b, sfb, n, k, ldb, block_n)
                        : encode_b_side(o, b, sfb, 1, n, k, ldb, block_n, pair ? block_n / 2 : block_n);

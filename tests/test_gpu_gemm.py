@@ -121,6 +121,31 @@ def test_dense_ragged(bn, with_c, M, N, K):
     _no_device_error()
 
 
+@pytest.mark.parametrize("ks", [1, 4])
+@pytest.mark.parametrize("M", [1, 7, 33, 64, 127])
+def test_short_m_block_ignores_stale_shared_memory(ks, M):
+    """A single M block shorter than 128 rows loads only round_up(M, 8) rows of
+    A; the rest of the A tile holds whatever an earlier launch left there.  A
+    launch whose A is all NaN codes runs first, then the short one must still
+    match the oracle on every row it writes."""
+    N, K = 392, 2048
+    nan_a = torch.full((512, K), 0x7F, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+    w = workloads.dense(M, N, K, seed=700 + M, with_c=True)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    o = oracle.gemm_nt(qa, sa, qb, sb, P.bf16_bits(w.c))
+    b_dev, sfb_dev = P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128)
+    ones = P.dev_packed_sf(np.ones((512, K // 128)), 512, K, 1)
+    buf = P.sentinel_like((M, N + 24))
+    d = buf[:, :N]
+    with block_n(128), split_k(ks):
+        dg.fp8_gemm_nt(nan_a, ones, b_dev, sfb_dev)
+        dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), b_dev, sfb_dev, d=d, c=w.c.cuda())
+    P.assert_close(P.bf16_to_f64(d), o, "M=%d after a NaN launch" % M)
+    assert (P.bf16_bits(buf[:, N:]) == P.SENTINEL_BITS).all()
+    _no_device_error()
+
+
 def test_dense_c_aliases_d():
     M, N, K = 192, 256, 512
     w = workloads.dense(M, N, K, seed=5, with_c=True)
@@ -303,6 +328,30 @@ def test_dense_split_k(ks, with_c, M, N, K):
         dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb),
                        P.dev_packed_sf(sb, N, K, 128), d=d, c=w.c.cuda() if with_c else None)
     P.assert_close(P.bf16_to_f64(d), o, "split-K %d %dx%dx%d" % (ks, M, N, K))
+    assert (P.bf16_bits(buf[:, N:]) == P.SENTINEL_BITS).all()
+    _no_device_error()
+
+
+@pytest.mark.parametrize("ks", [2, 4])
+def test_dense_split_k_many_tiles_per_cluster(ks):
+    """Few SMs, so each cluster runs many tiles in turn: the exchange buffers
+    are reused from tile to tile, and the last M block (44 rows) has quarters
+    with no rows, which every CTA of the cluster skips."""
+    M, N, K = 300, 392, 1536
+    w = workloads.dense(M, N, K, seed=900 + ks, with_c=True)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    o = oracle.gemm_nt(qa, sa, qb, sb, P.bf16_bits(w.c))
+    buf = P.sentinel_like((M, N + 24))
+    d = buf[:, :N]
+    dg.set_num_sms(2 * ks)
+    try:
+        with split_k(ks):
+            dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb),
+                           P.dev_packed_sf(sb, N, K, 128), d=d, c=w.c.cuda())
+    finally:
+        dg.set_num_sms(0)
+    P.assert_close(P.bf16_to_f64(d), o, "split-K %d, 2 clusters" % ks)
     assert (P.bf16_bits(buf[:, N:]) == P.SENTINEL_BITS).all()
     _no_device_error()
 
