@@ -312,9 +312,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-// Whole-cluster barrier (every thread of both CTAs).
+// Whole-cluster barrier (every thread of every CTA of the cluster).
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Whole-cluster barrier without memory ordering: only keeps every CTA
+// resident until all have arrived (data hand-offs are ordered by mbarriers).
+__device__ __forceinline__ void cluster_sync_all_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.

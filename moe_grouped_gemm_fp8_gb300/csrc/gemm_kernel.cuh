@@ -875,32 +875,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (n_xchg > 0 &&
             !warp_wait_cluster(recv_free(quarter), kpar ^ 1u, abort_flag, tmo, err, kSiteSplitFree))
           break;
+        // chunks sent to other CTAs; the next one's TMEM load overlaps the
+        // current one's remote stores (conditions are warp-uniform)
+        auto sent = [&](int ch) { return ch / SCH != (int)krank && ncol0 + ch * 32 < args.n; };
+        uint32_t va[32], vb[32];
+        if (sent(0)) tc_ld_32x32b_x32(taddr, va);
+#pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t(&cur)[32] = (ch & 1) ? vb : va;
+          uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
+          const bool here = sent(ch);
+          if (here) tc_wait_ld_regs(cur);
+          if (ch + 1 < NCH && sent(ch + 1)) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
+          if (!here) continue;
           const int o = ch / SCH;
-          if (o == (int)krank || ncol0 + ch * 32 >= args.n) continue;
-          uint32_t v[32];
-          tc_ld_32x32b_x32(taddr + ch * 32, v);
-          tc_wait_ld_regs(v);
           const int sslot = (int)krank < o ? (int)krank : (int)krank - 1;
           const uint32_t dst = mapa_shared(
               smem_u32(recv + (quarter * (KSPLIT - 1) + sslot) * P::kXSlot + (ch % SCH) * 4096 + lane * 16),
               (uint32_t)o);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            st_shared_cluster_v4(dst + j * 512, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            st_shared_cluster_v4(dst + j * 512, cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
         }
         __syncwarp();
         if (lane == 0)
           for (int o = 0; o < KSPLIT; ++o)
             if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_full(quarter), (uint32_t)o));
+        // the first chunk of the own slice is read from TMEM while waiting
+        if (ncol0 + (int)krank * P::kSlice < args.n) tc_ld_32x32b_x32(taddr + (int)krank * P::kSlice, va);
         if (!warp_wait_cluster(recv_full(quarter), kpar, abort_flag, tmo, err, kSiteSplitFull)) break;
 #pragma unroll
         for (int c = 0; c < SCH; ++c) {
           const int ch = (int)krank * SCH + c;
           const int col0 = ncol0 + ch * 32;
           if (col0 >= args.n) break;
-          uint32_t v[32];
-          tc_ld_32x32b_x32(taddr + ch * 32, v);
+          uint32_t(&v)[32] = va;
+          if (c > 0) tc_ld_32x32b_x32(taddr + ch * 32, v);
           tc_wait_ld_regs(v);
           float f[32];
 #pragma unroll
@@ -930,13 +940,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ++nchunk;
         }
         // all of this accumulator's columns have been read; the received
-        // partials have been consumed
+        // partials have been consumed.  After the CTA's last tile nobody
+        // waits for the buffers again (a remote release-arrive costs ~0.5 us).
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(tempty(acc));
-          for (int o = 0; o < KSPLIT; ++o)
-            if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)o));
+          if (t + tile_stride < sched.total)
+            for (int o = 0; o < KSPLIT; ++o)
+              if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)o));
         }
         ++n_xchg;
         if (++acc == NUM_ACC) {
@@ -1013,7 +1025,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncthreads();
-  if (KSPLIT > 1) cluster_sync_all();  // no CTA leaves while others may still reach its memory
+  // No CTA leaves while others may still reach its shared memory.  Every
+  // exchange into it has completed (its mbarrier waits acquired them), so
+  // the barrier needs no memory ordering (a release here would also wait for
+  // this CTA's outstanding global writes).
+  if (KSPLIT > 1) cluster_sync_all_relaxed();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
