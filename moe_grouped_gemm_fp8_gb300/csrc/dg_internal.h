@@ -101,6 +101,15 @@ cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUten
                         const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                         GemmArgs args, int grid, cudaStream_t stream);
 cudaError_t gemm_fetch_error(unsigned long long* word);  // reads and clears
+// 256-row tiles (dense NT): block_n 192 or 224; 0 stages = not compiled
+int gemm_tall_stages(int block_n);
+cudaError_t gemm_tall_launch(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                             const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
+                             GemmArgs args, int grid, cudaStream_t stream);
+cudaError_t gemm_tall_launch_impl(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                                  const CUtensorMap& sfa, const CUtensorMap& sfb,
+                                  const CUtensorMap& d, const GemmArgs& args, int grid,
+                                  cudaStream_t stream);
 
 // gemm_bn*.cu: one tile width each (compiled in parallel)
 #define DG_DECLARE_GEMM_BN(BN)                                                                  \

@@ -67,23 +67,26 @@ namespace dg {
 constexpr int kGemmThreads = 224;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_103
 
-template <int BN>
+// BM: rows of A per tile, 128 or 256 (two 128-row MMAs sharing B).
+template <int BN, int BM = kBlockM>
 struct GemmLayout {
+  static constexpr int kMH = BM / kBlockM;              // 128-row halves of the tile
   static constexpr int kSfbChunks = (BN + 127) / 128;  // 128-row chunks of B scales
-  static constexpr int kBytesA = kBlockM * kBlockK;
+  static constexpr int kBytesA = BM * kBlockK;
   static constexpr int kBytesB = BN * kBlockK;
   static constexpr int kOffB = kBytesA;
   static constexpr int kStageBytes = (kBytesA + kBytesB + 1023) / 1024 * 1024;
-  // scale buffer: TMA-loaded words of A (128) and B (BN), then the same words
+  // scale buffer: TMA-loaded words of A (BM) and B (BN), then the same words
   // in tcgen05.cp order
   static constexpr int kRawA = 0;
-  static constexpr int kRawB = 512;
+  static constexpr int kRawB = BM * 4;
   static constexpr int kCpA = kRawB + kSfbChunks * 512;
-  static constexpr int kCpB = kCpA + 512;
+  static constexpr int kCpB = kCpA + kMH * 512;
   static constexpr int kSfBufBytes = kCpB + kSfbChunks * 512;
   static constexpr uint32_t kTxAB = kBytesA + kBytesB;
-  static constexpr uint32_t kTxSF = 128 * 4 + BN * 4;
-  static constexpr int kSfCols = 4 + 4 * kSfbChunks;  // TMEM columns of one scale slot
+  static constexpr uint32_t kTxSF = BM * 4 + BN * 4;
+  // TMEM columns of one scale slot: A scales of each half, then B scales
+  static constexpr int kSfCols = 4 * kMH + 4 * kSfbChunks;
 };
 
 constexpr int kSfSlots = 4;      // scale buffers / TMEM scale slots
@@ -101,11 +104,12 @@ static constexpr size_t gemm_ctrl_bytes(int stages, int mode) {
 // once per pack - words landed (TMA), words laid out (scale warp), slot free
 // (tcgen05.commit after the pack's last MMA) - and every waiter visits every
 // pack in order, so no wait ever skips a phase.
-template <int BN, int STAGES, int KSPLIT = 1>
+template <int BN, int STAGES, int KSPLIT = 1, int BM = kBlockM>
 struct GemmPlan {
-  using L = GemmLayout<BN>;
-  static constexpr int kNumAcc = (2 * BN + kSfSlots * L::kSfCols <= 512) ? 2 : 1;
-  static constexpr int kSfBase = kNumAcc * BN;
+  using L = GemmLayout<BN, BM>;
+  // accumulators of BM x BN (kMH blocks of BN columns each)
+  static constexpr int kNumAcc = (2 * L::kMH * BN + kSfSlots * L::kSfCols <= 512) ? 2 : 1;
+  static constexpr int kSfBase = kNumAcc * L::kMH * BN;
   static_assert(kSfBase + kSfSlots * L::kSfCols <= 512, "TMEM over-subscribed");
   static_assert(KSPLIT == 1 || KSPLIT == 2 || KSPLIT == 4, "split-K over 1, 2 or 4 CTAs");
   // split-K: CTA r of a cluster owns columns [r, r + 1) * kSlice of every
@@ -429,17 +433,20 @@ __device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
   }
 }
 
-template <int BN, int STAGES, int MODE, int KSPLIT>
+template <int BN, int STAGES, int MODE, int KSPLIT, int BM = kBlockM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
                     const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
-  using L = GemmLayout<BN>;
-  using P = GemmPlan<BN, STAGES, KSPLIT>;
+  using L = GemmLayout<BN, BM>;
+  using P = GemmPlan<BN, STAGES, KSPLIT, BM>;
   constexpr int NUM_ACC = P::kNumAcc;
+  constexpr int MH = L::kMH;  // 128-row halves of a tile
   static_assert(KSPLIT == 1 || MODE == kDense, "split-K is for the dense form");
+  static_assert(BM == kBlockM || (BM == 2 * kBlockM && MODE == kDense && KSPLIT == 1),
+                "256-row tiles are for the dense NT form without split-K");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -598,7 +605,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sb = smem_u32(smem + stage * L::kStageBytes);
           const uint32_t fb = full(stage);
           mbar_arrive_expect_tx(fb, tx_ab);
-          const int kx = kb * kBlockK, my = tile.mb * kBlockM;
+          const int kx = kb * kBlockK, my = tile.mb * BM;
           if (args.debug_drop_load && blockIdx.x == 0 && t == first_tile &&
               kb + 1 == args.debug_drop_load) {
             // injected failure: the stage is armed but never filled
@@ -655,7 +662,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MH * BN);
         int kb0, kb1;
         sched.k_range(tile, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -687,10 +694,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           constexpr uint32_t b_step = b_mn_major(MODE) ? 256u : 2u;
           constexpr uint32_t major_bits = (a_mn_major(MODE) ? kIdescMnMajorA : 0u) |
                                           (b_mn_major(MODE) ? kIdescMnMajorB : 0u);
+          // a 256-row tile: the second half's A rows start 16 KB further
+          // (1024 descriptor units), its accumulator BN columns further
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tc_mma_mxf8(d_tmem, adesc + a_step * j, bdesc + b_step * j, idesc | major_bits, sf_tmem,
-                        sf_tmem + 4, (kb != kb0 || j != 0) ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < MH; ++h)
+              tc_mma_mxf8(d_tmem + h * BN, adesc + 1024u * h + a_step * j, bdesc + b_step * j,
+                          idesc | major_bits, sf_tmem + 4 * h, sf_tmem + 4 * MH,
+                          (kb != kb0 || j != 0) ? 1u : 0u);
           tc_commit(empty(stage));
           if ((kb & 3) == 3 || kb == kb1 - 1) {
             tc_commit(sfempty(slot));  // the pack's buffer and TMEM slot are free
@@ -732,7 +744,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (go) {
             const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
             const uint32_t bar = sffull(slot);
-            const int my = ld.tile.mb * kBlockM, kp = ld.kp;
+            const int my = ld.tile.mb * BM, kp = ld.kp;
             mbar_arrive_expect_tx(bar, L::kTxSF);
             if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
             else tma_load_2d(buf + L::kRawA, &tm_sfa, bar, my, kp);
@@ -755,10 +767,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       uint8_t* buf = sfbuf + slot * L::kSfBufBytes;
-      {
-        const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawA);
+#pragma unroll
+      for (int h = 0; h < MH; ++h) {
+        const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawA + h * 512);
         const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
-        *reinterpret_cast<uint4*>(buf + L::kCpA + lane * 16) = v;
+        *reinterpret_cast<uint4*>(buf + L::kCpA + h * 512 + lane * 16) = v;
       }
 #pragma unroll
       for (int c = 0; c < L::kSfbChunks; ++c) {
@@ -775,10 +788,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // this pack was loaded.
       if (lane == 0) {
         const uint32_t sft = tmem_base + (uint32_t)(P::kSfBase + slot * L::kSfCols);
-        tc_cp_32x128b_warpx4(sft, smem_desc_sf_chunk(smem_u32(buf + L::kCpA)));
+#pragma unroll
+        for (int h = 0; h < MH; ++h)
+          tc_cp_32x128b_warpx4(sft + 4 * h, smem_desc_sf_chunk(smem_u32(buf + L::kCpA + h * 512)));
 #pragma unroll
         for (int c = 0; c < L::kSfbChunks; ++c)
-          tc_cp_32x128b_warpx4(sft + 4 + 4 * c, smem_desc_sf_chunk(smem_u32(buf + L::kCpB + c * 512)));
+          tc_cp_32x128b_warpx4(sft + 4 * MH + 4 * c,
+                               smem_desc_sf_chunk(smem_u32(buf + L::kCpB + c * 512)));
         tc_commit(sfready(slot));
       }
       ++n_laid;
@@ -809,210 +825,216 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!sched.get(t, tile)) continue;
       if (!warp_wait<kSuspendHintNs>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
       tc_fence_after();
-      const int row0 = tile.mb * kBlockM + quarter * 32;
-      const int row = row0 + lane;
-      bool row_ok;
-      int64_t out_row0;
-      if (is_dense_mode(MODE)) {
-        row_ok = row < args.m;
-        out_row0 = row0;
-      } else if (MODE == kContiguous) {
-        const int gi = row < args.m ? __ldg(args.m_indices + row) : -1;
-        row_ok = gi == tile.g;
-        if (gi >= 0 && gi != tile.g) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteContiguousIndex);
-        out_row0 = row0;
-      } else if (MODE == kKGrouped) {
-        row_ok = row < args.m;
-        out_row0 = (int64_t)tile.g * args.m + row0;
-      } else {
-        row_ok = row < group_valid[tile.g];
-        out_row0 = (int64_t)tile.g * args.m + row0;
-      }
-      // The TMA store clips at M and N, so dense quarters always use it; a
-      // grouped quarter uses it only when every one of its rows is written.
-      const bool use_tma = is_dense_mode(MODE)   ? true
-                           : (MODE == kKGrouped) ? false
-                                                 : (__all_sync(0xffffffffu, row_ok) != 0);
-      __nv_bfloat16* drow = args.d + (out_row0 + lane) * args.ldd;
-      const __nv_bfloat16* crow = args.c ? args.c + (out_row0 + lane) * args.ldc : nullptr;
-      // K-grouped: FP32 rows of D[g] / C[g]; a tile without K blocks writes C (or 0)
-      float* drow32 = MODE == kKGrouped ? args.d_f32 + (out_row0 + lane) * args.n : nullptr;
-      const float* crow32 =
-          (MODE == kKGrouped && args.c_f32) ? args.c_f32 + (out_row0 + lane) * args.n : nullptr;
-      bool k_empty = false;
-      if (MODE == kKGrouped) {
-        int kb0, kb1;
-        sched.k_range(tile, kb0, kb1);
-        k_empty = kb0 >= kb1;
-      }
-      // A quarter none of whose rows is written hands its accumulator back
-      // unread: no TMEM load, no exchange, no store.  For dense and K-grouped
-      // tiles the test (first row past M) is the same in every CTA of a
-      // split-K cluster, so all of them skip the same quarters.
-      const bool quarter_live = (is_dense_mode(MODE) || MODE == kKGrouped)
-                                    ? row0 < args.m
-                                    : __any_sync(0xffffffffu, row_ok) != 0;
-      if (!quarter_live) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty(acc));
-        if (++acc == NUM_ACC) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-        continue;
-      }
-      const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
-      constexpr int NCH = BN / 32;
-      if constexpr (KSPLIT > 1) {
-        // Split-K exchange (dense tiles only).  Every CTA owns one column
-        // slice of this quarter: it sends the other slices of its partial to
-        // their owners, then adds the partials of its own slice in CTA-rank
-        // order (the same result whatever the timing) and stores them.
-        constexpr int SCH = P::kSlice / 32;  // chunks per slice
-        const uint32_t kpar = n_xchg & 1u;
-        const int ncol0 = tile.nb * BN;
-        // every owner has read what this warp sent it for the previous tile
-        if (n_xchg > 0 &&
-            !warp_wait_cluster(recv_free(quarter), kpar ^ 1u, abort_flag, tmo, err, kSiteSplitFree))
-          break;
-        // chunks sent to other CTAs; the next one's TMEM load overlaps the
-        // current one's remote stores (conditions are warp-uniform)
-        auto sent = [&](int ch) { return ch / SCH != (int)krank && ncol0 + ch * 32 < args.n; };
-        uint32_t va[32], vb[32];
-        if (sent(0)) tc_ld_32x32b_x32(taddr, va);
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-          uint32_t(&cur)[32] = (ch & 1) ? vb : va;
-          uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
-          const bool here = sent(ch);
-          if (here) tc_wait_ld_regs(cur);
-          if (ch + 1 < NCH && sent(ch + 1)) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
-          if (!here) continue;
-          const int o = ch / SCH;
-          const int sslot = (int)krank < o ? (int)krank : (int)krank - 1;
-          const uint32_t dst = mapa_shared(
-              smem_u32(recv + (quarter * (KSPLIT - 1) + sslot) * P::kXSlot + (ch % SCH) * 4096 + lane * 16),
-              (uint32_t)o);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_cluster_v4(dst + j * 512, cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
-        }
-        __syncwarp();
-        if (lane == 0)
-          for (int o = 0; o < KSPLIT; ++o)
-            if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_full(quarter), (uint32_t)o));
-        // the first chunk of the own slice is read from TMEM while waiting
-        if (ncol0 + (int)krank * P::kSlice < args.n) tc_ld_32x32b_x32(taddr + (int)krank * P::kSlice, va);
-        if (!warp_wait_cluster(recv_full(quarter), kpar, abort_flag, tmo, err, kSiteSplitFull)) break;
-#pragma unroll
-        for (int c = 0; c < SCH; ++c) {
-          const int ch = (int)krank * SCH + c;
-          const int col0 = ncol0 + ch * 32;
-          if (col0 >= args.n) break;
-          uint32_t(&v)[32] = va;
-          if (c > 0) tc_ld_32x32b_x32(taddr + ch * 32, v);
-          tc_wait_ld_regs(v);
-          float f[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) f[i] = 0.0f;
-#pragma unroll
-          for (int rr = 0; rr < KSPLIT; ++rr) {
-            if (rr == (int)krank) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) f[i] += __uint_as_float(v[i]);
-            } else {
-              const int sslot = rr < (int)krank ? rr : rr - 1;
-              const uint8_t* src = recv + (quarter * (KSPLIT - 1) + sslot) * P::kXSlot + c * 4096 + lane * 16;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 w = *reinterpret_cast<const float4*>(src + j * 512);
-                f[4 * j] += w.x;
-                f[4 * j + 1] += w.y;
-                f[4 * j + 2] += w.z;
-                f[4 * j + 3] += w.w;
-              }
-            }
-          }
-          uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
-          if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
-          __syncwarp();
-          emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, true, lane);
-          ++nchunk;
-        }
-        // all of this accumulator's columns have been read; the received
-        // partials have been consumed.  After the CTA's last tile nobody
-        // waits for the buffers again (a remote release-arrive costs ~0.5 us).
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(tempty(acc));
-          if (t + tile_stride < sched.total)
-            for (int o = 0; o < KSPLIT; ++o)
-              if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)o));
-        }
-        ++n_xchg;
-        if (++acc == NUM_ACC) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-        continue;
-      }
-      uint32_t ra[32], rb[32];
-      tc_ld_32x32b_x32(taddr, ra);
-#pragma unroll
-      for (int ch = 0; ch < NCH; ++ch) {
-        uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
-        uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
-        tc_wait_ld_regs(cur);
-        if (ch + 1 < NCH) {
-          tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
+      bool stop = false;
+      // the tile's 128-row halves in turn; TMEM goes back after the last one
+      for (int h = 0; h < MH; ++h) {
+        const bool last_half = h == MH - 1;
+        const int row0 = tile.mb * BM + h * kBlockM + quarter * 32;
+        const int row = row0 + lane;
+        bool row_ok;
+        int64_t out_row0;
+        if (is_dense_mode(MODE)) {
+          row_ok = row < args.m;
+          out_row0 = row0;
+        } else if (MODE == kContiguous) {
+          const int gi = row < args.m ? __ldg(args.m_indices + row) : -1;
+          row_ok = gi == tile.g;
+          if (gi >= 0 && gi != tile.g) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteContiguousIndex);
+          out_row0 = row0;
+        } else if (MODE == kKGrouped) {
+          row_ok = row < args.m;
+          out_row0 = (int64_t)tile.g * args.m + row0;
         } else {
-          // every column of this accumulator is in registers: hand it back
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty(acc));
+          row_ok = row < group_valid[tile.g];
+          out_row0 = (int64_t)tile.g * args.m + row0;
         }
-        const int col0 = tile.nb * BN + ch * 32;
-        if (col0 >= args.n) continue;
+        // The TMA store clips at M and N, so dense quarters always use it; a
+        // grouped quarter uses it only when every one of its rows is written.
+        const bool use_tma = is_dense_mode(MODE)   ? true
+                             : (MODE == kKGrouped) ? false
+                                                   : (__all_sync(0xffffffffu, row_ok) != 0);
+        __nv_bfloat16* drow = args.d + (out_row0 + lane) * args.ldd;
+        const __nv_bfloat16* crow = args.c ? args.c + (out_row0 + lane) * args.ldc : nullptr;
+        // K-grouped: FP32 rows of D[g] / C[g]; a tile without K blocks writes C (or 0)
+        float* drow32 = MODE == kKGrouped ? args.d_f32 + (out_row0 + lane) * args.n : nullptr;
+        const float* crow32 =
+            (MODE == kKGrouped && args.c_f32) ? args.c_f32 + (out_row0 + lane) * args.n : nullptr;
+        bool k_empty = false;
         if (MODE == kKGrouped) {
-          // a quarter whose 32 rows all lie inside M goes through the TMA
-          // store; one that crosses M (into the next expert's rows) does not
-          if (row0 + 32 <= args.m) {
-            float f[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = k_empty ? 0.0f : __uint_as_float(cur[i]);
-            if (crow32) {
-#pragma unroll
-              for (int p = 0; p < 8; ++p) {
-                if (col0 + 4 * p < args.n) {
-                  const float4 c4 = *reinterpret_cast<const float4*>(crow32 + col0 + 4 * p);
-                  f[4 * p] += c4.x;
-                  f[4 * p + 1] += c4.y;
-                  f[4 * p + 2] += c4.z;
-                  f[4 * p + 3] += c4.w;
-                }
-              }
-            }
-            emit_chunk_tma_f32(f, ebuf, nchunk, &tm_d, col0, args.n, out_row0, lane);
-          } else if (row_ok) {
-            store_row_chunk_f32(cur, drow32 + col0, crow32 ? crow32 + col0 : nullptr, args.n - col0,
-                                k_empty);
+          int kb0, kb1;
+          sched.k_range(tile, kb0, kb1);
+          k_empty = kb0 >= kb1;
+        }
+        // A quarter none of whose rows is written hands its accumulator back
+        // unread: no TMEM load, no exchange, no store.  For dense and K-grouped
+        // tiles the test (first row past M) is the same in every CTA of a
+        // split-K cluster, so all of them skip the same quarters.
+        const bool quarter_live = (is_dense_mode(MODE) || MODE == kKGrouped)
+                                      ? row0 < args.m
+                                      : __any_sync(0xffffffffu, row_ok) != 0;
+        if (!quarter_live) {
+          if (last_half) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(acc));
           }
           continue;
         }
-        if (use_tma) {
-          uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
-          if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
-          __syncwarp();
-          float f[32];
+        const uint32_t taddr =
+            tmem_base + (uint32_t)((acc * MH + h) * BN) + ((uint32_t)(quarter * 32) << 16);
+        constexpr int NCH = BN / 32;
+        if constexpr (KSPLIT > 1) {
+          // Split-K exchange (dense tiles only).  Every CTA owns one column
+          // slice of this quarter: it sends the other slices of its partial to
+          // their owners, then adds the partials of its own slice in CTA-rank
+          // order (the same result whatever the timing) and stores them.
+          constexpr int SCH = P::kSlice / 32;  // chunks per slice
+          const uint32_t kpar = n_xchg & 1u;
+          const int ncol0 = tile.nb * BN;
+          // every owner has read what this warp sent it for the previous tile
+          if (n_xchg > 0 &&
+              !warp_wait_cluster(recv_free(quarter), kpar ^ 1u, abort_flag, tmo, err, kSiteSplitFree)) {
+            stop = true;
+            break;
+          }
+          // chunks sent to other CTAs; the next one's TMEM load overlaps the
+          // current one's remote stores (conditions are warp-uniform)
+          auto sent = [&](int ch) { return ch / SCH != (int)krank && ncol0 + ch * 32 < args.n; };
+          uint32_t va[32], vb[32];
+          if (sent(0)) tc_ld_32x32b_x32(taddr, va);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
-          emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, is_dense_mode(MODE), lane);
-          ++nchunk;
-        } else if (row_ok) {
-          store_row_chunk(cur, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
+          for (int ch = 0; ch < NCH; ++ch) {
+            uint32_t(&cur)[32] = (ch & 1) ? vb : va;
+            uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
+            const bool here = sent(ch);
+            if (here) tc_wait_ld_regs(cur);
+            if (ch + 1 < NCH && sent(ch + 1)) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
+            if (!here) continue;
+            const int o = ch / SCH;
+            const int sslot = (int)krank < o ? (int)krank : (int)krank - 1;
+            const uint32_t dst = mapa_shared(
+                smem_u32(recv + (quarter * (KSPLIT - 1) + sslot) * P::kXSlot + (ch % SCH) * 4096 + lane * 16),
+                (uint32_t)o);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_shared_cluster_v4(dst + j * 512, cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
+          }
+          __syncwarp();
+          if (lane == 0)
+            for (int o = 0; o < KSPLIT; ++o)
+              if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_full(quarter), (uint32_t)o));
+          // the first chunk of the own slice is read from TMEM while waiting
+          if (ncol0 + (int)krank * P::kSlice < args.n) tc_ld_32x32b_x32(taddr + (int)krank * P::kSlice, va);
+          if (!warp_wait_cluster(recv_full(quarter), kpar, abort_flag, tmo, err, kSiteSplitFull)) {
+            stop = true;
+            break;
+          }
+#pragma unroll
+          for (int c = 0; c < SCH; ++c) {
+            const int ch = (int)krank * SCH + c;
+            const int col0 = ncol0 + ch * 32;
+            if (col0 >= args.n) break;
+            uint32_t(&v)[32] = va;
+            if (c > 0) tc_ld_32x32b_x32(taddr + ch * 32, v);
+            tc_wait_ld_regs(v);
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = 0.0f;
+#pragma unroll
+            for (int rr = 0; rr < KSPLIT; ++rr) {
+              if (rr == (int)krank) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) f[i] += __uint_as_float(v[i]);
+              } else {
+                const int sslot = rr < (int)krank ? rr : rr - 1;
+                const uint8_t* src = recv + (quarter * (KSPLIT - 1) + sslot) * P::kXSlot + c * 4096 + lane * 16;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 w = *reinterpret_cast<const float4*>(src + j * 512);
+                  f[4 * j] += w.x;
+                  f[4 * j + 1] += w.y;
+                  f[4 * j + 2] += w.z;
+                  f[4 * j + 3] += w.w;
+                }
+              }
+            }
+            uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
+            if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+            __syncwarp();
+            emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, true, lane);
+            ++nchunk;
+          }
+          // all of this accumulator's columns have been read; the received
+          // partials have been consumed.  After the CTA's last tile nobody
+          // waits for the buffers again (a remote release-arrive costs ~0.5 us).
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(tempty(acc));
+            if (t + tile_stride < sched.total)
+              for (int o = 0; o < KSPLIT; ++o)
+                if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)o));
+          }
+          ++n_xchg;
+          continue;
         }
-      }
+        uint32_t ra[32], rb[32];
+        tc_ld_32x32b_x32(taddr, ra);
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+          uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
+          uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
+          tc_wait_ld_regs(cur);
+          if (ch + 1 < NCH) {
+            tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
+          } else if (last_half) {
+            // every column of this accumulator is in registers: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(acc));
+          }
+          const int col0 = tile.nb * BN + ch * 32;
+          if (col0 >= args.n) continue;
+          if (MODE == kKGrouped) {
+            // a quarter whose 32 rows all lie inside M goes through the TMA
+            // store; one that crosses M (into the next expert's rows) does not
+            if (row0 + 32 <= args.m) {
+              float f[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) f[i] = k_empty ? 0.0f : __uint_as_float(cur[i]);
+              if (crow32) {
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                  if (col0 + 4 * p < args.n) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(crow32 + col0 + 4 * p);
+                    f[4 * p] += c4.x;
+                    f[4 * p + 1] += c4.y;
+                    f[4 * p + 2] += c4.z;
+                    f[4 * p + 3] += c4.w;
+                  }
+                }
+              }
+              emit_chunk_tma_f32(f, ebuf, nchunk, &tm_d, col0, args.n, out_row0, lane);
+            } else if (row_ok) {
+              store_row_chunk_f32(cur, drow32 + col0, crow32 ? crow32 + col0 : nullptr, args.n - col0,
+                                  k_empty);
+            }
+            continue;
+          }
+          if (use_tma) {
+            uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
+            if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+            __syncwarp();
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
+            emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, is_dense_mode(MODE), lane);
+            ++nchunk;
+          } else if (row_ok) {
+            store_row_chunk(cur, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
+          }
+        }
+      }  // halves
+      if (stop) break;
       if (++acc == NUM_ACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -1054,16 +1076,16 @@ static cudaError_t set_smem_once(Kern kern, size_t smem) {
   return e;
 }
 
-template <int BN, int STAGES, int MODE, int KSPLIT = 1>
+template <int BN, int STAGES, int MODE, int KSPLIT = 1, int BM = kBlockM>
 static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
                                     const CUtensorMap& sfa, const CUtensorMap& sfb,
                                     const CUtensorMap& d, const GemmArgs& args, int grid,
                                     cudaStream_t stream) {
-  static_assert(GemmPlan<BN, STAGES, KSPLIT>::smem_bytes(MODE) <= (size_t)kSmemLimit,
-                "shared memory over the per-CTA limit");
-  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT>;
-  const size_t smem = GemmPlan<BN, STAGES, KSPLIT>::smem_bytes(MODE);
-  cudaError_t e = set_smem_once<KernelTag<BN, STAGES, MODE, KSPLIT, 1>>(kern, smem);
+  using Plan = GemmPlan<BN, STAGES, KSPLIT, BM>;
+  static_assert(Plan::smem_bytes(MODE) <= (size_t)kSmemLimit, "shared memory over the per-CTA limit");
+  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT, BM>;
+  const size_t smem = Plan::smem_bytes(MODE);
+  cudaError_t e = set_smem_once<KernelTag<BN, STAGES, MODE, KSPLIT, BM == kBlockM ? 1 : 3>>(kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   unsigned n_attr = 0;

@@ -138,9 +138,10 @@ dg_status encode_b_side(Operands& o, const void* b, const int32_t* sfb, int64_t 
   }
 }
 
-// box_rows: rows per A box (kBlockM, or fewer for a single short M block).
+// box_rows: rows per A box (kBlockM, fewer for a single short M block, or
+// 256 for 256-row tiles); sf_rows: rows per scale box (kBlockM or 256).
 dg_status encode_a_2d(Operands& o, const void* a, const int32_t* sfa, int64_t m, int64_t k,
-                      int64_t lda, int box_rows = kBlockM) {
+                      int64_t lda, int box_rows = kBlockM, int sf_rows = kBlockM) {
   const int64_t kp = (k / kBlockK + 3) / 4;
   const int64_t m_pad = align4(m);
   {
@@ -154,7 +155,7 @@ dg_status encode_a_2d(Operands& o, const void* a, const int32_t* sfa, int64_t m,
   {
     uint64_t dims[2] = {(uint64_t)m_pad, (uint64_t)kp};
     uint64_t strides[1] = {(uint64_t)(m_pad * 4)};
-    uint32_t box[2] = {(uint32_t)kBlockM, 1};
+    uint32_t box[2] = {(uint32_t)sf_rows, 1};
     return encode(&o.sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa, dims, strides, box,
                   CU_TENSOR_MAP_SWIZZLE_NONE);
   }
@@ -255,6 +256,50 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
     }
   }
   return best;
+}
+
+// 256-row tiles (dense NT): estimated like choose_block_n, in the same units
+// (time of one K block of a 128 x 256 tile = 160), from measured rates: a
+// K block of a 256 x 192 tile costs ~223 units and of a 256 x 224 tile ~232;
+// the single accumulator's epilogue does not overlap the next tile (~8 and
+// ~10.5 K blocks, about twice that with C).  Returns the width, or 0 when no
+// 256-row tile beats `best_cost` (the 128-row estimate).
+int choose_tall_block_n(int64_t m, int64_t n, int64_t k_blocks, int slots, bool with_c,
+                        double best_cost) {
+  const int forced_m = env_int("DG_BLOCK_M", 0);
+  if (forced_m == 128) return 0;
+  const int forced_n = env_int("DG_BLOCK_N", 0);
+  if (forced_m == 256) return (forced_n == 192 || forced_n == 224) ? forced_n : 192;
+  if (forced_n != 0) return 0;  // a forced width means 128-row tiles
+  static const int widths[2] = {192, 224};
+  static const double per_kb[2] = {223.0, 232.0};
+  static const double epi[2] = {8.0, 10.5};
+  const int sms = slots > 0 ? slots : 1;
+  const int64_t m_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
+  int best = 0;
+  for (int i = 0; i < 2; ++i) {
+    const int64_t tiles = m_blocks * ((n + widths[i] - 1) / widths[i]);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double cost = (double)waves * ((double)k_blocks + epi[i] * (with_c ? 2.0 : 1.0)) * per_kb[i];
+    if (cost < best_cost * 0.97) {
+      best_cost = cost;
+      best = widths[i];
+    }
+  }
+  return best;
+}
+
+// Estimated cost of 128-row tiles of width bn (units of choose_tall_block_n).
+double dense_tile_cost(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, bool with_c, int bn) {
+  static const int widths[4] = {128, 192, 224, 256};
+  static const double rate[4] = {1.0, 1.35, 1.5, 1.6};
+  int i = 0;
+  while (i < 3 && widths[i] != bn) ++i;
+  const double epi = bn == 256 ? (with_c ? 10.0 : 4.0) : 0.5;
+  const int sms = slots > 0 ? slots : 1;
+  const int64_t tiles = m_blocks * ((n + bn - 1) / bn);
+  const int64_t waves = (tiles + sms - 1) / sms;
+  return (double)waves * ((double)k_blocks + epi) * bn / rate[i];
 }
 
 // Tile width for masked problems with few rows per group, which are bound by
@@ -401,8 +446,23 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, c != nullptr, false,
                              mode != kDense);
   }
+  // 256-row tiles (dense NT, more than one 128-row block) where the estimate
+  // says they are faster; DG_BLOCK_M=256 (with DG_BLOCK_N 192 or 224) or
+  // DG_BLOCK_M=128 forces the choice.
+  bool tall = false;
+  if (!pair && mode == kDense && args.m_blocks >= 2) {
+    const double cost128 =
+        dense_tile_cost(args.m_blocks, n, k / kBlockK, sms, c != nullptr, block_n);
+    const int tall_n = choose_tall_block_n(m, n, k / kBlockK, sms, c != nullptr, cost128);
+    if (tall_n != 0 && gemm_tall_stages(tall_n) > 0) {
+      tall = true;
+      block_n = tall_n;
+      args.m_blocks = (int32_t)((m + 2 * kBlockM - 1) / (2 * kBlockM));
+    }
+  }
   Operands o;
   s = a_mn_major(mode) ? encode_a_mn(o, a, sfa, m, k, lda)
+      : tall           ? encode_a_2d(o, a, sfa, m, k, lda, 2 * kBlockM, 2 * kBlockM)
                        : encode_a_2d(o, a, sfa, m, k, lda, args.a_box_rows > 0 ? args.a_box_rows : kBlockM);
   if (s != DG_OK) return s;
   s = b_mn_major(mode) ? encode_b_mn(o, b, sfb, n, k, ldb, block_n)
@@ -419,7 +479,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   args.num_groups = 1;
   args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
   args.k_blocks = (int32_t)(k / kBlockK);
-  args.band = env_int("DG_RASTER_BAND", 16) / (pair ? 2 : 1);
+  args.band = env_int("DG_RASTER_BAND", 16) / ((pair || tall) ? 2 : 1);
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
   args.pdl = g_pdl.load();
@@ -433,7 +493,10 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   }
   const int grid = (int)(tiles < sms ? tiles : sms);
   args.debug_drop_load = env_int("DG_DEBUG_DROP_LOAD", 0);
-  print_config(name, m, n, k, 1, block_n, grid, args.band);
+  print_config(tall ? "fp8_gemm_nt (256-row tiles)" : name, m, n, k, 1, block_n, grid, args.band);
+  if (tall)
+    return from_cuda(gemm_tall_launch(block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
+                                      static_cast<cudaStream_t>(stream)));
   return from_cuda(gemm_launch(mode, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                static_cast<cudaStream_t>(stream)));
 }

@@ -146,6 +146,65 @@ def test_short_m_block_ignores_stale_shared_memory(ks, M):
     _no_device_error()
 
 
+@contextmanager
+def tall_tiles(bn):
+    old = {k: os.environ.get(k) for k in ("DG_BLOCK_M", "DG_BLOCK_N", "DG_CTA_PAIR")}
+    os.environ["DG_BLOCK_M"] = "256"
+    os.environ["DG_BLOCK_N"] = str(bn)
+    os.environ["DG_CTA_PAIR"] = "0"
+    try:
+        yield
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+@pytest.mark.parametrize("bn", [192, 224])
+@pytest.mark.parametrize("with_c", [False, True])
+@pytest.mark.parametrize("M,N,K", [(129, 264, 384), (300, 392, 1024), (512, 448, 640), (700, 200, 1536)])
+def test_dense_256_row_tiles(bn, with_c, M, N, K):
+    """256-row tiles: two 128-row MMAs per K step share the B tile; ragged M
+    leaves the second half partly or wholly outside the problem."""
+    w = workloads.dense(M, N, K, seed=M + 3 * N + K + bn, with_c=with_c)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    cb = P.bf16_bits(w.c) if with_c else None
+    o = oracle.gemm_nt(qa, sa, qb, sb, cb)
+    buf = P.sentinel_like((M, N + 24))
+    d = buf[:, :N]
+    with tall_tiles(bn):
+        dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb),
+                       P.dev_packed_sf(sb, N, K, 128), d=d, c=w.c.cuda() if with_c else None)
+    P.assert_close(P.bf16_to_f64(d), o, "256-row tiles BN=%d %dx%dx%d" % (bn, M, N, K))
+    assert (P.bf16_bits(buf[:, N:]) == P.SENTINEL_BITS).all()
+    _no_device_error()
+
+
+@pytest.mark.parametrize("bn", [192, 224])
+def test_dense_256_row_tiles_exact_many_tiles_per_sm(bn):
+    """Exact integer products (bit-exact BF16 of the oracle) with few SMs, so
+    every CTA runs many 256-row tiles through its single accumulator."""
+    rng = np.random.default_rng(31 + bn)
+    M, N, K = 600, 520, 1024
+    qa, qb = _int_operand(rng, M, K), _int_operand(rng, N, K)
+    ea = rng.integers(-2, 3, size=(M, K // 128))
+    eb = rng.integers(-2, 3, size=((N + 127) // 128, K // 128))
+    sa, sb = np.ldexp(1.0, ea), np.ldexp(1.0, eb)
+    want = oracle.bf16_rne(oracle.gemm_nt(qa, sa, qb, sb))
+    args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    dg.set_num_sms(3)
+    try:
+        with tall_tiles(bn):
+            got = P.bf16_bits(dg.fp8_gemm_nt(*args))
+    finally:
+        dg.set_num_sms(0)
+    assert np.array_equal(got, want)
+    _no_device_error()
+
+
 def test_dense_c_aliases_d():
     M, N, K = 192, 256, 512
     w = workloads.dense(M, N, K, seed=5, with_c=True)
