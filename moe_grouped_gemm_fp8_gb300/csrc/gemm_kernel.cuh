@@ -383,14 +383,13 @@ __device__ __forceinline__ void emit_chunk_tma_f32(const float (&f)[32], uint8_t
   }
 }
 
-// One 32 x 32 output chunk of a warp's quarter: + C (coalesced loads staged
-// through `buf`), round to BF16, write into `buf` with the 64-byte swizzle and
-// TMA-store it at (col0, out_row0).  `buf` must be free (its previous store
-// has finished reading it).  Rows past m are skipped for C when dense_rows.
-__device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
-                                               const CUtensorMap* tm_d, const GemmArgs& args,
-                                               int col0, int64_t out_row0, int row0,
-                                               bool dense_rows, int lane) {
+// One 32 x 32 output chunk of a warp's quarter (row = lane): + C (coalesced
+// loads staged through `buf`), round to BF16 and write into `buf` with the
+// 64-byte swizzle.  `buf` must be free.  Rows past m are skipped for C when
+// dense_rows.
+__device__ __forceinline__ void stage_chunk_bf16(float (&f)[32], uint8_t* buf, const GemmArgs& args,
+                                                 int col0, int64_t out_row0, int row0,
+                                                 bool dense_rows, int lane) {
   const uint32_t my_row_off = (uint32_t)lane * 64u;
   const uint32_t my_swz = ((uint32_t)lane >> 1) & 3u;
   if (args.c) {
@@ -425,6 +424,15 @@ __device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
     o.w = pack_bf16x2(f[8 * j + 6], f[8 * j + 7]);
     *reinterpret_cast<uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz)) = o;
   }
+}
+
+// The chunk staged, then TMA-stored at (col0, out_row0) (the store clips at M
+// and N).  `buf` must be free: its previous store has finished reading it.
+__device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
+                                               const CUtensorMap* tm_d, const GemmArgs& args,
+                                               int col0, int64_t out_row0, int row0,
+                                               bool dense_rows, int lane) {
+  stage_chunk_bf16(f, buf, args, col0, out_row0, row0, dense_rows, lane);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
