@@ -426,6 +426,26 @@ __device__ __forceinline__ void stage_chunk_bf16(float (&f)[32], uint8_t* buf, c
   }
 }
 
+// A chunk already rounded to BF16 (row = lane, 16 words of column pairs)
+// written into `buf` with the 64-byte swizzle and TMA-stored at
+// (col0, out_row0).  `buf` must be free.
+__device__ __forceinline__ void emit_packed_tma(const uint32_t (&p)[16], uint8_t* buf,
+                                                const CUtensorMap* tm_d, int col0, int64_t out_row0,
+                                                int lane) {
+  const uint32_t my_row_off = (uint32_t)lane * 64u;
+  const uint32_t my_swz = ((uint32_t)lane >> 1) & 3u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz)) =
+        make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm_d, smem_u32(buf), col0, (int32_t)out_row0);
+    bulk_commit_group();
+  }
+}
+
 // The chunk staged, then TMA-stored at (col0, out_row0) (the store clips at M
 // and N).  `buf` must be free: its previous store has finished reading it.
 __device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
@@ -984,6 +1004,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           ++n_xchg;
           continue;
+        }
+        if constexpr (MH == 2) {
+          if (args.c == nullptr) {
+            // 256-row tile, no C: the whole half is read from TMEM and rounded
+            // to BF16 in registers first, so the single accumulator goes back
+            // to the MMA before the second half's stores instead of after.
+            uint32_t pk[NCH][16];
+            uint32_t va[32], vb[32];
+            tc_ld_32x32b_x32(taddr, va);
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              uint32_t(&cur)[32] = (ch & 1) ? vb : va;
+              uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
+              tc_wait_ld_regs(cur);
+              if (ch + 1 < NCH) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[ch][i] = pack_bf16x2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
+            }
+            if (last_half) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(tempty(acc));
+            }
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              const int col0 = tile.nb * BN + ch * 32;
+              if (col0 >= args.n) continue;
+              uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
+              if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+              __syncwarp();
+              emit_packed_tma(pk[ch], buf, &tm_d, col0, out_row0, lane);
+              ++nchunk;
+            }
+            continue;
+          }
         }
         uint32_t ra[32], rb[32];
         tc_ld_32x32b_x32(taddr, ra);

@@ -260,10 +260,11 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
 
 // 256-row tiles (dense NT): estimated like choose_block_n, in the same units
 // (time of one K block of a 128 x 256 tile = 160), from measured rates: a
-// K block of a 256 x 192 tile costs ~223 units and of a 256 x 224 tile ~232;
-// the single accumulator's epilogue does not overlap the next tile (~8 and
-// ~10.5 K blocks, about twice that with C).  Returns the width, or 0 when no
-// 256-row tile beats `best_cost` (the 128-row estimate).
+// K block of a 256 x 192 tile costs ~221 units and of a 256 x 224 tile ~237;
+// the single accumulator's epilogue does not overlap the next tile (~6 K
+// blocks without C; with C, whose epilogue keeps FP32 chunks and reads C,
+// ~16 and ~21).  Returns the width, or 0 when no 256-row tile beats
+// `best_cost` (the 128-row estimate) by 3%.
 int choose_tall_block_n(int64_t m, int64_t n, int64_t k_blocks, int slots, bool with_c,
                         double best_cost) {
   const int forced_m = env_int("DG_BLOCK_M", 0);
@@ -272,15 +273,16 @@ int choose_tall_block_n(int64_t m, int64_t n, int64_t k_blocks, int slots, bool 
   if (forced_m == 256) return (forced_n == 192 || forced_n == 224) ? forced_n : 192;
   if (forced_n != 0) return 0;  // a forced width means 128-row tiles
   static const int widths[2] = {192, 224};
-  static const double per_kb[2] = {223.0, 232.0};
-  static const double epi[2] = {8.0, 10.5};
+  static const double per_kb[2] = {221.0, 237.0};
+  static const double epi[2] = {6.2, 6.5};
+  static const double epi_c[2] = {16.0, 21.0};
   const int sms = slots > 0 ? slots : 1;
   const int64_t m_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
   int best = 0;
   for (int i = 0; i < 2; ++i) {
     const int64_t tiles = m_blocks * ((n + widths[i] - 1) / widths[i]);
     const int64_t waves = (tiles + sms - 1) / sms;
-    const double cost = (double)waves * ((double)k_blocks + epi[i] * (with_c ? 2.0 : 1.0)) * per_kb[i];
+    const double cost = (double)waves * ((double)k_blocks + (with_c ? epi_c[i] : epi[i])) * per_kb[i];
     if (cost < best_cost * 0.97) {
       best_cost = cost;
       best = widths[i];
