@@ -1006,11 +1006,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           continue;
         }
         if constexpr (MH == 2) {
-          if (args.c == nullptr) {
-            // 256-row tile, no C: the whole half is read from TMEM and rounded
-            // to BF16 in registers first, so the single accumulator goes back
-            // to the MMA before the second half's stores instead of after.
+          {
+            // 256-row tile: the whole half is read from TMEM, C added and the
+            // sum rounded to BF16 in registers first, so the single
+            // accumulator goes back to the MMA before the second half's
+            // stores instead of after.  pk first holds this lane's row of C.
             uint32_t pk[NCH][16];
+            if (args.c) {
+#pragma unroll
+              for (int ch = 0; ch < NCH; ++ch) {
+                const int col0 = tile.nb * BN + ch * 32;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                  if (row_ok && col0 + 8 * q < args.n) v = __ldg(reinterpret_cast<const uint4*>(crow + col0 + 8 * q));
+                  pk[ch][4 * q] = v.x;
+                  pk[ch][4 * q + 1] = v.y;
+                  pk[ch][4 * q + 2] = v.z;
+                  pk[ch][4 * q + 3] = v.w;
+                }
+              }
+            }
             uint32_t va[32], vb[32];
             tc_ld_32x32b_x32(taddr, va);
 #pragma unroll
@@ -1020,8 +1036,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               tc_wait_ld_regs(cur);
               if (ch + 1 < NCH) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                pk[ch][i] = pack_bf16x2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
+              for (int i = 0; i < 16; ++i) {
+                float lo = __uint_as_float(cur[2 * i]), hi = __uint_as_float(cur[2 * i + 1]);
+                if (args.c) {
+                  lo += __uint_as_float(pk[ch][i] << 16);
+                  hi += __uint_as_float(pk[ch][i] & 0xFFFF0000u);
+                }
+                pk[ch][i] = pack_bf16x2(lo, hi);
+              }
             }
             if (last_half) {
               tc_fence_before();
