@@ -446,6 +446,47 @@ __device__ __forceinline__ void emit_packed_tma(const uint32_t (&p)[16], uint8_t
   }
 }
 
+// C of one 32 x 32 chunk, fetched coalesced (lane l: 16 bytes of rows l/4 + 8i,
+// piece l % 4) into registers, ahead of the chunk's turn; zero past M and N.
+__device__ __forceinline__ void load_c_chunk(uint4 (&cv)[4], const GemmArgs& args, int col0,
+                                             int64_t out_row0, int row0, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = (lane >> 2) + 8 * i, pc = lane & 3;
+    const int gcol = col0 + pc * 8;
+    cv[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (gcol < args.n && row0 + r < args.m)
+      cv[i] = __ldg(reinterpret_cast<const uint4*>(args.c + (out_row0 + r) * args.ldc + gcol));
+  }
+}
+
+// The chunk + C (prefetched by load_c_chunk, passed through `buf` to reach
+// each row's lane), rounded to BF16, staged and TMA-stored at (col0,
+// out_row0).  `buf` must be free.
+__device__ __forceinline__ void emit_chunk_tma_c(float (&f)[32], const uint4 (&cv)[4], uint8_t* buf,
+                                                 const CUtensorMap* tm_d, int col0, int64_t out_row0,
+                                                 int lane) {
+  const uint32_t my_row_off = (uint32_t)lane * 64u;
+  const uint32_t my_swz = ((uint32_t)lane >> 1) & 3u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = (lane >> 2) + 8 * i, pc = lane & 3;
+    *reinterpret_cast<uint4*>(buf + r * 64 + 16 * (pc ^ ((r >> 1) & 3))) = cv[i];
+  }
+  __syncwarp();
+  uint32_t p[16];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 c4 = *reinterpret_cast<const uint4*>(buf + my_row_off + 16u * ((uint32_t)j ^ my_swz));
+    const uint32_t cw[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      p[4 * j + i] = pack_bf16x2(f[8 * j + 2 * i] + __uint_as_float(cw[i] << 16),
+                                 f[8 * j + 2 * i + 1] + __uint_as_float(cw[i] & 0xFFFF0000u));
+  }
+  emit_packed_tma(p, buf, tm_d, col0, out_row0, lane);
+}
+
 // The chunk staged, then TMA-stored at (col0, out_row0) (the store clips at M
 // and N).  `buf` must be free: its previous store has finished reading it.
 __device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
@@ -851,6 +892,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int t = first_tile; t < sched.total; t += tile_stride) {
       Tile tile;
       if (!sched.get(t, tile)) continue;
+      // Dense tiles with C (128-row, no split): C of the next chunk is
+      // fetched while the current one is processed, the first chunk's while
+      // the accumulator is still being computed.
+      const bool c_ahead = is_dense_mode(MODE) && MH == 1 && KSPLIT == 1 && args.c != nullptr;
+      uint4 cA[4], cB[4];
+      if (c_ahead) load_c_chunk(cA, args, tile.nb * BN, tile.mb * BM + quarter * 32, tile.mb * BM + quarter * 32, lane);
       if (!warp_wait<kSuspendHintNs>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
       tc_fence_after();
       bool stop = false;
@@ -1069,6 +1116,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
           uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
+          uint4(&c_cur)[4] = (ch & 1) ? cB : cA;
+          uint4(&c_nxt)[4] = (ch & 1) ? cA : cB;
+          if (c_ahead && ch + 1 < NCH) load_c_chunk(c_nxt, args, tile.nb * BN + (ch + 1) * 32, out_row0, row0, lane);
           tc_wait_ld_regs(cur);
           if (ch + 1 < NCH) {
             tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
@@ -1113,7 +1163,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             float f[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
-            emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, is_dense_mode(MODE), lane);
+            if (c_ahead) emit_chunk_tma_c(f, c_cur, buf, &tm_d, col0, out_row0, lane);
+            else emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, is_dense_mode(MODE), lane);
             ++nchunk;
           } else if (row_ok) {
             store_row_chunk(cur, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
