@@ -101,12 +101,13 @@ cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUten
                         const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                         GemmArgs args, int grid, cudaStream_t stream);
 cudaError_t gemm_fetch_error(unsigned long long* word);  // reads and clears
-// 256-row tiles (dense NT): block_n 192 or 224; 0 stages = not compiled
+// 256-row tiles (dense NT, contiguous): block_n 192 or 224; 0 stages = not compiled
 int gemm_tall_stages(int block_n);
-cudaError_t gemm_tall_launch(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+constexpr int kMaxTallPairs = 1024;  // contiguous: most block pairs per launch
+cudaError_t gemm_tall_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                              const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                              GemmArgs args, int grid, cudaStream_t stream);
-cudaError_t gemm_tall_launch_impl(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t gemm_tall_launch_impl(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                                   const CUtensorMap& sfa, const CUtensorMap& sfb,
                                   const CUtensorMap& d, const GemmArgs& args, int grid,
                                   cudaStream_t stream);

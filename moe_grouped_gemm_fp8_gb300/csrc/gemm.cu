@@ -54,14 +54,14 @@ cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUten
   return cudaErrorInvalidValue;
 }
 
-cudaError_t gemm_tall_launch(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t gemm_tall_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                              const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                              GemmArgs args, int grid, cudaStream_t stream) {
   unsigned long long* err = nullptr;
   cudaError_t e = error_word_address(&err);
   if (e != cudaSuccess) return e;
   args.err = err;
-  return gemm_tall_launch_impl(block_n, a, b, sfa, sfb, d, args, grid, stream);
+  return gemm_tall_launch_impl(mode, block_n, a, b, sfa, sfb, d, args, grid, stream);
 }
 
 bool gemm2_block_n_supported(int block_n) {

@@ -94,9 +94,16 @@ constexpr int kEpiBuf = 32 * 32 * 2;  // one 32 x 32 BF16 staging chunk
 constexpr int kEpiBytes = 4 * 2 * kEpiBuf;  // 4 epilogue warps x 2 buffers
 constexpr int kSfLookahead = 3;  // packs loaded ahead of the one being laid out
 
-static constexpr size_t gemm_ctrl_bytes(int stages, int mode) {
+// Contiguous form with 256-row tiles: most 128-row block pairs per launch
+// (block indices kept as 16-bit halves of one word).
+constexpr int kMaxBlockPairs = kMaxTallPairs;
+
+static constexpr size_t gemm_ctrl_bytes(int stages, int mode, int bm = kBlockM) {
   return (size_t)8 * (2 * stages + 3 * kSfSlots + 5 + 8) + 16 +
-         ((mode == kMasked || mode == kKGrouped) ? (size_t)4 * (2 * kMaxMaskedGroups + 1) : 0);
+         ((mode == kMasked || mode == kKGrouped) ? (size_t)4 * (2 * kMaxMaskedGroups + 1) : 0) +
+         ((mode == kContiguous && bm == 2 * kBlockM)
+              ? (size_t)4 * (2 * kMaxMaskedGroups + 1) + (size_t)4 * kMaxBlockPairs
+              : 0);
 }
 
 // Scale buffers and TMEM scale slots are indexed by a running count of scale
@@ -122,12 +129,13 @@ struct GemmPlan {
   static constexpr int kRecvBytes = KSPLIT > 1 ? 4 * (KSPLIT - 1) * kXSlot : 0;
   static constexpr size_t smem_bytes(int mode) {
     return (size_t)STAGES * L::kStageBytes + (size_t)kSfSlots * L::kSfBufBytes + kEpiBytes +
-           (size_t)kRecvBytes + 1024 + gemm_ctrl_bytes(STAGES, mode);
+           (size_t)kRecvBytes + 1024 + gemm_ctrl_bytes(STAGES, mode, BM);
   }
 };
 
 struct Tile {
   int g, mb, nb;
+  int b0, b1;  // contiguous 256-row tiles: the two 128-row blocks (b1 < 0: none)
 };
 
 // Maps a linear tile index to (group, M block, N block).  Dense and
@@ -138,11 +146,13 @@ struct Tile {
 // enumerated expert by expert, each expert's M x N tiles rastered like dense
 // ones.  k_range gives the K blocks a tile accumulates: this CTA's split-K
 // slice, or the expert's own K blocks for the K-grouped form.
-template <int MODE>
+template <int MODE, int BM = kBlockM>
 struct Scheduler {
   const GemmArgs* args;
-  const int* tile_start;   // masked: [G + 1] first tile; K-grouped: [G + 1] first K block
+  const int* tile_start;   // masked: [G + 1] first tile; K-grouped: [G + 1] first K block;
+                           // contiguous 256-row tiles: [G + 1] first block pair
   const int* group_valid;  // masked: [G]
+  const uint32_t* pairs;   // contiguous 256-row tiles: 128-row blocks of each pair
   int total;
   int cursor;              // masked: current group (tile indices only increase)
   int kb_lo, kb_hi;        // K blocks of every tile (not K-grouped)
@@ -158,6 +168,29 @@ struct Scheduler {
   }
 
   __device__ bool get(int t, Tile& tile) {
+    if (MODE == kContiguous && BM == 2 * kBlockM) {
+      // pairs of one group's 128-row blocks, rastered like dense M blocks
+      const int npairs = tile_start[args->num_groups];
+      const int per_band = args->band * args->n_blocks;
+      const int b = t / per_band;
+      const int rem = t - b * per_band;
+      const int rows = min(args->band, npairs - b * args->band);
+      tile.nb = rem / rows;
+      const int p = b * args->band + rem % rows;
+      tile.mb = p;
+      const uint32_t w = pairs[p];
+      tile.b0 = (int)(w & 0xFFFFu);
+      tile.b1 = (w >> 16) == 0xFFFFu ? -1 : (int)(w >> 16);
+      // the group: the last g with tile_start[g] <= p (it has pairs)
+      int lo = 0, hi = args->num_groups;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tile_start[mid] <= p) lo = mid;
+        else hi = mid;
+      }
+      tile.g = lo;
+      return true;
+    }
     if (MODE == kKGrouped) {
       const int per_group = args->m_blocks * args->n_blocks;
       tile.g = t / per_group;
@@ -426,6 +459,16 @@ __device__ __forceinline__ void stage_chunk_bf16(float (&f)[32], uint8_t* buf, c
   }
 }
 
+// One row of a chunk already rounded to BF16, 16 bytes at a time, the columns
+// at or past n skipped (n % 8 == 0).
+__device__ __forceinline__ void store_packed_row(const uint32_t (&p)[16], __nv_bfloat16* dp,
+                                                 int cols_left) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (8 * q < cols_left)
+      *reinterpret_cast<uint4*>(dp + 8 * q) = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+}
+
 // A chunk already rounded to BF16 (row = lane, 16 words of column pairs)
 // written into `buf` with the 64-byte swizzle and TMA-stored at
 // (col0, out_row0).  `buf` must be free.
@@ -514,8 +557,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int NUM_ACC = P::kNumAcc;
   constexpr int MH = L::kMH;  // 128-row halves of a tile
   static_assert(KSPLIT == 1 || MODE == kDense, "split-K is for the dense form");
-  static_assert(BM == kBlockM || (BM == 2 * kBlockM && MODE == kDense && KSPLIT == 1),
-                "256-row tiles are for the dense NT form without split-K");
+  static_assert(BM == kBlockM || (BM == 2 * kBlockM && (MODE == kDense || MODE == kContiguous) && KSPLIT == 1),
+                "256-row tiles are for the dense NT and contiguous forms without split-K");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -599,6 +642,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tile_start[args.num_groups] = acc;
     }
   }
+  // Contiguous form with 256-row tiles: each group's 128-row blocks (found by
+  // the group id of their first row; all -1 blocks are skipped) are paired in
+  // any order - rows are independent, so the pairing does not change a
+  // result - and a group with an odd count ends with a half-empty pair.
+  // tile_start[g] = first pair of group g; pairs[p] = block ids (16 bits each,
+  // 0xFFFF = none).  The host bounds the pairs by kMaxBlockPairs.
+  uint32_t* const pair_words = reinterpret_cast<uint32_t*>(group_valid + kMaxMaskedGroups);
+  if (MODE == kContiguous && BM == 2 * kBlockM && warp == 2) {
+    int* counts = group_valid;
+    uint16_t* slot = reinterpret_cast<uint16_t*>(pair_words);
+    for (int g = lane; g < args.num_groups; g += 32) counts[g] = 0;
+    for (int i = lane; i < kMaxBlockPairs; i += 32) pair_words[i] = 0xFFFFFFFFu;
+    __syncwarp();
+    for (int b = lane; b < args.m_blocks; b += 32) {
+      const int g = __ldg(args.m_indices + (int64_t)b * kBlockM);
+      if (g >= args.num_groups) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteContiguousIndex);
+      else if (g >= 0) atomicAdd(counts + g, 1);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      int acc = 0;
+      for (int g = 0; g < args.num_groups; ++g) {
+        tile_start[g] = acc;
+        const int c = counts[g];
+        counts[g] = 2 * acc;  // from here: the group's next free block slot
+        acc += (c + 1) / 2;
+      }
+      tile_start[args.num_groups] = acc < kMaxBlockPairs ? acc : kMaxBlockPairs;
+    }
+    __syncwarp();
+    for (int b = lane; b < args.m_blocks; b += 32) {
+      const int g = __ldg(args.m_indices + (int64_t)b * kBlockM);
+      if (g >= 0 && g < args.num_groups) {
+        const int pos = atomicAdd(counts + g, 1);
+        if (pos < 2 * kMaxBlockPairs) slot[pos] = (uint16_t)b;
+      }
+    }
+  }
   if (MODE == kKGrouped && warp == 2) {
     // Experts' K blocks: sizes must be >= 0 and multiples of 128; a bad size
     // counts as 0 and K blocks past the end of A and B are dropped, both
@@ -638,15 +719,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int kb_begin = KSPLIT > 1 ? min(args.k_blocks, (int)krank * kb_per) : 0;
   const int kb_end = KSPLIT > 1 ? min(args.k_blocks, kb_begin + kb_per) : args.k_blocks;
 
-  Scheduler<MODE> sched;
+  Scheduler<MODE, BM> sched;
   sched.args = &args;
   sched.tile_start = tile_start;
   sched.group_valid = group_valid;
+  sched.pairs = pair_words;
   sched.cursor = 0;
   sched.kb_lo = kb_begin;
   sched.kb_hi = kb_end;
   sched.total = MODE == kMasked      ? tile_start[args.num_groups]
                 : MODE == kKGrouped ? args.num_groups * args.m_blocks * args.n_blocks
+                : (MODE == kContiguous && BM == 2 * kBlockM) ? tile_start[args.num_groups] * args.n_blocks
                                     : args.m_blocks * args.n_blocks;
   const uint64_t tmo = args.timeout_ns;
 
@@ -690,7 +773,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // per box; a 256-column B tile is two boxes 16 KB apart
           if constexpr (a_mn_major(MODE)) tma_load_2d(sb, &tm_a, fb, my, kx);
           else if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
-          else tma_load_2d(sb, &tm_a, fb, kx, my);
+          else if (MODE == kContiguous && BM == 2 * kBlockM) {
+            // the pair's two blocks (a half-empty pair loads its block twice)
+            tma_load_2d(sb, &tm_a, fb, kx, tile.b0 * kBlockM);
+            tma_load_2d(sb + kBlockM * kBlockK, &tm_a, fb, kx, (tile.b1 >= 0 ? tile.b1 : tile.b0) * kBlockM);
+          } else tma_load_2d(sb, &tm_a, fb, kx, my);
           if constexpr (b_mn_major(MODE)) {
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h)
@@ -798,7 +885,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ scale warp
     // Two cursors walk the same sequence of packs (tile, K block / 4): one
     // loads up to kSfLookahead packs ahead, the other lays them out in order.
-    PackCursor<Scheduler<MODE>> ld, lay;
+    PackCursor<Scheduler<MODE, BM>> ld, lay;
     ld.init(sched, first_tile, tile_stride);
     lay.init(sched, first_tile, tile_stride);
     uint32_t n_loaded = 0, n_laid = 0;
@@ -816,7 +903,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int my = ld.tile.mb * BM, kp = ld.kp;
             mbar_arrive_expect_tx(bar, L::kTxSF);
             if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
-            else tma_load_2d(buf + L::kRawA, &tm_sfa, bar, my, kp);
+            else if (MODE == kContiguous && BM == 2 * kBlockM) {
+              tma_load_2d(buf + L::kRawA, &tm_sfa, bar, ld.tile.b0 * kBlockM, kp);
+              tma_load_2d(buf + L::kRawA + 512, &tm_sfa, bar,
+                          (ld.tile.b1 >= 0 ? ld.tile.b1 : ld.tile.b0) * kBlockM, kp);
+            } else tma_load_2d(buf + L::kRawA, &tm_sfa, bar, my, kp);
             tma_load_3d(buf + L::kRawB, &tm_sfb, bar, ld.tile.nb * BN, kp,
                         MODE == kKGrouped ? 0 : ld.tile.g);
           }
@@ -904,7 +995,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // the tile's 128-row halves in turn; TMEM goes back after the last one
       for (int h = 0; h < MH; ++h) {
         const bool last_half = h == MH - 1;
-        const int row0 = tile.mb * BM + h * kBlockM + quarter * 32;
+        // contiguous 256-row tiles: the halves are the pair's blocks; the
+        // second half of a half-empty pair stores nothing
+        constexpr bool kPairs = MODE == kContiguous && BM == 2 * kBlockM;
+        const bool half_dead = kPairs && h == 1 && tile.b1 < 0;
+        const int row0 = kPairs ? (h == 0 || half_dead ? tile.b0 : tile.b1) * kBlockM + quarter * 32
+                                : tile.mb * BM + h * kBlockM + quarter * 32;
         const int row = row0 + lane;
         bool row_ok;
         int64_t out_row0;
@@ -946,7 +1042,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // split-K cluster, so all of them skip the same quarters.
         const bool quarter_live = (is_dense_mode(MODE) || MODE == kKGrouped)
                                       ? row0 < args.m
-                                      : __any_sync(0xffffffffu, row_ok) != 0;
+                                      : (__any_sync(0xffffffffu, row_ok) != 0 && !half_dead);
         if (!quarter_live) {
           if (last_half) {
             __syncwarp();
@@ -1101,6 +1197,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int ch = 0; ch < NCH; ++ch) {
               const int col0 = tile.nb * BN + ch * 32;
               if (col0 >= args.n) continue;
+              if (!use_tma) {
+                // a contiguous quarter with rows of other groups or padding
+                if (row_ok) store_packed_row(pk[ch], drow + col0, args.n - col0);
+                continue;
+              }
               uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
               if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
               __syncwarp();

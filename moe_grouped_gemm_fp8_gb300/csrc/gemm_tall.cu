@@ -1,20 +1,29 @@
-// FP8 GEMM kernels with 256-row output tiles for the dense NT form: two
-// 128-row MMAs per K step share the B tile, so each K block moves 32 KB of A
-// and BN x 128 bytes of B for twice the work of a 128-row tile (3-stage
-// pipeline, one TMEM accumulator of 2 x BN columns).
+// FP8 GEMM kernels with 256-row output tiles for the dense NT and the
+// M-grouped contiguous forms: two 128-row MMAs per K step share the B tile,
+// so each K block moves 32 KB of A and BN x 128 bytes of B for twice the work
+// of a 128-row tile (3-stage pipeline, one TMEM accumulator of 2 x BN
+// columns).  Contiguous tiles pair two 128-row blocks of one group.
 #include "gemm_kernel.cuh"
 
 namespace dg {
 
 int gemm_tall_stages(int block_n) { return (block_n == 192 || block_n == 224) ? 3 : 0; }
 
-cudaError_t gemm_tall_launch_impl(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t gemm_tall_launch_impl(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                                   const CUtensorMap& sfa, const CUtensorMap& sfb,
                                   const CUtensorMap& d, const GemmArgs& args, int grid,
                                   cudaStream_t stream) {
-  switch (block_n) {
-    case 192: return gemm_launch_impl<192, 3, kDense, 1, 2 * kBlockM>(a, b, sfa, sfb, d, args, grid, stream);
-    case 224: return gemm_launch_impl<224, 3, kDense, 1, 2 * kBlockM>(a, b, sfa, sfb, d, args, grid, stream);
+  constexpr int BM = 2 * kBlockM;
+  if (mode == kDense) {
+    switch (block_n) {
+      case 192: return gemm_launch_impl<192, 3, kDense, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
+      case 224: return gemm_launch_impl<224, 3, kDense, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
+    }
+  } else if (mode == kContiguous) {
+    switch (block_n) {
+      case 192: return gemm_launch_impl<192, 3, kContiguous, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
+      case 224: return gemm_launch_impl<224, 3, kContiguous, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
+    }
   }
   return cudaErrorInvalidValue;
 }

@@ -497,7 +497,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   args.debug_drop_load = env_int("DG_DEBUG_DROP_LOAD", 0);
   print_config(tall ? "fp8_gemm_nt (256-row tiles)" : name, m, n, k, 1, block_n, grid, args.band);
   if (tall)
-    return from_cuda(gemm_tall_launch(block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
+    return from_cuda(gemm_tall_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                       static_cast<cudaStream_t>(stream)));
   return from_cuda(gemm_launch(mode, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                static_cast<cudaStream_t>(stream)));
@@ -609,7 +609,21 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)(m_sum / kBlockM);
-  const int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, false, false);
+  int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, false, false);
+  // 256-row tiles pair two 128-row blocks of one group (at most (blocks +
+  // groups) / 2 pairs, which must fit the kernel's table); estimated as dense
+  // tiles over the expected pairs, blocks / 2 + groups / 2.
+  bool tall = false;
+  if (num_groups <= kMaxMaskedGroups && args.m_blocks < 0xFFFF &&
+      ((int64_t)args.m_blocks + num_groups + 1) / 2 <= kMaxTallPairs) {
+    const int64_t pairs = ((int64_t)args.m_blocks + num_groups + 1) / 2;
+    const double cost128 = dense_tile_cost(args.m_blocks, n, k / kBlockK, sms, false, block_n);
+    const int tall_n = choose_tall_block_n(pairs * 2 * kBlockM, n, k / kBlockK, sms, false, cost128);
+    if (tall_n != 0 && gemm_tall_stages(tall_n) > 0) {
+      tall = true;
+      block_n = tall_n;
+    }
+  }
   Operands o;
   if ((s = encode_a_2d(o, a, sfa, m_sum, k, k)) != DG_OK) return s;
   if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n, block_n)) != DG_OK) return s;
@@ -623,14 +637,18 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   args.num_groups = num_groups;
   args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
   args.k_blocks = (int32_t)(k / kBlockK);
-  args.band = env_int("DG_RASTER_BAND", 16);
+  args.band = env_int("DG_RASTER_BAND", 16) / (tall ? 2 : 1);
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
   args.pdl = g_pdl.load();
   const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  print_config("m_grouped_fp8_gemm_nt_contiguous", m_sum, n, k, num_groups, block_n, grid, args.band);
+  print_config(tall ? "m_grouped_fp8_gemm_nt_contiguous (256-row tiles)" : "m_grouped_fp8_gemm_nt_contiguous",
+               m_sum, n, k, num_groups, block_n, grid, args.band);
+  if (tall)
+    return from_cuda(gemm_tall_launch(kContiguous, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
+                                      static_cast<cudaStream_t>(stream)));
   return from_cuda(gemm_launch(kContiguous, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                static_cast<cudaStream_t>(stream)));
 }

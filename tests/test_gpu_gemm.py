@@ -244,6 +244,51 @@ def test_contiguous_routing_and_values(bn):
     _no_device_error()
 
 
+@pytest.mark.parametrize("bn", [192, 224])
+@pytest.mark.parametrize("sms", [0, 5])
+def test_contiguous_256_row_tiles(bn, sms):
+    """256-row tiles pair two 128-row blocks of one expert: experts with odd
+    block counts end with a half-empty pair, padding rows stay untouched, an
+    expert with no rows gets no pair; with few SMs each CTA runs many pairs."""
+    G, N, K = 6, 264, 384
+    w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [100, 0, 250, 128, 600, 384], seed=81 + bn)
+    mi = w.m_indices.numpy()
+    o, written = oracle.gemm_contiguous(qa, sa, qb, sb, mi)
+    d = P.sentinel_like((mi.size, N))
+    dg.set_num_sms(sms)
+    try:
+        with tall_tiles(bn):
+            dg.m_grouped_fp8_gemm_nt_contiguous(*dev, w.m_indices.cuda(), d=d)
+    finally:
+        dg.set_num_sms(0)
+    bits = P.bf16_bits(d)
+    wr = written.astype(bool)
+    assert np.array_equal(wr, mi >= 0)
+    assert (bits[~wr] == P.SENTINEL_BITS).all(), "padding rows were written"
+    P.assert_close(P.bf16_to_f64(d)[wr], o[wr], "contiguous, 256-row tiles")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("bn", [192, 224])
+def test_contiguous_256_row_tiles_match_128_row_tiles_bitwise(bn):
+    """Each output element is the same sum in the same K order whichever way
+    the blocks are paired, so both tile heights give identical bits."""
+    G, N, K = 5, 448, 1024
+    w, _, dev = _contig_setup(G, N, K, [300, 520, 0, 129, 1000], seed=90)
+    mi = w.m_indices.cuda()
+    d128 = P.sentinel_like((mi.numel(), N))
+    d256 = P.sentinel_like((mi.numel(), N))
+    os.environ["DG_BLOCK_M"] = "128"
+    try:
+        dg.m_grouped_fp8_gemm_nt_contiguous(*dev, mi, d=d128)
+    finally:
+        os.environ.pop("DG_BLOCK_M", None)
+    with tall_tiles(bn):
+        dg.m_grouped_fp8_gemm_nt_contiguous(*dev, mi, d=d256)
+    assert torch.equal(d128.view(torch.int16), d256.view(torch.int16))
+    _no_device_error()
+
+
 def test_contiguous_single_group_equals_dense():
     G, N, K = 1, 256, 512
     w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [384], seed=78)
@@ -252,7 +297,8 @@ def test_contiguous_single_group_equals_dense():
     assert torch.equal(d.view(torch.int16), dd.view(torch.int16))
 
 
-def test_contiguous_bad_index_is_flagged_not_written():
+@pytest.mark.parametrize("tall", [0, 192])
+def test_contiguous_bad_index_is_flagged_not_written(tall):
     G, N, K = 2, 128, 256
     w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [128, 200], seed=79)
     mi = w.m_indices.clone()
@@ -260,7 +306,15 @@ def test_contiguous_bad_index_is_flagged_not_written():
     mi[128 * 2] = 9          # a whole block tagged with an expert id >= G
     d = P.sentinel_like((mi.numel(), N))
     dg.get_device_error()
-    dg.m_grouped_fp8_gemm_nt_contiguous(*dev, mi.cuda(), d=d)
+    if tall:
+        with tall_tiles(tall):
+            dg.m_grouped_fp8_gemm_nt_contiguous(*dev, mi.cuda(), d=d)
+    else:
+        os.environ["DG_BLOCK_M"] = "128"
+        try:
+            dg.m_grouped_fp8_gemm_nt_contiguous(*dev, mi.cuda(), d=d)
+        finally:
+            os.environ.pop("DG_BLOCK_M", None)
     st, word = dg.get_device_error()
     assert st == 6, "expected DG_ERR_DEVICE_BAD_INDEX, got %d (0x%x)" % (st, word)
     bits = P.bf16_bits(d)
