@@ -12,14 +12,15 @@
 // The block-scaled MMA of the main kernel only takes power-of-two (UE8M0)
 // scales, so here the promotion is done explicitly, Blackwell-style: per K
 // block the tensor core writes a fresh FP32 partial tile P = A_kb @ B_kb^T
-// (tcgen05.mma kind::f8f6f4, no scaling) into one of two TMEM buffers; four
-// promotion warps (one TMEM lane quarter each) read P with tcgen05.ld,
-// multiply by sa * sb and accumulate into FP32 registers (one output row of
-// 128 columns per thread), then run the usual epilogue (+ C, BF16, TMA
-// store).  The MMA of K block kb+1 overlaps the promotion of kb, and the
-// next tile's MMAs overlap this tile's epilogue.
+// (tcgen05.mma kind::f8f6f4, no scaling) into one of four TMEM buffers; eight
+// promotion warps (two per TMEM lane quarter, 64 columns each) read P with
+// tcgen05.ld (both 32-column loads in flight at once), multiply by sa * sb and
+// accumulate into FP32 registers (64 columns of one output row per thread),
+// then run the usual epilogue (+ C, BF16, TMA store).  The MMAs run up to three K blocks ahead of the promotion (the
+// commit-to-wake latency of a partial, ~650 cycles, is longer than its MMAs),
+// and the next tile's MMAs overlap this tile's epilogue.
 //
-// One persistent CTA per SM, 6 warps: 0 TMA producer, 1 MMA issuer, 2-5
+// One persistent CTA per SM, 10 warps: 0 TMA producer, 1 MMA issuer, 2-9
 // promotion + epilogue.  128 x 128 output tiles.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -28,14 +29,16 @@
 
 namespace dg {
 
-constexpr int kPromoteThreads = 192;
+constexpr int kPromoteThreads = 320;
+constexpr int kPromoteWarps = 8;  // promotion / epilogue warps
 constexpr int kPromoteBN = 128;
 constexpr int kPromoteStages = 6;
 constexpr int kPromoteStageBytes = 32768;  // A 128 x 128 + B 128 x 128, E4M3
+constexpr int kPromoteBufs = 4;            // TMEM partial buffers of 128 columns
 
 static constexpr size_t promote_smem_bytes() {
-  return (size_t)kPromoteStages * kPromoteStageBytes + kEpiBytes + 1024 +
-         8 * (2 * kPromoteStages + 5) + 16;
+  return (size_t)kPromoteStages * kPromoteStageBytes + (size_t)kPromoteWarps * 2 * kEpiBuf + 1024 +
+         8 * (2 * kPromoteStages + 2 * kPromoteBufs + 1) + 16;
 }
 
 // Instruction descriptor of kind::f8f6f4 without block scaling: FP32 D
@@ -65,13 +68,14 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
   uint8_t* epi_smem = smem + STAGES * kPromoteStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + kEpiBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + kPromoteWarps * 2 * kEpiBuf);
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  constexpr int NB = kPromoteBufs;
   auto pfull = [&](int b) { return smem_u32(bars + 2 * STAGES + b); };
-  auto pempty = [&](int b) { return smem_u32(bars + 2 * STAGES + 2 + b); };
-  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  auto pempty = [&](int b) { return smem_u32(bars + 2 * STAGES + NB + b); };
+  const uint32_t drain = smem_u32(bars + 2 * STAGES + 2 * NB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NB + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned long long* const err = args.err;
   const int warp = threadIdx.x >> 5;
@@ -82,9 +86,9 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(pfull(b), 1);
-      mbar_init(pempty(b), 4);  // the four promotion warps
+      mbar_init(pempty(b), kPromoteWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
     tma_prefetch_desc(&tm_d);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 256);  // two 128-column partial buffers
+    tmem_alloc(smem_u32(tmem_slot), NB * BN);  // NB 128-column partial buffers
     tmem_relinquish();
     tc_fence_before();
   }
@@ -154,12 +158,12 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f8_e4m3(kBlockM, BN);
       int stage = 0;
-      uint32_t phase = 0, pk = 0;  // pk: partial tiles issued so far (buffer pk & 1)
+      uint32_t phase = 0, pk = 0;  // pk: partial tiles issued so far (buffer pk % NB)
       bool ok = true;
       for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
         for (int kb = 0; kb < kbs; ++kb, ++pk) {
           if (!wait_one<kSuspendHintNs>(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull) ||
-              !wait_one<kSuspendHintNs>(pempty(pk & 1u), ((pk >> 1) & 1u) ^ 1u, abort_flag, tmo,
+              !wait_one<kSuspendHintNs>(pempty(pk % NB), ((pk / NB) & 1u) ^ 1u, abort_flag, tmo,
                                         err, kSiteMmaTmemEmpty)) {
             ok = false;
             break;
@@ -168,12 +172,12 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
           const uint8_t* st = smem + stage * kPromoteStageBytes;
           const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(st));
           const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(st + 16384));
-          const uint32_t d_tmem = tmem_base + (pk & 1u) * BN;
+          const uint32_t d_tmem = tmem_base + (pk % NB) * BN;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             tc_mma_f8(d_tmem, adesc + 2 * j, bdesc + 2 * j, idesc, j != 0 ? 1u : 0u);
           tc_commit(empty(stage));
-          tc_commit(pfull(pk & 1u));
+          tc_commit(pfull(pk % NB));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -187,6 +191,8 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
   } else {
     // ------------------------------------------------------------ promotion + epilogue
     const int quarter = warp & 3;
+    const int colh = (warp - 2) >> 2;  // which 64 columns of the quarter's rows
+    constexpr int HC = BN / 2;
     uint8_t* ebuf = epi_smem + (warp - 2) * 2 * kEpiBuf;
     uint32_t nchunk = 0, pk = 0;
     bool ok = true;
@@ -198,47 +204,57 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
       const bool row_ok = row < args.m;
       const float* sa_col = args.sfa_f32 + row;                       // + kb * sfa_ld
       const float* sb_row = args.sfb_f32 + (int64_t)tile.nb * kbs;    // + kb
-      float acc[BN];
+      float acc[HC];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) acc[i] = 0.0f;
-      float sa_next = row_ok ? __ldg(sa_col) : 0.0f;
-      float sb_next = __ldg(sb_row);
-      for (int kb = 0; kb < kbs; ++kb, ++pk) {
-        const float s = sa_next * sb_next;
-        if (kb + 1 < kbs) {
-          sa_next = row_ok ? __ldg(sa_col + (int64_t)(kb + 1) * args.sfa_ld) : 0.0f;
-          sb_next = __ldg(sb_row + kb + 1);
+      for (int i = 0; i < HC; ++i) acc[i] = 0.0f;
+      // scales are fetched kSd K blocks ahead (a global load's latency is
+      // longer than one K block's promotion); slot j of the unrolled loop
+      // always holds the scales of K block kb + j
+      constexpr int kSd = 4;
+      float sa_q[kSd], sb_q[kSd];
+#pragma unroll
+      for (int j = 0; j < kSd; ++j) {
+        sa_q[j] = (row_ok && j < kbs) ? __ldg(sa_col + (int64_t)j * args.sfa_ld) : 0.0f;
+        sb_q[j] = j < kbs ? __ldg(sb_row + j) : 0.0f;
+      }
+      for (int kb0 = 0; kb0 < kbs && ok; kb0 += kSd) {
+#pragma unroll
+      for (int j = 0; j < kSd; ++j) {
+        const int kb = kb0 + j;
+        if (kb >= kbs) break;
+        const float s = sa_q[j] * sb_q[j];
+        if (kb + kSd < kbs) {
+          sa_q[j] = row_ok ? __ldg(sa_col + (int64_t)(kb + kSd) * args.sfa_ld) : 0.0f;
+          sb_q[j] = __ldg(sb_row + kb + kSd);
         }
-        if (!warp_wait<kSuspendHintNs>(pfull(pk & 1u), (pk >> 1) & 1u, abort_flag, tmo, err,
+        if (!warp_wait<kSuspendHintNs>(pfull(pk % NB), (pk / NB) & 1u, abort_flag, tmo, err,
                                        kSiteEpilogueTmemFull)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (pk & 1u) * BN + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t taddr =
+            tmem_base + (pk % NB) * BN + colh * HC + ((uint32_t)(quarter * 32) << 16);
         uint32_t ra[32], rb[32];
         tc_ld_32x32b_x32(taddr, ra);
+        tc_ld_32x32b_x32(taddr + 32, rb);
+        tc_wait_ld_regs(ra);
+        tc_wait_ld_regs(rb);
+        // the partial is in registers: hand the buffer back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pempty(pk % NB));
 #pragma unroll
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
-          uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
-          tc_wait_ld_regs(cur);
-          if (ch + 1 < BN / 32) {
-            tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
-          } else {
-            // the whole partial is in registers: hand the buffer back
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pempty(pk & 1u));
-          }
+        for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(ra[i]), s, acc[i]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[ch * 32 + i] = fmaf(__uint_as_float(cur[i]), s, acc[ch * 32 + i]);
-        }
+        for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(__uint_as_float(rb[i]), s, acc[32 + i]);
+        ++pk;
+      }
       }
       if (!ok) break;
 #pragma unroll
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        const int col0 = tile.nb * BN + ch * 32;
+      for (int ch = 0; ch < HC / 32; ++ch) {
+        const int col0 = tile.nb * BN + colh * HC + ch * 32;
         if (col0 >= args.n) continue;
         uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
         if (lane == 0) bulk_wait_group_read<1>();
@@ -257,7 +273,7 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 256);
+    tmem_dealloc(tmem_base, NB * BN);
   }
 }
 
