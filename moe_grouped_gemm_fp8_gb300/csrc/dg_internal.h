@@ -101,12 +101,24 @@ cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUten
                         const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                         GemmArgs args, int grid, cudaStream_t stream);
 cudaError_t gemm_fetch_error(unsigned long long* word);  // reads and clears
+// device address of the error word on the current device (every launch passes
+// it as GemmArgs::err)
+cudaError_t error_word_address(unsigned long long** out);
 // 256-row tiles (dense NT, contiguous): block_n 192 or 224; 0 stages = not compiled
 int gemm_tall_stages(int block_n);
 constexpr int kMaxTallPairs = 1024;  // contiguous: most block pairs per launch
 cudaError_t gemm_tall_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                              const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
                              GemmArgs args, int grid, cudaStream_t stream);
+// single M block of at most 64 rows, dense NT: 64-row A slots (block_n 128 or 192)
+bool gemm_short_supported(int block_n);
+cudaError_t gemm_short_launch(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                              const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
+                              GemmArgs args, int grid, cudaStream_t stream);
+cudaError_t gemm_short_launch_impl(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                                   const CUtensorMap& sfa, const CUtensorMap& sfb,
+                                   const CUtensorMap& d, const GemmArgs& args, int grid,
+                                   cudaStream_t stream);
 cudaError_t gemm_tall_launch_impl(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                                   const CUtensorMap& sfa, const CUtensorMap& sfb,
                                   const CUtensorMap& d, const GemmArgs& args, int grid,
@@ -130,14 +142,14 @@ DG_DECLARE_GEMM2_BN(224)
 DG_DECLARE_GEMM2_BN(256)
 #undef DG_DECLARE_GEMM2_BN
 // gemm_splitk.cu: dense split-K over 2 or 4 CTAs, 128-column tiles
-cudaError_t gemm_splitk_launch(int ksplit, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t gemm_splitk_launch(int ksplit, bool short_a, const CUtensorMap& a, const CUtensorMap& b,
                                const CUtensorMap& sfa, const CUtensorMap& sfb,
                                const CUtensorMap& d, GemmArgs args, int clusters,
                                cudaStream_t stream);
 int gemm_splitk_max_clusters(int ksplit);
 // gemm_promote.cu: arbitrary FP32 scales, partials promoted out of TMEM
 cudaError_t gemm_promote_launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                                const GemmArgs& args, int grid, cudaStream_t stream);
+                                GemmArgs args, int grid, cudaStream_t stream);
 DG_DECLARE_GEMM_BN(128)
 DG_DECLARE_GEMM_BN(192)
 DG_DECLARE_GEMM_BN(224)

@@ -10,7 +10,7 @@ __device__ unsigned long long g_gemm_err = 0ull;
 // Device address of the error word on the current device.  Host code must
 // pass this address, not the host-side shadow the symbol name denotes here;
 // looked up once per device.
-static cudaError_t error_word_address(unsigned long long** out) {
+cudaError_t error_word_address(unsigned long long** out) {
   static unsigned long long* addr[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -62,6 +62,16 @@ cudaError_t gemm_tall_launch(int mode, int block_n, const CUtensorMap& a, const 
   if (e != cudaSuccess) return e;
   args.err = err;
   return gemm_tall_launch_impl(mode, block_n, a, b, sfa, sfb, d, args, grid, stream);
+}
+
+cudaError_t gemm_short_launch(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                              const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,
+                              GemmArgs args, int grid, cudaStream_t stream) {
+  unsigned long long* err = nullptr;
+  cudaError_t e = error_word_address(&err);
+  if (e != cudaSuccess) return e;
+  args.err = err;
+  return gemm_short_launch_impl(block_n, a, b, sfa, sfb, d, args, grid, stream);
 }
 
 bool gemm2_block_n_supported(int block_n) {

@@ -67,10 +67,13 @@ namespace dg {
 constexpr int kGemmThreads = 224;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_103
 
-// BM: rows of A per tile, 128 or 256 (two 128-row MMAs sharing B).
+// BM: rows of A per tile, 128 or 256 (two 128-row MMAs sharing B), or 64:
+// a single M block of at most 64 rows, whose A slot holds only those rows
+// (the 128-row MMA then reads rows 64-127 from the B slot that follows; they
+// reach only accumulator rows that are never stored), so more stages fit.
 template <int BN, int BM = kBlockM>
 struct GemmLayout {
-  static constexpr int kMH = BM / kBlockM;              // 128-row halves of the tile
+  static constexpr int kMH = (BM + kBlockM - 1) / kBlockM;  // 128-row halves of the tile
   static constexpr int kSfbChunks = (BN + 127) / 128;  // 128-row chunks of B scales
   static constexpr int kBytesA = BM * kBlockK;
   static constexpr int kBytesB = BN * kBlockK;
@@ -79,12 +82,12 @@ struct GemmLayout {
   // scale buffer: TMA-loaded words of A (BM) and B (BN), then the same words
   // in tcgen05.cp order
   static constexpr int kRawA = 0;
-  static constexpr int kRawB = BM * 4;
+  static constexpr int kRawB = kMH * kBlockM * 4;
   static constexpr int kCpA = kRawB + kSfbChunks * 512;
   static constexpr int kCpB = kCpA + kMH * 512;
   static constexpr int kSfBufBytes = kCpB + kSfbChunks * 512;
   static constexpr uint32_t kTxAB = kBytesA + kBytesB;
-  static constexpr uint32_t kTxSF = BM * 4 + BN * 4;
+  static constexpr uint32_t kTxSF = kMH * kBlockM * 4 + BN * 4;
   // TMEM columns of one scale slot: A scales of each half, then B scales
   static constexpr int kSfCols = 4 * kMH + 4 * kSfbChunks;
 };
@@ -557,8 +560,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int NUM_ACC = P::kNumAcc;
   constexpr int MH = L::kMH;  // 128-row halves of a tile
   static_assert(KSPLIT == 1 || MODE == kDense, "split-K is for the dense form");
-  static_assert(BM == kBlockM || (BM == 2 * kBlockM && (MODE == kDense || MODE == kContiguous) && KSPLIT == 1),
-                "256-row tiles are for the dense NT and contiguous forms without split-K");
+  static_assert(BM == kBlockM || (BM == 2 * kBlockM && (MODE == kDense || MODE == kContiguous) && KSPLIT == 1) ||
+                    (BM == kBlockM / 2 && MODE == kDense),
+                "256-row tiles are for the dense NT and contiguous forms without split-K; "
+                "64-row A slots for the dense NT form");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -1323,7 +1328,8 @@ static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
   static_assert(Plan::smem_bytes(MODE) <= (size_t)kSmemLimit, "shared memory over the per-CTA limit");
   auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT, BM>;
   const size_t smem = Plan::smem_bytes(MODE);
-  cudaError_t e = set_smem_once<KernelTag<BN, STAGES, MODE, KSPLIT, BM == kBlockM ? 1 : 3>>(kern, smem);
+  cudaError_t e =
+      set_smem_once<KernelTag<BN, STAGES, MODE, KSPLIT, BM == kBlockM ? 1 : (BM > kBlockM ? 3 : 4)>>(kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   unsigned n_attr = 0;

@@ -278,10 +278,14 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
 }
 
 cudaError_t gemm_promote_launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
-                                const GemmArgs& args, int grid, cudaStream_t stream) {
+                                GemmArgs args, int grid, cudaStream_t stream) {
   static_assert(promote_smem_bytes() <= (size_t)kSmemLimit, "shared memory over the per-CTA limit");
   const size_t smem = promote_smem_bytes();
-  cudaError_t e = set_smem_once<KernelTag<kPromoteBN, kPromoteStages, 100, 1, 1>>(
+  unsigned long long* err = nullptr;
+  cudaError_t e = error_word_address(&err);
+  if (e != cudaSuccess) return e;
+  args.err = err;
+  e = set_smem_once<KernelTag<kPromoteBN, kPromoteStages, 100, 1, 1>>(
       fp8_gemm_promote_kernel, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];

@@ -5,15 +5,24 @@
 
 namespace dg {
 
-cudaError_t gemm_splitk_launch(int ksplit, const CUtensorMap& a, const CUtensorMap& b,
+// short_a: M <= 64, so the A slot of a stage holds 64 rows (8 KB instead of
+// 16) and two more stages fit.
+cudaError_t gemm_splitk_launch(int ksplit, bool short_a, const CUtensorMap& a, const CUtensorMap& b,
                                const CUtensorMap& sfa, const CUtensorMap& sfb,
                                const CUtensorMap& d, GemmArgs args, int clusters,
                                cudaStream_t stream) {
   if (clusters <= 0) return cudaErrorInvalidValue;
+  unsigned long long* err = nullptr;
+  cudaError_t e = error_word_address(&err);
+  if (e != cudaSuccess) return e;
+  args.err = err;
+  constexpr int kShort = kBlockM / 2;
   if (ksplit == 2)
-    return gemm_launch_impl<128, 5, kDense, 2>(a, b, sfa, sfb, d, args, 2 * clusters, stream);
+    return short_a ? gemm_launch_impl<128, 7, kDense, 2, kShort>(a, b, sfa, sfb, d, args, 2 * clusters, stream)
+                   : gemm_launch_impl<128, 5, kDense, 2>(a, b, sfa, sfb, d, args, 2 * clusters, stream);
   if (ksplit == 4)
-    return gemm_launch_impl<128, 4, kDense, 4>(a, b, sfa, sfb, d, args, 4 * clusters, stream);
+    return short_a ? gemm_launch_impl<128, 6, kDense, 4, kShort>(a, b, sfa, sfb, d, args, 4 * clusters, stream)
+                   : gemm_launch_impl<128, 4, kDense, 4>(a, b, sfa, sfb, d, args, 4 * clusters, stream);
   return cudaErrorInvalidValue;
 }
 

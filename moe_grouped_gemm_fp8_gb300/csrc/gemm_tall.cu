@@ -9,6 +9,22 @@ namespace dg {
 
 int gemm_tall_stages(int block_n) { return (block_n == 192 || block_n == 224) ? 3 : 0; }
 
+// Dense NT with a single M block of at most 64 rows (decode): 64-row A slots,
+// so 8 (BN = 128) or 6 (BN = 192) stages instead of 6 and 4.
+bool gemm_short_supported(int block_n) { return block_n == 128 || block_n == 192; }
+
+cudaError_t gemm_short_launch_impl(int block_n, const CUtensorMap& a, const CUtensorMap& b,
+                                   const CUtensorMap& sfa, const CUtensorMap& sfb,
+                                   const CUtensorMap& d, const GemmArgs& args, int grid,
+                                   cudaStream_t stream) {
+  constexpr int BM = kBlockM / 2;
+  switch (block_n) {
+    case 128: return gemm_launch_impl<128, 8, kDense, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
+    case 192: return gemm_launch_impl<192, 6, kDense, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t gemm_tall_launch_impl(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                                   const CUtensorMap& sfa, const CUtensorMap& sfb,
                                   const CUtensorMap& d, const GemmArgs& args, int grid,

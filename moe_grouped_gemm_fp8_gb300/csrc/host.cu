@@ -429,7 +429,8 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     if (clusters <= 0) return DG_ERR_CUDA;
     print_config(ksplit == 2 ? "fp8_gemm_nt (split-K 2)" : "fp8_gemm_nt (split-K 4)", m, n, k, 1,
                  block_n, ksplit * clusters, args.band);
-    return from_cuda(gemm_splitk_launch(ksplit, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
+    args.debug_drop_load = env_int("DG_DEBUG_DROP_LOAD", 0);
+    return from_cuda(gemm_splitk_launch(ksplit, m <= kBlockM / 2, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
                                         static_cast<cudaStream_t>(stream)));
   }
   // CTA pairs (256-row tiles) only on request (DG_CTA_PAIR=1): on the
@@ -499,6 +500,10 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   if (tall)
     return from_cuda(gemm_tall_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                       static_cast<cudaStream_t>(stream)));
+  // a single M block of at most 64 rows: 64-row A slots, more stages
+  if (mode == kDense && !pair && m <= kBlockM / 2 && gemm_short_supported(block_n))
+    return from_cuda(gemm_short_launch(block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
+                                       static_cast<cudaStream_t>(stream)));
   return from_cuda(gemm_launch(mode, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                static_cast<cudaStream_t>(stream)));
 }

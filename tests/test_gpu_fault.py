@@ -48,3 +48,36 @@ def test_dropped_stage_times_out_and_context_survives():
     d = dg.fp8_gemm_nt(*dev)
     assert dg.get_device_error()[0] == 0
     P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "after the injected timeout")
+
+
+def test_dropped_stage_in_a_split_k_cluster_times_out_everywhere():
+    """The same hook in a 4-CTA split-K cluster: CTA 0 never finishes its K
+    slice, so the other CTAs' waits for its partials expire too; every CTA
+    ends by itself, the error word holds a timeout, and the context stays
+    usable."""
+    M, N, K = 64, 256, 2048
+    g = torch.Generator().manual_seed(114)
+    a = torch.randn(M, K, generator=g); b = torch.randn(N, K, generator=g)
+    qa, _, sa = oracle.quantize(a.numpy(), 1)
+    qb, _, sb = oracle.quantize(b.numpy(), 128)
+    dev = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    assert dg.get_device_error()[0] == 0
+    dg.set_wait_timeout_ns(2_000_000)  # 2 ms
+    os.environ["DG_DEBUG_DROP_LOAD"] = "2"
+    os.environ["DG_SPLIT_K"] = "4"
+    try:
+        dg.fp8_gemm_nt(*dev)
+        st, word = dg.get_device_error()
+    finally:
+        os.environ.pop("DG_DEBUG_DROP_LOAD", None)
+        os.environ.pop("DG_SPLIT_K", None)
+        dg.set_wait_timeout_ns(2_000_000_000)
+    assert st == DG_ERR_DEVICE_TIMEOUT, (st, hex(word))
+    assert word & 0xFF == DG_ERR_DEVICE_TIMEOUT, hex(word)
+    os.environ["DG_SPLIT_K"] = "4"
+    try:
+        d = dg.fp8_gemm_nt(*dev)
+    finally:
+        os.environ.pop("DG_SPLIT_K", None)
+    assert dg.get_device_error()[0] == 0
+    P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "after the injected split-K timeout")
