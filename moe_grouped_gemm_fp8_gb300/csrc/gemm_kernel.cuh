@@ -674,6 +674,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         counts[g] = 2 * acc;  // from here: the group's next free block slot
         acc += (c + 1) / 2;
       }
+      // the host bounds the pairs; past the table a block would be dropped
+      if (acc > kMaxBlockPairs) record_error(err, DG_ERR_DEVICE_BAD_INDEX, kSiteContiguousIndex);
       tile_start[args.num_groups] = acc < kMaxBlockPairs ? acc : kMaxBlockPairs;
     }
     __syncwarp();
