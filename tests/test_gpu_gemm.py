@@ -289,6 +289,27 @@ def test_contiguous_256_row_tiles_match_128_row_tiles_bitwise(bn):
     _no_device_error()
 
 
+@pytest.mark.parametrize("G,count", [(600, 128), (4, 67200)])
+def test_contiguous_256_row_tiles_fall_back_past_the_pair_table(G, count):
+    """More experts than the pair table holds (600 > 512), or more 128-row
+    blocks than it can pair (4 x 525 blocks > 2 x 1024): 256-row tiles are
+    refused on the host and the 128-row kernel runs, bit-identical."""
+    N, K = 64, 128
+    w, _, dev = _contig_setup(G, N, K, [count] * G, seed=91)
+    mi = w.m_indices.cuda()
+    d_ref = P.sentinel_like((mi.numel(), N))
+    d_req = P.sentinel_like((mi.numel(), N))
+    os.environ["DG_BLOCK_M"] = "128"
+    try:
+        dg.m_grouped_fp8_gemm_nt_contiguous(*dev, mi, d=d_ref)
+    finally:
+        os.environ.pop("DG_BLOCK_M", None)
+    with tall_tiles(192):
+        dg.m_grouped_fp8_gemm_nt_contiguous(*dev, mi, d=d_req)
+    assert torch.equal(d_ref.view(torch.int16), d_req.view(torch.int16))
+    _no_device_error()
+
+
 def test_contiguous_single_group_equals_dense():
     G, N, K = 1, 256, 512
     w, (qa, sa, qb, sb), dev = _contig_setup(G, N, K, [384], seed=78)

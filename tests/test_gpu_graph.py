@@ -96,3 +96,26 @@ def test_contiguous_and_k_grouped_capture():
         dg.m_grouped_fp8_gemm_nt_contiguous(qa, sfa, qb, sfb, mi, d=d)
         dg.k_grouped_fp8_gemm_tn_contiguous(ka, ksa, kb, ksb, ks, d=dk)
     _replay_matches_eager(fn, [d, dk])
+
+
+@pytest.mark.parametrize("bn", ["192", "224"])
+def test_256_row_tiles_capture(bn, monkeypatch):
+    """Dense (with C) and contiguous GEMMs on 256-row tiles, captured in one
+    graph: the contiguous pair table is rebuilt from m_indices at every replay."""
+    monkeypatch.setenv("DG_BLOCK_M", "256")
+    monkeypatch.setenv("DG_BLOCK_N", bn)
+    w = workloads.dense(600, 520, 1024, seed=69, with_c=True)
+    qa, sfa = dg.quantize_fp8(w.a.cuda(), 1)
+    qb, sfb = dg.quantize_fp8(w.b.cuda(), 128)
+    c = w.c.cuda()
+    d = torch.empty(600, 520, dtype=torch.bfloat16, device="cuda")
+    cw = workloads.contiguous(4, 264, 512, seed=72, counts=[300, 0, 129, 520])
+    cqa, csfa = dg.quantize_fp8(cw.a.cuda(), 1)
+    cqb, csfb = dg.quantize_fp8(cw.b.cuda(), 128)
+    mi = cw.m_indices.cuda()
+    dc = torch.zeros(cw.a.shape[0], 264, dtype=torch.bfloat16, device="cuda")
+
+    def fn():
+        dg.fp8_gemm_nt(qa, sfa, qb, sfb, d=d, c=c)
+        dg.m_grouped_fp8_gemm_nt_contiguous(cqa, csfa, cqb, csfb, mi, d=dc)
+    _replay_matches_eager(fn, [d, dc])
