@@ -205,15 +205,25 @@ def test_dense_256_row_tiles_exact_many_tiles_per_sm(bn):
     _no_device_error()
 
 
-def test_dense_c_aliases_d():
-    M, N, K = 192, 256, 512
+@pytest.mark.parametrize("tiles", ["auto", "256x192", "256x224"])
+def test_dense_c_aliases_d(tiles):
+    """D may be C itself: every element's C is read before its D is written
+    (the 128-row epilogue fetches C a chunk ahead, the 256-row one a half
+    ahead)."""
+    M, N, K = 192 if tiles == "auto" else 520, 256 if tiles == "auto" else 392, 512
     w = workloads.dense(M, N, K, seed=5, with_c=True)
     qa, _, sa = P.quantize(w.a, 1)
     qb, _, sb = P.quantize(w.b, 128)
     args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
-    ref = dg.fp8_gemm_nt(*args, c=w.c.cuda())
-    inplace = w.c.cuda().clone()
-    dg.fp8_gemm_nt(*args, d=inplace, c=inplace)
+    if tiles == "auto":
+        ref = dg.fp8_gemm_nt(*args, c=w.c.cuda())
+        inplace = w.c.cuda().clone()
+        dg.fp8_gemm_nt(*args, d=inplace, c=inplace)
+    else:
+        with tall_tiles(int(tiles.split("x")[1])):
+            ref = dg.fp8_gemm_nt(*args, c=w.c.cuda())
+            inplace = w.c.cuda().clone()
+            dg.fp8_gemm_nt(*args, d=inplace, c=inplace)
     assert torch.equal(inplace.view(torch.int16), ref.view(torch.int16))
 
 
