@@ -1218,6 +1218,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             continue;
           }
         }
+        // K-grouped: FP32 rows of D[g] (+ C[g]).  A quarter whose 32 rows all
+        // lie inside M goes through the TMA store; one that crosses M (into
+        // the next expert's rows) does not.
+        auto kgrouped_chunk = [&](const uint32_t(&cur)[32], int col0) {
+          if (row0 + 32 <= args.m) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = k_empty ? 0.0f : __uint_as_float(cur[i]);
+            if (crow32) {
+#pragma unroll
+              for (int p = 0; p < 8; ++p) {
+                if (col0 + 4 * p < args.n) {
+                  const float4 c4 = *reinterpret_cast<const float4*>(crow32 + col0 + 4 * p);
+                  f[4 * p] += c4.x;
+                  f[4 * p + 1] += c4.y;
+                  f[4 * p + 2] += c4.z;
+                  f[4 * p + 3] += c4.w;
+                }
+              }
+            }
+            emit_chunk_tma_f32(f, ebuf, nchunk, &tm_d, col0, args.n, out_row0, lane);
+          } else if (row_ok) {
+            store_row_chunk_f32(cur, drow32 + col0, crow32 ? crow32 + col0 : nullptr, args.n - col0,
+                                k_empty);
+          }
+        };
+        if constexpr (MODE == kKGrouped && NUM_ACC == 1 && NCH == 8) {
+          // single 256-column accumulator: each 128-column half is read from
+          // TMEM in full before it is stored, so TMEM goes back to the MMA
+          // once the second half is read rather than once it is stored
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t hv[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(taddr + (hh * 4 + c) * 32, hv[c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc_wait_ld_regs(hv[c]);
+            if (hh == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(tempty(acc));
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int col0 = tile.nb * BN + (hh * 4 + c) * 32;
+              if (col0 < args.n) kgrouped_chunk(hv[c], col0);
+            }
+          }
+          continue;
+        }
         uint32_t ra[32], rb[32];
         tc_ld_32x32b_x32(taddr, ra);
 #pragma unroll
@@ -1239,29 +1289,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int col0 = tile.nb * BN + ch * 32;
           if (col0 >= args.n) continue;
           if (MODE == kKGrouped) {
-            // a quarter whose 32 rows all lie inside M goes through the TMA
-            // store; one that crosses M (into the next expert's rows) does not
-            if (row0 + 32 <= args.m) {
-              float f[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) f[i] = k_empty ? 0.0f : __uint_as_float(cur[i]);
-              if (crow32) {
-#pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                  if (col0 + 4 * p < args.n) {
-                    const float4 c4 = *reinterpret_cast<const float4*>(crow32 + col0 + 4 * p);
-                    f[4 * p] += c4.x;
-                    f[4 * p + 1] += c4.y;
-                    f[4 * p + 2] += c4.z;
-                    f[4 * p + 3] += c4.w;
-                  }
-                }
-              }
-              emit_chunk_tma_f32(f, ebuf, nchunk, &tm_d, col0, args.n, out_row0, lane);
-            } else if (row_ok) {
-              store_row_chunk_f32(cur, drow32 + col0, crow32 ? crow32 + col0 : nullptr, args.n - col0,
-                                  k_empty);
-            }
+            kgrouped_chunk(cur, col0);
             continue;
           }
           if (use_tma) {
