@@ -1155,12 +1155,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ++n_xchg;
           continue;
         }
-        if constexpr (MH == 2) {
+        if constexpr (MH == 2 || (NUM_ACC == 1 && MODE != kKGrouped && KSPLIT == 1)) {
           {
-            // 256-row tile: the whole half is read from TMEM, C added and the
-            // sum rounded to BF16 in registers first, so the single
-            // accumulator goes back to the MMA before the second half's
-            // stores instead of after.  pk first holds this lane's row of C.
+            // A single accumulator (256-row tiles, or 256 columns): the whole
+            // half (the whole row of 256 columns) is read from TMEM, C added
+            // and the sum rounded to BF16 in registers first, so TMEM goes
+            // back to the MMA before the (second half's) stores instead of
+            // after.  pk first holds this lane's row of C.
             uint32_t pk[NCH][16];
             if (args.c) {
 #pragma unroll
