@@ -44,7 +44,7 @@ def parse_args():
                    choices=["prefill", "decode", "contiguous", "masked", "kgrouped", "fp32scales", "small"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--pdl", action="store_true",
-                   help="decode/masked/contiguous/kgrouped: launch with programmatic dependent launch")
+                   help="launch the library's kernels with programmatic dependent launch")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--profile-steps", type=int, default=0,
                    help="run this many untimed steps and exit (for an external profiler)")
@@ -304,6 +304,7 @@ def prefill_roofline(res, fp8_peak, peak_source):
 
 
 def run_prefill(args, ranks, dg, workloads, dev):
+    dg.set_pdl(bool(args.pdl))
     shapes = prefill_setup(dg, workloads, dev, args.shape)
     if args.profile_steps:
         for _ in range(args.profile_steps):
@@ -675,7 +676,7 @@ def main():
                                "(1x128, packed UE8M0), D = A@B.T and D2 = C + A@B.T per shape; B "
                                "quantised (128x128) once at setup" % (workloads.PREFILL_NK,),
                    "l2": "inputs larger than L2 (per-step working set %.2f GB)" % res["working_set_gb"],
-                   "replicas": ranks.world},
+                   "replicas": ranks.world, "pdl": bool(args.pdl)},
         "roofline": prefill_roofline(res, fp8_peak, "%s bf16 burst %.1f TFLOP/s x %.1f nominal FP8:BF16 ratio" %
                                      (peak_src, peaks["bf16_tflops"], FP8_OVER_BF16)),
         "gpu_launches": res["launches"],
