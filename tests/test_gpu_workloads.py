@@ -20,7 +20,9 @@ pytestmark = pytest.mark.gpu
 
 def _sample_rows(m, seed, extra=48):
     rng = np.random.default_rng(seed)
-    fixed = [0, 1, 2, 127, 128, 129, m // 2, m - 129, m - 128, m - 2, m - 1]
+    # 128- and 256-row tile boundaries (both tile heights run at these sizes)
+    fixed = [0, 1, 2, 127, 128, 129, 255, 256, 257, m // 2, m - 257, m - 256, m - 129, m - 128,
+             m - 2, m - 1]
     rows = set(r for r in fixed if 0 <= r < m)
     rows.update(rng.choice(m, size=min(extra, m), replace=False).tolist())
     return np.array(sorted(rows), dtype=np.int64)
