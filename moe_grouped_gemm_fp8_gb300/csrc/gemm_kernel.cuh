@@ -999,8 +999,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!warp_wait<kSuspendHintNs>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
       tc_fence_after();
       bool stop = false;
+      bool both_halves = false;  // the first half's pass stored both (256 x 192 dense)
       // the tile's 128-row halves in turn; TMEM goes back after the last one
       for (int h = 0; h < MH; ++h) {
+        if (both_halves) break;
         const bool last_half = h == MH - 1;
         // contiguous 256-row tiles: the halves are the pair's blocks; the
         // second half of a half-empty pair stores nothing
@@ -1153,6 +1155,68 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)o));
           }
           ++n_xchg;
+          continue;
+        }
+        if constexpr (MODE == kDense && MH == 2 && NCH == 6) {
+          // 256 x 192 dense tile: both halves (2 x 96 words of BF16 pairs,
+          // + C) are read into registers before any store, so TMEM goes back
+          // to the MMA after 12 TMEM loads rather than after half the stores
+          const int row0b = row0 + kBlockM;
+          const bool row_ok_b = row0b + lane < args.m;
+          uint32_t pa[NCH][16], pb[NCH][16];
+          if (args.c) {
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              const int col0 = tile.nb * BN + ch * 32;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const bool in_n = col0 + 8 * q < args.n;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u), w = v;
+                if (row_ok && in_n) v = __ldg(reinterpret_cast<const uint4*>(crow + col0 + 8 * q));
+                if (row_ok_b && in_n)
+                  w = __ldg(reinterpret_cast<const uint4*>(crow + (int64_t)kBlockM * args.ldc + col0 + 8 * q));
+                pa[ch][4 * q] = v.x; pa[ch][4 * q + 1] = v.y; pa[ch][4 * q + 2] = v.z; pa[ch][4 * q + 3] = v.w;
+                pb[ch][4 * q] = w.x; pb[ch][4 * q + 1] = w.y; pb[ch][4 * q + 2] = w.z; pb[ch][4 * q + 3] = w.w;
+              }
+            }
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              uint32_t v[32];
+              tc_ld_32x32b_x32(taddr + hh * BN + ch * 32, v);
+              tc_wait_ld_regs(v);
+              uint32_t(&pk)[16] = hh ? pb[ch] : pa[ch];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float lo = __uint_as_float(v[2 * i]), hi = __uint_as_float(v[2 * i + 1]);
+                if (args.c) {
+                  lo += __uint_as_float(pk[i] << 16);
+                  hi += __uint_as_float(pk[i] & 0xFFFF0000u);
+                }
+                pk[i] = pack_bf16x2(lo, hi);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty(acc));
+          both_halves = true;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            if (hh == 1 && row0b >= args.m) break;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              const int col0 = tile.nb * BN + ch * 32;
+              if (col0 >= args.n) continue;
+              uint8_t* buf = ebuf + (nchunk & 1u) * kEpiBuf;
+              if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+              __syncwarp();
+              emit_packed_tma(hh ? pb[ch] : pa[ch], buf, &tm_d, col0, out_row0 + hh * kBlockM, lane);
+              ++nchunk;
+            }
+          }
           continue;
         }
         if constexpr (MH == 2 || (NUM_ACC == 1 && MODE != kKGrouped && KSPLIT == 1)) {
