@@ -1,6 +1,8 @@
 // FP8 GEMM with fine-grained scaling on sm_103a: D = C + A @ B.T, dense and
-// M-grouped (contiguous / masked).  Kernel template; each tile width BN is
-// instantiated in its own translation unit (gemm_bn*.cu).
+// M-grouped (contiguous / masked), K-grouped, and the NN / TN / TT layouts.
+// Kernel template; each tile width BN is instantiated in its own translation
+// unit (gemm_bn*.cu), the split-K clusters in gemm_splitk.cu, the 256-row and
+// 64-row-A-slot tiles in gemm_tall.cu.
 //
 // Operation and layouts: "DeepGEMM: kernels GEMM FP8 limpos e eficientes por
 // meio de scaling granular" (pt.news.hada.io), sections "Interface GEMM e
@@ -12,11 +14,12 @@
 // FP32 accumulator lives in TMEM, so no CUDA-core promotion is needed.
 //
 // One persistent CTA per SM, 7 warps:
-//   warp 0      TMA producer (one lane): A tile [128 x 128] and B tile
+//   warp 0      TMA producer (one lane): A tile [BM x 128] and B tile
 //               [BN x 128] (E4M3, 128-byte swizzle) per 128-wide K block into
 //               an S-stage ring.
 //   warp 1      MMA issuer (one lane, kept free of any other work): per K
-//               block issues four 128 x BN x 32 block-scaled MMAs, the
+//               block issues four 128 x BN x 32 block-scaled MMAs per 128-row
+//               half of the tile (BM = 256: two halves sharing B), the
 //               instruction descriptor selecting the byte of the current K
 //               block in the pack's scale slot; commits the stage back to the
 //               producer.  Also owns the TMEM allocation.
@@ -37,8 +40,11 @@
 //               Quarters of grouped tiles with rows that must stay untouched
 //               use row-predicated 16-byte stores instead.  TMEM is released
 //               as soon as the last chunk is in registers.
-// The accumulator is double-buffered in TMEM when 2 x BN columns leave room
-// for the scales, so the epilogue of one tile overlaps the next tile's MMAs.
+// The accumulator is double-buffered in TMEM when 2 x BM/128 x BN columns
+// leave room for the scales, so the epilogue of one tile overlaps the next
+// tile's MMAs.  A single accumulator (128 x 256, 256-row tiles) is read into
+// registers (rounded to BF16) in as few steps as registers allow before any
+// store, so the MMA waits only for the TMEM loads.
 //
 // Split-K (KSPLIT = 2 or 4, dense only, for problems with fewer output tiles
 // than SMs): a cluster of KSPLIT CTAs shares each output tile, CTA r taking a
