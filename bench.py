@@ -205,8 +205,9 @@ def algorithmic_bytes_gemm(m, n, k, with_c):
 
 def oracle_sample(workloads, rows_per_shape, seed=0):
     """Bounded sample of the prefill workload for the CPU oracle: per shape,
-    `rows_per_shape` rows of A (quantised 1x128 by the oracle) against the
-    oracle-quantised B, computing D and D2 = C + D for those rows."""
+    `rows_per_shape` randomly chosen rows of A (quantised 1x128 by the oracle)
+    against the oracle-quantised B, computing D and D2 = C + D for those rows.
+    `take(items, r)` keeps the first r of them (still a random subset)."""
     import oracle
     rng = np.random.default_rng(seed)
     items = []
@@ -214,11 +215,16 @@ def oracle_sample(workloads, rows_per_shape, seed=0):
         m, n, k = cfg["m"], cfg["n"], cfg["k"]
         w = workloads.dense(m, n, k, cfg["seed"], with_c=True)
         qb, _, sb = oracle.quantize(w.b.numpy(), 128)
-        rows = np.sort(rng.choice(m, size=rows_per_shape, replace=False))
+        rows = rng.choice(m, size=min(m, rows_per_shape), replace=False)
         a_rows = np.ascontiguousarray(w.a.numpy()[rows])
         c_rows = np.ascontiguousarray(w.c[torch.from_numpy(rows)].view(torch.int16).numpy().view(np.uint16))
         items.append(dict(n=n, k=k, a=a_rows, c=c_rows, qb=qb, sb=sb))
     return items
+
+
+def take(items, rows):
+    return [dict(it, a=np.ascontiguousarray(it["a"][:rows]), c=np.ascontiguousarray(it["c"][:rows]))
+            for it in items]
 
 
 def oracle_run(items):
@@ -233,15 +239,27 @@ def oracle_run(items):
     return flops
 
 
-def cpu_baseline(workloads, rows_per_shape=16):
+def calibrated_rows(items, seconds, probe_rows=16):
+    """Rows per prefill shape that keep one oracle pass near `seconds` of wall
+    time on this host: time a small probe pass, then scale linearly (at most
+    the rows the sample holds)."""
+    t0 = time.perf_counter()
+    oracle_run(take(items, probe_rows))
+    dt = max(time.perf_counter() - t0, 1e-3)
+    return int(min(len(items[0]["a"]), max(probe_rows, probe_rows * seconds / dt)))
+
+
+def cpu_baseline(workloads, seconds=12.0):
     import oracle
-    items = oracle_sample(workloads, rows_per_shape)
+    items = oracle_sample(workloads, 2048)
+    rows_per_shape = calibrated_rows(items, seconds)
+    items = take(items, rows_per_shape)
     t0 = time.perf_counter()
     flops = oracle_run(items)
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.get_threads(),
             "kind": "oracle",
-            "sample": "%d rows of A per prefill shape (quantise + D and C + D rows), FP64, %.1f s" %
+            "sample": "%d random rows of A per prefill shape (quantise + D and C + D rows), FP64, %.1f s" %
                       (rows_per_shape, dt)}
 
 
@@ -250,8 +268,9 @@ def run_reference(args, ranks):
     import oracle
     if ranks.rank != 0:
         return 0
-    rows = 4
-    items = oracle_sample(workloads, rows)
+    items = oracle_sample(workloads, 2048)
+    rows = calibrated_rows(items, 0.5)
+    items = take(items, rows)
     for _ in range(args.warmup):
         oracle_run(items)
     t0 = time.perf_counter()
