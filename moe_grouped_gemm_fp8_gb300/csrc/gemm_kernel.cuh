@@ -35,8 +35,10 @@
 //               quarter each, 32 columns at a time, the next chunk loading
 //               while the current one is converted), + C, round to BF16.  A
 //               32 x 32 chunk is staged in shared memory (64-byte swizzle,
-//               conflict-free for one row per thread) and written by a TMA
-//               store; C arrives through coalesced loads staged the same way.
+//               conflict-free for one row per thread; two staging chunks
+//               per warp) and written by a TMA store; C arrives through
+//               coalesced loads staged the same way, a whole tile's worth
+//               issued before the accumulator is ready.
 //               Quarters of grouped tiles with rows that must stay untouched
 //               use row-predicated 16-byte stores instead.  TMEM is released
 //               as soon as the last chunk is in registers.
@@ -996,12 +998,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int t = first_tile; t < sched.total; t += tile_stride) {
       Tile tile;
       if (!sched.get(t, tile)) continue;
-      // Dense tiles with C (128-row, no split): C of the next chunk is
-      // fetched while the current one is processed, the first chunk's while
-      // the accumulator is still being computed.
-      const bool c_ahead = is_dense_mode(MODE) && MH == 1 && KSPLIT == 1 && args.c != nullptr;
-      uint4 cA[4], cB[4];
-      if (c_ahead) load_c_chunk(cA, args, tile.nb * BN, tile.mb * BM + quarter * 32, tile.mb * BM + quarter * 32, lane);
+      // C of dense tiles is fetched while the accumulator is still being
+      // computed, so the epilogue never waits for a load from HBM.  128-row
+      // tiles with two accumulators (no split): this quarter's whole C tile,
+      // coalesced (BN / 32 chunks, 16 registers each).  Register-held
+      // epilogues (one accumulator): this lane's row of C as BF16 pairs, for
+      // the first 128-row half (both halves of a 256 x 192 tile); the
+      // epilogue adds the accumulator in place.
+      const bool c_ahead =
+          is_dense_mode(MODE) && MH == 1 && KSPLIT == 1 && NUM_ACC == 2 && args.c != nullptr;
+      uint4 cpre[BN / 32][4];
+      if (c_ahead) {
+        const int crow0 = tile.mb * BM + quarter * 32;
+#pragma unroll
+        for (int ch = 0; ch < BN / 32; ++ch) load_c_chunk(cpre[ch], args, tile.nb * BN + ch * 32, crow0, crow0, lane);
+      }
+      constexpr bool kRegHeld = MH == 2 || (NUM_ACC == 1 && MODE != kKGrouped && KSPLIT == 1);
+      constexpr int kPreHalves = (MODE == kDense && MH == 2 && BN == 192) ? 2 : 1;
+      uint32_t cpk[kPreHalves][BN / 32][16];
+      if (kRegHeld && is_dense_mode(MODE) && args.c != nullptr) {
+#pragma unroll
+        for (int hh = 0; hh < kPreHalves; ++hh) {
+          const int crow = tile.mb * BM + hh * kBlockM + quarter * 32 + lane;
+#pragma unroll
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            const int col0 = tile.nb * BN + ch * 32;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v = make_uint4(0u, 0u, 0u, 0u);
+              if (crow < args.m && col0 + 8 * q < args.n)
+                v = __ldg(reinterpret_cast<const uint4*>(args.c + (int64_t)crow * args.ldc + col0 + 8 * q));
+              cpk[hh][ch][4 * q] = v.x;
+              cpk[hh][ch][4 * q + 1] = v.y;
+              cpk[hh][ch][4 * q + 2] = v.z;
+              cpk[hh][ch][4 * q + 3] = v.w;
+            }
+          }
+        }
+      }
       if (!warp_wait<kSuspendHintNs>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
       tc_fence_after();
       bool stop = false;
@@ -1168,24 +1202,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // + C) are read into registers before any store, so TMEM goes back
           // to the MMA after 12 TMEM loads rather than after half the stores
           const int row0b = row0 + kBlockM;
-          const bool row_ok_b = row0b + lane < args.m;
-          uint32_t pa[NCH][16], pb[NCH][16];
-          if (args.c) {
-#pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-              const int col0 = tile.nb * BN + ch * 32;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const bool in_n = col0 + 8 * q < args.n;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u), w = v;
-                if (row_ok && in_n) v = __ldg(reinterpret_cast<const uint4*>(crow + col0 + 8 * q));
-                if (row_ok_b && in_n)
-                  w = __ldg(reinterpret_cast<const uint4*>(crow + (int64_t)kBlockM * args.ldc + col0 + 8 * q));
-                pa[ch][4 * q] = v.x; pa[ch][4 * q + 1] = v.y; pa[ch][4 * q + 2] = v.z; pa[ch][4 * q + 3] = v.w;
-                pb[ch][4 * q] = w.x; pb[ch][4 * q + 1] = w.y; pb[ch][4 * q + 2] = w.z; pb[ch][4 * q + 3] = w.w;
-              }
-            }
-          }
+          // C of both halves is already in cpk (fetched before the wait)
+          uint32_t(&pa)[NCH][16] = cpk[0];
+          uint32_t(&pb)[NCH][16] = cpk[kPreHalves - 1];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -1231,9 +1250,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // half (the whole row of 256 columns) is read from TMEM, C added
             // and the sum rounded to BF16 in registers first, so TMEM goes
             // back to the MMA before the (second half's) stores instead of
-            // after.  pk first holds this lane's row of C.
-            uint32_t pk[NCH][16];
-            if (args.c) {
+            // after.  pk first holds this lane's row of C: the first half's
+            // was fetched before the wait, the second half's is fetched once
+            // the first half's stores have been issued.
+            uint32_t(&pk)[NCH][16] = cpk[0];
+            if (args.c && h > 0) {
 #pragma unroll
               for (int ch = 0; ch < NCH; ++ch) {
                 const int col0 = tile.nb * BN + ch * 32;
@@ -1345,9 +1366,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int ch = 0; ch < NCH; ++ch) {
           uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
           uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
-          uint4(&c_cur)[4] = (ch & 1) ? cB : cA;
-          uint4(&c_nxt)[4] = (ch & 1) ? cA : cB;
-          if (c_ahead && ch + 1 < NCH) load_c_chunk(c_nxt, args, tile.nb * BN + (ch + 1) * 32, out_row0, row0, lane);
           tc_wait_ld_regs(cur);
           if (ch + 1 < NCH) {
             tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
@@ -1370,7 +1388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             float f[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(cur[i]);
-            if (c_ahead) emit_chunk_tma_c(f, c_cur, buf, &tm_d, col0, out_row0, lane);
+            if (c_ahead) emit_chunk_tma_c(f, cpre[ch], buf, &tm_d, col0, out_row0, lane);
             else emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, is_dense_mode(MODE), lane);
             ++nchunk;
           } else if (row_ok) {

@@ -240,8 +240,10 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
     return forced;
   static const int widths[4] = {128, 192, 224, 256};
   static const double rate[4] = {1.0, 1.35, 1.5, 1.6};  // per-column MMA throughput
-  // epilogue not overlapped with MMAs (only the single-accumulator width)
-  const double epi_blocks[4] = {0.5, 0.5, 0.5, with_c ? 10.0 : 4.0};
+  // epilogue time not hidden behind MMAs, in K blocks: a little for two
+  // accumulators (reading C costs ~3 more), more for the single-accumulator width
+  const double epi_blocks[4] = {with_c ? 3.5 : 0.5, with_c ? 3.5 : 0.5, with_c ? 3.5 : 0.5,
+                                with_c ? 10.0 : 4.0};
   const int sms = slots > 0 ? slots : 1;
   int best = pair ? 256 : 128;
   double best_cost = 1e300;
@@ -262,9 +264,9 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
 // (time of one K block of a 128 x 256 tile = 160), from measured rates: a
 // K block of a 256 x 192 tile costs ~221 units and of a 256 x 224 tile ~237;
 // the single accumulator's epilogue does not overlap the next tile (~6 K
-// blocks without C; with C, whose epilogue keeps FP32 chunks and reads C,
-// ~16 and ~21).  Returns the width, or 0 when no 256-row tile beats
-// `best_cost` (the 128-row estimate) by 3%.
+// blocks without C; ~11 and ~16.5 with C, fetched before the accumulator is
+// ready).  Returns the width, or 0 when no 256-row tile beats `best_cost` (the
+// 128-row estimate) by 3%.
 int choose_tall_block_n(int64_t m, int64_t n, int64_t k_blocks, int slots, bool with_c,
                         double best_cost) {
   const int forced_m = env_int("DG_BLOCK_M", 0);
@@ -275,7 +277,7 @@ int choose_tall_block_n(int64_t m, int64_t n, int64_t k_blocks, int slots, bool 
   static const int widths[2] = {192, 224};
   static const double per_kb[2] = {221.0, 237.0};
   static const double epi[2] = {6.2, 6.5};
-  static const double epi_c[2] = {16.0, 21.0};
+  static const double epi_c[2] = {11.0, 16.5};
   const int sms = slots > 0 ? slots : 1;
   const int64_t m_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
   int best = 0;
@@ -297,7 +299,7 @@ double dense_tile_cost(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots,
   static const double rate[4] = {1.0, 1.35, 1.5, 1.6};
   int i = 0;
   while (i < 3 && widths[i] != bn) ++i;
-  const double epi = bn == 256 ? (with_c ? 10.0 : 4.0) : 0.5;
+  const double epi = bn == 256 ? (with_c ? 10.0 : 4.0) : (with_c ? 3.5 : 0.5);
   const int sms = slots > 0 ? slots : 1;
   const int64_t tiles = m_blocks * ((n + bn - 1) / bn);
   const int64_t waves = (tiles + sms - 1) / sms;
