@@ -405,6 +405,35 @@ def test_masked_all_zero_writes_nothing():
     _no_device_error()
 
 
+
+@pytest.mark.parametrize("tiles", [("cta", 128), ("cta", 192), ("cta", 224), ("cta", 256),
+                                   ("pair", 256), ("tall", 192), ("tall", 224)],
+                         ids=lambda t: "%s%d" % t)
+def test_dense_c_exact_many_tiles_per_sm(tiles):
+    """D = C + A@B.T with exact integer products and an integer C (so the FP32
+    sum is exact and D is the bit-exact BF16 rounding of the oracle) on three
+    SMs: every CTA runs many ragged tiles, and each tile's C is fetched while
+    its accumulator is still being computed."""
+    kind, bn = tiles
+    rng = np.random.default_rng(41 + bn)
+    M, N, K = 600, 520, 1024
+    qa, qb = _int_operand(rng, M, K), _int_operand(rng, N, K)
+    ea = rng.integers(-2, 3, size=(M, K // 128))
+    eb = rng.integers(-2, 3, size=((N + 127) // 128, K // 128))
+    sa, sb = np.ldexp(1.0, ea), np.ldexp(1.0, eb)
+    c = torch.from_numpy(rng.integers(-64, 65, size=(M, N)).astype(np.float32)).to(torch.bfloat16)
+    want = oracle.bf16_rne(oracle.gemm_nt(qa, sa, qb, sb, P.bf16_bits(c)))
+    args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    ctx = tall_tiles(bn) if kind == "tall" else tile_config((1 if kind == "pair" else 0, bn))
+    dg.set_num_sms(3)
+    try:
+        with ctx:
+            got = P.bf16_bits(dg.fp8_gemm_nt(*args, c=c.cuda()))
+    finally:
+        dg.set_num_sms(0)
+    assert np.array_equal(got, want)
+    _no_device_error()
+
 def test_num_sms_limit_does_not_change_results():
     M, N, K = 512, 1024, 512
     w = workloads.dense(M, N, K, seed=9)
