@@ -1251,10 +1251,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // and the sum rounded to BF16 in registers first, so TMEM goes
             // back to the MMA before the (second half's) stores instead of
             // after.  pk first holds this lane's row of C: the first half's
-            // was fetched before the wait, the second half's is fetched once
-            // the first half's stores have been issued.
+            // was fetched before the wait; the second half's chunk c is
+            // fetched into pk[c] as soon as the first half's chunk c has been
+            // staged for its store (dense 256-row tiles).
             uint32_t(&pk)[NCH][16] = cpk[0];
-            if (args.c && h > 0) {
+            if (args.c && h > 0 && !(is_dense_mode(MODE) && MH == 2)) {
 #pragma unroll
               for (int ch = 0; ch < NCH; ++ch) {
                 const int col0 = tile.nb * BN + ch * 32;
@@ -1306,6 +1307,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               __syncwarp();
               emit_packed_tma(pk[ch], buf, &tm_d, col0, out_row0, lane);
               ++nchunk;
+              if (is_dense_mode(MODE) && MH == 2 && h == 0 && args.c) {
+                // the second half's C of these columns, into the registers just staged
+                const int row1 = row + kBlockM;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                  if (row1 < args.m && col0 + 8 * q < args.n)
+                    v = __ldg(reinterpret_cast<const uint4*>(args.c + (int64_t)row1 * args.ldc + col0 + 8 * q));
+                  pk[ch][4 * q] = v.x;
+                  pk[ch][4 * q + 1] = v.y;
+                  pk[ch][4 * q + 2] = v.z;
+                  pk[ch][4 * q + 3] = v.w;
+                }
+              }
             }
             continue;
           }
