@@ -302,7 +302,7 @@ def run_reference(args, ranks):
 # ncu capture summarised in profiles/fp8_gemm_bm256_bn192_m4096_n7168_k16384.md
 # (D = A @ B.T, M=4096 N=7168 K=16384, 256 x 192 tiles).
 DOMINANT_SHAPE = (4096, 7168, 16384, False)
-DOMINANT_TRAFFIC = 366.9e6 + 47.7e6
+DOMINANT_TRAFFIC = 366.6e6 + 47.1e6
 
 
 def prefill_roofline(res, fp8_peak, peak_source):
