@@ -37,16 +37,17 @@
 //               32 x 32 chunk is staged in shared memory (64-byte swizzle,
 //               conflict-free for one row per thread; two staging chunks
 //               per warp) and written by a TMA store; C arrives through
-//               coalesced loads staged the same way, a whole tile's worth
-//               issued before the accumulator is ready.
+//               coalesced loads staged the same way, the quarter's whole C
+//               tile issued before the accumulator is ready.
 //               Quarters of grouped tiles with rows that must stay untouched
 //               use row-predicated 16-byte stores instead.  TMEM is released
 //               as soon as the last chunk is in registers.
 // The accumulator is double-buffered in TMEM when 2 x BM/128 x BN columns
 // leave room for the scales, so the epilogue of one tile overlaps the next
 // tile's MMAs.  A single accumulator (128 x 256, 256-row tiles) is read into
-// registers (rounded to BF16) in as few steps as registers allow before any
-// store, so the MMA waits only for the TMEM loads.
+// registers in as few steps as registers allow before any store, so the MMA
+// waits only for the TMEM loads: each lane's row of C (BF16 pairs, fetched
+// before the accumulator is ready) is added in place and rounded to BF16.
 //
 // Split-K (KSPLIT = 2 or 4, dense only, for problems with fewer output tiles
 // than SMs): a cluster of KSPLIT CTAs shares each output tile, CTA r taking a
