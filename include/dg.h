@@ -263,6 +263,23 @@ int64_t dg_get_tma_aligned_size(int64_t x, int32_t element_size);
 /* Row alignment of each expert segment in the contiguous layout: 128. */
 int32_t dg_get_mk_alignment_for_contiguous_layout(void);
 
+/* The tile configuration dg_fp8_gemm_nt chooses for an M x N x K problem,
+ * with C (has_c != 0) or without, on a device with num_sms SMs (pass the
+ * device's SM count, or the dg_set_num_sms limit when one is set).  Pure host
+ * arithmetic: no device, no CUDA call.  The DG_BLOCK_M, DG_BLOCK_N, DG_SPLIT_K
+ * and DG_CTA_PAIR environment overrides apply as they do to the call.
+ * Writes block_m (rows of A per output tile: 64 for the 64-row A slots of a
+ * single short M block, 128, or 256), block_n (columns per tile), split_k
+ * (CTAs of one cluster sharing each tile's K blocks: 1, 2 or 4) and cta_pair
+ * (1 when a 256-row tile spans two CTAs).  All four are 0 for an empty
+ * problem.  Errors as dg_fp8_gemm_nt's shape checks; num_sms < 1 or a NULL
+ * output gives DG_ERR_INVALID_ARG.  Cited: same page, section "Utilitários e
+ * variáveis de ambiente" (DG_PRINT_CONFIGS prints the configuration chosen
+ * for a shape); this query returns it instead. */
+dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,
+                              int32_t* block_m, int32_t* block_n, int32_t* split_k,
+                              int32_t* cta_pair);
+
 /* Upper bound on the SMs the persistent GEMM grid uses; 0 = all SMs of the
  * device.  Process-wide; returns DG_ERR_INVALID_ARG for n < 0. */
 dg_status dg_set_num_sms(int32_t n);

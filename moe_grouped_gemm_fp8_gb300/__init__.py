@@ -21,6 +21,7 @@ from .api import (  # noqa: F401
     k_grouped_fp8_gemm_tn_contiguous,
     m_grouped_fp8_gemm_nt_contiguous,
     m_grouped_fp8_gemm_nt_masked,
+    plan_fp8_gemm_nt,
     quantize_fp8,
     quantize_fp8_cols,
     set_num_sms,

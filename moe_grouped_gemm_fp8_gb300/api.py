@@ -61,6 +61,19 @@ def get_mk_alignment_for_contiguous_layout() -> int:
     return int(_lib.lib().dg_get_mk_alignment_for_contiguous_layout())
 
 
+def plan_fp8_gemm_nt(m: int, n: int, k: int, has_c: bool = False, num_sms: int = 152) -> dict:
+    """The tile configuration fp8_gemm_nt chooses for an M x N x K problem on
+    a device with num_sms SMs, computed on the host (no GPU needed):
+    {"block_m": 64 | 128 | 256, "block_n": ..., "split_k": 1 | 2 | 4,
+    "cta_pair": bool}; all zero for an empty problem."""
+    out = [C.c_int32(0) for _ in range(4)]
+    st = _lib.lib().dg_plan_fp8_gemm_nt(int(m), int(n), int(k), 1 if has_c else 0, int(num_sms),
+                                        *[C.byref(o) for o in out])
+    _check(st, "dg_plan_fp8_gemm_nt")
+    bm, bn, sk, pair = (int(o.value) for o in out)
+    return {"block_m": bm, "block_n": bn, "split_k": sk, "cta_pair": bool(pair)}
+
+
 def set_num_sms(n: int) -> None:
     _check(_lib.lib().dg_set_num_sms(int(n)), "dg_set_num_sms")
 

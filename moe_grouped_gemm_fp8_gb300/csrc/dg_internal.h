@@ -106,6 +106,12 @@ cudaError_t gemm_fetch_error(unsigned long long* word);  // reads and clears
 cudaError_t error_word_address(unsigned long long** out);
 // 256-row tiles (dense NT, contiguous): block_n 192 or 224; 0 stages = not compiled
 int gemm_tall_stages(int block_n);
+// pipeline stages of the 64-row-A-slot kernels (0: width not supported)
+int gemm_short_stages(int block_n);
+// pipeline stages of the split-K kernels
+int gemm_splitk_stages(int ksplit, bool short_a);
+// pipeline stages of the FP32-scale (promotion) kernel
+int gemm_promote_stages();
 constexpr int kMaxTallPairs = 1024;  // contiguous: most block pairs per launch
 cudaError_t gemm_tall_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,
                              const CUtensorMap& sfa, const CUtensorMap& sfb, const CUtensorMap& d,

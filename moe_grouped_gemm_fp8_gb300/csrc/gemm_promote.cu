@@ -277,6 +277,8 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
   }
 }
 
+int gemm_promote_stages() { return kPromoteStages; }
+
 cudaError_t gemm_promote_launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& d,
                                 GemmArgs args, int grid, cudaStream_t stream) {
   static_assert(promote_smem_bytes() <= (size_t)kSmemLimit, "shared memory over the per-CTA limit");

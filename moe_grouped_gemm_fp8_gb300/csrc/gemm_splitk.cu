@@ -7,6 +7,13 @@ namespace dg {
 
 // short_a: M <= 64, so the A slot of a stage holds 64 rows (8 KB instead of
 // 16) and two more stages fit.
+constexpr int kSplit2Stages = 5, kSplit4Stages = 4, kSplit2ShortStages = 7, kSplit4ShortStages = 6;
+int gemm_splitk_stages(int ksplit, bool short_a) {
+  if (ksplit == 2) return short_a ? kSplit2ShortStages : kSplit2Stages;
+  if (ksplit == 4) return short_a ? kSplit4ShortStages : kSplit4Stages;
+  return 0;
+}
+
 cudaError_t gemm_splitk_launch(int ksplit, bool short_a, const CUtensorMap& a, const CUtensorMap& b,
                                const CUtensorMap& sfa, const CUtensorMap& sfb,
                                const CUtensorMap& d, GemmArgs args, int clusters,
@@ -18,11 +25,11 @@ cudaError_t gemm_splitk_launch(int ksplit, bool short_a, const CUtensorMap& a, c
   args.err = err;
   constexpr int kShort = kBlockM / 2;
   if (ksplit == 2)
-    return short_a ? gemm_launch_impl<128, 7, kDense, 2, kShort>(a, b, sfa, sfb, d, args, 2 * clusters, stream)
-                   : gemm_launch_impl<128, 5, kDense, 2>(a, b, sfa, sfb, d, args, 2 * clusters, stream);
+    return short_a ? gemm_launch_impl<128, kSplit2ShortStages, kDense, 2, kShort>(a, b, sfa, sfb, d, args, 2 * clusters, stream)
+                   : gemm_launch_impl<128, kSplit2Stages, kDense, 2>(a, b, sfa, sfb, d, args, 2 * clusters, stream);
   if (ksplit == 4)
-    return short_a ? gemm_launch_impl<128, 6, kDense, 4, kShort>(a, b, sfa, sfb, d, args, 4 * clusters, stream)
-                   : gemm_launch_impl<128, 4, kDense, 4>(a, b, sfa, sfb, d, args, 4 * clusters, stream);
+    return short_a ? gemm_launch_impl<128, kSplit4ShortStages, kDense, 4, kShort>(a, b, sfa, sfb, d, args, 4 * clusters, stream)
+                   : gemm_launch_impl<128, kSplit4Stages, kDense, 4>(a, b, sfa, sfb, d, args, 4 * clusters, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -33,8 +40,8 @@ int gemm_splitk_max_clusters(int ksplit) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int i = ksplit == 2 ? 0 : 1;
   if (!filled[dev][i]) {
-    cache[dev][i] = ksplit == 2 ? gemm_splitk_max_clusters_impl<128, 5, 2>()
-                                : gemm_splitk_max_clusters_impl<128, 4, 4>();
+    cache[dev][i] = ksplit == 2 ? gemm_splitk_max_clusters_impl<128, kSplit2Stages, 2>()
+                                : gemm_splitk_max_clusters_impl<128, kSplit4Stages, 4>();
     filled[dev][i] = true;
   }
   return cache[dev][i];

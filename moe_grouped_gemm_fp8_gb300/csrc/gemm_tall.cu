@@ -11,7 +11,11 @@ int gemm_tall_stages(int block_n) { return (block_n == 192 || block_n == 224) ? 
 
 // Dense NT with a single M block of at most 64 rows (decode): 64-row A slots,
 // so 8 (BN = 128) or 6 (BN = 192) stages instead of 6 and 4.
-bool gemm_short_supported(int block_n) { return block_n == 128 || block_n == 192; }
+constexpr int kShortStages128 = 8, kShortStages192 = 6;
+int gemm_short_stages(int block_n) {
+  return block_n == 128 ? kShortStages128 : block_n == 192 ? kShortStages192 : 0;
+}
+bool gemm_short_supported(int block_n) { return gemm_short_stages(block_n) > 0; }
 
 cudaError_t gemm_short_launch_impl(int block_n, const CUtensorMap& a, const CUtensorMap& b,
                                    const CUtensorMap& sfa, const CUtensorMap& sfb,
@@ -19,8 +23,8 @@ cudaError_t gemm_short_launch_impl(int block_n, const CUtensorMap& a, const CUte
                                    cudaStream_t stream) {
   constexpr int BM = kBlockM / 2;
   switch (block_n) {
-    case 128: return gemm_launch_impl<128, 8, kDense, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
-    case 192: return gemm_launch_impl<192, 6, kDense, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
+    case 128: return gemm_launch_impl<128, kShortStages128, kDense, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
+    case 192: return gemm_launch_impl<192, kShortStages192, kDense, 1, BM>(a, b, sfa, sfb, d, args, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -335,12 +335,72 @@ int choose_block_n_masked_streaming(int64_t groups, int64_t expected_m, int64_t 
   return best;
 }
 
-void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_n,
-                  int grid, int band, bool pair = false) {
+void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_m,
+                  int block_n, int stages, int grid, int band) {
   if (!env_flag("DG_PRINT_CONFIGS")) return;
   fprintf(stderr, "dg: %s m=%lld n=%lld k=%lld groups=%d block_m=%d block_n=%d stages=%d grid=%d band=%d\n",
-          what, (long long)m, (long long)n, (long long)k, groups, pair ? 256 : 128, block_n,
-          pair ? 6 : gemm_stages(block_n), grid, band);
+          what, (long long)m, (long long)n, (long long)k, groups, block_m, block_n, stages, grid, band);
+}
+
+// Tile configuration of a dense GEMM: pure host arithmetic on the shape and
+// the SM count (the DG_* overrides apply), shared by the launch and by
+// dg_plan_fp8_gemm_nt.
+struct DensePlan {
+  int ksplit = 1;        // CTAs of a cluster sharing each tile's K blocks (1, 2, 4)
+  int block_n = 128;     // output columns per tile
+  bool pair = false;     // 256-row tiles on a pair of CTAs (only on request)
+  bool tall = false;     // 256-row tiles on one CTA
+  bool short_a = false;  // 64-row A slots: a single M block of at most 64 rows
+};
+
+DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int sms) {
+  DensePlan p;
+  const int64_t kb = k / kBlockK;
+  const int64_t m_blocks = (m + kBlockM - 1) / kBlockM;
+  // Split-K over a cluster of 2 or 4 CTAs when 128-column tiles would leave
+  // most SMs idle (decode-sized M); DG_SPLIT_K = 1, 2 or 4 forces a factor.
+  // Every CTA's K slice (ceil(K blocks / factor) blocks) must be non-empty.
+  {
+    const int64_t tiles128 = m_blocks * ((n + 127) / 128);
+    const int forced = env_int("DG_SPLIT_K", 0);
+    if (mode != kDense) p.ksplit = 1;
+    else if (forced == 1 || forced == 2 || forced == 4) p.ksplit = forced;
+    else if (tiles128 * 4 <= sms && kb >= 16) p.ksplit = 4;
+    else if (tiles128 * 2 <= sms && kb >= 8) p.ksplit = 2;
+    while (p.ksplit > 1) {
+      const int64_t per = (kb + p.ksplit - 1) / p.ksplit;
+      if ((p.ksplit - 1) * per < kb) break;
+      p.ksplit /= 2;
+    }
+  }
+  if (p.ksplit > 1) {
+    p.block_n = 128;
+    p.short_a = m <= kBlockM / 2;
+    return p;
+  }
+  // CTA pairs (256-row tiles) only on request (DG_CTA_PAIR=1): on the
+  // measured shapes they match, not beat, single-CTA tiles.
+  p.pair = mode == kDense && sms >= 2 && m_blocks >= 2 && env_int("DG_CTA_PAIR", 0) == 1;
+  if (p.pair) {
+    const int64_t p_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
+    p.block_n = choose_block_n(p_blocks, n, kb, sms / 2, with_c, true);
+    return p;
+  }
+  p.block_n = choose_block_n(m_blocks, n, kb, sms, with_c, false, mode != kDense);
+  // 256-row tiles (dense NT, more than one 128-row block) where the estimate
+  // says they are faster; DG_BLOCK_M=256 (with DG_BLOCK_N 192 or 224) or
+  // DG_BLOCK_M=128 forces the choice.
+  if (mode == kDense && m_blocks >= 2) {
+    const double cost128 = dense_tile_cost(m_blocks, n, kb, sms, with_c, p.block_n);
+    const int tall_n = choose_tall_block_n(m, n, kb, sms, with_c, cost128);
+    if (tall_n != 0 && gemm_tall_stages(tall_n) > 0) {
+      p.tall = true;
+      p.block_n = tall_n;
+    }
+  }
+  // a single M block of at most 64 rows: 64-row A slots, more stages
+  p.short_a = mode == kDense && !p.tall && m <= kBlockM / 2 && gemm_short_supported(p.block_n);
+  return p;
 }
 
 dg_status check_common_k_n(int64_t n, int64_t k) {
@@ -382,31 +442,15 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   if ((s = current_device(&sms)) != DG_OK) return s;
   if ((s = get_encoder()) != DG_OK) return s;
 
+  const DensePlan plan = plan_dense(mode, m, n, k, c != nullptr, sms);
+  const int ksplit = plan.ksplit;
   GemmArgs args = {};
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
-  // Split-K over a cluster of 2 or 4 CTAs when 128-column tiles would leave
-  // most SMs idle (decode-sized M); DG_SPLIT_K = 1, 2 or 4 forces a factor.
-  // Every CTA's K slice (ceil(K blocks / factor) blocks) must be non-empty.
-  int ksplit = 1;
-  {
-    const int64_t kb = k / kBlockK;
-    const int64_t tiles128 = (int64_t)args.m_blocks * ((n + 127) / 128);
-    const int forced = env_int("DG_SPLIT_K", 0);
-    if (mode != kDense) ksplit = 1;
-    else if (forced == 1 || forced == 2 || forced == 4) ksplit = forced;
-    else if (tiles128 * 4 <= sms && kb >= 16) ksplit = 4;
-    else if (tiles128 * 2 <= sms && kb >= 8) ksplit = 2;
-    while (ksplit > 1) {
-      const int64_t per = (kb + ksplit - 1) / ksplit;
-      if ((ksplit - 1) * per < kb) break;
-      ksplit /= 2;
-    }
-  }
   // A single M block shorter than 128 rows loads only round_up(M, 8) rows of A
   // per K block (dense NT; decode-sized M).
   if (mode == kDense && m < kBlockM) args.a_box_rows = (int32_t)((m + 7) / 8 * 8);
   if (ksplit > 1) {
-    const int block_n = 128;
+    const int block_n = plan.block_n;
     Operands o;
     if ((s = encode_a_2d(o, a, sfa, m, k, lda, args.a_box_rows > 0 ? args.a_box_rows : kBlockM)) != DG_OK)
       return s;
@@ -425,48 +469,31 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     args.band = env_int("DG_RASTER_BAND", 16);
     if (args.band < 1) args.band = 1;
     args.timeout_ns = g_timeout_ns.load();
-  args.pdl = g_pdl.load();
+    args.pdl = g_pdl.load();
     const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
     int clusters = gemm_splitk_max_clusters(ksplit);
     if (clusters > sms / ksplit) clusters = sms / ksplit;
     if (tiles < clusters) clusters = (int)tiles;
     if (clusters <= 0) return DG_ERR_CUDA;
     print_config(ksplit == 2 ? "fp8_gemm_nt (split-K 2)" : "fp8_gemm_nt (split-K 4)", m, n, k, 1,
-                 block_n, ksplit * clusters, args.band);
+                 plan.short_a ? kBlockM / 2 : kBlockM, block_n, gemm_splitk_stages(ksplit, plan.short_a),
+                 ksplit * clusters, args.band);
     args.debug_drop_load = env_int("DG_DEBUG_DROP_LOAD", 0);
-    return from_cuda(gemm_splitk_launch(ksplit, m <= kBlockM / 2, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
+    return from_cuda(gemm_splitk_launch(ksplit, plan.short_a, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
                                         static_cast<cudaStream_t>(stream)));
   }
-  // CTA pairs (256-row tiles) only on request (DG_CTA_PAIR=1): on the
-  // measured shapes they match, not beat, single-CTA tiles.
-  const bool pair = mode == kDense && sms >= 2 && args.m_blocks >= 2 &&
-                    env_int("DG_CTA_PAIR", 0) == 1;
+  const bool pair = plan.pair;
+  const bool tall = plan.tall;
+  const int block_n = plan.block_n;
   const int64_t p_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
-  int block_n, clusters = 0;
+  int clusters = 0;
   if (pair) {
-    block_n = choose_block_n(p_blocks, n, k / kBlockK, sms / 2, c != nullptr, true);
     clusters = gemm2_max_clusters(kDense, block_n);
     const int limit = sms / 2;
     if (clusters > limit) clusters = limit;
     if (clusters <= 0) return DG_ERR_CUDA;
-  } else {
-    block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, c != nullptr, false,
-                             mode != kDense);
   }
-  // 256-row tiles (dense NT, more than one 128-row block) where the estimate
-  // says they are faster; DG_BLOCK_M=256 (with DG_BLOCK_N 192 or 224) or
-  // DG_BLOCK_M=128 forces the choice.
-  bool tall = false;
-  if (!pair && mode == kDense && args.m_blocks >= 2) {
-    const double cost128 =
-        dense_tile_cost(args.m_blocks, n, k / kBlockK, sms, c != nullptr, block_n);
-    const int tall_n = choose_tall_block_n(m, n, k / kBlockK, sms, c != nullptr, cost128);
-    if (tall_n != 0 && gemm_tall_stages(tall_n) > 0) {
-      tall = true;
-      block_n = tall_n;
-      args.m_blocks = (int32_t)((m + 2 * kBlockM - 1) / (2 * kBlockM));
-    }
-  }
+  if (tall) args.m_blocks = (int32_t)p_blocks;
   Operands o;
   s = a_mn_major(mode) ? encode_a_mn(o, a, sfa, m, k, lda)
       : tall           ? encode_a_2d(o, a, sfa, m, k, lda, 2 * kBlockM, 2 * kBlockM)
@@ -494,18 +521,20 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   if (pair) {
     if (tiles < clusters) clusters = (int)tiles;
-    print_config("fp8_gemm_nt (cta pair)", m, n, k, 1, block_n, 2 * clusters, args.band, true);
+    print_config("fp8_gemm_nt (cta pair)", m, n, k, 1, 2 * kBlockM, block_n, 6, 2 * clusters, args.band);
     return from_cuda(gemm2_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
                                   static_cast<cudaStream_t>(stream)));
   }
   const int grid = (int)(tiles < sms ? tiles : sms);
   args.debug_drop_load = env_int("DG_DEBUG_DROP_LOAD", 0);
-  print_config(tall ? "fp8_gemm_nt (256-row tiles)" : name, m, n, k, 1, block_n, grid, args.band);
+  print_config(tall ? "fp8_gemm_nt (256-row tiles)" : plan.short_a ? "fp8_gemm_nt (64-row A slots)" : name,
+               m, n, k, 1, tall ? 2 * kBlockM : plan.short_a ? kBlockM / 2 : kBlockM, block_n,
+               tall ? gemm_tall_stages(block_n) : plan.short_a ? gemm_short_stages(block_n) : gemm_stages(block_n),
+               grid, args.band);
   if (tall)
     return from_cuda(gemm_tall_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                       static_cast<cudaStream_t>(stream)));
-  // a single M block of at most 64 rows: 64-row A slots, more stages
-  if (mode == kDense && !pair && m <= kBlockM / 2 && gemm_short_supported(block_n))
+  if (plan.short_a)
     return from_cuda(gemm_short_launch(block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                        static_cast<cudaStream_t>(stream)));
   return from_cuda(gemm_launch(mode, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
@@ -517,6 +546,24 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
                          int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
   return dense_gemm(kDense, "fp8_gemm_nt", a, sfa, b, sfb, c, d, m, n, k, lda, ldb, ldc, ldd,
                     stream);
+}
+
+dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,
+                              int32_t* block_m, int32_t* block_n, int32_t* split_k,
+                              int32_t* cta_pair) {
+  if (!block_m || !block_n || !split_k || !cta_pair) return DG_ERR_INVALID_ARG;
+  *block_m = *block_n = *split_k = *cta_pair = 0;
+  if (m < 0 || num_sms < 1) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (m >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  if (m == 0 || n == 0) return DG_OK;  // nothing is launched
+  const DensePlan p = plan_dense(kDense, m, n, k, has_c != 0, num_sms);
+  *block_m = (p.pair || p.tall) ? 2 * kBlockM : p.short_a ? kBlockM / 2 : kBlockM;
+  *block_n = p.block_n;
+  *split_k = p.ksplit;
+  *cta_pair = p.pair ? 1 : 0;
+  return DG_OK;
 }
 
 dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b, const float* sfb,
@@ -574,7 +621,8 @@ dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b,
   const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  print_config("fp8_gemm_nt_fp32_sf (promotion)", m, n, k, 1, 128, grid, args.band);
+  print_config("fp8_gemm_nt_fp32_sf (promotion)", m, n, k, 1, kBlockM, 128, gemm_promote_stages(), grid,
+               args.band);
   return from_cuda(gemm_promote_launch(o.a, o.b, o.d, args, grid, static_cast<cudaStream_t>(stream)));
 }
 
@@ -654,7 +702,8 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
   print_config(tall ? "m_grouped_fp8_gemm_nt_contiguous (256-row tiles)" : "m_grouped_fp8_gemm_nt_contiguous",
-               m_sum, n, k, num_groups, block_n, grid, args.band);
+               m_sum, n, k, num_groups, tall ? 2 * kBlockM : kBlockM, block_n,
+               tall ? gemm_tall_stages(block_n) : gemm_stages(block_n), grid, args.band);
   if (tall)
     return from_cuda(gemm_tall_launch(kContiguous, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                       static_cast<cudaStream_t>(stream)));
@@ -742,7 +791,8 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa,
   const int64_t tiles = (int64_t)num_groups * args.m_blocks * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  print_config("k_grouped_fp8_gemm_tn_contiguous", m, n, sum_k, num_groups, block_n, grid, args.band);
+  print_config("k_grouped_fp8_gemm_tn_contiguous", m, n, sum_k, num_groups, kBlockM, block_n,
+               gemm_stages(block_n), grid, args.band);
   return from_cuda(gemm_launch(kKGrouped, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid, st));
 }
 
@@ -804,12 +854,13 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
   args.pdl = g_pdl.load();
   if ((int64_t)num_groups * args.m_blocks * args.n_blocks >= kMaxCoord) return DG_ERR_TOO_LARGE;
   if (pair) {
-    print_config("m_grouped_fp8_gemm_nt_masked (cta pair)", max_m, n, k, num_groups, block_n,
-                 2 * grid_units, 0, true);
+    print_config("m_grouped_fp8_gemm_nt_masked (cta pair)", max_m, n, k, num_groups, 2 * kBlockM, block_n,
+                 6, 2 * grid_units, 0);
     return from_cuda(gemm2_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid_units,
                                   static_cast<cudaStream_t>(stream)));
   }
-  print_config("m_grouped_fp8_gemm_nt_masked", max_m, n, k, num_groups, block_n, grid_units, 0);
+  print_config("m_grouped_fp8_gemm_nt_masked", max_m, n, k, num_groups, kBlockM, block_n,
+               gemm_stages(block_n), grid_units, 0);
   return from_cuda(gemm_launch(kMasked, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid_units,
                                static_cast<cudaStream_t>(stream)));
 }

@@ -1,0 +1,148 @@
+"""CPU-only checks of the dense tile chooser (dg_plan_fp8_gemm_nt): the same
+host arithmetic dg_fp8_gemm_nt uses to pick its launch, queried without a
+GPU.  Pins the choices measured fastest on GB300 (152 SMs) for the prefill and
+decode shapes, and checks invariants any choice must satisfy."""
+import ctypes as C
+import os
+from contextlib import contextmanager
+
+import numpy as np
+import pytest
+
+import moe_grouped_gemm_fp8_gb300 as dg
+from moe_grouped_gemm_fp8_gb300 import _lib, workloads
+
+SMS = 152
+OVERRIDES = ("DG_BLOCK_M", "DG_BLOCK_N", "DG_SPLIT_K", "DG_CTA_PAIR")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from moe_grouped_gemm_fp8_gb300 import build
+    build.build()
+
+
+@contextmanager
+def env(**kw):
+    old = {k: os.environ.get(k) for k in OVERRIDES}
+    for k in OVERRIDES:
+        os.environ.pop(k, None)
+    os.environ.update({k: str(v) for k, v in kw.items()})
+    try:
+        yield
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def plan(m, n, k, has_c=False, sms=SMS):
+    p = dg.plan_fp8_gemm_nt(m, n, k, has_c, sms)
+    return p["block_m"], p["block_n"], p["split_k"], p["cta_pair"]
+
+
+# (N, K) -> (block_m, block_n) at M = 4096, with and without C: the tiles the
+# prefill sweeps on GB300 measured fastest (or within noise of it)
+PREFILL_CHOICE = {
+    (2112, 7168): (128, 256),
+    (24576, 1536): (128, 224),
+    (7168, 16384): (256, 192),
+    (4096, 7168): (256, 224),
+    (7168, 2048): (128, 224),
+}
+
+
+@pytest.mark.parametrize("has_c", [False, True])
+def test_prefill_shapes_take_the_measured_tiles(has_c):
+    with env():
+        for cfg in workloads.PREFILL:
+            want = PREFILL_CHOICE[(cfg["n"], cfg["k"])]
+            assert plan(cfg["m"], cfg["n"], cfg["k"], has_c) == want + (1, False), cfg
+
+
+# decode: split-K over clusters of 4 or 2 where 128-column tiles leave SMs idle,
+# none where they already fill the GPU (N = 24576); 64-row A slots for M = 64
+DECODE_CHOICE = {
+    (2112, 7168): (128, 4),
+    (24576, 1536): (192, 1),
+    (7168, 16384): (128, 2),
+    (4096, 7168): (128, 4),
+    (7168, 2048): (128, 2),
+}
+
+
+@pytest.mark.parametrize("m", [64, 128])
+def test_decode_shapes_split_k(m):
+    with env():
+        for cfg in workloads.PREFILL:
+            bn, ks = DECODE_CHOICE[(cfg["n"], cfg["k"])]
+            assert plan(m, cfg["n"], cfg["k"]) == (m if m == 64 else 128, bn, ks, False), cfg
+
+
+def test_invariants_over_random_shapes():
+    rng = np.random.default_rng(5)
+    with env():
+        for _ in range(400):
+            m = int(rng.choice([1, 7, 64, 65, 127, 128, 129, 255, 256, 257, 1000, 4096, 16384]))
+            n = 8 * int(rng.integers(1, 4000))
+            k = 128 * int(rng.integers(1, 130))
+            sms = int(rng.choice([1, 2, 8, 66, 132, 152]))
+            bm, bn, ks, pair = plan(m, n, k, bool(rng.integers(0, 2)), sms)
+            kb = k // 128
+            m_blocks = -(-m // 128)
+            assert bn in (128, 192, 224, 256)
+            assert ks in (1, 2, 4) and not pair
+            if ks > 1:
+                # only when the split's clusters fit on the SMs, every CTA's K slice non-empty
+                assert bn == 128 and m_blocks * (-(-n // 128)) * ks <= sms
+                assert (ks - 1) * (-(-kb // ks)) < kb
+            assert bm in (64, 128, 256)
+            if bm == 64:
+                assert m <= 64 and bn in (128, 192)
+            if bm == 256:
+                assert m > 128 and bn in (192, 224) and ks == 1
+            if m <= 64 and ks == 1 and bn in (128, 192):
+                assert bm == 64
+
+
+def test_environment_overrides():
+    with env(DG_BLOCK_N=192):
+        assert plan(4096, 7168, 16384) == (128, 192, 1, False)  # a forced width means 128-row tiles
+    with env(DG_BLOCK_M=256):
+        assert plan(4096, 2112, 7168) == (256, 192, 1, False)
+    with env(DG_BLOCK_M=256, DG_BLOCK_N=224):
+        assert plan(4096, 2112, 7168) == (256, 224, 1, False)
+    with env(DG_BLOCK_M=128):
+        assert plan(4096, 7168, 16384)[0] == 128
+    with env(DG_SPLIT_K=1):
+        assert plan(64, 4096, 7168)[2] == 1
+    with env(DG_SPLIT_K=2):
+        assert plan(64, 4096, 7168) == (64, 128, 2, False)
+    with env(DG_SPLIT_K=4):
+        assert plan(64, 4096, 256)[2] == 2  # 2 K blocks cannot feed 4 CTAs
+    with env(DG_CTA_PAIR=1):
+        bm, bn, ks, pair = plan(4096, 7168, 16384)
+        assert pair and bm == 256 and bn in (192, 224, 256)
+
+
+def test_fewer_sms_change_the_split():
+    with env():
+        assert plan(64, 2112, 7168, sms=SMS)[2] == 4
+        assert plan(64, 2112, 7168, sms=40)[2] == 2   # 17 tiles x 2 <= 40 < 17 x 4
+        assert plan(64, 2112, 7168, sms=20)[2] == 1
+
+
+def test_argument_checks():
+    L = _lib.lib()
+    out = [C.c_int32(-1) for _ in range(4)]
+    refs = [C.byref(o) for o in out]
+    assert L.dg_plan_fp8_gemm_nt(128, 256, 512, 0, SMS, *refs) == 0
+    assert L.dg_plan_fp8_gemm_nt(0, 256, 512, 0, SMS, *refs) == 0
+    assert [o.value for o in out] == [0, 0, 0, 0]                       # empty: nothing launched
+    assert L.dg_plan_fp8_gemm_nt(128, 256, 500, 0, SMS, *refs) == 2      # K % 128
+    assert L.dg_plan_fp8_gemm_nt(128, 260, 512, 0, SMS, *refs) == 2      # N % 8
+    assert L.dg_plan_fp8_gemm_nt(-1, 256, 512, 0, SMS, *refs) == 1
+    assert L.dg_plan_fp8_gemm_nt(128, 256, 512, 0, 0, *refs) == 1        # no SMs
+    assert L.dg_plan_fp8_gemm_nt(128, 256, 512, 0, SMS, None, *refs[1:]) == 1
