@@ -1,6 +1,8 @@
 // Tile-width dispatch and the device error word of the GEMM kernels.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "dg_internal.h"
 
 namespace dg {
@@ -11,18 +13,22 @@ __device__ unsigned long long g_gemm_err = 0ull;
 // pass this address, not the host-side shadow the symbol name denotes here;
 // looked up once per device.
 cudaError_t error_word_address(unsigned long long** out) {
-  static unsigned long long* addr[64];
+  // host threads may call concurrently: the cache is atomic (a lookup that
+  // races another stores the same address)
+  static std::atomic<unsigned long long*> addr[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!addr[dev]) {
+  unsigned long long* a = addr[dev].load(std::memory_order_acquire);
+  if (!a) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_gemm_err);
     if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<unsigned long long*>(p);
+    a = static_cast<unsigned long long*>(p);
+    addr[dev].store(a, std::memory_order_release);
   }
-  *out = addr[dev];
+  *out = a;
   return cudaSuccess;
 }
 
@@ -79,23 +85,24 @@ bool gemm2_block_n_supported(int block_n) {
 }
 
 int gemm2_max_clusters(int mode, int block_n) {
-  // cached per (device, mode, width); the occupancy query is host-side only
-  static int cache[64][3][3];
-  static bool filled[64][3][3];
+  // cached per (device, mode, width) as count + 1 (0: not yet queried); the
+  // occupancy query is host-side only, and racing callers store the same value
+  static std::atomic<int> cache[64][3][3];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int wi = block_n == 192 ? 0 : (block_n == 224 ? 1 : 2);
-  if (!filled[dev][mode][wi]) {
+  int c = cache[dev][mode][wi].load(std::memory_order_relaxed);
+  if (c == 0) {
     int n = 0;
     switch (block_n) {
       case 192: n = gemm2_max_clusters_bn192(mode); break;
       case 224: n = gemm2_max_clusters_bn224(mode); break;
       case 256: n = gemm2_max_clusters_bn256(mode); break;
     }
-    cache[dev][mode][wi] = n;
-    filled[dev][mode][wi] = true;
+    c = n + 1;
+    cache[dev][mode][wi].store(c, std::memory_order_relaxed);
   }
-  return cache[dev][mode][wi];
+  return c - 1;
 }
 
 cudaError_t gemm2_launch(int mode, int block_n, const CUtensorMap& a, const CUtensorMap& b,

@@ -69,6 +69,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "dg_device.cuh"
 
 namespace dg {
@@ -1444,13 +1446,15 @@ struct KernelTag {};
 
 template <class Tag, class Kern>
 static cudaError_t set_smem_once(Kern kern, size_t smem) {
-  static bool done[64];
+  // host threads may launch concurrently: the flags are atomic (setting the
+  // attribute twice is harmless)
+  static std::atomic<bool> done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
   return e;
 }
 

@@ -1,6 +1,8 @@
 // Dense FP8 GEMM with split-K over a cluster of 2 or 4 CTAs (128-column
 // tiles): for problems with fewer output tiles than SMs, such as decode-sized
 // M.  The partial sums are reduced through distributed shared memory.
+#include <atomic>
+
 #include "gemm_kernel.cuh"
 
 namespace dg {
@@ -34,17 +36,19 @@ cudaError_t gemm_splitk_launch(int ksplit, bool short_a, const CUtensorMap& a, c
 }
 
 int gemm_splitk_max_clusters(int ksplit) {
-  static int cache[64][2];
-  static bool filled[64][2];
+  // cached per (device, factor) as count + 1 (0: not yet queried); racing
+  // callers store the same value
+  static std::atomic<int> cache[64][2];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int i = ksplit == 2 ? 0 : 1;
-  if (!filled[dev][i]) {
-    cache[dev][i] = ksplit == 2 ? gemm_splitk_max_clusters_impl<128, kSplit2Stages, 2>()
-                                : gemm_splitk_max_clusters_impl<128, kSplit4Stages, 4>();
-    filled[dev][i] = true;
+  int c = cache[dev][i].load(std::memory_order_relaxed);
+  if (c == 0) {
+    c = 1 + (ksplit == 2 ? gemm_splitk_max_clusters_impl<128, kSplit2Stages, 2>()
+                         : gemm_splitk_max_clusters_impl<128, kSplit4Stages, 4>());
+    cache[dev][i].store(c, std::memory_order_relaxed);
   }
-  return cache[dev][i];
+  return c - 1;
 }
 
 }  // namespace dg
