@@ -280,6 +280,21 @@ dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, in
                               int32_t* block_m, int32_t* block_n, int32_t* split_k,
                               int32_t* cta_pair);
 
+/* The same query for the two M-grouped forms: the tile configuration
+ * dg_m_grouped_fp8_gemm_nt_contiguous / _masked chooses (block_m 256 when a
+ * tile pairs two 128-row blocks of one expert, contiguous, or spans a CTA
+ * pair, masked).  The per-expert row counts stay on the device, so the masked
+ * choice depends on expected_m as the call's does.  Pure host arithmetic; the
+ * same checks and overrides as the calls; all outputs 0 for an empty problem.
+ * Cited as above. */
+dg_status dg_plan_m_grouped_fp8_gemm_nt_contiguous(int64_t m_sum, int64_t n, int64_t k,
+                                                   int32_t num_groups, int32_t num_sms,
+                                                   int32_t* block_m, int32_t* block_n);
+dg_status dg_plan_m_grouped_fp8_gemm_nt_masked(int32_t num_groups, int64_t max_m, int64_t n,
+                                               int64_t k, int64_t expected_m, int32_t num_sms,
+                                               int32_t* block_m, int32_t* block_n,
+                                               int32_t* cta_pair);
+
 /* Upper bound on the SMs the persistent GEMM grid uses; 0 = all SMs of the
  * device.  Process-wide; returns DG_ERR_INVALID_ARG for n < 0. */
 dg_status dg_set_num_sms(int32_t n);

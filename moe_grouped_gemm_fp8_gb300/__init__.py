@@ -22,6 +22,8 @@ from .api import (  # noqa: F401
     m_grouped_fp8_gemm_nt_contiguous,
     m_grouped_fp8_gemm_nt_masked,
     plan_fp8_gemm_nt,
+    plan_m_grouped_fp8_gemm_nt_contiguous,
+    plan_m_grouped_fp8_gemm_nt_masked,
     quantize_fp8,
     quantize_fp8_cols,
     set_num_sms,

@@ -74,6 +74,28 @@ def plan_fp8_gemm_nt(m: int, n: int, k: int, has_c: bool = False, num_sms: int =
     return {"block_m": bm, "block_n": bn, "split_k": sk, "cta_pair": bool(pair)}
 
 
+def plan_m_grouped_fp8_gemm_nt_contiguous(m_sum: int, n: int, k: int, num_groups: int,
+                                          num_sms: int = 152) -> dict:
+    """The tile configuration m_grouped_fp8_gemm_nt_contiguous chooses, on the
+    host: {"block_m": 128 | 256, "block_n": ...}; zeros for an empty problem."""
+    out = [C.c_int32(0) for _ in range(2)]
+    _check(_lib.lib().dg_plan_m_grouped_fp8_gemm_nt_contiguous(
+        int(m_sum), int(n), int(k), int(num_groups), int(num_sms), *[C.byref(o) for o in out]),
+        "dg_plan_m_grouped_fp8_gemm_nt_contiguous")
+    return {"block_m": int(out[0].value), "block_n": int(out[1].value)}
+
+
+def plan_m_grouped_fp8_gemm_nt_masked(num_groups: int, max_m: int, n: int, k: int,
+                                      expected_m: int = 0, num_sms: int = 152) -> dict:
+    """The tile configuration m_grouped_fp8_gemm_nt_masked chooses, on the
+    host: {"block_m": 128 | 256, "block_n": ..., "cta_pair": bool}."""
+    out = [C.c_int32(0) for _ in range(3)]
+    _check(_lib.lib().dg_plan_m_grouped_fp8_gemm_nt_masked(
+        int(num_groups), int(max_m), int(n), int(k), int(expected_m), int(num_sms),
+        *[C.byref(o) for o in out]), "dg_plan_m_grouped_fp8_gemm_nt_masked")
+    return {"block_m": int(out[0].value), "block_n": int(out[1].value), "cta_pair": bool(out[2].value)}
+
+
 def set_num_sms(n: int) -> None:
     _check(_lib.lib().dg_set_num_sms(int(n)), "dg_set_num_sms")
 

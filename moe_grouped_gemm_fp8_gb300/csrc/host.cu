@@ -403,6 +403,52 @@ DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int
   return p;
 }
 
+// Tile configuration of the M-grouped forms (pure host arithmetic, the
+// DG_* overrides apply), shared by the launches and the plan queries.
+struct GroupedPlan {
+  int block_n = 128;
+  bool tall = false;  // contiguous: 256-row tiles pairing two blocks of one group
+  bool pair = false;  // masked: 256-row tiles on a CTA pair (only on request)
+};
+
+GroupedPlan plan_contiguous(int64_t m_sum, int64_t n, int64_t k, int32_t num_groups, int sms) {
+  GroupedPlan p;
+  const int64_t m_blocks = m_sum / kBlockM;
+  p.block_n = choose_block_n(m_blocks, n, k / kBlockK, sms, false, false);
+  // 256-row tiles pair two 128-row blocks of one group (at most (blocks +
+  // groups) / 2 pairs, which must fit the kernel's table); estimated as dense
+  // tiles over the expected pairs, blocks / 2 + groups / 2.
+  if (num_groups <= kMaxMaskedGroups && m_blocks < 0xFFFF &&
+      (m_blocks + num_groups + 1) / 2 <= kMaxTallPairs) {
+    const int64_t pairs = (m_blocks + num_groups + 1) / 2;
+    const double cost128 = dense_tile_cost(m_blocks, n, k / kBlockK, sms, false, p.block_n);
+    const int tall_n = choose_tall_block_n(pairs * 2 * kBlockM, n, k / kBlockK, sms, false, cost128);
+    if (tall_n != 0 && gemm_tall_stages(tall_n) > 0) {
+      p.tall = true;
+      p.block_n = tall_n;
+    }
+  }
+  return p;
+}
+
+GroupedPlan plan_masked(int32_t num_groups, int64_t max_m, int64_t n, int64_t k, int64_t expected_m,
+                        int sms) {
+  GroupedPlan p;
+  // CTA pairs only on request (DG_CTA_PAIR=1); with few valid rows per group
+  // the peer's half of the tile is mostly empty.
+  p.pair = sms >= 2 && max_m > kBlockM && env_int("DG_CTA_PAIR", 0) == 1;
+  const int64_t m_est = expected_m > 0 ? expected_m : max_m;
+  if (p.pair)
+    p.block_n = choose_block_n(((m_est + 2 * kBlockM - 1) / (2 * kBlockM)) * num_groups, n,
+                               k / kBlockK, sms / 2, false, true);
+  else if (expected_m > 0 && expected_m <= 2 * kBlockM)
+    p.block_n = choose_block_n_masked_streaming(num_groups, std::min<int64_t>(expected_m, max_m), n, sms);
+  else
+    p.block_n = choose_block_n(((m_est + kBlockM - 1) / kBlockM) * num_groups, n, k / kBlockK, sms,
+                               false, false);
+  return p;
+}
+
 dg_status check_common_k_n(int64_t n, int64_t k) {
   if (n < 0 || k < 0) return DG_ERR_INVALID_ARG;
   if (k == 0) return DG_ERR_INVALID_ARG;
@@ -566,6 +612,42 @@ dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, in
   return DG_OK;
 }
 
+dg_status dg_plan_m_grouped_fp8_gemm_nt_contiguous(int64_t m_sum, int64_t n, int64_t k,
+                                                   int32_t num_groups, int32_t num_sms,
+                                                   int32_t* block_m, int32_t* block_n) {
+  if (!block_m || !block_n) return DG_ERR_INVALID_ARG;
+  *block_m = *block_n = 0;
+  if (m_sum < 0 || num_groups < 0 || num_sms < 1) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (m_sum == 0 || n == 0 || num_groups == 0) return DG_OK;
+  if (m_sum % kBlockM != 0) return DG_ERR_ALIGNMENT;
+  if (m_sum >= kMaxCoord || (int64_t)num_groups * n >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  const GroupedPlan p = plan_contiguous(m_sum, n, k, num_groups, num_sms);
+  *block_m = p.tall ? 2 * kBlockM : kBlockM;
+  *block_n = p.block_n;
+  return DG_OK;
+}
+
+dg_status dg_plan_m_grouped_fp8_gemm_nt_masked(int32_t num_groups, int64_t max_m, int64_t n,
+                                               int64_t k, int64_t expected_m, int32_t num_sms,
+                                               int32_t* block_m, int32_t* block_n,
+                                               int32_t* cta_pair) {
+  if (!block_m || !block_n || !cta_pair) return DG_ERR_INVALID_ARG;
+  *block_m = *block_n = *cta_pair = 0;
+  if (max_m < 0 || num_groups < 0 || expected_m < 0 || num_sms < 1) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (max_m == 0 || n == 0 || num_groups == 0) return DG_OK;
+  if (num_groups > kMaxMaskedGroups) return DG_ERR_TOO_LARGE;
+  if (max_m >= kMaxCoord || (int64_t)num_groups * max_m >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  const GroupedPlan p = plan_masked(num_groups, max_m, n, k, expected_m, num_sms);
+  *block_m = p.pair ? 2 * kBlockM : kBlockM;
+  *block_n = p.block_n;
+  *cta_pair = p.pair ? 1 : 0;
+  return DG_OK;
+}
+
 dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b, const float* sfb,
                                  const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
                                  int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
@@ -666,21 +748,9 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)(m_sum / kBlockM);
-  int block_n = choose_block_n(args.m_blocks, n, k / kBlockK, sms, false, false);
-  // 256-row tiles pair two 128-row blocks of one group (at most (blocks +
-  // groups) / 2 pairs, which must fit the kernel's table); estimated as dense
-  // tiles over the expected pairs, blocks / 2 + groups / 2.
-  bool tall = false;
-  if (num_groups <= kMaxMaskedGroups && args.m_blocks < 0xFFFF &&
-      ((int64_t)args.m_blocks + num_groups + 1) / 2 <= kMaxTallPairs) {
-    const int64_t pairs = ((int64_t)args.m_blocks + num_groups + 1) / 2;
-    const double cost128 = dense_tile_cost(args.m_blocks, n, k / kBlockK, sms, false, block_n);
-    const int tall_n = choose_tall_block_n(pairs * 2 * kBlockM, n, k / kBlockK, sms, false, cost128);
-    if (tall_n != 0 && gemm_tall_stages(tall_n) > 0) {
-      tall = true;
-      block_n = tall_n;
-    }
-  }
+  const GroupedPlan plan = plan_contiguous(m_sum, n, k, num_groups, sms);
+  const bool tall = plan.tall;
+  const int block_n = plan.block_n;
   Operands o;
   if ((s = encode_a_2d(o, a, sfa, m_sum, k, k)) != DG_OK) return s;
   if ((s = encode_b_side(o, b, sfb, num_groups, n, k, k, block_n, block_n)) != DG_OK) return s;
@@ -815,25 +885,14 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
 
   GemmArgs args = {};
   args.m_blocks = (int32_t)((max_m + kBlockM - 1) / kBlockM);
-  // CTA pairs only on request (DG_CTA_PAIR=1); with few valid rows per group
-  // the peer's half of the tile is mostly empty.
-  const bool pair = sms >= 2 && max_m > kBlockM && env_int("DG_CTA_PAIR", 0) == 1;
-  const int64_t m_est = expected_m > 0 ? expected_m : max_m;
-  int block_n, grid_units;
+  const GroupedPlan plan = plan_masked(num_groups, max_m, n, k, expected_m, sms);
+  const bool pair = plan.pair;
+  const int block_n = plan.block_n;
+  int grid_units = sms;
   if (pair) {
-    block_n = choose_block_n(((m_est + 2 * kBlockM - 1) / (2 * kBlockM)) * num_groups, n,
-                             k / kBlockK, sms / 2, false, true);
     grid_units = gemm2_max_clusters(kMasked, block_n);
     if (grid_units > sms / 2) grid_units = sms / 2;
     if (grid_units <= 0) return DG_ERR_CUDA;
-  } else if (expected_m > 0 && expected_m <= 2 * kBlockM) {
-    block_n = choose_block_n_masked_streaming(num_groups, std::min<int64_t>(expected_m, max_m), n,
-                                              sms);
-    grid_units = sms;
-  } else {
-    block_n = choose_block_n(((m_est + kBlockM - 1) / kBlockM) * num_groups, n, k / kBlockK, sms,
-                             false, false);
-    grid_units = sms;
   }
   Operands o;
   if ((s = encode_a_3d(o, a, sfa, num_groups, max_m, k)) != DG_OK) return s;

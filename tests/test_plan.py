@@ -1,7 +1,8 @@
-"""CPU-only checks of the dense tile chooser (dg_plan_fp8_gemm_nt): the same
-host arithmetic dg_fp8_gemm_nt uses to pick its launch, queried without a
-GPU.  Pins the choices measured fastest on GB300 (152 SMs) for the prefill and
-decode shapes, and checks invariants any choice must satisfy."""
+"""CPU-only checks of the tile choosers (dg_plan_fp8_gemm_nt and the two
+M-grouped queries): the same host arithmetic the calls use to pick their
+launch, queried without a GPU.  Pins the choices measured fastest on GB300
+(152 SMs) for the prefill, decode, contiguous and masked workloads, and checks
+invariants any choice must satisfy."""
 import ctypes as C
 import os
 from contextlib import contextmanager
@@ -146,3 +147,50 @@ def test_argument_checks():
     assert L.dg_plan_fp8_gemm_nt(-1, 256, 512, 0, SMS, *refs) == 1
     assert L.dg_plan_fp8_gemm_nt(128, 256, 512, 0, 0, *refs) == 1        # no SMs
     assert L.dg_plan_fp8_gemm_nt(128, 256, 512, 0, SMS, None, *refs[1:]) == 1
+
+
+# ------------------------------------------------------------------ M-grouped forms
+
+def test_contiguous_workload_takes_256_row_pairs():
+    # 8 experts of the seed-31 contiguous workload: 40448 padded rows, N=4096, K=7168
+    with env():
+        assert dg.plan_m_grouped_fp8_gemm_nt_contiguous(40448, 4096, 7168, 8) == {"block_m": 256, "block_n": 224}
+    with env(DG_BLOCK_M=128):
+        assert dg.plan_m_grouped_fp8_gemm_nt_contiguous(40448, 4096, 7168, 8)["block_m"] == 128
+
+
+def test_contiguous_pairs_only_when_the_pair_table_fits():
+    with env():
+        for m_blocks, groups in ((10, 3), (300, 8), (2000, 40), (2100, 8), (100, 600)):
+            p = dg.plan_m_grouped_fp8_gemm_nt_contiguous(128 * m_blocks, 4096, 7168, groups)
+            assert p["block_n"] in (128, 192, 224, 256)
+            if p["block_m"] == 256:
+                assert groups <= 512 and (m_blocks + groups + 1) // 2 <= 1024 and p["block_n"] in (192, 224)
+
+
+def test_masked_workload_streams_256_columns():
+    # 16 experts x 256 rows, N=7168, K=2048; the bench passes the mean count (102)
+    with env():
+        assert dg.plan_m_grouped_fp8_gemm_nt_masked(16, 256, 7168, 2048, 102) == \
+            {"block_m": 128, "block_n": 256, "cta_pair": False}
+        # without a hint the capacity (2 blocks per expert) drives the estimate
+        assert dg.plan_m_grouped_fp8_gemm_nt_masked(16, 256, 7168, 2048, 0)["block_n"] == 224
+    with env(DG_CTA_PAIR=1):
+        p = dg.plan_m_grouped_fp8_gemm_nt_masked(16, 256, 7168, 2048, 102)
+        assert p["cta_pair"] and p["block_m"] == 256
+
+
+def test_grouped_argument_checks():
+    L = _lib.lib()
+    o = [C.c_int32(-1) for _ in range(3)]
+    r = [C.byref(x) for x in o]
+    assert L.dg_plan_m_grouped_fp8_gemm_nt_contiguous(0, 4096, 7168, 8, SMS, r[0], r[1]) == 0
+    assert [x.value for x in o[:2]] == [0, 0]
+    assert L.dg_plan_m_grouped_fp8_gemm_nt_contiguous(1000, 4096, 7168, 8, SMS, r[0], r[1]) == 2   # M % 128
+    assert L.dg_plan_m_grouped_fp8_gemm_nt_contiguous(1024, 4096, 7168, 8, 0, r[0], r[1]) == 1     # no SMs
+    assert L.dg_plan_m_grouped_fp8_gemm_nt_contiguous(1024, 4096, 7168, 8, SMS, None, r[1]) == 1
+    assert L.dg_plan_m_grouped_fp8_gemm_nt_masked(16, 256, 7168, 2000, 0, SMS, *r) == 2          # K % 128
+    assert L.dg_plan_m_grouped_fp8_gemm_nt_masked(16, 256, 7168, 2048, -1, SMS, *r) == 1         # expected_m
+    assert L.dg_plan_m_grouped_fp8_gemm_nt_masked(100000, 16, 7168, 2048, 0, SMS, *r) == 7       # groups
+    assert L.dg_plan_m_grouped_fp8_gemm_nt_masked(0, 256, 7168, 2048, 0, SMS, *r) == 0
+    assert [x.value for x in o] == [0, 0, 0]
