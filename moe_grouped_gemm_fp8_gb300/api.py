@@ -38,6 +38,19 @@ def _stream(stream) -> C.c_void_p:
     return C.c_void_p(int(stream))
 
 
+def _on_current_device(stream, *tensors) -> None:
+    """The library launches on the current CUDA device: every tensor (and an
+    explicit torch stream) must live there.  A pointer of another device would
+    reach a kernel that cannot use it."""
+    dev = torch.cuda.current_device()
+    for t in tensors:
+        if t is not None and t.device.index != dev:
+            raise ValueError("tensor on %s, but the current CUDA device is cuda:%d "
+                             "(use torch.cuda.device(...) around the call)" % (t.device, dev))
+    if isinstance(stream, torch.cuda.Stream) and stream.device.index != dev:
+        raise ValueError("stream of %s, but the current CUDA device is cuda:%d" % (stream.device, dev))
+
+
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else C.c_void_p(t.data_ptr())
 
@@ -160,6 +173,7 @@ def quantize_fp8(x: torch.Tensor, block_rows: int, packed: bool = True, out=None
         if tuple(q.shape) != tuple(x.shape) or tuple(sf.shape) != tuple(sf_shape) or \
                 not q.is_contiguous() or not sf.is_contiguous():
             raise ValueError("out tensors must be contiguous %s / %s" % (tuple(x.shape), sf_shape))
+    _on_current_device(stream, x, q, sf)
     st = _lib.lib().dg_quantize_fp8(_ptr(x), _ptr(q), _ptr(sf), groups, rows, cols, int(block_rows),
                                     _lib.DG_SF_UE8M0_PACKED if packed else _lib.DG_SF_FP32,
                                     _stream(stream))
@@ -189,6 +203,7 @@ def quantize_fp8_cols(x: torch.Tensor, packed: bool = True, out=None, stream=Non
         if tuple(q.shape) != tuple(x.shape) or tuple(sf.shape) != tuple(sf_shape) or \
                 not q.is_contiguous() or not sf.is_contiguous():
             raise ValueError("out tensors must be contiguous %s / %s" % (tuple(x.shape), sf_shape))
+    _on_current_device(stream, x, q, sf)
     st = _lib.lib().dg_quantize_fp8_cols(_ptr(x), _ptr(q), _ptr(sf), rows, cols,
                                          _lib.DG_SF_UE8M0_PACKED if packed else _lib.DG_SF_FP32,
                                          _stream(stream))
@@ -206,6 +221,7 @@ def transform_sf_into_required_layout(sf: torch.Tensor, mn: int, k: int, block_r
     sf = sf.contiguous()
     out = torch.empty(sf_packed_shape(mn, k, groups if grouped else None), dtype=torch.int32,
                       device=sf.device)
+    _on_current_device(stream, sf, out)
     st = _lib.lib().dg_transform_sf(_ptr(sf), _ptr(out), groups, int(mn), int(k), int(block_rows),
                                     _stream(stream))
     _check(st, "dg_transform_sf")
@@ -238,6 +254,7 @@ def fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.
         _need(c, "c", (torch.bfloat16,), 2)
         if tuple(c.shape) != (m, n) or c.stride(1) != 1:
             raise ValueError("c must be [M, N] with unit column stride")
+    _on_current_device(stream, a, sfa, b, sfb, c, d)
     st = _lib.lib().dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                                    m, n, k, a.stride(0), b.stride(0),
                                    c.stride(0) if c is not None else 0, d.stride(0), _stream(stream))
@@ -275,6 +292,7 @@ def fp8_gemm_nt_fp32_sf(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb
         _need(c, "c", (torch.bfloat16,), 2)
         if tuple(c.shape) != (m, n) or c.stride(1) != 1:
             raise ValueError("c must be [M, N] with unit column stride")
+    _on_current_device(stream, a, sfa, b, sfb, c, d)
     st = _lib.lib().dg_fp8_gemm_nt_fp32_sf(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                                            m, n, k, a.stride(0), b.stride(0),
                                            c.stride(0) if c is not None else 0, d.stride(0),
@@ -310,6 +328,7 @@ def _dense_layout(layout: str, a, sfa, b, sfb, d, c, stream):
         if tuple(c.shape) != (m, n) or c.stride(1) != 1:
             raise ValueError("c must be [M, N] with unit column stride")
     fn = "dg_fp8_gemm_" + layout
+    _on_current_device(stream, a, sfa, b, sfb, c, d)
     st = getattr(_lib.lib(), fn)(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d), m, n, k,
                                  a.stride(0), b.stride(0), c.stride(0) if c is not None else 0,
                                  d.stride(0), _stream(stream))
@@ -355,6 +374,7 @@ def m_grouped_fp8_gemm_nt_contiguous(a: torch.Tensor, sfa: torch.Tensor, b: torc
     _need(d, "d", (torch.bfloat16,), 2)
     if tuple(d.shape) != (m_sum, n) or not d.is_contiguous():
         raise ValueError("d must be contiguous [m_sum, N]")
+    _on_current_device(stream, a, sfa, b, sfb, d, m_indices)
     st = _lib.lib().dg_m_grouped_fp8_gemm_nt_contiguous(
         _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(m_indices), m_sum, n, k, g,
         _stream(stream))
@@ -393,6 +413,7 @@ def k_grouped_fp8_gemm_tn_contiguous(a: torch.Tensor, sfa: torch.Tensor, b: torc
         _need(c, "c", (torch.float32,), 3)
         if tuple(c.shape) != (g, m, n) or not c.is_contiguous():
             raise ValueError("c must be contiguous [G, M, N]")
+    _on_current_device(stream, a, sfa, b, sfb, c, d, ks)
     st = _lib.lib().dg_k_grouped_fp8_gemm_tn_contiguous(
         _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d), _ptr(ks), m, n, sum_k, g,
         _stream(stream))
@@ -423,6 +444,7 @@ def m_grouped_fp8_gemm_nt_masked(a: torch.Tensor, sfa: torch.Tensor, b: torch.Te
     _need(d, "d", (torch.bfloat16,), 3)
     if tuple(d.shape) != (g, max_m, n) or not d.is_contiguous():
         raise ValueError("d must be contiguous [G, max_m, N]")
+    _on_current_device(stream, a, sfa, b, sfb, d, masked_m)
     st = _lib.lib().dg_m_grouped_fp8_gemm_nt_masked(
         _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(d), _ptr(masked_m), g, max_m, n, k,
         int(expected_m), _stream(stream))

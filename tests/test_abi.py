@@ -147,3 +147,19 @@ def test_fp32_scale_gemm_host_checks(L):
     assert fn(P, None, P, P, None, P, 128, 256, 512, 512, 512, 0, 256, None) == INVALID
     assert fn(P, C.c_void_p(0x1002), P, P, None, P, 128, 256, 512, 512, 512, 0, 256, None) == ALIGN
     assert fn(P, P, P, P, None, P, 128, 256, 512, 256, 512, 0, 256, None) == INVALID  # lda < K
+
+
+def test_tensors_must_be_on_the_current_device(monkeypatch):
+    """The binding refuses tensors of another CUDA device than the current one
+    (the library launches on the current device)."""
+    import torch
+    from moe_grouped_gemm_fp8_gb300 import api
+
+    class On:
+        def __init__(self, i):
+            self.device = torch.device("cuda", i)
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    api._on_current_device(None, On(1), None, On(1))           # all on cuda:1: accepted
+    with pytest.raises(ValueError, match="current CUDA device is cuda:1"):
+        api._on_current_device(None, On(1), On(0))
