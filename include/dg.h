@@ -86,7 +86,7 @@ typedef enum dg_sf_format {
  *   d    BF16 [m, n], row stride ldd (ldd >= n, ldd % 8 == 0)
  * Cited: "DeepGEMM: kernels GEMM FP8 limpos e eficientes por meio de scaling
  * granular", sections "Interface GEMM e restrições de layout" and "GEMM denso
- * e grouped" (fp8_gemm_{nt, nn, tn, tt}; NT implemented here). */
+ * e grouped" (fp8_gemm_{nt, nn, tn, tt}; the other three layouts below). */
 dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
                          const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
                          int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
