@@ -24,6 +24,21 @@ def test_exports_every_declared_function(L):
         assert n in _lib.SIGNATURES, "binding lacks a signature for %s" % n
 
 
+def test_exports_nothing_the_header_does_not_declare(L):
+    """Every dg_* symbol libdg.so exports is declared in include/dg.h (the
+    library's own exported names, read with nm)."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = sorted({line.split()[-1] for line in out.splitlines()
+                       if line.split() and line.split()[-1].startswith("dg_")})
+    assert exported == _lib.header_functions()
+
+
 def test_pure_host_utilities(L):
     assert L.dg_get_tma_aligned_size(4097, 4) == 4100
     assert L.dg_get_tma_aligned_size(4096, 4) == 4096
