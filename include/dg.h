@@ -162,8 +162,12 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
  *   d         BF16 [num_groups, max_m, n]
  *   masked_m  int32 [num_groups] on the device: rows [0, masked_m[g]) of
  *             group g are computed and written; rows at or beyond it are left
- *             untouched (their A rows are never used).  Values outside
- *             [0, max_m] are clamped and set DG_ERR_DEVICE_BAD_INDEX.
+ *             untouched.  The 128-row blocks of A that hold no valid row are
+ *             never read; inside a block that holds one, the rows past
+ *             masked_m[g] are loaded and multiplied like the others, but their
+ *             results are never stored (so A's contents there do not matter).
+ *             Values outside [0, max_m] are clamped and set
+ *             DG_ERR_DEVICE_BAD_INDEX.
  *   expected_m  host hint of the typical masked_m (tile selection only);
  *               0 = unknown.  Never affects results.
  * num_groups <= 512.  masked_m is never read on the host, so the call can
@@ -320,8 +324,23 @@ dg_status dg_set_wait_timeout_ns(uint64_t ns);
 /* Synchronises `stream`, then reads and clears the device error words of the
  * current device.  Returns DG_OK or the first recorded DG_ERR_DEVICE_* code.
  * If detail is not NULL it receives the raw word (code in bits 0-7, the
- * recording site in bits 8-23, block index in bits 32-63).  Debug/test use. */
+ * recording site in bits 8-23, block index in bits 32-63).  Debug/test use.
+ * The words are one per device and per process, shared by every launch on
+ * every stream: the result is only meaningful when no other work of this
+ * library is in flight on the device (a kernel still running on another
+ * stream may have its condition cleared here or reported against this call). */
 dg_status dg_get_device_error(void* stream, uint64_t* detail);
+
+/* Test hook for failure detection, process-wide, off (0) by default.  With
+ * k > 0, the next dense NT launches make CTA 0 arm the pipeline stage of K
+ * block k - 1 of its first tile without filling it: that stage never
+ * completes, so the kernel's bounded waits must end the launch by themselves
+ * and record DG_ERR_DEVICE_TIMEOUT (the result D is then incomplete).  Nothing
+ * faults or hangs; the context stays usable.  Pair it with a short
+ * dg_set_wait_timeout_ns and reset it to 0 afterwards.  k < 0 gives
+ * DG_ERR_INVALID_ARG.  No counterpart on the pages: it exists to test the
+ * library's own bounded waits. */
+dg_status dg_debug_set_drop_load(int32_t k);
 
 /* Static description of a status code. */
 const char* dg_status_string(dg_status s);

@@ -50,6 +50,7 @@ SIGNATURES = {
     "dg_get_pdl": (_i32, []),
     "dg_set_wait_timeout_ns": (_st, [C.c_uint64]),
     "dg_get_device_error": (_st, [_p, C.POINTER(C.c_uint64)]),
+    "dg_debug_set_drop_load": (_st, [_i32]),
     "dg_status_string": (C.c_char_p, [_st]),
     "dg_version": (_i32, []),
 }

@@ -130,6 +130,13 @@ def set_wait_timeout_ns(ns: int) -> None:
     _check(_lib.lib().dg_set_wait_timeout_ns(int(ns)), "dg_set_wait_timeout_ns")
 
 
+def debug_set_drop_load(k: int) -> None:
+    """Test hook: with k > 0 the next dense NT launches leave the stage of K
+    block k - 1 of CTA 0's first tile unfilled, so the kernel's bounded waits
+    must end the launch with DG_ERR_DEVICE_TIMEOUT; 0 turns it off."""
+    _check(_lib.lib().dg_debug_set_drop_load(int(k)), "dg_debug_set_drop_load")
+
+
 def get_device_error(stream=None) -> Tuple[int, int]:
     """Synchronises the stream; returns (status, raw word) and clears the word."""
     detail = C.c_uint64(0)

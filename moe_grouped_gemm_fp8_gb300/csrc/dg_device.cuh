@@ -317,10 +317,17 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Whole-cluster barrier without memory ordering: only keeps every CTA
-// resident until all have arrived (data hand-offs are ordered by mbarriers).
-__device__ __forceinline__ void cluster_sync_all_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+// Whole-cluster barrier whose arrive carries no ordering but whose wait
+// acquires: paired with fence_acq_rel_cluster() before it in the threads that
+// have something to publish (release pattern), it orders only their writes.
+__device__ __forceinline__ void cluster_arrive_relaxed_wait_acquire() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Orders this thread's earlier memory accesses (shared memory of other CTAs of
+// the cluster included) before its later ones, at cluster scope.
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 
 // Address of the same shared-memory location in CTA `rank` of the cluster.
@@ -334,6 +341,10 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
   return v;
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // 16-byte store into the shared memory of a CTA of the cluster.

@@ -78,7 +78,7 @@ struct GemmArgs {
   const float* c_f32;      // nullable, [num_groups, m, n]
   float* d_f32;            // [num_groups, m, n]
   int32_t pdl;             // host side: launch with programmatic stream serialisation
-  // Test hook (DG_DEBUG_DROP_LOAD): 1 + the K block whose operand copies CTA 0
+  // Test hook (dg_debug_set_drop_load): 1 + the K block whose operand copies CTA 0
   // skips on its first tile, so that stage's barrier never completes and the
   // bounded waits must end the launch with DG_ERR_DEVICE_TIMEOUT; 0 = off.
   int32_t debug_drop_load;

@@ -485,6 +485,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   {
     // After an abort, copies the peer issued towards this CTA's barriers may
     // still be in flight: give them time to land before the memory goes away.
+    // The release/acquire barriers around this block order every thread's
+    // own loads and stores, but not TMA copies: those are asynchronous, and
+    // a peer's operand copy completes on the leader's stage barrier, never
+    // on one of its own.  The leader drains every stage it armed, but after
+    // an abort the peer may have issued a copy into a stage the leader never
+    // armed (its wait ran out first), and no barrier in either CTA tracks
+    // that copy.  Nothing can be waited on for it, so a fixed grace period
+    // (many times a copy's latency) is the only bound; it is spent only on
+    // the abort path, never in a clean launch.
     const int peer_abort = (int)ld_shared_cluster_u32(
         mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u));
     if (*abort_flag || peer_abort) {

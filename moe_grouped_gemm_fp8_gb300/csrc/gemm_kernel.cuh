@@ -602,6 +602,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto recv_free = [&](int q) { return smem_u32(bars + kB0 + 9 + q); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kB0 + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // split-K: set by another CTA of the cluster that aborted (see the teardown)
+  volatile int* peer_abort = reinterpret_cast<volatile int*>(tmem_slot + 2);
   int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
   int* group_valid = tile_start + (kMaxMaskedGroups + 1);
   unsigned long long* const err = args.err;
@@ -626,6 +628,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(recv_free(q), KSPLIT > 1 ? KSPLIT - 1 : 1);
     }
     *abort_flag = 0;
+    *peer_abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
@@ -1427,11 +1430,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncthreads();
-  // No CTA leaves while others may still reach its shared memory.  Every
-  // exchange into it has completed (its mbarrier waits acquired them), so
-  // the barrier needs no memory ordering (a release here would also wait for
-  // this CTA's outstanding global writes).
-  if (KSPLIT > 1) cluster_sync_all_relaxed();
+  // No CTA leaves while others may still reach its shared memory.
+  if constexpr (KSPLIT > 1) {
+    // Clean path: every exchange into this CTA has completed (its mbarrier
+    // waits acquired it), so the barrier needs no release (a release would
+    // also wait for this CTA's outstanding global writes).  After an abort
+    // that no longer holds: a CTA that gave up on a wait never acquired what
+    // its peers sent it, and their remote stores and arrivals may still be in
+    // flight.  An aborted CTA therefore marks every peer before the barrier
+    // (its fence orders those marks and its own remote stores before the
+    // arrival; the waits acquire them), so that every CTA of the cluster sees
+    // the abort and all of them take a second, release/acquire barrier, which
+    // orders every thread's remote accesses before any CTA exits.  abort_flag
+    // is final here (only the roles above raise it), so the choice is the same
+    // in every CTA.
+    if (*abort_flag) {
+      if (threadIdx.x == 0)
+        for (uint32_t r = 0; r < (uint32_t)KSPLIT; ++r)
+          if (r != krank) st_shared_cluster_u32(mapa_shared(smem_u32((const void*)peer_abort), r), 1u);
+      fence_acq_rel_cluster();
+    }
+    cluster_arrive_relaxed_wait_acquire();
+    if (*abort_flag || *peer_abort) cluster_sync_all();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);

@@ -25,6 +25,7 @@ constexpr int64_t kMaxCoord = (int64_t)1 << 31;  // TMA coordinates are 32-bit s
 std::atomic<int32_t> g_num_sms_limit{0};
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_pdl{0};
+std::atomic<int32_t> g_debug_drop_load{0};  // test hook, see dg_debug_set_drop_load
 
 struct DeviceInfo {
   std::once_flag once;
@@ -524,7 +525,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     print_config(ksplit == 2 ? "fp8_gemm_nt (split-K 2)" : "fp8_gemm_nt (split-K 4)", m, n, k, 1,
                  plan.short_a ? kBlockM / 2 : kBlockM, block_n, gemm_splitk_stages(ksplit, plan.short_a),
                  ksplit * clusters, args.band);
-    args.debug_drop_load = env_int("DG_DEBUG_DROP_LOAD", 0);
+    args.debug_drop_load = g_debug_drop_load.load(std::memory_order_relaxed);
     return from_cuda(gemm_splitk_launch(ksplit, plan.short_a, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
                                         static_cast<cudaStream_t>(stream)));
   }
@@ -572,7 +573,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
                                   static_cast<cudaStream_t>(stream)));
   }
   const int grid = (int)(tiles < sms ? tiles : sms);
-  args.debug_drop_load = env_int("DG_DEBUG_DROP_LOAD", 0);
+  args.debug_drop_load = g_debug_drop_load.load(std::memory_order_relaxed);
   print_config(tall ? "fp8_gemm_nt (256-row tiles)" : plan.short_a ? "fp8_gemm_nt (64-row A slots)" : name,
                m, n, k, 1, tall ? 2 * kBlockM : plan.short_a ? kBlockM / 2 : kBlockM, block_n,
                tall ? gemm_tall_stages(block_n) : plan.short_a ? gemm_short_stages(block_n) : gemm_stages(block_n),
@@ -1006,6 +1007,12 @@ int32_t dg_get_pdl(void) { return g_pdl.load(); }
 dg_status dg_set_wait_timeout_ns(uint64_t ns) {
   if (ns == 0) return DG_ERR_INVALID_ARG;
   g_timeout_ns.store(ns);
+  return DG_OK;
+}
+
+dg_status dg_debug_set_drop_load(int32_t k) {
+  if (k < 0) return DG_ERR_INVALID_ARG;
+  g_debug_drop_load.store(k);
   return DG_OK;
 }
 

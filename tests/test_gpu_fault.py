@@ -32,13 +32,13 @@ def test_dropped_stage_times_out_and_context_survives():
     dev = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
     assert dg.get_device_error()[0] == 0
     dg.set_wait_timeout_ns(2_000_000)  # 2 ms
-    os.environ["DG_DEBUG_DROP_LOAD"] = "3"  # K block 2 of CTA 0's first tile
+    dg.debug_set_drop_load(3)  # K block 2 of CTA 0's first tile
     os.environ["DG_SPLIT_K"] = "1"  # the hook is in the single-CTA pipeline
     try:
         dg.fp8_gemm_nt(*dev)
         st, word = dg.get_device_error()
     finally:
-        os.environ.pop("DG_DEBUG_DROP_LOAD", None)
+        dg.debug_set_drop_load(0)
         os.environ.pop("DG_SPLIT_K", None)
         dg.set_wait_timeout_ns(2_000_000_000)
     assert st == DG_ERR_DEVICE_TIMEOUT, (st, hex(word))
@@ -63,13 +63,13 @@ def test_dropped_stage_in_a_split_k_cluster_times_out_everywhere():
     dev = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
     assert dg.get_device_error()[0] == 0
     dg.set_wait_timeout_ns(2_000_000)  # 2 ms
-    os.environ["DG_DEBUG_DROP_LOAD"] = "2"
+    dg.debug_set_drop_load(2)
     os.environ["DG_SPLIT_K"] = "4"
     try:
         dg.fp8_gemm_nt(*dev)
         st, word = dg.get_device_error()
     finally:
-        os.environ.pop("DG_DEBUG_DROP_LOAD", None)
+        dg.debug_set_drop_load(0)
         os.environ.pop("DG_SPLIT_K", None)
         dg.set_wait_timeout_ns(2_000_000_000)
     assert st == DG_ERR_DEVICE_TIMEOUT, (st, hex(word))
