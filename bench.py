@@ -1,16 +1,23 @@
 #!/usr/bin/env python
 """Throughput of the FP8 fine-grained-scaled GEMM path on GB300.
 
-Default workload (one step): the dense NT prefill-like shapes, M=4096 and
+Headline workload (one step): the dense NT prefill-like shapes, M=4096 and
 (N, K) in {(2112,7168), (24576,1536), (7168,16384), (4096,7168), (7168,2048)}.
 Per shape a step quantises the FP32 activations A (1x128 groups, packed UE8M0
 scales) and runs D = A @ B.T and D2 = C + A @ B.T.  The weights B are
 quantised (128x128 blocks) once at setup.  Inputs are seeded N(0, 1); the
-per-step working set (~1.6 GB) is larger than L2.
+per-step working set (~2 GB) is larger than L2.  `value` is the step's GEMM
+FLOPs over the device time of exactly --steps steps.
+
+The same run then measures, GEMM only, the four other workloads of the benchmark spec
+(dense small, dense decode-like, contiguous MoE, masked MoE) and reports each
+under "configs" with its own roofline and CPU-oracle baseline; a sustained
+prefill figure over >= 1.5 s of back-to-back steps is reported beside the
+headline, and the clocks are sampled over the whole measured window.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle
-instead, on a bounded row sample of the same workload.  Other workloads
-(`--workload decode|contiguous|masked|small`) print their own line.
+instead, on a bounded row sample of the headline workload.  `--workload X`
+measures one other workload alone and prints its own line.
 """
 import argparse
 import json
@@ -32,6 +39,8 @@ import torch  # noqa: E402
 METRIC = "FP8 TFLOPS (and % of GB300 FP8 peak / HBM roofline) per shape at 1 GPU"
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor throughput (4.5 : 2.25 PFLOP/s)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+OTHER_CONFIGS = ("small", "decode", "contiguous", "masked")
+SUSTAINED_SECONDS = 1.5
 
 
 def parse_args():
@@ -43,6 +52,8 @@ def parse_args():
     p.add_argument("--workload", default="prefill",
                    choices=["prefill", "decode", "contiguous", "masked", "kgrouped", "fp32scales", "small"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="headline workload only (no per-config entries)")
     p.add_argument("--pdl", action="store_true",
                    help="launch the library's kernels with programmatic dependent launch")
     p.add_argument("--no-e2e", action="store_true")
@@ -135,26 +146,57 @@ class ClockSampler:
         rows = [line.strip().split(", ") for line in self.file if line.strip()]
         self.file.close()
         os.unlink(self.file.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-            except ValueError:
-                continue
-            for name, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return summarise_clocks(rows)
 
 
-# --------------------------------------------------------------------------- workloads
+def summarise_clocks(rows):
+    """Median SM clock over the samples taken under load (power above half of
+    the largest draw seen), the max clock and the throttle reasons seen."""
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    samples = []
+    for r in rows:
+        if len(r) < 9:
+            continue
+        try:
+            samples.append((float(r[1]), float(r[2]), float(r[3]),
+                            [n for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"]))
+        except ValueError:
+            continue
+    if not samples:
+        return None
+    pmax = max(s[2] for s in samples)
+    loaded = [s for s in samples if s[2] >= 0.5 * pmax] or samples
+    reasons = sorted({n for s in loaded for n in s[3]})
+    return {"sm_mhz": statistics.median(s[0] for s in loaded), "sm_max_mhz": max(s[1] for s in samples),
+            "samples": len(samples), "samples_under_load": len(loaded),
+            "power_w_max": pmax, "reasons": reasons}
+
+
+# --------------------------------------------------------------------------- byte counts
+
+
+def algorithmic_bytes_gemm(m, n, k, with_c):
+    """Bytes a dense NT GEMM must move: A, B, their packed UE8M0 scale words
+    (one 32-bit word per row per 4 K blocks), D, and C when present."""
+    kb = k // 128
+    return (m * k + n * k + m * ((kb + 3) // 4) * 4 + n * ((kb + 3) // 4) * 4 + 2 * m * n +
+            (2 * m * n if with_c else 0))
+
+
+def algorithmic_bytes_contiguous(valid_rows, groups, n, k):
+    """Valid rows of A and D, every expert's B, and the scale words."""
+    kp = (k // 128 + 3) // 4
+    return valid_rows * k + groups * n * k + 2 * valid_rows * n + 4 * kp * (valid_rows + groups * n)
+
+
+def algorithmic_bytes_masked(valid_rows, used_groups, n, k):
+    """Valid rows of A and D, B of the experts with at least one row, and the
+    scale words."""
+    kp = (k // 128 + 3) // 4
+    return valid_rows * k + used_groups * n * k + 2 * valid_rows * n + 4 * kp * (valid_rows + used_groups * n)
+
+
+# --------------------------------------------------------------------------- headline workload
 
 
 def prefill_setup(dg, workloads, dev, only=-1):
@@ -194,135 +236,45 @@ def step_flops(shapes):
     return sum(2 * 2.0 * s["m"] * s["n"] * s["k"] for s in shapes)
 
 
-def algorithmic_bytes_gemm(m, n, k, with_c):
-    kb = k // 128
-    return (m * k + n * k + m * ((kb + 3) // 4) * 4 + n * ((kb + 3) // 4) * 4 + 2 * m * n +
-            (2 * m * n if with_c else 0))
+# DRAM bytes (read + write) of one launch of the step's largest GEMM, from an
+# ncu capture of that launch, keyed by the shape and the tile configuration
+# the library chose for it at capture time: (m, n, k, with C, block_m,
+# block_n, split_k, cta_pair).  A launch whose configuration is not listed has
+# no traffic figure (the counters would be stale).
+CAPTURED_TRAFFIC = {
+    (4096, 7168, 16384, False, 256, 192, 1, 0): 366.6e6 + 47.1e6,
+}
 
 
-# --------------------------------------------------------------------------- CPU oracle timing
+def captured_traffic(dg, m, n, k, with_c, num_sms):
+    plan = dg.plan_fp8_gemm_nt(m, n, k, has_c=with_c, num_sms=num_sms)
+    key = (m, n, k, bool(with_c), plan["block_m"], plan["block_n"], plan["split_k"], int(plan["cta_pair"]))
+    return CAPTURED_TRAFFIC.get(key), plan
 
 
-def oracle_sample(workloads, rows_per_shape, seed=0):
-    """Bounded sample of the prefill workload for the CPU oracle: per shape,
-    `rows_per_shape` randomly chosen rows of A (quantised 1x128 by the oracle)
-    against the oracle-quantised B, computing D and D2 = C + D for those rows.
-    `take(items, r)` keeps the first r of them (still a random subset)."""
-    import oracle
-    rng = np.random.default_rng(seed)
-    items = []
-    for cfg in workloads.PREFILL:
-        m, n, k = cfg["m"], cfg["n"], cfg["k"]
-        w = workloads.dense(m, n, k, cfg["seed"], with_c=True)
-        qb, _, sb = oracle.quantize(w.b.numpy(), 128)
-        rows = rng.choice(m, size=min(m, rows_per_shape), replace=False)
-        a_rows = np.ascontiguousarray(w.a.numpy()[rows])
-        c_rows = np.ascontiguousarray(w.c[torch.from_numpy(rows)].view(torch.int16).numpy().view(np.uint16))
-        items.append(dict(n=n, k=k, a=a_rows, c=c_rows, qb=qb, sb=sb))
-    return items
-
-
-def take(items, rows):
-    return [dict(it, a=np.ascontiguousarray(it["a"][:rows]), c=np.ascontiguousarray(it["c"][:rows]))
-            for it in items]
-
-
-def oracle_run(items):
-    import oracle
-    flops = 0.0
-    for it in items:
-        qa, _, sa = oracle.quantize(it["a"], 1)
-        idx = np.arange(qa.shape[0], dtype=np.int64)
-        oracle.gemm_nt_rows(qa, sa, it["qb"], it["sb"], idx)
-        oracle.gemm_nt_rows(qa, sa, it["qb"], it["sb"], idx, it["c"])
-        flops += 2 * 2.0 * qa.shape[0] * it["qb"].shape[0] * it["k"]
-    return flops
-
-
-def calibrated_rows(items, seconds, probe_rows=16):
-    """Rows per prefill shape that keep one oracle pass near `seconds` of wall
-    time on this host: time a small probe pass, then scale linearly (at most
-    the rows the sample holds)."""
-    t0 = time.perf_counter()
-    oracle_run(take(items, probe_rows))
-    dt = max(time.perf_counter() - t0, 1e-3)
-    return int(min(len(items[0]["a"]), max(probe_rows, probe_rows * seconds / dt)))
-
-
-def cpu_baseline(workloads, seconds=12.0):
-    import oracle
-    items = oracle_sample(workloads, 2048)
-    rows_per_shape = calibrated_rows(items, seconds)
-    items = take(items, rows_per_shape)
-    t0 = time.perf_counter()
-    flops = oracle_run(items)
-    dt = time.perf_counter() - t0
-    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.get_threads(),
-            "kind": "oracle",
-            "sample": "%d random rows of A per prefill shape (quantise + D and C + D rows), FP64, %.1f s" %
-                      (rows_per_shape, dt)}
-
-
-def run_reference(args, ranks):
-    from moe_grouped_gemm_fp8_gb300 import workloads
-    import oracle
-    if ranks.rank != 0:
-        return 0
-    items = oracle_sample(workloads, 2048)
-    rows = calibrated_rows(items, 0.5)
-    items = take(items, rows)
-    for _ in range(args.warmup):
-        oracle_run(items)
-    t0 = time.perf_counter()
-    flops = 0.0
-    for _ in range(args.steps):
-        flops += oracle_run(items)
-    dt = time.perf_counter() - t0
-    value = flops / dt / 1e12
-    sample = "%d rows of A per prefill shape per step (quantise + D and C + D rows), FP64" % rows
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": "dense NT prefill-like M=4096, (N,K) in %s, with and without C; CPU oracle row sample" %
-                   workloads.PREFILL_NK},
-        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.get_threads(), "kind": "oracle",
-                         "sample": sample},
-        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
-    return 0
-
-
-# --------------------------------------------------------------------------- main arm
-
-
-# DRAM bytes (read + write) of one launch of the step's largest GEMM, from the
-# ncu capture summarised in profiles/fp8_gemm_bm256_bn192_m4096_n7168_k16384.md
-# (D = A @ B.T, M=4096 N=7168 K=16384, 256 x 192 tiles).
-DOMINANT_SHAPE = (4096, 7168, 16384, False)
-DOMINANT_TRAFFIC = 366.6e6 + 47.1e6
-
-
-def prefill_roofline(res, fp8_peak, peak_source):
+def prefill_roofline(res, fp8_peak, peak_source, traffic=None, plan=None):
     """Roofline of the dominant kernel: the D = A @ B.T launch (no C) with the
     largest share of the step (per-launch CUDA-event times of the timed
     region; its D = C + A @ B.T twin runs the same kernel), plus the same
     figure over every GEMM launch of the step."""
-    dom = max((e for e in res["per_shape"] if not e["c"]), key=lambda e: e["us"])
-    key = (dom["m"], dom["n"], dom["k"], dom["c"])
-    return {"bound": "tensor", "achieved": dom["tflops"], "peak": fp8_peak, "unit": "TFLOP/s",
-            "frac": dom["tflops"] / fp8_peak,
-            "traffic": DOMINANT_TRAFFIC if key == DOMINANT_SHAPE else None,
-            "traffic_unit": "bytes per launch (dram read + write)",
-            "kernel": "fp8_gemm_kernel, D%s = A@B.T, M=%d N=%d K=%d (largest GEMM of the step)" %
-                      (" = C +" if dom["c"] else "", dom["m"], dom["n"], dom["k"]),
-            "all_gemms": {"achieved": res["achieved"], "frac": res["achieved"] / fp8_peak},
-            "peak_source": peak_source}
+    dom = dominant_launch(res["per_shape"])
+    r = {"bound": "tensor", "achieved": dom["tflops"], "peak": fp8_peak, "unit": "TFLOP/s",
+         "frac": dom["tflops"] / fp8_peak, "traffic": traffic,
+         "traffic_unit": "bytes per launch (dram read + write)",
+         "kernel": "fp8_gemm_kernel, D%s = A@B.T, M=%d N=%d K=%d (largest GEMM of the step)" %
+                   (" = C +" if dom["c"] else "", dom["m"], dom["n"], dom["k"]),
+         "all_gemms": {"achieved": res["achieved"], "frac": res["achieved"] / fp8_peak},
+         "peak_source": peak_source}
+    if plan is not None:
+        r["tile"] = plan
+    return r
 
 
-def run_prefill(args, ranks, dg, workloads, dev):
+def dominant_launch(per_shape):
+    return max((e for e in per_shape if not e["c"]), key=lambda e: e["us"])
+
+
+def run_prefill(args, ranks, dg, workloads, dev, clocks):
     dg.set_pdl(bool(args.pdl))
     shapes = prefill_setup(dg, workloads, dev, args.shape)
     if args.profile_steps:
@@ -330,10 +282,6 @@ def run_prefill(args, ranks, dg, workloads, dev):
             prefill_step(dg, shapes)
         torch.cuda.synchronize()
         return None
-    # clocks are sampled from the first warm-up step to the end of the timed
-    # region (the sampler needs a few hundred ms to start reporting)
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
     t_warm = time.perf_counter()
     while True:
         for _ in range(max(3, args.warmup)):
@@ -345,7 +293,7 @@ def run_prefill(args, ranks, dg, workloads, dev):
     if st != 0:
         raise RuntimeError("device error after warm-up: 0x%x" % word)
 
-    # device-timed region: inputs resident in HBM
+    # device-timed region: exactly --steps steps, inputs resident in HBM
     events = []
     ranks.barrier()
     torch.cuda.synchronize()
@@ -356,7 +304,6 @@ def run_prefill(args, ranks, dg, workloads, dev):
         prefill_step(dg, shapes, events)
     t1.record()
     torch.cuda.synchronize()
-    clk = clocks.stop()
     ranks.barrier()
     ms = t0.elapsed_time(t1) / args.steps
     ms_max = ranks.max(ms)
@@ -376,17 +323,36 @@ def run_prefill(args, ranks, dg, workloads, dev):
             per_shape.append({"m": s["m"], "n": s["n"], "k": s["k"], "c": with_c, "us": t * 1e3,
                               "tflops": f / (t * 1e-3) / 1e12, "gbs": byt / (t * 1e-3) / 1e9})
 
+    # sustained: the same step back to back for >= SUSTAINED_SECONDS (clocks
+    # settle under the power cap; the short headline region cannot show that)
+    n_sus = max(args.steps, int(math.ceil(SUSTAINED_SECONDS / max(ms * 1e-3, 1e-6))))
+    ranks.barrier()
+    torch.cuda.synchronize()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(n_sus):
+        prefill_step(dg, shapes)
+    s1.record()
+    torch.cuda.synchronize()
+    ms_sus = ranks.max(s0.elapsed_time(s1) / n_sus)
+    sustained = {"value": ranks.sum(flops_step) / (ms_sus * 1e-3) / 1e12, "unit": "TFLOPS",
+                 "steps": n_sus, "ms_per_step": ms_sus, "seconds": ms_sus * n_sus * 1e-3}
+
     st, word = dg.get_device_error()
     if st != 0:
         raise RuntimeError("device error in timed region: 0x%x" % word)
 
-    # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
         e2e = run_prefill_e2e(args, ranks, dg, shapes, dev)
     ws = sum(s["a"].numel() * 4 + s["qa"].numel() + s["qb"].numel() + 3 * 2 * s["m"] * s["n"] for s in shapes)
-    return dict(value=value, ms=ms_max, achieved=achieved, per_shape=per_shape, clocks=clk, e2e=e2e,
-                launches=args.steps * len(shapes) * 3, flops_step=flops_step, working_set_gb=ws / 1e9)
+    res = dict(value=value, ms=ms_max, achieved=achieved, per_shape=per_shape, e2e=e2e,
+               sustained=sustained, launches=args.steps * len(shapes) * 3, flops_step=flops_step,
+               working_set_gb=ws / 1e9)
+    del shapes
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_prefill_e2e(args, ranks, dg, shapes, dev):
@@ -451,6 +417,188 @@ def run_prefill_e2e(args, ranks, dg, shapes, dev):
     return {"value": ranks.sum(step_flops(shapes)) / dt / 1e12, "unit": "TFLOPS",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
 
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+
+def calibrate(run, probe, seconds, limit):
+    """Sample size (rows) that keeps one call of run(size) near `seconds` of
+    wall time on this host: time run(probe), then scale linearly (at most
+    `limit`)."""
+    t0 = time.perf_counter()
+    run(probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    return int(min(limit, max(probe, probe * seconds / dt)))
+
+
+def timed_baseline(run, size, what):
+    import oracle
+    t0 = time.perf_counter()
+    flops = run(size)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": what % size + ", FP64, %.1f s" % dt}
+
+
+def oracle_sample(workloads, rows_per_shape, seed=0):
+    """Bounded sample of the prefill workload for the CPU oracle: per shape,
+    `rows_per_shape` randomly chosen rows of A (quantised 1x128 by the oracle)
+    against the oracle-quantised B, computing D and D2 = C + D for those rows.
+    `take(items, r)` keeps the first r of them (still a random subset)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    items = []
+    for cfg in workloads.PREFILL:
+        m, n, k = cfg["m"], cfg["n"], cfg["k"]
+        w = workloads.dense(m, n, k, cfg["seed"], with_c=True)
+        qb, _, sb = oracle.quantize(w.b.numpy(), 128)
+        rows = rng.choice(m, size=min(m, rows_per_shape), replace=False)
+        a_rows = np.ascontiguousarray(w.a.numpy()[rows])
+        c_rows = np.ascontiguousarray(w.c[torch.from_numpy(rows)].view(torch.int16).numpy().view(np.uint16))
+        items.append(dict(n=n, k=k, a=a_rows, c=c_rows, qb=qb, sb=sb))
+    return items
+
+
+def take(items, rows):
+    return [dict(it, a=np.ascontiguousarray(it["a"][:rows]), c=np.ascontiguousarray(it["c"][:rows]))
+            for it in items]
+
+
+def oracle_run(items):
+    import oracle
+    flops = 0.0
+    for it in items:
+        qa, _, sa = oracle.quantize(it["a"], 1)
+        idx = np.arange(qa.shape[0], dtype=np.int64)
+        oracle.gemm_nt_rows(qa, sa, it["qb"], it["sb"], idx)
+        oracle.gemm_nt_rows(qa, sa, it["qb"], it["sb"], idx, it["c"])
+        flops += 2 * 2.0 * qa.shape[0] * it["qb"].shape[0] * it["k"]
+    return flops
+
+
+def calibrated_rows(items, seconds, probe_rows=16):
+    return calibrate(lambda r: oracle_run(take(items, r)), probe_rows, seconds, len(items[0]["a"]))
+
+
+def cpu_baseline(workloads, seconds=8.0):
+    items = oracle_sample(workloads, 2048)
+    rows = calibrated_rows(items, seconds)
+    return timed_baseline(lambda r: oracle_run(take(items, r)), rows,
+                          "%d random rows of A per prefill shape (quantise + D and C + D rows)")
+
+
+def cpu_baseline_config(name, workloads, seconds=3.0):
+    """The oracle on a bounded sample of one of the other workloads: the rows
+    of A quantised by the oracle and their output rows computed against the
+    oracle-quantised B (B is quantised once, outside the timed part, as the
+    GPU side's weights are)."""
+    import oracle
+    rng = np.random.default_rng(1)
+    if name == "small":
+        cfg = workloads.SMALL
+        w = workloads.dense(cfg["m"], cfg["n"], cfg["k"], cfg["seed"])
+        a, b = w.a.numpy(), w.b.numpy()
+
+        def run(reps):
+            f = 0.0
+            for _ in range(reps):
+                qa, _, sa = oracle.quantize(a, 1)
+                qb, _, sb = oracle.quantize(b, 128)
+                oracle.gemm_nt(qa, sa, qb, sb)
+                f += 2.0 * cfg["m"] * cfg["n"] * cfg["k"]
+            return f
+        reps = calibrate(run, 2, seconds, 100000)
+        return timed_baseline(run, reps, "%d repetitions of the whole workload (quantise A and B + GEMM)")
+    if name == "decode":
+        items = []
+        for cfg in workloads.DECODE:
+            w = workloads.dense(cfg["m"], cfg["n"], cfg["k"], cfg["seed"])
+            qb, _, sb = oracle.quantize(w.b.numpy(), 128)
+            rows = rng.choice(cfg["m"], size=cfg["m"], replace=False)
+            items.append(dict(a=np.ascontiguousarray(w.a.numpy()[rows]), qb=qb, sb=sb, k=cfg["k"]))
+
+        def run(r):
+            f = 0.0
+            for it in items:
+                qa, _, sa = oracle.quantize(it["a"][:r], 1)
+                oracle.gemm_nt_rows(qa, sa, it["qb"], it["sb"], np.arange(qa.shape[0], dtype=np.int64))
+                f += 2.0 * qa.shape[0] * it["qb"].shape[0] * it["k"]
+            return f
+        r = calibrate(run, 1, seconds, 64)
+        return timed_baseline(run, r, "%d random rows of A per decode shape (quantise + D rows)")
+    if name == "contiguous":
+        cfg = workloads.CONTIG
+        w = workloads.contiguous(cfg["num_groups"], cfg["n"], cfg["k"], cfg["seed"])
+        G, n, k = cfg["num_groups"], cfg["n"], cfg["k"]
+        qbs = [oracle.quantize(w.b[g].numpy(), 128) for g in range(G)]
+        qb, sb = np.stack([x[0] for x in qbs]), np.stack([x[2] for x in qbs])
+        mi = w.m_indices.numpy()
+        per = [rng.permutation(np.nonzero(mi == g)[0]) for g in range(G)]
+        a = w.a.numpy()
+
+        def run(r):
+            rows = np.concatenate([p[:r] for p in per])
+            qa, _, sa = oracle.quantize(np.ascontiguousarray(a[rows]), 1)
+            oracle.gemm_contiguous(qa, sa, qb, sb, mi[rows])
+            return 2.0 * rows.size * n * k
+        r = calibrate(run, 1, seconds, min(p.size for p in per))
+        return timed_baseline(run, r, "%d random valid rows of A per expert (quantise + D rows)")
+    if name == "masked":
+        cfg = workloads.MASKED
+        G, cap, n, k = cfg["num_groups"], cfg["cap"], cfg["n"], cfg["k"]
+        w = workloads.masked(G, cap, n, k, cfg["seed"])
+        qbs = [oracle.quantize(w.b[g].numpy(), 128) for g in range(G)]
+        qb, sb = np.stack([x[0] for x in qbs]), np.stack([x[2] for x in qbs])
+        mm = w.masked_m.numpy()
+        a = w.a.numpy()
+
+        def run(r):
+            take_m = np.minimum(mm, r).astype(np.int32)
+            qa = np.zeros((G, r, k), dtype=np.uint8)
+            sa = np.ones((G, r, k // 128))
+            for g in range(G):
+                if take_m[g]:
+                    q, _, s = oracle.quantize(np.ascontiguousarray(a[g, :take_m[g]]), 1)
+                    qa[g, :take_m[g]], sa[g, :take_m[g]] = q, s
+            oracle.gemm_masked(qa, sa, qb, sb, take_m)
+            return 2.0 * float(take_m.sum()) * n * k
+        r = calibrate(run, 1, seconds, cap)
+        return timed_baseline(run, r, "the first min(masked_m, %d) rows of A per expert (quantise + D rows)")
+    raise ValueError(name)
+
+
+def run_reference(args, ranks):
+    from moe_grouped_gemm_fp8_gb300 import workloads
+    import oracle
+    if ranks.rank != 0:
+        return 0
+    items = oracle_sample(workloads, 2048)
+    rows = calibrated_rows(items, 0.5)
+    items = take(items, rows)
+    for _ in range(args.warmup):
+        oracle_run(items)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += oracle_run(items)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = "%d rows of A per prefill shape per step (quantise + D and C + D rows), FP64" % rows
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "dense NT prefill-like M=4096, (N,K) in %s, with and without C; CPU oracle row sample" %
+                   workloads.PREFILL_NK},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.get_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # --------------------------------------------------------------------------- other workloads
 
 
@@ -507,27 +655,18 @@ def _time_graph(fns, replays):
     return statistics.median(ts)
 
 
-def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
-    """GEMM-only timing of the decode, contiguous, masked or small workloads.
-
-    Each case owns enough copies of its inputs and outputs that the copies
-    together exceed L2 several times over (B of the decode shapes alone would
-    fit); one launch per copy is captured into a CUDA graph, so the timed
-    launches run back to back with no host gaps and read their operands from
-    HBM. A single launch after an L2 flush is timed too, as a second figure
-    that includes the launch latency an isolated call pays."""
-    flush = torch.zeros(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    dg.set_pdl(bool(args.pdl))
-    hbm = peaks["hbm_gbs"]
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+def build_cases(name, dg, workloads, dev):
+    """GEMM-only launch closures of one workload.  Each case owns enough
+    copies of its inputs and outputs that the copies together exceed L2
+    several times over (B of the decode shapes alone would fit)."""
     cases = []
 
     def rotate(tensors, nbytes):
         r = _copies_for(nbytes)
         return [tensors] + [tuple(t.clone() for t in tensors) for _ in range(r - 1)]
 
-    if args.workload in ("decode", "small"):
-        cfgs = workloads.DECODE if args.workload == "decode" else [workloads.SMALL]
+    if name in ("decode", "small"):
+        cfgs = workloads.DECODE if name == "decode" else [workloads.SMALL]
         for cfg in cfgs:
             m, n, k = cfg["m"], cfg["n"], cfg["k"]
             w = workloads.dense(m, n, k, cfg["seed"])
@@ -538,8 +677,8 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
             fns = [(lambda t=t: dg.fp8_gemm_nt(t[0], t[1], t[2], t[3], d=t[4]))
                    for t in rotate((qa, sfa, qb, sfb, d), byt)]
             cases.append(dict(name="dense m=%d n=%d k=%d" % (m, n, k), fns=fns, flops=2.0 * m * n * k,
-                              bytes=byt))
-    elif args.workload == "contiguous":
+                              bytes=byt, shape=(m, n, k)))
+    elif name == "contiguous":
         cfg = workloads.CONTIG
         w = workloads.contiguous(cfg["num_groups"], cfg["n"], cfg["k"], cfg["seed"])
         qa, sfa = dg.quantize_fp8(w.a.to(dev), 1)
@@ -548,12 +687,12 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
         d = torch.empty(w.a.shape[0], cfg["n"], dtype=torch.bfloat16, device=dev)
         valid = int(w.counts.sum())
         n, k, G = cfg["n"], cfg["k"], cfg["num_groups"]
-        byt = valid * k + G * n * k + 2 * valid * n + valid * k // 128 + G * n * k // 128 // 32
+        byt = algorithmic_bytes_contiguous(valid, G, n, k)
         fns = [(lambda t=t: dg.m_grouped_fp8_gemm_nt_contiguous(t[0], t[1], t[2], t[3], t[4], d=t[5]))
                for t in rotate((qa, sfa, qb, sfb, mi, d), byt)]
         cases.append(dict(name="contiguous G=%d valid_rows=%d padded_rows=%d n=%d k=%d" %
                           (G, valid, w.a.shape[0], n, k), fns=fns, flops=2.0 * valid * n * k, bytes=byt))
-    elif args.workload == "fp32scales":
+    elif name == "fp32scales":
         # the prefill shapes through the FP32-scale (promotion) kernel; the
         # scales are the quantiser's (powers of two), passed as FP32
         for cfg in workloads.PREFILL:
@@ -570,7 +709,7 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
                    for t in rotate((qa, fa, qb, fb, d), byt)]
             cases.append(dict(name="fp32-scale dense m=%d n=%d k=%d" % (m, n, k), fns=fns,
                               flops=2.0 * m * n * k, bytes=byt))
-    elif args.workload == "kgrouped":
+    elif name == "kgrouped":
         cfg = workloads.KGROUPED
         w = workloads.k_grouped(cfg["num_groups"], cfg["m"], cfg["n"], cfg["seed"])
         qa, sfa = dg.quantize_fp8_cols(w.a.to(dev))
@@ -585,7 +724,7 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
                for t in rotate((qa, sfa, qb, sfb, ks, d), byt)]
         cases.append(dict(name="k-grouped G=%d valid_k=%d padded_k=%d m=%d n=%d" % (G, valid, sum_k, m, n),
                           fns=fns, flops=2.0 * valid * m * n, bytes=byt))
-    elif args.workload == "masked":
+    elif name == "masked":
         cfg = workloads.MASKED
         G, cap, n, k = cfg["num_groups"], cfg["cap"], cfg["n"], cfg["k"]
         w = workloads.masked(G, cap, n, k, cfg["seed"])
@@ -595,13 +734,36 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
         d = torch.empty(G, cap, n, dtype=torch.bfloat16, device=dev)
         valid = int(w.masked_m.sum())
         used = int((w.masked_m > 0).sum())
-        byt = valid * k + used * n * k + 2 * valid * n + valid * k // 128 + used * n * (k // 512) * 4
+        byt = algorithmic_bytes_masked(valid, used, n, k)
         exp_m = int(w.masked_m.float().mean())
         fns = [(lambda t=t: dg.m_grouped_fp8_gemm_nt_masked(t[0], t[1], t[2], t[3], t[4], exp_m, d=t[5]))
                for t in rotate((qa, sfa, qb, sfb, mm, d), byt)]
         cases.append(dict(name="masked G=%d cap=%d valid_rows=%d n=%d k=%d" % (G, cap, valid, n, k),
                           fns=fns, flops=2.0 * valid * n * k, bytes=byt))
-    if args.shape >= 0:
+    return cases
+
+
+# which roofline bounds each workload (the tensor-core rate for the
+# compute-bound ones, HBM for the memory-bound ones)
+CONFIG_BOUND = {"small": "tensor", "decode": "hbm", "contiguous": "tensor", "masked": "hbm",
+                "kgrouped": "tensor", "fp32scales": "tensor"}
+CONFIG_DESC = {
+    "small": "dense NT M=128 N=256 K=512, no C",
+    "decode": "dense NT decode-like M in {64,128}, (N,K) in the five prefill pairs, no C",
+    "contiguous": "M-grouped contiguous MoE: 8 experts, B [8,4096,7168], per-expert rows U[256,8192] "
+                  "padded to 128 (padding rows tagged -1)",
+    "masked": "M-grouped masked MoE decode: 16 experts x capacity 256, B [16,7168,2048], masked_m U[0,256]",
+    "kgrouped": "K-grouped MoE weight gradient: 8 experts, M=4096, N=7168, token rows U[256,8192] padded to 128",
+    "fp32scales": "dense NT prefill shapes through the FP32-scale (promotion) kernel",
+}
+
+
+def measure_config(name, args, dg, workloads, dev, peaks, peak_src, flush):
+    """GEMM-only device timing of one workload (CUDA-graph replays over input
+    copies exceeding L2, and one isolated launch after an L2 flush) with its
+    roofline."""
+    cases = build_cases(name, dg, workloads, dev)
+    if args.shape >= 0 and name == args.workload:
         cases = [cases[args.shape]]
     for c in cases:
         for _ in range(max(3, args.warmup)):
@@ -617,45 +779,48 @@ def run_other(args, ranks, dg, workloads, dev, peaks, peak_src):
                 c["fns"][0]()
         torch.cuda.synchronize()
         return None
-    clocks = ClockSampler(torch.cuda.current_device())
-    ranks.barrier()
-    clocks.start()
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    replays = max(args.steps, 20)
     res = []
     for c in cases:
-        t = _time_graph(c["fns"], args.steps)
-        t1 = _time_gemm(c["fns"][0], max(3, args.steps // 3), flush)
+        t = _time_graph(c["fns"], replays)
+        t1 = _time_gemm(c["fns"][0], max(3, replays // 3), flush)
         res.append({"case": c["name"], "us": t * 1e3, "copies": len(c["fns"]),
                     "tflops": c["flops"] / (t * 1e-3) / 1e12,
                     "gbs": c["bytes"] / (t * 1e-3) / 1e9,
                     "frac_fp8_peak": c["flops"] / (t * 1e-3) / 1e12 / fp8_peak,
                     "frac_hbm": c["bytes"] / (t * 1e-3) / 1e9 / hbm,
                     "us_isolated_after_flush": t1 * 1e3})
-    clk = clocks.stop()
-    ranks.barrier()
-    tot_t = ranks.max(sum(r["us"] for r in res) * 1e-6)
-    tot_f = ranks.sum(sum(c["flops"] for c in cases))
+    st, word = dg.get_device_error()
+    if st != 0:
+        raise RuntimeError("device error: 0x%x" % word)
+    tot_t = sum(r["us"] for r in res) * 1e-6
+    tot_f = sum(c["flops"] for c in cases)
     tot_b = sum(c["bytes"] for c in cases)
-    hbm_bound = args.workload in ("decode", "masked")
-    achieved = (tot_b / tot_t / 1e9) if hbm_bound else (sum(c["flops"] for c in cases) / tot_t / 1e12)
-    peak = hbm if hbm_bound else fp8_peak
-    line = {
-        "metric": METRIC, "value": tot_f / tot_t / 1e12, "unit": "TFLOPS", "n_gpus": ranks.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
-        "data": "synthetic",
-        "config": {"workload": args.workload, "pdl": bool(args.pdl),
-                   "l2": "inputs larger than L2: each case rotates over input copies totalling "
-                         ">2.5x L2, launched back to back in a CUDA graph"},
-        "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s" if hbm_bound else "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                     "peak_source": peak_src},
-        "gpu_launches": sum(len(c["fns"]) for c in cases) * args.steps
-                        + len(cases) * max(3, args.steps // 3),
-        "cases": res, "impl": "ours",
-    }
-    if clk:
-        line["clocks"] = clk
-    return line
+    bound = CONFIG_BOUND[name]
+    achieved = (tot_b / tot_t / 1e9) if bound == "hbm" else (tot_f / tot_t / 1e12)
+    peak = hbm if bound == "hbm" else fp8_peak
+    roof = {"bound": bound, "achieved": achieved, "peak": peak,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak, "traffic": None,
+            "peak_source": peak_src if bound == "hbm" else
+            "%s bf16 burst %.1f TFLOP/s x %.1f nominal FP8:BF16 ratio" % (peak_src, peaks["bf16_tflops"],
+                                                                         FP8_OVER_BF16)}
+    if name == "small":
+        roof["limited_by"] = "launch latency (0.03 GFLOP per launch)"
+    entry = {"workload": CONFIG_DESC[name], "value": tot_f / tot_t / 1e12, "unit": "TFLOPS",
+             "us": tot_t * 1e6, "gbs": tot_b / tot_t / 1e9, "roofline": roof, "cases": res,
+             "gpu_launches": sum(len(c["fns"]) for c in cases) * (replays + 1)
+                             + len(cases) * max(3, replays // 3),
+             "timing": "CUDA-graph replays of one launch per input copy (copies totalling > 2.5x L2), "
+                       "median replay time / launches; us_isolated_after_flush: one launch after an L2 flush"}
+    if name == "decode":
+        entry["plans"] = [dict(shape=list(c["shape"]), **dg.plan_fp8_gemm_nt(*c["shape"],
+                                                                                num_sms=torch.cuda.get_device_properties(dev).multi_processor_count))
+                          for c in cases]
+    del cases
+    torch.cuda.empty_cache()
+    return entry
 
 
 def main():
@@ -673,19 +838,61 @@ def main():
     torch.cuda.set_device(ranks.local)
     dev = torch.device("cuda", ranks.local)
     peaks, peak_src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    flush = torch.zeros(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
+    clocks = ClockSampler(torch.cuda.current_device())
     if args.workload != "prefill":
-        line = run_other(args, ranks, dg, workloads, dev, peaks, peak_src)
-        if ranks.rank == 0 and line:
+        dg.set_pdl(bool(args.pdl))
+        ranks.barrier()
+        clocks.start()
+        entry = measure_config(args.workload, args, dg, workloads, dev, peaks, peak_src, flush)
+        clk = clocks.stop()
+        ranks.barrier()
+        if entry is None:
+            ranks.close()
+            return 0
+        t = ranks.max(entry["us"] * 1e-6)
+        f = ranks.sum(entry["value"] * 1e12 * entry["us"] * 1e-6)
+        line = {
+            "metric": METRIC, "value": f / t / 1e12, "unit": "TFLOPS", "n_gpus": ranks.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+            "data": "synthetic",
+            "config": {"workload": entry["workload"], "pdl": bool(args.pdl),
+                       "l2": "inputs larger than L2: each case rotates over input copies totalling "
+                             ">2.5x L2, launched back to back in a CUDA graph"},
+            "roofline": entry["roofline"], "gpu_launches": entry["gpu_launches"], "cases": entry["cases"],
+            "impl": "ours",
+        }
+        if "plans" in entry:
+            line["plans"] = entry["plans"]
+        if clk:
+            line["clocks"] = clk
+        if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline and args.workload in OTHER_CONFIGS:
+            line["cpu_baseline"] = cpu_baseline_config(args.workload, workloads)
+        if ranks.rank == 0:
             print(json.dumps(line), flush=True)
         ranks.close()
         return 0
 
-    res = run_prefill(args, ranks, dg, workloads, dev)
+    # clocks are sampled from the first warm-up step to the end of the last
+    # measurement (the sampler needs a few hundred ms to start reporting)
+    clocks.start()
+    res = run_prefill(args, ranks, dg, workloads, dev, clocks)
     if res is None:
+        clocks.stop()
         ranks.close()
         return 0
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    configs = {}
+    if not args.no_configs:
+        dg.set_pdl(bool(args.pdl))
+        for name in OTHER_CONFIGS:
+            configs[name] = measure_config(name, args, dg, workloads, dev, peaks, peak_src, flush)
+    clk = clocks.stop()
+    dom = dominant_launch(res["per_shape"])
+    traffic, plan = captured_traffic(dg, dom["m"], dom["n"], dom["k"], dom["c"], num_sms)
     line = {
         "metric": METRIC, "value": res["value"], "unit": "TFLOPS", "n_gpus": ranks.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms"],
@@ -697,17 +904,22 @@ def main():
                    "l2": "inputs larger than L2 (per-step working set %.2f GB)" % res["working_set_gb"],
                    "replicas": ranks.world, "pdl": bool(args.pdl)},
         "roofline": prefill_roofline(res, fp8_peak, "%s bf16 burst %.1f TFLOP/s x %.1f nominal FP8:BF16 ratio" %
-                                     (peak_src, peaks["bf16_tflops"], FP8_OVER_BF16)),
+                                     (peak_src, peaks["bf16_tflops"], FP8_OVER_BF16), traffic, plan),
         "gpu_launches": res["launches"],
         "shapes": res["per_shape"],
+        "sustained": res["sustained"],
         "impl": "ours",
     }
-    if res["clocks"]:
-        line["clocks"] = res["clocks"]
+    if clk:
+        line["clocks"] = clk
     if res["e2e"]:
         line["e2e"] = res["e2e"]
+    if configs:
+        line["configs"] = configs
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(workloads)
+        for name, entry in configs.items():
+            entry["cpu_baseline"] = cpu_baseline_config(name, workloads)
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
     ranks.close()

@@ -56,17 +56,26 @@ def sentinel_like(shape, device="cuda") -> torch.Tensor:
     return torch.full(shape, SENTINEL_BITS, dtype=torch.int16, device=device).view(torch.bfloat16)
 
 
-def assert_close(d: np.ndarray, o: np.ndarray, what: str = ""):
+# (label, elements compared, sum((d-o)^2)/sum(o^2), max|d-o| / max|o|) of every
+# comparison made with record=True; printed at the end of the session.
+REPORT = []
+
+
+def assert_close(d: np.ndarray, o: np.ndarray, what: str = "", record: bool = False):
     """d, o: FP64 arrays of the written rows."""
     assert d.shape == o.shape, (d.shape, o.shape)
     if o.size == 0:
         return
     assert np.isfinite(d).all(), "%s: non-finite output" % what
     err = d - o
-    denom = float((o * o).sum())
-    rel = float((err * err).sum()) / denom if denom > 0 else float((err * err).sum())
+    denom = float(np.einsum("i,i->", o.ravel(), o.ravel()))
+    num = float(np.einsum("i,i->", err.ravel(), err.ravel()))
+    rel = num / denom if denom > 0 else num
     mx = float(np.abs(err).max())
-    lim = MAX_ABS_TOL * float(np.abs(o).max())
+    omax = float(np.abs(o).max())
+    lim = MAX_ABS_TOL * omax
+    if record:
+        REPORT.append((what, int(o.size), rel, mx / omax if omax > 0 else mx))
     assert rel <= REL_SQ_TOL, "%s: relative squared error %.3e > %.0e" % (what, rel, REL_SQ_TOL)
     assert mx <= lim, "%s: max abs error %.4g > %.4g" % (what, mx, lim)
     return rel, mx

@@ -28,12 +28,57 @@ def test_roofline_takes_the_largest_launch_without_c():
         dict(m=4096, n=7168, k=16384, c=False, us=320.0, tflops=3004.0),
         dict(m=4096, n=7168, k=16384, c=True, us=326.0, tflops=2953.0),
     ]
-    r = bench.prefill_roofline({"per_shape": per_shape, "achieved": 2600.0}, 3901.4, "measured")
+    assert bench.dominant_launch(per_shape) is per_shape[1]
+    r = bench.prefill_roofline({"per_shape": per_shape, "achieved": 2600.0}, 3901.4, "measured", 1.5e8)
     assert r["achieved"] == 3004.0 and abs(r["frac"] - 3004.0 / 3901.4) < 1e-12
-    assert r["traffic"] == bench.DOMINANT_TRAFFIC          # the captured shape
+    assert r["traffic"] == 1.5e8
     assert abs(r["all_gemms"]["frac"] - 2600.0 / 3901.4) < 1e-12
-    other = [dict(m=4096, n=2112, k=7168, c=False, us=56.0, tflops=2213.0)]
-    assert bench.prefill_roofline({"per_shape": other, "achieved": 1.0}, 3901.4, "measured")["traffic"] is None
+
+
+class _FakePlanner:
+    """Stands in for the binding's tile-choice query (pure host arithmetic)."""
+
+    def __init__(self, plan):
+        self.plan = plan
+
+    def plan_fp8_gemm_nt(self, m, n, k, has_c=False, num_sms=152):
+        return dict(self.plan)
+
+
+def test_traffic_only_for_the_captured_tile_configuration():
+    key = next(iter(bench.CAPTURED_TRAFFIC))
+    m, n, k, c, bm, bn, sk, pair = key
+    same = _FakePlanner(dict(block_m=bm, block_n=bn, split_k=sk, cta_pair=bool(pair)))
+    t, plan = bench.captured_traffic(same, m, n, k, c, 152)
+    assert t == bench.CAPTURED_TRAFFIC[key] and plan["block_n"] == bn
+    other = _FakePlanner(dict(block_m=bm, block_n=bn + 32, split_k=sk, cta_pair=bool(pair)))
+    assert bench.captured_traffic(other, m, n, k, c, 152)[0] is None  # a changed tile: stale counters
+    assert bench.captured_traffic(same, m, n + 128, k, c, 152)[0] is None  # another shape
+
+
+def test_grouped_byte_counts():
+    # contiguous: valid rows of A and D, all experts' B, packed scale words
+    assert bench.algorithmic_bytes_contiguous(1000, 8, 4096, 7168) == (
+        1000 * 7168 + 8 * 4096 * 7168 + 2 * 1000 * 4096 + 4 * 14 * (1000 + 8 * 4096))
+    # masked: only experts with rows read their B
+    assert bench.algorithmic_bytes_masked(300, 3, 7168, 2048) == (
+        300 * 2048 + 3 * 7168 * 2048 + 2 * 300 * 7168 + 4 * 4 * (300 + 3 * 7168))
+
+
+def test_clock_summary_uses_samples_under_load():
+    idle = ["0", "1000", "2070", "100.0", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"]
+    busy = ["0", "1900", "2070", "1300.0", "0x4", "Not Active", "Not Active", "Not Active", "Active"]
+    c = bench.summarise_clocks([idle] * 5 + [busy] * 7 + [["garbage"]])
+    assert c["samples"] == 12 and c["samples_under_load"] == 7
+    assert c["sm_mhz"] == 1900.0 and c["sm_max_mhz"] == 2070.0 and c["reasons"] == ["sw_power_cap"]
+    assert bench.summarise_clocks([]) is None
+
+
+def test_cpu_baseline_of_the_small_config():
+    cb = bench.cpu_baseline_config("small", __import__("moe_grouped_gemm_fp8_gb300.workloads",
+                                                       fromlist=["x"]), seconds=0.2)
+    assert cb["kind"] == "oracle" and cb["unit"] == "TFLOPS" and cb["value"] > 0 and cb["cores"] >= 1
+    assert "repetitions" in cb["sample"]
 
 
 def test_reference_arm_prints_one_contract_line():

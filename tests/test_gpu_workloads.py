@@ -1,11 +1,17 @@
 """GPU parity at the full workload sizes, in the launch configuration the
-bench uses: dense prefill-like (M=4096, five (N, K) pairs, with and without
-C), dense decode-like (M in {64, 128}), contiguous MoE (8 experts, N=4096,
-K=7168) and masked MoE (16 experts x 256 rows, N=7168, K=2048).
+bench uses: dense small (M=128, N=256, K=512), dense prefill-like (M=4096,
+five (N, K) pairs, with and without C), dense decode-like (M in {64, 128}),
+contiguous MoE (8 experts, N=4096, K=7168) and masked MoE (16 experts x 256
+rows, N=7168, K=2048).
 
-Which rows are written is checked on every row (sentinel fill); values are
-checked against the oracle on sampled rows (every row for the decode shapes),
-always including the first and last rows and rows on tile boundaries."""
+Every written element is compared with the CPU oracle (FP64) on the same
+seeded inputs, per tensor: sum((d - o)^2) / sum(o^2) <= 1e-5 and
+max|d - o| <= 2e-2 * max|o|.  Which rows are written is checked bit for bit
+on every row (sentinel fill).  The oracle runs the full products on the
+host's cores (about 2 TFLOP for the prefill set with and without C, 2.3 for
+the contiguous workload)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -18,51 +24,53 @@ import _parity as P
 pytestmark = pytest.mark.gpu
 
 
-def _sample_rows(m, seed, extra=48):
-    rng = np.random.default_rng(seed)
-    # 128- and 256-row tile boundaries (both tile heights run at these sizes)
-    fixed = [0, 1, 2, 127, 128, 129, 255, 256, 257, m // 2, m - 257, m - 256, m - 129, m - 128,
-             m - 2, m - 1]
-    rows = set(r for r in fixed if 0 <= r < m)
-    rows.update(rng.choice(m, size=min(extra, m), replace=False).tolist())
-    return np.array(sorted(rows), dtype=np.int64)
-
-
 def _no_device_error():
     st, word = dg.get_device_error()
     assert st == 0, "device error word 0x%x" % word
+
+
+def _dense_case(cfg, with_c):
+    m, n, k = cfg["m"], cfg["n"], cfg["k"]
+    w = workloads.dense(m, n, k, cfg["seed"], with_c=with_c)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    dev = (P.dev_codes(qa), P.dev_packed_sf(sa, m, k, 1), P.dev_codes(qb), P.dev_packed_sf(sb, n, k, 128))
+    return w, (qa, sa, qb, sb), dev
+
+
+def test_small_config():
+    cfg = workloads.SMALL
+    _, (qa, sa, qb, sb), dev = _dense_case(cfg, False)
+    d = dg.fp8_gemm_nt(*dev, d=P.sentinel_like((cfg["m"], cfg["n"])))
+    _no_device_error()
+    P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "small m=128 n=256 k=512", record=True)
 
 
 @pytest.mark.parametrize("idx", range(len(workloads.PREFILL)))
 def test_prefill_dense(idx):
     cfg = workloads.PREFILL[idx]
     m, n, k = cfg["m"], cfg["n"], cfg["k"]
-    w = workloads.dense(m, n, k, cfg["seed"], with_c=True)
-    qa, _, sa = P.quantize(w.a, 1)
-    qb, _, sb = P.quantize(w.b, 128)
-    args = (P.dev_codes(qa), P.dev_packed_sf(sa, m, k, 1), P.dev_codes(qb), P.dev_packed_sf(sb, n, k, 128))
-    rows = _sample_rows(m, cfg["seed"])
-    d = dg.fp8_gemm_nt(*args)
-    o = oracle.gemm_nt_rows(qa, sa, qb, sb, rows)
-    P.assert_close(P.bf16_to_f64(d[torch.from_numpy(rows).cuda()]), o, "prefill %s" % (cfg,))
-    cbits = P.bf16_bits(w.c)
-    dc = dg.fp8_gemm_nt(*args, c=w.c.cuda())
-    oc = oracle.gemm_nt_rows(qa, sa, qb, sb, rows, cbits)
-    P.assert_close(P.bf16_to_f64(dc[torch.from_numpy(rows).cuda()]), oc, "prefill+C %s" % (cfg,))
+    w, (qa, sa, qb, sb), dev = _dense_case(cfg, True)
+    tag = "prefill m=%d n=%d k=%d" % (m, n, k)
+    d = dg.fp8_gemm_nt(*dev, d=P.sentinel_like((m, n)))
     _no_device_error()
+    P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), tag, record=True)
+    del d
+    dc = dg.fp8_gemm_nt(*dev, c=w.c.cuda(), d=P.sentinel_like((m, n)))
+    _no_device_error()
+    P.assert_close(P.bf16_to_f64(dc), oracle.gemm_nt(qa, sa, qb, sb, P.bf16_bits(w.c)), tag + " +C",
+                   record=True)
 
 
 @pytest.mark.parametrize("idx", range(len(workloads.DECODE)))
 def test_decode_dense(idx):
     cfg = workloads.DECODE[idx]
     m, n, k = cfg["m"], cfg["n"], cfg["k"]
-    w = workloads.dense(m, n, k, cfg["seed"])
-    qa, _, sa = P.quantize(w.a, 1)
-    qb, _, sb = P.quantize(w.b, 128)
-    d = dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, m, k, 1), P.dev_codes(qb),
-                       P.dev_packed_sf(sb, n, k, 128))
-    P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "decode %s" % (cfg,))
+    _, (qa, sa, qb, sb), dev = _dense_case(cfg, False)
+    d = dg.fp8_gemm_nt(*dev, d=P.sentinel_like((m, n)))
     _no_device_error()
+    P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "decode m=%d n=%d k=%d" % (m, n, k),
+                   record=True)
 
 
 def test_contiguous_moe_config():
@@ -81,18 +89,11 @@ def test_contiguous_moe_config():
     bits = P.bf16_bits(d)
     valid = mi >= 0
     assert (bits[~valid] == P.SENTINEL_BITS).all(), "padding rows were written"
-    assert not (bits[valid] == P.SENTINEL_BITS).all(axis=1).any(), "a valid row was not written"
-    # sampled rows: per expert the first, last and random valid rows
-    rng = np.random.default_rng(cfg["seed"])
-    rows = []
-    for g in range(cfg["num_groups"]):
-        idx = np.nonzero(mi == g)[0]
-        if idx.size:
-            rows += [idx[0], idx[-1]] + rng.choice(idx, size=min(6, idx.size), replace=False).tolist()
-    rows = np.array(sorted(set(int(r) for r in rows)), dtype=np.int64)
-    o, written = oracle.gemm_contiguous(qa, sa, qb, sb, mi, rows=rows)
-    assert written.all()
-    P.assert_close(P.bf16_to_f64(d[torch.from_numpy(rows).cuda()]), o, "contiguous config")
+    o, written = oracle.gemm_contiguous(qa, sa, qb, sb, mi)
+    assert np.array_equal(written.astype(bool), valid)
+    got = P.bf16_to_f64(d)[valid]
+    del d, bits
+    P.assert_close(got, o[valid], "contiguous G=8 rows=%d n=%d k=%d" % (int(valid.sum()), n, k), record=True)
 
 
 def test_masked_moe_config():
@@ -108,38 +109,28 @@ def test_masked_moe_config():
                                     w.masked_m.cuda(), expected_m=int(mm.mean()), d=d)
     _no_device_error()
     bits = P.bf16_bits(d)
-    for g in range(G):
-        assert (bits[g, mm[g]:] == P.SENTINEL_BITS).all(), "group %d: rows past masked_m written" % g
-        if mm[g]:
-            assert not (bits[g, :mm[g]] == P.SENTINEL_BITS).all(axis=1).any()
-    rng = np.random.default_rng(cfg["seed"])
-    flat = []
-    for g in range(G):
-        if mm[g]:
-            rr = {0, mm[g] - 1} | set(rng.choice(mm[g], size=min(6, mm[g]), replace=False).tolist())
-            flat += [g * cap + r for r in rr]
-    rows = np.array(sorted(flat), dtype=np.int64)
-    o, written = oracle.gemm_masked(qa, sa, qb, sb, mm, rows=rows)
-    assert written.all()
-    got = P.bf16_to_f64(d.view(G * cap, n)[torch.from_numpy(rows).cuda()])
-    P.assert_close(got, o, "masked config")
+    o, written = oracle.gemm_masked(qa, sa, qb, sb, mm)
+    wr = written.astype(bool)
+    assert np.array_equal(wr, np.arange(cap)[None, :] < mm[:, None])
+    assert (bits[~wr] == P.SENTINEL_BITS).all(), "rows past masked_m were written"
+    P.assert_close(P.bf16_to_f64(d)[wr], o[wr], "masked G=16 cap=256 rows=%d n=%d k=%d" % (int(mm.sum()), n, k),
+                   record=True)
 
 
 @pytest.mark.parametrize("counts", ["uniform128", "seeded"])
 def test_masked_moe_every_tile_width_full_grid(counts):
     """The masked MoE shape at every tile width on all SMs: many CTAs with
     several tiles each and 5- and 6-stage pipelines, the setting in which a
-    waiter that skips phases of a stage barrier would read stale scales."""
-    import os
+    waiter that skips phases of a stage barrier would read stale scales.
+    Every written element is compared."""
     cfg = workloads.MASKED
     G, cap, n, k = cfg["num_groups"], cfg["cap"], cfg["n"], cfg["k"]
     w = workloads.masked(G, cap, n, k, cfg["seed"], masked_m=[128] * G if counts == "uniform128" else None)
     qa, _, sa = P.quantize(w.a, 1)
     qb, _, sb = P.quantize(w.b, 128)
     mm = w.masked_m.numpy()
-    rows = np.array(sorted({g * cap + r for g in range(G) for r in range(0, mm[g], 29)} |
-                           {g * cap + mm[g] - 1 for g in range(G) if mm[g]}), dtype=np.int64)
-    o, _ = oracle.gemm_masked(qa, sa, qb, sb, mm, rows=rows)
+    o, written = oracle.gemm_masked(qa, sa, qb, sb, mm)
+    wr = written.astype(bool)
     dev = (P.dev_codes(qa), P.dev_packed_sf(sa, cap, k, 1), P.dev_codes(qb), P.dev_packed_sf(sb, n, k, 128))
     old = {k: os.environ.get(k) for k in ("DG_BLOCK_N", "DG_CTA_PAIR")}
     try:
@@ -150,10 +141,8 @@ def test_masked_moe_every_tile_width_full_grid(counts):
             dg.m_grouped_fp8_gemm_nt_masked(*dev, w.masked_m.cuda(), d=d)
             _no_device_error()
             bits = P.bf16_bits(d)
-            for g in range(G):
-                assert (bits[g, mm[g]:] == P.SENTINEL_BITS).all(), "pair=%d bn=%d g=%d" % (pair, bn, g)
-            got = P.bf16_to_f64(d.view(G * cap, n)[torch.from_numpy(rows).cuda()])
-            P.assert_close(got, o, "masked pair=%d bn=%d" % (pair, bn))
+            assert (bits[~wr] == P.SENTINEL_BITS).all(), "pair=%d bn=%d: rows past masked_m written" % (pair, bn)
+            P.assert_close(P.bf16_to_f64(d)[wr], o[wr], "masked pair=%d bn=%d" % (pair, bn))
     finally:
         for k, v in old.items():
             if v is None:
