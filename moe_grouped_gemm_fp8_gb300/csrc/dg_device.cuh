@@ -85,10 +85,13 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
 // (returns false) when the shared abort flag is raised by another role, or
 // after `timeout_ns`, or after a fixed iteration cap; in the two last cases
 // it records DG_ERR_DEVICE_TIMEOUT with `site` and raises the abort flag.
+// wait_bounded keeps this slow path out of line; kernels that move registers
+// between warpgroups with setmaxnreg cannot call an out-of-line function (the
+// register allocator rejects the call), so they inline wait_bounded_body.
 template <uint32_t HINT_NS = 0>
-static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint64_t timeout_ns, unsigned long long* err,
-                                          uint32_t site) {
+__device__ __forceinline__ bool wait_bounded_body(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t timeout_ns, unsigned long long* err,
+                                                  uint32_t site) {
   if (mbar_try_wait_hint<HINT_NS>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -102,6 +105,13 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
       }
     }
   }
+}
+
+template <uint32_t HINT_NS = 0>
+static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t timeout_ns, unsigned long long* err,
+                                          uint32_t site) {
+  return wait_bounded_body<HINT_NS>(bar, parity, abort_flag, timeout_ns, err, site);
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch

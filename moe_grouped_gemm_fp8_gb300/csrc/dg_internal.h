@@ -82,6 +82,8 @@ struct GemmArgs {
   // skips on its first tile, so that stage's barrier never completes and the
   // bounded waits must end the launch with DG_ERR_DEVICE_TIMEOUT; 0 = off.
   int32_t debug_drop_load;
+  // 256-row dense tiles: drain the accumulator with eight epilogue warps
+  int32_t epi8;
   // FP32-scale (promotion) form only
   const float* sfa_f32;    // [ceil(k/128), sfa_ld]: per K block, one scale per row of A
   const float* sfb_f32;    // [ceil(n/128), k/128]: one scale per 128 x 128 block of B

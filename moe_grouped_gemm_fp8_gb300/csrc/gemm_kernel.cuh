@@ -76,6 +76,14 @@
 namespace dg {
 
 constexpr int kGemmThreads = 224;
+// 256-row dense tiles with eight epilogue warps (two per TMEM lane quarter,
+// one per 128-row half): warps 0-2 keep their roles, warp 3 idles, warps
+// 4-11 drain the single accumulator.  Registers are shifted to the epilogue
+// warpgroups with setmaxnreg: 128 x kRegsRoles + 256 x kRegsEpi must equal
+// the 384 x 168 registers the block is launched with.
+constexpr int kGemmThreadsEpi8 = 384;
+constexpr int kRegsRoles = 56, kRegsEpi = 224;
+static_assert(128 * kRegsRoles + 256 * kRegsEpi == kGemmThreadsEpi8 * 168, "setmaxnreg split");
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_103
 
 // BM: rows of A per tile, 128 or 256 (two 128-row MMAs sharing B), or 64:
@@ -284,8 +292,9 @@ struct PackCursor {
 
 // Waits until the phase with `parity` of `bar` has completed, ignoring the
 // abort flag (used to drain in-flight work before exit), bounded in time.
-static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
-                                               unsigned long long* err, uint32_t site) {
+// INL: inlined (kernels using setmaxnreg), else out of line.
+__device__ __forceinline__ void wait_drain_body(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                                unsigned long long* err, uint32_t site) {
   if (mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -296,29 +305,40 @@ static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, ui
     }
   }
 }
+static __device__ __noinline__ void wait_drain_outlined(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                                        unsigned long long* err, uint32_t site) {
+  wait_drain_body(bar, parity, timeout_ns, err, site);
+}
+template <bool INL = false>
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                           unsigned long long* err, uint32_t site) {
+  if constexpr (INL) wait_drain_body(bar, parity, timeout_ns, err, site);
+  else wait_drain_outlined(bar, parity, timeout_ns, err, site);
+}
 
 // Suspend-time hint of the single-CTA kernel's waits (see mbar_try_wait_hint).
 constexpr uint32_t kSuspendHintNs = 32;
 
 // Single-thread wait: one try first (the usual case), the bounded loop only
 // when the phase is not complete yet.
-template <uint32_t HINT_NS = 0>
+template <uint32_t HINT_NS = 0, bool INL = false>
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          uint64_t timeout_ns, unsigned long long* err,
                                          uint32_t site) {
-  return mbar_try_wait_hint<HINT_NS>(bar, parity) ||
-         wait_bounded<HINT_NS>(bar, parity, abort_flag, timeout_ns, err, site);
+  if (mbar_try_wait_hint<HINT_NS>(bar, parity)) return true;
+  if constexpr (INL) return wait_bounded_body<HINT_NS>(bar, parity, abort_flag, timeout_ns, err, site);
+  else return wait_bounded<HINT_NS>(bar, parity, abort_flag, timeout_ns, err, site);
 }
 
 // Whole-warp wait: lane 0 waits, the result is broadcast, and the warp
 // reconverges (so the other lanes observe what lane 0 acquired).
-template <uint32_t HINT_NS = 0>
+template <uint32_t HINT_NS = 0, bool INL = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t timeout_ns, unsigned long long* err,
                                           uint32_t site) {
   const int lane = threadIdx.x & 31;
   int ok = 0;
-  if (lane == 0) ok = wait_one<HINT_NS>(bar, parity, abort_flag, timeout_ns, err, site) ? 1 : 0;
+  if (lane == 0) ok = wait_one<HINT_NS, INL>(bar, parity, abort_flag, timeout_ns, err, site) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
@@ -559,8 +579,8 @@ __device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
   }
 }
 
-template <int BN, int STAGES, int MODE, int KSPLIT, int BM = kBlockM>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int BN, int STAGES, int MODE, int KSPLIT, int BM = kBlockM, bool EPI8 = false>
+__global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa,
@@ -571,6 +591,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int NUM_ACC = P::kNumAcc;
   constexpr int MH = L::kMH;  // 128-row halves of a tile
   static_assert(KSPLIT == 1 || MODE == kDense, "split-K is for the dense form");
+  static_assert(!EPI8 || (BM == 2 * kBlockM && MODE == kDense && NUM_ACC == 1),
+                "eight epilogue warps: 256-row dense tiles with one accumulator");
   static_assert(BM == kBlockM || (BM == 2 * kBlockM && (MODE == kDense || MODE == kContiguous) && KSPLIT == 1) ||
                     (BM == kBlockM / 2 && MODE == kDense),
                 "256-row tiles are for the dense NT and contiguous forms without split-K; "
@@ -620,7 +642,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < NUM_ACC; ++a) {
       mbar_init(tfull(a), 1);
-      mbar_init(tempty(a), 4);
+      mbar_init(tempty(a), EPI8 ? 8 : 4);
     }
     mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) {
@@ -754,243 +776,335 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                     : args.m_blocks * args.n_blocks;
   const uint64_t tmo = args.timeout_ns;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // A single M block of fewer than 128 rows is loaded as a box of
-    // round_up(M, 8) rows: the rest of the A tile keeps stale bytes, which
-    // only reach accumulator rows that are never stored.
-    const uint32_t tx_ab = args.a_box_rows > 0 ? (uint32_t)(args.a_box_rows * kBlockK + L::kBytesB) : L::kTxAB;
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0, issued_parity = 0;  // stages: last fill's phase parity
-      bool ok = true;
-      for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
-        Tile tile;
-        if (!sched.get(t, tile)) continue;
-        int kb0, kb1;
-        sched.k_range(tile, kb0, kb1);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_one<kSuspendHintNs>(empty(stage), phase ^ 1u, abort_flag, tmo, err, kSiteProducerEmpty)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sb = smem_u32(smem + stage * L::kStageBytes);
-          const uint32_t fb = full(stage);
-          mbar_arrive_expect_tx(fb, tx_ab);
-          const int kx = kb * kBlockK, my = tile.mb * BM;
-          if (args.debug_drop_load && blockIdx.x == 0 && t == first_tile &&
-              kb + 1 == args.debug_drop_load) {
-            // injected failure: the stage is armed but never filled
+  // Roles: warp 0 producer, warp 1 MMA issuer, warp 2 scale warp, the rest
+  // epilogue.  With eight epilogue warps, warpgroup 0 (the three role warps
+  // and an idle warp) hands registers to the two epilogue warpgroups at the
+  // start of each warpgroup's branch.
+  if (EPI8 ? warp < 4 : warp < 3) {
+    if constexpr (EPI8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRoles) : "memory");
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      // A single M block of fewer than 128 rows is loaded as a box of
+      // round_up(M, 8) rows: the rest of the A tile keeps stale bytes, which
+      // only reach accumulator rows that are never stored.
+      const uint32_t tx_ab = args.a_box_rows > 0 ? (uint32_t)(args.a_box_rows * kBlockK + L::kBytesB) : L::kTxAB;
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0, issued_parity = 0;  // stages: last fill's phase parity
+        bool ok = true;
+        for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
+          Tile tile;
+          if (!sched.get(t, tile)) continue;
+          int kb0, kb1;
+          sched.k_range(tile, kb0, kb1);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_one<kSuspendHintNs, EPI8>(empty(stage), phase ^ 1u, abort_flag, tmo, err, kSiteProducerEmpty)) {
+              ok = false;
+              break;
+            }
+            const uint32_t sb = smem_u32(smem + stage * L::kStageBytes);
+            const uint32_t fb = full(stage);
+            mbar_arrive_expect_tx(fb, tx_ab);
+            const int kx = kb * kBlockK, my = tile.mb * BM;
+            if (args.debug_drop_load && blockIdx.x == 0 && t == first_tile &&
+                kb + 1 == args.debug_drop_load) {
+              // injected failure: the stage is armed but never filled
+              issued |= 1u << stage;
+              issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
+              continue;
+            }
+            // MN-major tiles ([K, M] / [K, N] storage): 128 K rows of 128 bytes
+            // per box; a 256-column B tile is two boxes 16 KB apart
+            if constexpr (a_mn_major(MODE)) tma_load_2d(sb, &tm_a, fb, my, kx);
+            else if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
+            else if (MODE == kContiguous && BM == 2 * kBlockM) {
+              // the pair's two blocks (a half-empty pair loads its block twice)
+              tma_load_2d(sb, &tm_a, fb, kx, tile.b0 * kBlockM);
+              tma_load_2d(sb + kBlockM * kBlockK, &tm_a, fb, kx, (tile.b1 >= 0 ? tile.b1 : tile.b0) * kBlockM);
+            } else tma_load_2d(sb, &tm_a, fb, kx, my);
+            if constexpr (b_mn_major(MODE)) {
+  #pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
+                tma_load_2d(sb + L::kOffB + h * 16384, &tm_b, fb, tile.nb * BN + h * 128, kx);
+            } else {
+              tma_load_3d(sb + L::kOffB, &tm_b, fb, kx, tile.nb * BN, tile.g);
+            }
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
-            continue;
-          }
-          // MN-major tiles ([K, M] / [K, N] storage): 128 K rows of 128 bytes
-          // per box; a 256-column B tile is two boxes 16 KB apart
-          if constexpr (a_mn_major(MODE)) tma_load_2d(sb, &tm_a, fb, my, kx);
-          else if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
-          else if (MODE == kContiguous && BM == 2 * kBlockM) {
-            // the pair's two blocks (a half-empty pair loads its block twice)
-            tma_load_2d(sb, &tm_a, fb, kx, tile.b0 * kBlockM);
-            tma_load_2d(sb + kBlockM * kBlockK, &tm_a, fb, kx, (tile.b1 >= 0 ? tile.b1 : tile.b0) * kBlockM);
-          } else tma_load_2d(sb, &tm_a, fb, kx, my);
-          if constexpr (b_mn_major(MODE)) {
-#pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-              tma_load_2d(sb + L::kOffB + h * 16384, &tm_b, fb, tile.nb * BN + h * 128, kx);
-          } else {
-            tma_load_3d(sb + L::kOffB, &tm_b, fb, kx, tile.nb * BN, tile.g);
-          }
-          issued |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
           }
         }
+        // Drain: every copy this thread issued has landed before smem is released.
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s))
+            wait_drain<EPI8>(full(s), (issued_parity >> s) & 1u, tmo, err, kSiteProducerDrain);
       }
-      // Drain: every copy this thread issued has landed before smem is released.
-      for (int s = 0; s < STAGES; ++s)
-        if (issued & (1u << s))
-          wait_drain(full(s), (issued_parity >> s) & 1u, tmo, err, kSiteProducerDrain);
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc0 = idesc_mxf8_e4m3(kBlockM, BN, 0, 0);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t pack = 0;
-      uint32_t sf_tmem = tmem_base + (uint32_t)P::kSfBase;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
-        Tile tile;
-        if (!sched.get(t, tile)) continue;
-        if (!wait_one<kSuspendHintNs>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, err, kSiteMmaTmemEmpty)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MH * BN);
-        int kb0, kb1;
-        sched.k_range(tile, kb0, kb1);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_one<kSuspendHintNs>(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull)) {
+      __syncwarp();
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc0 = idesc_mxf8_e4m3(kBlockM, BN, 0, 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t pack = 0;
+        uint32_t sf_tmem = tmem_base + (uint32_t)P::kSfBase;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
+          Tile tile;
+          if (!sched.get(t, tile)) continue;
+          if (!wait_one<kSuspendHintNs, EPI8>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, err, kSiteMmaTmemEmpty)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + stage * L::kStageBytes;
-          const int slot = (int)(pack % kSfSlots);
-          if (kb == kb0 || (kb & 3) == 0) {
-            if (!wait_one<kSuspendHintNs>(sfready(slot), (pack / kSfSlots) & 1u, abort_flag, tmo, err,
-                          kSiteMmaScaleReady)) {
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MH * BN);
+          int kb0, kb1;
+          sched.k_range(tile, kb0, kb1);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_one<kSuspendHintNs, EPI8>(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull)) {
               ok = false;
               break;
             }
-            // the scale warp has copied this pack into the slot's TMEM columns
-            tc_fence_after();
-            sf_tmem = tmem_base + (uint32_t)(P::kSfBase + slot * L::kSfCols);
+            uint8_t* st = smem + stage * L::kStageBytes;
+            const int slot = (int)(pack % kSfSlots);
+            if (kb == kb0 || (kb & 3) == 0) {
+              if (!wait_one<kSuspendHintNs, EPI8>(sfready(slot), (pack / kSfSlots) & 1u, abort_flag, tmo, err,
+                            kSiteMmaScaleReady)) {
+                ok = false;
+                break;
+              }
+              // the scale warp has copied this pack into the slot's TMEM columns
+              tc_fence_after();
+              sf_tmem = tmem_base + (uint32_t)(P::kSfBase + slot * L::kSfCols);
+            }
+            const uint32_t sel = (uint32_t)(kb & 3);
+            const uint32_t idesc = idesc0 | (sel << 4) | (sel << 29);
+            // K-major operands advance 32 bytes per 32-deep K step; MN-major
+            // ones 4 groups of 8 K rows (4096 bytes): descriptor units of 16 B
+            const uint64_t adesc = a_mn_major(MODE) ? smem_desc_mnmajor_sw128(smem_u32(st))
+                                                    : smem_desc_kmajor_sw128(smem_u32(st));
+            const uint64_t bdesc = b_mn_major(MODE) ? smem_desc_mnmajor_sw128(smem_u32(st + L::kOffB))
+                                                    : smem_desc_kmajor_sw128(smem_u32(st + L::kOffB));
+            constexpr uint32_t a_step = a_mn_major(MODE) ? 256u : 2u;
+            constexpr uint32_t b_step = b_mn_major(MODE) ? 256u : 2u;
+            constexpr uint32_t major_bits = (a_mn_major(MODE) ? kIdescMnMajorA : 0u) |
+                                            (b_mn_major(MODE) ? kIdescMnMajorB : 0u);
+            // a 256-row tile: the second half's A rows start 16 KB further
+            // (1024 descriptor units), its accumulator BN columns further
+  #pragma unroll
+            for (int j = 0; j < 4; ++j)
+  #pragma unroll
+              for (int h = 0; h < MH; ++h)
+                tc_mma_mxf8(d_tmem + h * BN, adesc + 1024u * h + a_step * j, bdesc + b_step * j,
+                            idesc | major_bits, sf_tmem + 4 * h, sf_tmem + 4 * MH,
+                            (kb != kb0 || j != 0) ? 1u : 0u);
+            tc_commit(empty(stage));
+            if ((kb & 3) == 3 || kb == kb1 - 1) {
+              tc_commit(sfempty(slot));  // the pack's buffer and TMEM slot are free
+              ++pack;
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          const uint32_t sel = (uint32_t)(kb & 3);
-          const uint32_t idesc = idesc0 | (sel << 4) | (sel << 29);
-          // K-major operands advance 32 bytes per 32-deep K step; MN-major
-          // ones 4 groups of 8 K rows (4096 bytes): descriptor units of 16 B
-          const uint64_t adesc = a_mn_major(MODE) ? smem_desc_mnmajor_sw128(smem_u32(st))
-                                                  : smem_desc_kmajor_sw128(smem_u32(st));
-          const uint64_t bdesc = b_mn_major(MODE) ? smem_desc_mnmajor_sw128(smem_u32(st + L::kOffB))
-                                                  : smem_desc_kmajor_sw128(smem_u32(st + L::kOffB));
-          constexpr uint32_t a_step = a_mn_major(MODE) ? 256u : 2u;
-          constexpr uint32_t b_step = b_mn_major(MODE) ? 256u : 2u;
-          constexpr uint32_t major_bits = (a_mn_major(MODE) ? kIdescMnMajorA : 0u) |
-                                          (b_mn_major(MODE) ? kIdescMnMajorB : 0u);
-          // a 256-row tile: the second half's A rows start 16 KB further
-          // (1024 descriptor units), its accumulator BN columns further
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int h = 0; h < MH; ++h)
-              tc_mma_mxf8(d_tmem + h * BN, adesc + 1024u * h + a_step * j, bdesc + b_step * j,
-                          idesc | major_bits, sf_tmem + 4 * h, sf_tmem + 4 * MH,
-                          (kb != kb0 || j != 0) ? 1u : 0u);
-          tc_commit(empty(stage));
-          if ((kb & 3) == 3 || kb == kb1 - 1) {
-            tc_commit(sfempty(slot));  // the pack's buffer and TMEM slot are free
-            ++pack;
+          if (!ok) break;
+          tc_commit(tfull(acc));
+          if (++acc == NUM_ACC) {
+            acc = 0;
+            acc_phase ^= 1u;
           }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+        }
+        // Drain: all MMAs and TMEM copies issued here complete before TMEM is freed.
+        tc_commit(drain);
+        wait_drain<EPI8>(drain, 0, tmo, err, kSiteDrain);
+      }
+      __syncwarp();
+    } else if (warp == 2) {
+      // ------------------------------------------------------------ scale warp
+      // Two cursors walk the same sequence of packs (tile, K block / 4): one
+      // loads up to kSfLookahead packs ahead, the other lays them out in order.
+      PackCursor<Scheduler<MODE, BM>> ld, lay;
+      ld.init(sched, first_tile, tile_stride);
+      lay.init(sched, first_tile, tile_stride);
+      uint32_t n_loaded = 0, n_laid = 0;
+      bool ok = true;
+      while (!lay.done && ok) {
+        while (!ld.done && n_loaded < n_laid + kSfLookahead) {
+          const int slot = (int)(n_loaded % kSfSlots);
+          int go = 1;
+          if (lane == 0) {
+            go = wait_one<kSuspendHintNs, EPI8>(sfempty(slot), ((n_loaded / kSfSlots) & 1u) ^ 1u, abort_flag, tmo, err,
+                          kSiteScaleEmpty) ? 1 : 0;
+            if (go) {
+              const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
+              const uint32_t bar = sffull(slot);
+              const int my = ld.tile.mb * BM, kp = ld.kp;
+              mbar_arrive_expect_tx(bar, L::kTxSF);
+              if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
+              else if (MODE == kContiguous && BM == 2 * kBlockM) {
+                tma_load_2d(buf + L::kRawA, &tm_sfa, bar, ld.tile.b0 * kBlockM, kp);
+                tma_load_2d(buf + L::kRawA + 512, &tm_sfa, bar,
+                            (ld.tile.b1 >= 0 ? ld.tile.b1 : ld.tile.b0) * kBlockM, kp);
+              } else tma_load_2d(buf + L::kRawA, &tm_sfa, bar, my, kp);
+              tma_load_3d(buf + L::kRawB, &tm_sfb, bar, ld.tile.nb * BN, kp,
+                          MODE == kKGrouped ? 0 : ld.tile.g);
+            }
           }
+          go = __shfl_sync(0xffffffffu, go, 0);
+          if (!go) {
+            ok = false;
+            break;
+          }
+          ++n_loaded;
+          ld.advance();
         }
         if (!ok) break;
-        tc_commit(tfull(acc));
-        if (++acc == NUM_ACC) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-      }
-      // Drain: all MMAs and TMEM copies issued here complete before TMEM is freed.
-      tc_commit(drain);
-      wait_drain(drain, 0, tmo, err, kSiteDrain);
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ scale warp
-    // Two cursors walk the same sequence of packs (tile, K block / 4): one
-    // loads up to kSfLookahead packs ahead, the other lays them out in order.
-    PackCursor<Scheduler<MODE, BM>> ld, lay;
-    ld.init(sched, first_tile, tile_stride);
-    lay.init(sched, first_tile, tile_stride);
-    uint32_t n_loaded = 0, n_laid = 0;
-    bool ok = true;
-    while (!lay.done && ok) {
-      while (!ld.done && n_loaded < n_laid + kSfLookahead) {
-        const int slot = (int)(n_loaded % kSfSlots);
-        int go = 1;
-        if (lane == 0) {
-          go = wait_one<kSuspendHintNs>(sfempty(slot), ((n_loaded / kSfSlots) & 1u) ^ 1u, abort_flag, tmo, err,
-                        kSiteScaleEmpty) ? 1 : 0;
-          if (go) {
-            const uint32_t buf = smem_u32(sfbuf + slot * L::kSfBufBytes);
-            const uint32_t bar = sffull(slot);
-            const int my = ld.tile.mb * BM, kp = ld.kp;
-            mbar_arrive_expect_tx(bar, L::kTxSF);
-            if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
-            else if (MODE == kContiguous && BM == 2 * kBlockM) {
-              tma_load_2d(buf + L::kRawA, &tm_sfa, bar, ld.tile.b0 * kBlockM, kp);
-              tma_load_2d(buf + L::kRawA + 512, &tm_sfa, bar,
-                          (ld.tile.b1 >= 0 ? ld.tile.b1 : ld.tile.b0) * kBlockM, kp);
-            } else tma_load_2d(buf + L::kRawA, &tm_sfa, bar, my, kp);
-            tma_load_3d(buf + L::kRawB, &tm_sfb, bar, ld.tile.nb * BN, kp,
-                        MODE == kKGrouped ? 0 : ld.tile.g);
-          }
-        }
-        go = __shfl_sync(0xffffffffu, go, 0);
-        if (!go) {
+        const int slot = (int)(n_laid % kSfSlots);
+        if (!warp_wait<kSuspendHintNs, EPI8>(sffull(slot), (n_laid / kSfSlots) & 1u, abort_flag, tmo, err, kSiteScaleFull)) {
           ok = false;
           break;
         }
-        ++n_loaded;
-        ld.advance();
+        uint8_t* buf = sfbuf + slot * L::kSfBufBytes;
+  #pragma unroll
+        for (int h = 0; h < MH; ++h) {
+          const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawA + h * 512);
+          const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
+          *reinterpret_cast<uint4*>(buf + L::kCpA + h * 512 + lane * 16) = v;
+        }
+  #pragma unroll
+        for (int c = 0; c < L::kSfbChunks; ++c) {
+          const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawB + c * 512);
+          const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
+          *reinterpret_cast<uint4*>(buf + L::kCpB + c * 512 + lane * 16) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        // Copy the pack into the slot's TMEM columns from this warp (keeping the
+        // copies out of the MMA issuer's instruction stream; measured 2-5%
+        // faster) and signal the slot when they have completed.  The slot's
+        // previous pack is no longer read: its MMAs completed (sfempty) before
+        // this pack was loaded.
+        if (lane == 0) {
+          const uint32_t sft = tmem_base + (uint32_t)(P::kSfBase + slot * L::kSfCols);
+  #pragma unroll
+          for (int h = 0; h < MH; ++h)
+            tc_cp_32x128b_warpx4(sft + 4 * h, smem_desc_sf_chunk(smem_u32(buf + L::kCpA + h * 512)));
+  #pragma unroll
+          for (int c = 0; c < L::kSfbChunks; ++c)
+            tc_cp_32x128b_warpx4(sft + 4 * MH + 4 * c,
+                                 smem_desc_sf_chunk(smem_u32(buf + L::kCpB + c * 512)));
+          tc_commit(sfready(slot));
+        }
+        ++n_laid;
+        lay.advance();
       }
-      if (!ok) break;
-      const int slot = (int)(n_laid % kSfSlots);
-      if (!warp_wait<kSuspendHintNs>(sffull(slot), (n_laid / kSfSlots) & 1u, abort_flag, tmo, err, kSiteScaleFull)) {
-        ok = false;
-        break;
-      }
-      uint8_t* buf = sfbuf + slot * L::kSfBufBytes;
-#pragma unroll
-      for (int h = 0; h < MH; ++h) {
-        const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawA + h * 512);
-        const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
-        *reinterpret_cast<uint4*>(buf + L::kCpA + h * 512 + lane * 16) = v;
-      }
-#pragma unroll
-      for (int c = 0; c < L::kSfbChunks; ++c) {
-        const uint32_t* raw = reinterpret_cast<const uint32_t*>(buf + L::kRawB + c * 512);
-        const uint4 v = make_uint4(raw[lane], raw[32 + lane], raw[64 + lane], raw[96 + lane]);
-        *reinterpret_cast<uint4*>(buf + L::kCpB + c * 512 + lane * 16) = v;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      // Copy the pack into the slot's TMEM columns from this warp (keeping the
-      // copies out of the MMA issuer's instruction stream; measured 2-5%
-      // faster) and signal the slot when they have completed.  The slot's
-      // previous pack is no longer read: its MMAs completed (sfempty) before
-      // this pack was loaded.
+      // Drain: scale loads issued but not laid out (abort path) land before exit,
+      // and this warp's TMEM copies complete before TMEM can be freed.
       if (lane == 0) {
-        const uint32_t sft = tmem_base + (uint32_t)(P::kSfBase + slot * L::kSfCols);
-#pragma unroll
-        for (int h = 0; h < MH; ++h)
-          tc_cp_32x128b_warpx4(sft + 4 * h, smem_desc_sf_chunk(smem_u32(buf + L::kCpA + h * 512)));
-#pragma unroll
-        for (int c = 0; c < L::kSfbChunks; ++c)
-          tc_cp_32x128b_warpx4(sft + 4 * MH + 4 * c,
-                               smem_desc_sf_chunk(smem_u32(buf + L::kCpB + c * 512)));
-        tc_commit(sfready(slot));
+        for (uint32_t q = n_laid; q < n_loaded; ++q)
+          wait_drain<EPI8>(sffull((int)(q % kSfSlots)), (q / kSfSlots) & 1u, tmo, err, kSiteProducerDrain);
+        if (n_laid > 0)
+          wait_drain<EPI8>(sfready((int)((n_laid - 1) % kSfSlots)), ((n_laid - 1) / kSfSlots) & 1u, tmo, err,
+                     kSiteDrain);
       }
-      ++n_laid;
-      lay.advance();
+      __syncwarp();
     }
-    // Drain: scale loads issued but not laid out (abort path) land before exit,
-    // and this warp's TMEM copies complete before TMEM can be freed.
-    if (lane == 0) {
-      for (uint32_t q = n_laid; q < n_loaded; ++q)
-        wait_drain(sffull((int)(q % kSfSlots)), (q / kSfSlots) & 1u, tmo, err, kSiteProducerDrain);
-      if (n_laid > 0)
-        wait_drain(sfready((int)((n_laid - 1) % kSfSlots)), ((n_laid - 1) / kSfSlots) & 1u, tmo, err,
-                   kSiteDrain);
+  } else if constexpr (EPI8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi) : "memory");
+    // ------------------------------------------------------------ epilogue, eight warps
+    // Warp w >= 4 drains lane quarter (w & 3) of 128-row half (w - 4) / 4:
+    // the lane's whole row of BN columns is read from TMEM, C (fetched
+    // before the accumulator is ready) added and the sum rounded to BF16 in
+    // registers; TMEM goes back to the MMA as soon as all eight warps have
+    // read their rows, and only then are the chunks staged and TMA-stored.
+    {
+      if (warp >= 4) {
+        const int quarter = warp & 3;
+        const int hh = (warp - 4) >> 2;
+        uint8_t* ebuf = epi_smem + (warp - 4) * kEpiBuf;  // one staging chunk per warp
+        constexpr int NCH = BN / 32;
+        uint32_t pk[NCH][16];
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = first_tile; t < sched.total; t += tile_stride) {
+          Tile tile;
+          if (!sched.get(t, tile)) continue;
+          const int row0 = tile.mb * BM + hh * kBlockM + quarter * 32;
+          const int row = row0 + lane;
+          if (args.c != nullptr) {
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              const int col0 = tile.nb * BN + ch * 32;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (row < args.m && col0 + 8 * q < args.n)
+                  v = __ldg(reinterpret_cast<const uint4*>(args.c + (int64_t)row * args.ldc + col0 + 8 * q));
+                pk[ch][4 * q] = v.x;
+                pk[ch][4 * q + 1] = v.y;
+                pk[ch][4 * q + 2] = v.z;
+                pk[ch][4 * q + 3] = v.w;
+              }
+            }
+          }
+          if (!warp_wait<kSuspendHintNs, EPI8>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
+          tc_fence_after();
+          const bool live = row0 < args.m;
+          if (live) {
+            const uint32_t taddr =
+                tmem_base + (uint32_t)((acc * MH + hh) * BN) + ((uint32_t)(quarter * 32) << 16);
+            uint32_t va[32], vb[32];
+            tc_ld_32x32b_x32(taddr, va);
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              uint32_t(&cur)[32] = (ch & 1) ? vb : va;
+              uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
+              tc_wait_ld_regs(cur);
+              if (ch + 1 < NCH) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float lo = __uint_as_float(cur[2 * i]), hi = __uint_as_float(cur[2 * i + 1]);
+                if (args.c) {
+                  lo += __uint_as_float(pk[ch][i] << 16);
+                  hi += __uint_as_float(pk[ch][i] & 0xFFFF0000u);
+                }
+                pk[ch][i] = pack_bf16x2(lo, hi);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty(acc));
+          if (live) {
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+              const int col0 = tile.nb * BN + ch * 32;
+              if (col0 >= args.n) continue;
+              if (lane == 0) bulk_wait_group_read<0>();  // the staging chunk's previous store has read it
+              __syncwarp();
+              emit_packed_tma(pk[ch], ebuf, &tm_d, col0, row0, lane);
+            }
+          }
+          if (++acc == NUM_ACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+      }
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
@@ -1042,7 +1156,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (!warp_wait<kSuspendHintNs>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
+      if (!warp_wait<kSuspendHintNs, EPI8>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
       tc_fence_after();
       bool stop = false;
       bool both_halves = false;  // the first half's pass stored both (256 x 192 dense)
@@ -1479,17 +1593,17 @@ static cudaError_t set_smem_once(Kern kern, size_t smem) {
   return e;
 }
 
-template <int BN, int STAGES, int MODE, int KSPLIT = 1, int BM = kBlockM>
+template <int BN, int STAGES, int MODE, int KSPLIT = 1, int BM = kBlockM, bool EPI8 = false>
 static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
                                     const CUtensorMap& sfa, const CUtensorMap& sfb,
                                     const CUtensorMap& d, const GemmArgs& args, int grid,
                                     cudaStream_t stream) {
   using Plan = GemmPlan<BN, STAGES, KSPLIT, BM>;
   static_assert(Plan::smem_bytes(MODE) <= (size_t)kSmemLimit, "shared memory over the per-CTA limit");
-  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT, BM>;
+  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT, BM, EPI8>;
   const size_t smem = Plan::smem_bytes(MODE);
-  cudaError_t e =
-      set_smem_once<KernelTag<BN, STAGES, MODE, KSPLIT, BM == kBlockM ? 1 : (BM > kBlockM ? 3 : 4)>>(kern, smem);
+  cudaError_t e = set_smem_once<
+      KernelTag<BN, STAGES, MODE, KSPLIT, EPI8 ? 5 : (BM == kBlockM ? 1 : (BM > kBlockM ? 3 : 4))>>(kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   unsigned n_attr = 0;
@@ -1507,7 +1621,7 @@ static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.blockDim = dim3(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;

@@ -336,6 +336,58 @@ int choose_block_n_masked_streaming(int64_t groups, int64_t expected_m, int64_t 
   return best;
 }
 
+// Dense NT tile choice (single CTA, no split-K): every candidate tile of
+// block_m x block_n is costed as waves x (K blocks + epilogue) x time per K
+// block, the epilogue counted as the K blocks of MMA time it does not hide.
+// The two numbers per tile (and per with / without C) are least-squares fits
+// of the GB300 prefill sweeps (M = 4096, the five (N, K) pairs of the
+// prefill workload, every tile forced in turn; us per K block at the clock of
+// those runs): they rank the tiles as the measurements do on every shape of
+// that sweep but one near-tie.  256-row tiles drain their single accumulator
+// with eight epilogue warps, which is what makes them win at short K.
+struct DenseTileCost {
+  int block_m, block_n;
+  double us_per_kb, epi_kb, us_per_kb_c, epi_kb_c;
+};
+constexpr DenseTileCost kDenseTiles[] = {
+    {128, 128, 0.3278, 3.90, 0.3265, 5.95},  {128, 192, 0.3609, 4.73, 0.3596, 6.00},
+    {128, 224, 0.3836, 3.72, 0.3784, 6.91},  {128, 256, 0.4081, 5.88, 0.4065, 11.19},
+    {256, 192, 0.5463, 3.79, 0.5430, 11.57}, {256, 224, 0.5795, 5.00, 0.5773, 13.28},
+};
+
+double dense_nt_cost(const DenseTileCost& t, int64_t m, int64_t n, int64_t k_blocks, int slots, bool with_c) {
+  const int64_t tiles = ((m + t.block_m - 1) / t.block_m) * ((n + t.block_n - 1) / t.block_n);
+  const int64_t waves = (tiles + slots - 1) / slots;
+  return (double)waves * ((double)k_blocks + (with_c ? t.epi_kb_c : t.epi_kb)) *
+         (with_c ? t.us_per_kb_c : t.us_per_kb);
+}
+
+// The cheapest dense NT tile; DG_BLOCK_M (128 or 256) and DG_BLOCK_N restrict
+// the candidates (DG_BLOCK_N alone means 128-row tiles of that width).  A
+// single M block takes 128-row tiles.
+void choose_dense_nt_tile(int64_t m, int64_t n, int64_t k_blocks, int slots, bool with_c, int* block_m,
+                          int* block_n) {
+  int forced_m = env_int("DG_BLOCK_M", 0);
+  int forced_n = env_int("DG_BLOCK_N", 0);
+  if (forced_m == 256 && gemm_tall_stages(forced_n) == 0) forced_n = 0;  // no such 256-row width
+  if (forced_n != 0 && forced_m != 256 && gemm_block_n_supported(forced_n)) forced_m = 128;
+  const int sms = slots > 0 ? slots : 1;
+  double best = 1e300;
+  *block_m = kBlockM;
+  *block_n = 128;
+  for (const DenseTileCost& t : kDenseTiles) {
+    if (t.block_m == 2 * kBlockM && (m <= kBlockM || gemm_tall_stages(t.block_n) == 0)) continue;
+    if ((forced_m == 128 || forced_m == 256) && t.block_m != forced_m) continue;
+    if (forced_n != 0 && t.block_n != forced_n && gemm_block_n_supported(forced_n)) continue;
+    const double c = dense_nt_cost(t, m, n, k_blocks, sms, with_c);
+    if (c < best * 0.999) {
+      best = c;
+      *block_m = t.block_m;
+      *block_n = t.block_n;
+    }
+  }
+}
+
 void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_m,
                   int block_n, int stages, int grid, int band) {
   if (!env_flag("DG_PRINT_CONFIGS")) return;
@@ -387,17 +439,14 @@ DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int
     p.block_n = choose_block_n(p_blocks, n, kb, sms / 2, with_c, true);
     return p;
   }
-  p.block_n = choose_block_n(m_blocks, n, kb, sms, with_c, false, mode != kDense);
-  // 256-row tiles (dense NT, more than one 128-row block) where the estimate
-  // says they are faster; DG_BLOCK_M=256 (with DG_BLOCK_N 192 or 224) or
-  // DG_BLOCK_M=128 forces the choice.
   if (mode == kDense && m_blocks >= 2) {
-    const double cost128 = dense_tile_cost(m_blocks, n, kb, sms, with_c, p.block_n);
-    const int tall_n = choose_tall_block_n(m, n, kb, sms, with_c, cost128);
-    if (tall_n != 0 && gemm_tall_stages(tall_n) > 0) {
-      p.tall = true;
-      p.block_n = tall_n;
-    }
+    // NT with several M blocks: 128- or 256-row tiles from the measured cost
+    // table (a single M block is memory-bound, costed below)
+    int bm = kBlockM;
+    choose_dense_nt_tile(m, n, kb, sms, with_c, &bm, &p.block_n);
+    p.tall = bm == 2 * kBlockM;
+  } else {
+    p.block_n = choose_block_n(m_blocks, n, kb, sms, with_c, false, mode != kDense);
   }
   // a single M block of at most 64 rows: 64-row A slots, more stages
   p.short_a = mode == kDense && !p.tall && m <= kBlockM / 2 && gemm_short_supported(p.block_n);
@@ -578,6 +627,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
                m, n, k, 1, tall ? 2 * kBlockM : plan.short_a ? kBlockM / 2 : kBlockM, block_n,
                tall ? gemm_tall_stages(block_n) : plan.short_a ? gemm_short_stages(block_n) : gemm_stages(block_n),
                grid, args.band);
+  args.epi8 = env_int("DG_TALL_EPI8", 1) != 0 ? 1 : 0;
   if (tall)
     return from_cuda(gemm_tall_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                       static_cast<cudaStream_t>(stream)));

@@ -44,14 +44,15 @@ def plan(m, n, k, has_c=False, sms=SMS):
     return p["block_m"], p["block_n"], p["split_k"], p["cta_pair"]
 
 
-# (N, K) -> (block_m, block_n) at M = 4096, with and without C: the tiles the
-# prefill sweeps on GB300 measured fastest (or within noise of it)
+# (N, K, with C) -> (block_m, block_n) at M = 4096: the tiles the prefill
+# sweeps on GB300 measured fastest (or within noise of it), every tile forced
+# in turn; 256-row tiles drain their accumulator with eight epilogue warps
 PREFILL_CHOICE = {
-    (2112, 7168): (128, 256),
-    (24576, 1536): (128, 224),
-    (7168, 16384): (256, 192),
-    (4096, 7168): (256, 224),
-    (7168, 2048): (128, 224),
+    (2112, 7168, False): (128, 256), (2112, 7168, True): (128, 256),
+    (24576, 1536, False): (256, 224), (24576, 1536, True): (128, 224),
+    (7168, 16384, False): (256, 192), (7168, 16384, True): (256, 192),
+    (4096, 7168, False): (256, 224), (4096, 7168, True): (256, 224),
+    (7168, 2048, False): (256, 192), (7168, 2048, True): (256, 192),
 }
 
 
@@ -59,7 +60,7 @@ PREFILL_CHOICE = {
 def test_prefill_shapes_take_the_measured_tiles(has_c):
     with env():
         for cfg in workloads.PREFILL:
-            want = PREFILL_CHOICE[(cfg["n"], cfg["k"])]
+            want = PREFILL_CHOICE[(cfg["n"], cfg["k"], has_c)]
             assert plan(cfg["m"], cfg["n"], cfg["k"], has_c) == want + (1, False), cfg
 
 
