@@ -242,7 +242,6 @@ def step_flops(shapes):
 # block_n, split_k, cta_pair).  A launch whose configuration is not listed has
 # no traffic figure (the counters would be stale).
 CAPTURED_TRAFFIC = {
-    (4096, 7168, 16384, False, 256, 192, 1, 0): 366.6e6 + 47.1e6,
 }
 
 

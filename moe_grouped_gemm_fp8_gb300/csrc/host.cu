@@ -388,6 +388,22 @@ void choose_dense_nt_tile(int64_t m, int64_t n, int64_t k_blocks, int slots, boo
   }
 }
 
+// Raster band of the dense tile walk, in M blocks of block_m rows: inside a
+// band the M block varies fastest, so a wave of CTAs shares a few column
+// blocks of B and the band's rows of A.  B is read from DRAM once per band,
+// so the band covers as many M blocks as keep that strip of A within 32 MiB,
+// a quarter of L2: the strip is read by SMs of both dies and held in both
+// halves of L2, and a 64 MiB strip (the whole of M at K = 16384) was evicted
+// between waves (DRAM reads 393 MB against 366 MB for a 32 MiB strip on
+// M = 4096, N = 7168, K = 16384).  DG_RASTER_BAND (in 128-row blocks)
+// overrides.
+int raster_band(int64_t m_blocks, int block_m, int64_t k) {
+  const int forced = env_int("DG_RASTER_BAND", 0);
+  if (forced > 0) return std::max(1, forced * kBlockM / block_m);
+  const int64_t fit = ((int64_t)32 << 20) / ((int64_t)block_m * std::max<int64_t>(k, 1));
+  return (int)std::max<int64_t>(1, std::min<int64_t>(m_blocks, fit));
+}
+
 void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_m,
                   int block_n, int stages, int grid, int band) {
   if (!env_flag("DG_PRINT_CONFIGS")) return;
@@ -609,8 +625,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   args.num_groups = 1;
   args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
   args.k_blocks = (int32_t)(k / kBlockK);
-  args.band = env_int("DG_RASTER_BAND", 16) / ((pair || tall) ? 2 : 1);
-  if (args.band < 1) args.band = 1;
+  args.band = raster_band(args.m_blocks, (pair || tall) ? 2 * kBlockM : kBlockM, k);
   args.timeout_ns = g_timeout_ns.load();
   args.pdl = g_pdl.load();
   const int64_t tiles = (pair ? p_blocks : (int64_t)args.m_blocks) * args.n_blocks;

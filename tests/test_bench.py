@@ -45,8 +45,9 @@ class _FakePlanner:
         return dict(self.plan)
 
 
-def test_traffic_only_for_the_captured_tile_configuration():
-    key = next(iter(bench.CAPTURED_TRAFFIC))
+def test_traffic_only_for_the_captured_tile_configuration(monkeypatch):
+    key = (4096, 7168, 16384, False, 256, 192, 1, 0)
+    monkeypatch.setitem(bench.CAPTURED_TRAFFIC, key, 4.0e8)
     m, n, k, c, bm, bn, sk, pair = key
     same = _FakePlanner(dict(block_m=bm, block_n=bn, split_k=sk, cta_pair=bool(pair)))
     t, plan = bench.captured_traffic(same, m, n, k, c, 152)
