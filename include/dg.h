@@ -91,6 +91,41 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
                          const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
                          int64_t ldb, int64_t ldc, int64_t ldd, void* stream);
 
+/* Dense NT with a caller-provided workspace (scratch device memory), which
+ * lets the call split the K blocks of the output tiles of its last waves
+ * between SMs ("stream-K") when the tile count leaves the last wave mostly
+ * empty, e.g. M = 4096, N = 2112, K = 7168 on 152 SMs.  Same operation,
+ * arguments, layouts and checks as dg_fp8_gemm_nt, plus:
+ *   workspace        device pointer, 16-byte aligned, or NULL (then the call
+ *                    is exactly dg_fp8_gemm_nt)
+ *   workspace_bytes  its size; when it is below
+ *                    dg_fp8_gemm_nt_workspace_size for this problem the call
+ *                    runs without stream-K (no error)
+ * The workspace starts with 32 KiB of flags (one 32-bit word per SM and
+ * epilogue warp, for up to 1024 SMs), which must be zero before the first
+ * use; one FP32 partial-sum slot of 256 x block_n values per SM follows and
+ * needs no initialisation.  Every launch leaves the flags zero
+ * again, so the same buffer serves any number of later calls, also inside a
+ * CUDA graph.
+ * Calls that can overlap on the device (other streams, concurrent graphs)
+ * need separate workspaces.  After a DG_ERR_DEVICE_TIMEOUT the flags may be
+ * left set: zero the buffer again before reusing it.  Results are
+ * deterministic (the partial sums of a tile are added in K order) but may
+ * differ from dg_fp8_gemm_nt's in the last bit (another FP32 summation order).
+ * Cited: the same pages as dg_fp8_gemm_nt for the operation; splitting K
+ * between SMs to balance the last wave is this library's addition. */
+dg_status dg_fp8_gemm_nt_ws(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                            const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                            int64_t ldb, int64_t ldc, int64_t ldd, void* workspace,
+                            uint64_t workspace_bytes, void* stream);
+
+/* Bytes of workspace dg_fp8_gemm_nt_ws needs to use stream-K for an
+ * M x N x K problem (with C when has_c != 0) on num_sms SMs (the device's
+ * count, or the dg_set_num_sms limit); 0 when it would not use stream-K.
+ * Pure host arithmetic.  Errors as dg_plan_fp8_gemm_nt. */
+dg_status dg_fp8_gemm_nt_workspace_size(int64_t m, int64_t n, int64_t k, int32_t has_c,
+                                        int32_t num_sms, uint64_t* bytes);
+
 /* Dense NT with arbitrary FP32 scales (no power-of-two requirement):
  *   D[m, n] = C[m, n] + sum_kb (sum_{k in kb} A[m, k] B[n, k]) * sfa[kb][m] * sfb[n/128][kb]
  *   sfa  float [ceil(k/128), align(m, 4)]: one scale per 1x128 group of A,
@@ -283,6 +318,13 @@ int32_t dg_get_mk_alignment_for_contiguous_layout(void);
 dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,
                               int32_t* block_m, int32_t* block_n, int32_t* split_k,
                               int32_t* cta_pair);
+
+/* The tile configuration dg_fp8_gemm_nt_ws chooses when its workspace is
+ * large enough: the outputs of dg_plan_fp8_gemm_nt plus stream_k (1 when the
+ * K blocks of the last waves are split between SMs).  Same checks. */
+dg_status dg_plan_fp8_gemm_nt_ws(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,
+                                 int32_t* block_m, int32_t* block_n, int32_t* split_k,
+                                 int32_t* cta_pair, int32_t* stream_k);
 
 /* The same query for the two M-grouped forms: the tile configuration
  * dg_m_grouped_fp8_gemm_nt_contiguous / _masked chooses (block_m 256 when a

@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     fp8_gemm_nn,
     fp8_gemm_nt,
     fp8_gemm_nt_fp32_sf,
+    fp8_gemm_nt_workspace_size,
     fp8_gemm_tn,
     fp8_gemm_tt,
     get_device_error,
@@ -23,6 +24,7 @@ from .api import (  # noqa: F401
     m_grouped_fp8_gemm_nt_contiguous,
     m_grouped_fp8_gemm_nt_masked,
     plan_fp8_gemm_nt,
+    plan_fp8_gemm_nt_ws,
     plan_m_grouped_fp8_gemm_nt_contiguous,
     plan_m_grouped_fp8_gemm_nt_masked,
     quantize_fp8,

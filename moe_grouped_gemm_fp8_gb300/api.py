@@ -87,6 +87,17 @@ def plan_fp8_gemm_nt(m: int, n: int, k: int, has_c: bool = False, num_sms: int =
     return {"block_m": bm, "block_n": bn, "split_k": sk, "cta_pair": bool(pair)}
 
 
+def plan_fp8_gemm_nt_ws(m: int, n: int, k: int, has_c: bool = False, num_sms: int = 152) -> dict:
+    """The tile configuration fp8_gemm_nt chooses with a large enough
+    workspace: plan_fp8_gemm_nt's keys plus "stream_k" (bool)."""
+    out = [C.c_int32(0) for _ in range(5)]
+    st = _lib.lib().dg_plan_fp8_gemm_nt_ws(int(m), int(n), int(k), 1 if has_c else 0, int(num_sms),
+                                           *[C.byref(o) for o in out])
+    _check(st, "dg_plan_fp8_gemm_nt_ws")
+    bm, bn, sk, pair, strk = (int(o.value) for o in out)
+    return {"block_m": bm, "block_n": bn, "split_k": sk, "cta_pair": bool(pair), "stream_k": bool(strk)}
+
+
 def plan_m_grouped_fp8_gemm_nt_contiguous(m_sum: int, n: int, k: int, num_groups: int,
                                           num_sms: int = 152) -> dict:
     """The tile configuration m_grouped_fp8_gemm_nt_contiguous chooses, on the
@@ -138,9 +149,15 @@ def debug_set_drop_load(k: int) -> None:
 
 
 def get_device_error(stream=None) -> Tuple[int, int]:
-    """Synchronises the stream; returns (status, raw word) and clears the word."""
+    """Synchronises the stream; returns (status, raw word) and clears the word.
+    After a timeout the binding's own workspaces are zero-filled again (an
+    aborted stream-K launch may leave flags set)."""
     detail = C.c_uint64(0)
     st = _lib.lib().dg_get_device_error(_stream(stream), C.byref(detail))
+    if int(st) == 5:  # DG_ERR_DEVICE_TIMEOUT
+        for ws in _WORKSPACES.values():
+            ws[:min(ws.numel(), WORKSPACE_FLAG_BYTES)].zero_()
+        torch.cuda.synchronize()
     return int(st), int(detail.value)
 
 
@@ -235,10 +252,60 @@ def transform_sf_into_required_layout(sf: torch.Tensor, mn: int, k: int, block_r
     return out
 
 
+# Workspaces of dg_fp8_gemm_nt_ws kept by the binding, one per (device,
+# stream): flag words zeroed when allocated, left zero by every launch.
+_WORKSPACES = {}
+
+
+def fp8_gemm_nt_workspace_size(m: int, n: int, k: int, has_c: bool = False,
+                               num_sms: Optional[int] = None) -> int:
+    """Bytes of workspace the stream-K form of fp8_gemm_nt needs for this
+    problem (0: it would not use stream-K)."""
+    out = C.c_uint64(0)
+    _check(_lib.lib().dg_fp8_gemm_nt_workspace_size(int(m), int(n), int(k), 1 if has_c else 0,
+                                                    int(num_sms if num_sms else get_num_sms()),
+                                                    C.byref(out)), "dg_fp8_gemm_nt_workspace_size")
+    return int(out.value)
+
+
+# Leading bytes of a stream-K workspace that hold its flag words (dg.h).
+WORKSPACE_FLAG_BYTES = 32 * 1024
+
+
+def _new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A workspace of nbytes with its flag words zeroed (the partial-sum
+    slots after them need no initialisation)."""
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    ws[:min(nbytes, WORKSPACE_FLAG_BYTES)].zero_()
+    return ws
+
+
+def _cached_workspace(nbytes: int, stream, device) -> torch.Tensor:
+    """The binding's workspace for this device and stream, grown to nbytes.
+    While a CUDA graph is being captured a fresh one is taken from the
+    graph's memory pool instead (its flag words are zeroed by a captured
+    memset, so every replay starts from zero flags)."""
+    if torch.cuda.is_current_stream_capturing():
+        return _new_workspace(nbytes, device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    key = (device.index, s.cuda_stream if isinstance(s, torch.cuda.Stream) else int(s))
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = _new_workspace(nbytes, device)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 def fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.Tensor,
                 d: Optional[torch.Tensor] = None, c: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
-    """D = C + A @ B.T with A [M,K], B [N,K] E4M3 and packed UE8M0 scales."""
+                stream=None, workspace=None) -> torch.Tensor:
+    """D = C + A @ B.T with A [M,K], B [N,K] E4M3 and packed UE8M0 scales.
+
+    workspace: None lets the call use a workspace kept by this binding (one
+    buffer per device and stream; inside a CUDA-graph capture one from the
+    graph's pool) for the stream-K form when that is faster; False runs
+    without one (dg_fp8_gemm_nt); a uint8 CUDA tensor is used as given (its
+    flag words zero before its first use, see dg_fp8_gemm_nt_ws)."""
     _need(a, "a", FP8_DTYPES, 2)
     _need(b, "b", FP8_DTYPES, 2)
     _need(sfa, "sfa", (torch.int32,), 2)
@@ -262,10 +329,26 @@ def fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.
         if tuple(c.shape) != (m, n) or c.stride(1) != 1:
             raise ValueError("c must be [M, N] with unit column stride")
     _on_current_device(stream, a, sfa, b, sfb, c, d)
-    st = _lib.lib().dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
-                                   m, n, k, a.stride(0), b.stride(0),
-                                   c.stride(0) if c is not None else 0, d.stride(0), _stream(stream))
-    _check(st, "dg_fp8_gemm_nt")
+    ws = None
+    if workspace is None:
+        need = fp8_gemm_nt_workspace_size(m, n, k, c is not None)
+        if need:
+            ws = _cached_workspace(need, stream, d.device)
+    elif workspace is not False:
+        _need(workspace, "workspace", (torch.uint8,), 1)
+        _on_current_device(stream, workspace)
+        ws = workspace
+    if ws is None:
+        st = _lib.lib().dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                       m, n, k, a.stride(0), b.stride(0),
+                                       c.stride(0) if c is not None else 0, d.stride(0), _stream(stream))
+        _check(st, "dg_fp8_gemm_nt")
+    else:
+        st = _lib.lib().dg_fp8_gemm_nt_ws(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+                                          m, n, k, a.stride(0), b.stride(0),
+                                          c.stride(0) if c is not None else 0, d.stride(0), _ptr(ws),
+                                          ws.numel(), _stream(stream))
+        _check(st, "dg_fp8_gemm_nt_ws")
     return d
 
 

@@ -114,6 +114,43 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
   return wait_bounded_body<HINT_NS>(bar, parity, abort_flag, timeout_ns, err, site);
 }
 
+// ---------------------------------------------------------------- flags in global memory
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until the word at `flag` (written by another CTA) is non-zero, with
+// acquire semantics.  Bounded like wait_bounded: gives up when the abort flag
+// is raised, or after `timeout_ns` (recording DG_ERR_DEVICE_TIMEOUT with
+// `site` and raising the abort flag).  Inlined (usable under setmaxnreg).
+__device__ __forceinline__ bool wait_flag_gpu(const uint32_t* flag, volatile int* abort_flag,
+                                              uint64_t timeout_ns, unsigned long long* err,
+                                              uint32_t site) {
+  if (ld_acquire_gpu(flag) != 0u) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) != 0u) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns || it >= (1u << 28)) {
+        record_error(err, DG_ERR_DEVICE_TIMEOUT, site);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 
 // Waits until the grids this launch depends on programmatically have completed

@@ -51,6 +51,7 @@ enum ErrorSite : uint32_t {
   kSiteScaleEmpty = 9,
   kSiteSplitFree = 10,
   kSiteSplitFull = 11,
+  kSiteStreamKPartial = 12,
   kSiteContiguousIndex = 16,
   kSiteMaskedCount = 17,
   kSiteKGroupSize = 18,
@@ -84,6 +85,16 @@ struct GemmArgs {
   int32_t debug_drop_load;
   // 256-row dense tiles: drain the accumulator with eight epilogue warps
   int32_t epi8;
+  // Stream-K (256-row dense tiles with eight epilogue warps; 0 units = off):
+  // tiles [0, sk_dp_tiles) are walked one per CTA per wave, the K blocks of
+  // the remaining tiles (sk_units = their count x k_blocks) are shared out
+  // evenly.  sk_part holds one partial-accumulator slot of 256 x block_n
+  // floats per CTA, sk_flags one word per (CTA, epilogue warp); both belong
+  // to the caller's workspace, whose flags are zero between launches.
+  float* sk_part;
+  uint32_t* sk_flags;
+  int64_t sk_units;
+  int32_t sk_dp_tiles;
   // FP32-scale (promotion) form only
   const float* sfa_f32;    // [ceil(k/128), sfa_ld]: per K block, one scale per row of A
   const float* sfb_f32;    // [ceil(n/128), k/128]: one scale per 128 x 128 block of B

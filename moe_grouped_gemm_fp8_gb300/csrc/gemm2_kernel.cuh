@@ -69,10 +69,22 @@ struct PairScheduler {
   int total;
   int cursor;
   int p_blocks;  // dense: ceil(m / 256)
+  int first, stride;  // this cluster's first tile and the stride of its tile walk
 
   __device__ void k_range(const Tile&, int& kb0, int& kb1) const {
     kb0 = 0;
     kb1 = args->k_blocks;
+  }
+
+  // The it-th tile of this cluster's walk with its K blocks (-1: no more).
+  __device__ int item(int it, Tile& tile, int& kb0, int& kb1) {
+    const int t = first + it * stride;
+    if (t >= total) return -1;
+    tile.kind = kItemFull;
+    tile.sk = -1;
+    if (!get(t, tile)) return 0;
+    k_range(tile, kb0, kb1);
+    return 1;
   }
 
   __device__ bool get(int t, Tile& tile) {
@@ -196,6 +208,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   sched.cursor = 0;
   sched.p_blocks = (args.m + 2 * kBlockM - 1) / (2 * kBlockM);
   sched.total = MODE == kMasked ? tile_start[args.num_groups] : sched.p_blocks * args.n_blocks;
+  sched.first = cluster_id;
+  sched.stride = num_clusters;
   const uint64_t tmo = args.timeout_ns;
 
   if (warp == 0) {
@@ -318,8 +332,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale warp (both CTAs)
     PackCursor<PairScheduler<MODE>> ld, lay;
-    ld.init(sched, cluster_id, num_clusters);
-    lay.init(sched, cluster_id, num_clusters);
+    ld.init(sched);
+    lay.init(sched);
     uint32_t n_loaded = 0, n_laid = 0;
     bool ok = true;
     while (!lay.done && ok) {

@@ -121,7 +121,7 @@ constexpr int kSfLookahead = 3;  // packs loaded ahead of the one being laid out
 constexpr int kMaxBlockPairs = kMaxTallPairs;
 
 static constexpr size_t gemm_ctrl_bytes(int stages, int mode, int bm = kBlockM) {
-  return (size_t)8 * (2 * stages + 3 * kSfSlots + 5 + 8) + 16 +
+  return (size_t)8 * (2 * stages + 3 * kSfSlots + 5 + 8) + 32 +
          ((mode == kMasked || mode == kKGrouped) ? (size_t)4 * (2 * kMaxMaskedGroups + 1) : 0) +
          ((mode == kContiguous && bm == 2 * kBlockM)
               ? (size_t)4 * (2 * kMaxMaskedGroups + 1) + (size_t)4 * kMaxBlockPairs
@@ -155,9 +155,16 @@ struct GemmPlan {
   }
 };
 
+// Stream-K work items (dense 256-row tiles): a tile whose K blocks are split
+// between CTAs is finished by its owner, the CTA that holds its first K
+// blocks (as its last item); the others contribute partial sums.
+enum ItemKind : int { kItemFull = 0, kItemOwner = 1, kItemPart = 2 };
+
 struct Tile {
   int g, mb, nb;
   int b0, b1;  // contiguous 256-row tiles: the two 128-row blocks (b1 < 0: none)
+  int kind;    // ItemKind
+  int sk;      // stream-K: index of the tile among the split tiles
 };
 
 // Maps a linear tile index to (group, M block, N block).  Dense and
@@ -168,7 +175,7 @@ struct Tile {
 // enumerated expert by expert, each expert's M x N tiles rastered like dense
 // ones.  k_range gives the K blocks a tile accumulates: this CTA's split-K
 // slice, or the expert's own K blocks for the K-grouped form.
-template <int MODE, int BM = kBlockM>
+template <int MODE, int BM = kBlockM, bool SK = false>
 struct Scheduler {
   const GemmArgs* args;
   const int* tile_start;   // masked: [G + 1] first tile; K-grouped: [G + 1] first K block;
@@ -178,6 +185,8 @@ struct Scheduler {
   int total;
   int cursor;              // masked: current group (tile indices only increase)
   int kb_lo, kb_hi;        // K blocks of every tile (not K-grouped)
+  int first, stride;       // this CTA's first tile and the stride of its tile walk
+  const uint32_t* sk_ctl;  // stream-K kernels: this CTA's units [sk_ctl[0], sk_ctl[1])
 
   __device__ void k_range(const Tile& tile, int& kb0, int& kb1) const {
     if (MODE == kKGrouped) {
@@ -188,6 +197,52 @@ struct Scheduler {
       kb1 = kb_hi;
     }
   }
+
+  // The it-th work item of this CTA: a tile and the K blocks [kb0, kb1) this
+  // CTA accumulates for it.  Returns -1 past the last item, 0 for a tile the
+  // walk skips (contiguous blocks of padding), 1 otherwise.  Items are
+  // visited with it = 0, 1, 2, ... by every role.
+  __device__ int item(int it, Tile& tile, int& kb0, int& kb1) {
+    tile.kind = kItemFull;
+    tile.sk = -1;
+    if constexpr (SK) {
+      // stream-K: tiles [0, dp) go one per CTA per wave; the K blocks of the
+      // tiles [dp, total) form sk_units units of which CTA c takes
+      // [c * U / P, (c + 1) * U / P), tile after tile (the host keeps
+      // sk_units * P below 2^32; the range is computed once per CTA)
+      const int dp = args->sk_dp_tiles;
+      const int n_dp = first < dp ? (dp - first + stride - 1) / stride : 0;
+      if (it < n_dp) {
+        get(first + it * stride, tile);
+        kb0 = 0;
+        kb1 = args->k_blocks;
+        return 1;
+      }
+      const uint32_t lo = sk_ctl[0], hi = sk_ctl[1], kbt = (uint32_t)args->k_blocks;
+      const uint32_t ts = lo / kbt + (uint32_t)(it - n_dp);
+      const uint32_t t0 = ts * kbt;
+      if (lo >= hi || t0 >= hi) return -1;
+      kb0 = (int)((lo > t0 ? lo : t0) - t0);
+      kb1 = (int)((hi < t0 + kbt ? hi : t0 + kbt) - t0);
+      get(dp + (int)ts, tile);
+      tile.kind = kb0 > 0 ? kItemPart : ((uint32_t)kb1 < kbt ? kItemOwner : kItemFull);
+      tile.sk = (int)ts;
+      return 1;
+    }
+    const int t = first + it * stride;
+    if (t >= total) return -1;
+    if (!get(t, tile)) return 0;
+    k_range(tile, kb0, kb1);
+    return 1;
+  }
+  // Stream-K units of CTA c: [c * U / P, (c + 1) * U / P).
+  __device__ void sk_range(int c, uint32_t& lo, uint32_t& hi) const {
+    const uint32_t u = (uint32_t)args->sk_units;
+    lo = u * (uint32_t)c / gridDim.x;
+    hi = u * (uint32_t)(c + 1) / gridDim.x;
+  }
+  // Whether the tile walk (without stream-K) has an item after the it-th.
+  __device__ bool has_next(int it) const { return first + (it + 1) * stride < total; }
 
   __device__ bool get(int t, Tile& tile) {
     if (MODE == kContiguous && BM == 2 * kBlockM) {
@@ -262,28 +317,27 @@ struct Scheduler {
 template <class Sched>
 struct PackCursor {
   Sched s;
-  int t, stride, kp, kp_end;
+  int it, kp, kp_end;
   Tile tile;
   bool done;
 
-  __device__ void init(const Sched& sch, int first, int stride_) {
+  __device__ void init(const Sched& sch) {
     s = sch;
-    stride = stride_;
-    t = first - stride_;
+    it = -1;
     next_tile();
   }
   __device__ void next_tile() {
     done = true;
-    for (t += stride; t < s.total; t += stride)
-      if (s.get(t, tile)) {
-        int kb0, kb1;
-        s.k_range(tile, kb0, kb1);
-        if (kb0 >= kb1) continue;
-        kp = kb0 >> 2;
-        kp_end = ((kb1 - 1) >> 2) + 1;
-        done = false;
-        return;
-      }
+    for (++it;; ++it) {
+      int kb0, kb1;
+      const int st = s.item(it, tile, kb0, kb1);
+      if (st < 0) return;
+      if (st == 0 || kb0 >= kb1) continue;
+      kp = kb0 >> 2;
+      kp_end = ((kb1 - 1) >> 2) + 1;
+      done = false;
+      return;
+    }
   }
   __device__ void advance() {
     if (++kp >= kp_end) next_tile();
@@ -579,7 +633,7 @@ __device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
   }
 }
 
-template <int BN, int STAGES, int MODE, int KSPLIT, int BM = kBlockM, bool EPI8 = false>
+template <int BN, int STAGES, int MODE, int KSPLIT, int BM = kBlockM, bool EPI8 = false, bool SK = false>
 __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
@@ -593,6 +647,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   static_assert(KSPLIT == 1 || MODE == kDense, "split-K is for the dense form");
   static_assert(!EPI8 || (BM == 2 * kBlockM && MODE == kDense && NUM_ACC == 1),
                 "eight epilogue warps: 256-row dense tiles with one accumulator");
+  static_assert(!SK || EPI8, "stream-K: 256-row dense tiles with eight epilogue warps");
   static_assert(BM == kBlockM || (BM == 2 * kBlockM && (MODE == kDense || MODE == kContiguous) && KSPLIT == 1) ||
                     (BM == kBlockM / 2 && MODE == kDense),
                 "256-row tiles are for the dense NT and contiguous forms without split-K; "
@@ -626,7 +681,9 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // split-K: set by another CTA of the cluster that aborted (see the teardown)
   volatile int* peer_abort = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
+  // stream-K: this CTA's units [sk_ctl[0], sk_ctl[1]) and its tile-walk items
+  uint32_t* const sk_ctl = tmem_slot + 4;
+  int* tile_start = reinterpret_cast<int*>(tmem_slot + 8);
   int* group_valid = tile_start + (kMaxMaskedGroups + 1);
   unsigned long long* const err = args.err;
 
@@ -651,6 +708,11 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     }
     *abort_flag = 0;
     *peer_abort = 0;
+    if constexpr (SK) {
+      const uint32_t u = (uint32_t)args.sk_units;
+      sk_ctl[0] = u * blockIdx.x / gridDim.x;
+      sk_ctl[1] = u * (blockIdx.x + 1) / gridDim.x;
+    }
     fence_mbar_init();
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
@@ -762,7 +824,8 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   const int kb_begin = KSPLIT > 1 ? min(args.k_blocks, (int)krank * kb_per) : 0;
   const int kb_end = KSPLIT > 1 ? min(args.k_blocks, kb_begin + kb_per) : args.k_blocks;
 
-  Scheduler<MODE, BM> sched;
+  Scheduler<MODE, BM, SK> sched;
+  sched.sk_ctl = sk_ctl;
   sched.args = &args;
   sched.tile_start = tile_start;
   sched.group_valid = group_valid;
@@ -770,6 +833,8 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   sched.cursor = 0;
   sched.kb_lo = kb_begin;
   sched.kb_hi = kb_end;
+  sched.first = first_tile;
+  sched.stride = tile_stride;
   sched.total = MODE == kMasked      ? tile_start[args.num_groups]
                 : MODE == kKGrouped ? args.num_groups * args.m_blocks * args.n_blocks
                 : (MODE == kContiguous && BM == 2 * kBlockM) ? tile_start[args.num_groups] * args.n_blocks
@@ -793,11 +858,12 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
         uint32_t phase = 0;
         uint32_t issued = 0, issued_parity = 0;  // stages: last fill's phase parity
         bool ok = true;
-        for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
+        for (int it = 0; ok; ++it) {
           Tile tile;
-          if (!sched.get(t, tile)) continue;
           int kb0, kb1;
-          sched.k_range(tile, kb0, kb1);
+          const int st_it = sched.item(it, tile, kb0, kb1);
+          if (st_it < 0) break;
+          if (st_it == 0) continue;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!wait_one<kSuspendHintNs, EPI8>(empty(stage), phase ^ 1u, abort_flag, tmo, err, kSiteProducerEmpty)) {
               ok = false;
@@ -807,7 +873,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
             const uint32_t fb = full(stage);
             mbar_arrive_expect_tx(fb, tx_ab);
             const int kx = kb * kBlockK, my = tile.mb * BM;
-            if (args.debug_drop_load && blockIdx.x == 0 && t == first_tile &&
+            if (args.debug_drop_load && blockIdx.x == 0 && it == 0 &&
                 kb + 1 == args.debug_drop_load) {
               // injected failure: the stage is armed but never filled
               issued |= 1u << stage;
@@ -859,17 +925,18 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (int t = first_tile; t < sched.total && ok; t += tile_stride) {
+        for (int it = 0; ok; ++it) {
           Tile tile;
-          if (!sched.get(t, tile)) continue;
+          int kb0, kb1;
+          const int st_it = sched.item(it, tile, kb0, kb1);
+          if (st_it < 0) break;
+          if (st_it == 0) continue;
           if (!wait_one<kSuspendHintNs, EPI8>(tempty(acc), acc_phase ^ 1u, abort_flag, tmo, err, kSiteMmaTmemEmpty)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MH * BN);
-          int kb0, kb1;
-          sched.k_range(tile, kb0, kb1);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!wait_one<kSuspendHintNs, EPI8>(full(stage), phase, abort_flag, tmo, err, kSiteMmaFull)) {
               ok = false;
@@ -934,9 +1001,9 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
       // ------------------------------------------------------------ scale warp
       // Two cursors walk the same sequence of packs (tile, K block / 4): one
       // loads up to kSfLookahead packs ahead, the other lays them out in order.
-      PackCursor<Scheduler<MODE, BM>> ld, lay;
-      ld.init(sched, first_tile, tile_stride);
-      lay.init(sched, first_tile, tile_stride);
+      PackCursor<Scheduler<MODE, BM, SK>> ld, lay;
+      ld.init(sched);
+      lay.init(sched);
       uint32_t n_loaded = 0, n_laid = 0;
       bool ok = true;
       while (!lay.done && ok) {
@@ -1037,12 +1104,22 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
         uint32_t pk[NCH][16];
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = first_tile; t < sched.total; t += tile_stride) {
+        for (int it = 0;; ++it) {
           Tile tile;
-          if (!sched.get(t, tile)) continue;
+          int tkb0, tkb1;
+          const int st_it = sched.item(it, tile, tkb0, tkb1);
+          if (st_it < 0) break;
+          if (st_it == 0) continue;
           const int row0 = tile.mb * BM + hh * kBlockM + quarter * 32;
           const int row = row0 + lane;
-          if (args.c != nullptr) {
+          const bool part = SK && tile.kind == kItemPart;  // stream-K: a partial sum for another CTA
+          // stream-K slot of CTA c for this warp's rows: 32 lanes x BN columns,
+          // 16 bytes (4 columns) of a lane at ((col / 4) * 32 + lane) * 4 floats
+          auto slot = [&](int c) {
+            return args.sk_part + (size_t)c * (size_t)(2 * 4 * BN * 32) + (size_t)(hh * 4 + quarter) * (BN * 32);
+          };
+          uint32_t* const my_flags = args.sk_flags;  // [grid][8]
+          if (args.c != nullptr && !part) {
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
               const int col0 = tile.nb * BN + ch * 32;
@@ -1061,6 +1138,64 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
           if (!warp_wait<kSuspendHintNs, EPI8>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
           tc_fence_after();
           const bool live = row0 < args.m;
+          if constexpr (SK) if (part) {
+            // contributor: the FP32 partial goes to this CTA's slot as is
+            if (live) {
+              const uint32_t taddr =
+                  tmem_base + (uint32_t)((acc * MH + hh) * BN) + ((uint32_t)(quarter * 32) << 16);
+              float* dst = slot(blockIdx.x);
+              uint32_t va[32], vb[32];
+              tc_ld_32x32b_x32(taddr, va);
+#pragma unroll
+              for (int ch = 0; ch < NCH; ++ch) {
+                uint32_t(&cur)[32] = (ch & 1) ? vb : va;
+                uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
+                tc_wait_ld_regs(cur);
+                if (ch + 1 < NCH) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  *reinterpret_cast<float4*>(dst + ((ch * 8 + j) * 32 + lane) * 4) =
+                      make_float4(__uint_as_float(cur[4 * j]), __uint_as_float(cur[4 * j + 1]),
+                                  __uint_as_float(cur[4 * j + 2]), __uint_as_float(cur[4 * j + 3]));
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(acc));
+            if (live) {
+              // every lane's stores are ordered before the flag the owner acquires
+              __threadfence();
+              __syncwarp();
+              if (lane == 0) st_release_gpu(my_flags + blockIdx.x * 8 + (warp - 4), 1u);
+            }
+            if (++acc == NUM_ACC) {
+              acc = 0;
+              acc_phase ^= 1u;
+            }
+            continue;
+          }
+          // owner: the CTAs holding the tile's later K blocks (each a
+          // contiguous share of stream-K units starting inside the tile)
+          int c_end = (int)blockIdx.x + 1;
+          if constexpr (SK) if (tile.kind == kItemOwner && live) {
+            const uint32_t tend = (uint32_t)(tile.sk + 1) * (uint32_t)args.k_blocks;
+            bool ok = true;
+            for (; c_end < (int)gridDim.x; ++c_end) {
+              uint32_t lo, hi;
+              sched.sk_range(c_end, lo, hi);
+              if (lo >= tend) break;
+              int got = 1;
+              if (lane == 0 && lo < hi)
+                got = wait_flag_gpu(my_flags + c_end * 8 + (warp - 4), abort_flag, tmo, err,
+                                    kSiteStreamKPartial) ? 1 : 0;
+              if (!__shfl_sync(0xffffffffu, got, 0)) {
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
+            __threadfence();  // acquire side: the partials are read after the flags
+          }
           if (live) {
             const uint32_t taddr =
                 tmem_base + (uint32_t)((acc * MH + hh) * BN) + ((uint32_t)(quarter * 32) << 16);
@@ -1071,6 +1206,20 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
               uint32_t(&cur)[32] = (ch & 1) ? vb : va;
               uint32_t(&nxt)[32] = (ch & 1) ? va : vb;
               tc_wait_ld_regs(cur);
+              // owner: the contributors' partials of these 32 columns, in K
+              // order (added before the next TMEM load is issued, so their
+              // registers and that load's are never live together)
+              if constexpr (SK) for (int c = (int)blockIdx.x + 1; c < c_end; ++c) {
+                const float* src = slot(c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 w = __ldcg(reinterpret_cast<const float4*>(src + ((ch * 8 + j) * 32 + lane) * 4));
+                  cur[4 * j] = __float_as_uint(__uint_as_float(cur[4 * j]) + w.x);
+                  cur[4 * j + 1] = __float_as_uint(__uint_as_float(cur[4 * j + 1]) + w.y);
+                  cur[4 * j + 2] = __float_as_uint(__uint_as_float(cur[4 * j + 2]) + w.z);
+                  cur[4 * j + 3] = __float_as_uint(__uint_as_float(cur[4 * j + 3]) + w.w);
+                }
+              }
               if (ch + 1 < NCH) tc_ld_32x32b_x32(taddr + (ch + 1) * 32, nxt);
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -1087,6 +1236,10 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty(acc));
           if (live) {
+            // the contributors' flags go back to zero for the next launch
+            if constexpr (SK)
+              if (lane == 0)
+                for (int c = (int)blockIdx.x + 1; c < c_end; ++c) st_relaxed_gpu(my_flags + c * 8 + (warp - 4), 0u);
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
               const int col0 = tile.nb * BN + ch * 32;
@@ -1115,9 +1268,12 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t n_xchg = 0;  // split-K exchanges of this quarter so far (barrier phases)
-    for (int t = first_tile; t < sched.total; t += tile_stride) {
+    for (int it = 0;; ++it) {
       Tile tile;
-      if (!sched.get(t, tile)) continue;
+      int tkb0, tkb1;
+      const int st_it = sched.item(it, tile, tkb0, tkb1);
+      if (st_it < 0) break;
+      if (st_it == 0) continue;
       // C of dense tiles is fetched while the accumulator is still being
       // computed, so the epilogue never waits for a load from HBM.  128-row
       // tiles with two accumulators (no split): this quarter's whole C tile,
@@ -1199,12 +1355,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
         float* drow32 = MODE == kKGrouped ? args.d_f32 + (out_row0 + lane) * args.n : nullptr;
         const float* crow32 =
             (MODE == kKGrouped && args.c_f32) ? args.c_f32 + (out_row0 + lane) * args.n : nullptr;
-        bool k_empty = false;
-        if (MODE == kKGrouped) {
-          int kb0, kb1;
-          sched.k_range(tile, kb0, kb1);
-          k_empty = kb0 >= kb1;
-        }
+        const bool k_empty = MODE == kKGrouped && tkb0 >= tkb1;
         // A quarter none of whose rows is written hands its accumulator back
         // unread: no TMEM load, no exchange, no store.  For dense and K-grouped
         // tiles the test (first row past M) is the same in every CTA of a
@@ -1310,7 +1461,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(tempty(acc));
-            if (t + tile_stride < sched.total)
+            if (sched.has_next(it))
               for (int o = 0; o < KSPLIT; ++o)
                 if (o != (int)krank) mbar_arrive_cluster(mapa_shared(recv_free(quarter), (uint32_t)o));
           }
@@ -1593,20 +1744,26 @@ static cudaError_t set_smem_once(Kern kern, size_t smem) {
   return e;
 }
 
-template <int BN, int STAGES, int MODE, int KSPLIT = 1, int BM = kBlockM, bool EPI8 = false>
+template <int BN, int STAGES, int MODE, int KSPLIT = 1, int BM = kBlockM, bool EPI8 = false, bool SK = false>
 static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
                                     const CUtensorMap& sfa, const CUtensorMap& sfb,
                                     const CUtensorMap& d, const GemmArgs& args, int grid,
                                     cudaStream_t stream) {
   using Plan = GemmPlan<BN, STAGES, KSPLIT, BM>;
   static_assert(Plan::smem_bytes(MODE) <= (size_t)kSmemLimit, "shared memory over the per-CTA limit");
-  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT, BM, EPI8>;
+  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT, BM, EPI8, SK>;
   const size_t smem = Plan::smem_bytes(MODE);
   cudaError_t e = set_smem_once<
-      KernelTag<BN, STAGES, MODE, KSPLIT, EPI8 ? 5 : (BM == kBlockM ? 1 : (BM > kBlockM ? 3 : 4))>>(kern, smem);
+      KernelTag<BN, STAGES, MODE, KSPLIT, SK ? 6 : EPI8 ? 5 : (BM == kBlockM ? 1 : (BM > kBlockM ? 3 : 4))>>(kern, smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   unsigned n_attr = 0;
+  if (SK) {
+    // stream-K owners wait for partial sums of other CTAs: all co-resident
+    attr[n_attr].id = cudaLaunchAttributeCooperative;
+    attr[n_attr].val.cooperative = 1;
+    ++n_attr;
+  }
   if (KSPLIT > 1) {
     attr[n_attr].id = cudaLaunchAttributeClusterDimension;
     attr[n_attr].val.clusterDim.x = KSPLIT;

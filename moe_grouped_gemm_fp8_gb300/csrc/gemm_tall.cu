@@ -34,7 +34,12 @@ cudaError_t gemm_tall_launch_impl(int mode, int block_n, const CUtensorMap& a, c
                                   const CUtensorMap& d, const GemmArgs& args, int grid,
                                   cudaStream_t stream) {
   constexpr int BM = 2 * kBlockM;
-  if (mode == kDense && args.epi8) {
+  if (mode == kDense && args.sk_units > 0) {
+    switch (block_n) {
+      case 192: return gemm_launch_impl<192, 3, kDense, 1, BM, true, true>(a, b, sfa, sfb, d, args, grid, stream);
+      case 224: return gemm_launch_impl<224, 3, kDense, 1, BM, true, true>(a, b, sfa, sfb, d, args, grid, stream);
+    }
+  } else if (mode == kDense && args.epi8) {
     switch (block_n) {
       case 192: return gemm_launch_impl<192, 3, kDense, 1, BM, true>(a, b, sfa, sfb, d, args, grid, stream);
       case 224: return gemm_launch_impl<224, 3, kDense, 1, BM, true>(a, b, sfa, sfb, d, args, grid, stream);

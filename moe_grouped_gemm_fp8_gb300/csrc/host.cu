@@ -390,18 +390,16 @@ void choose_dense_nt_tile(int64_t m, int64_t n, int64_t k_blocks, int slots, boo
 
 // Raster band of the dense tile walk, in M blocks of block_m rows: inside a
 // band the M block varies fastest, so a wave of CTAs shares a few column
-// blocks of B and the band's rows of A.  B is read from DRAM once per band,
-// so the band covers as many M blocks as keep that strip of A within 32 MiB,
-// a quarter of L2: the strip is read by SMs of both dies and held in both
-// halves of L2, and a 64 MiB strip (the whole of M at K = 16384) was evicted
-// between waves (DRAM reads 393 MB against 366 MB for a 32 MiB strip on
-// M = 4096, N = 7168, K = 16384).  DG_RASTER_BAND (in 128-row blocks)
-// overrides.
+// blocks of B and the band's rows of A; B is read from DRAM once per band.
+// 2048 rows: on GB300 (M = 4096) bands of the whole of M were 2-3% slower for
+// the 256-row tiles at K <= 7168, and at K = 16384 their 64 MB strip of A
+// did not survive in L2 between waves (DRAM reads 393 MB against 366.6 MB):
+// A is read by SMs of both dies and held in both halves of L2.
+// DG_RASTER_BAND (in 128-row blocks) overrides.
 int raster_band(int64_t m_blocks, int block_m, int64_t k) {
-  const int forced = env_int("DG_RASTER_BAND", 0);
-  if (forced > 0) return std::max(1, forced * kBlockM / block_m);
-  const int64_t fit = ((int64_t)32 << 20) / ((int64_t)block_m * std::max<int64_t>(k, 1));
-  return (int)std::max<int64_t>(1, std::min<int64_t>(m_blocks, fit));
+  (void)k;
+  const int band128 = std::max(1, env_int("DG_RASTER_BAND", 16));
+  return (int)std::max<int64_t>(1, std::min<int64_t>(m_blocks, (int64_t)band128 * kBlockM / block_m));
 }
 
 void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_m,
@@ -420,9 +418,43 @@ struct DensePlan {
   bool pair = false;     // 256-row tiles on a pair of CTAs (only on request)
   bool tall = false;     // 256-row tiles on one CTA
   bool short_a = false;  // 64-row A slots: a single M block of at most 64 rows
+  // stream-K (256-row tiles, only with a workspace): tiles [0, sk_dp_tiles)
+  // one per CTA per wave, the K blocks of the rest (sk_units) shared evenly
+  bool stream_k = false;
+  int32_t sk_dp_tiles = 0;
+  int64_t sk_units = 0;
 };
 
-DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int sms) {
+// Workspace of a stream-K launch on `sms` CTAs with block_n columns: a fixed
+// 32 KiB of flag words (one per (CTA, epilogue warp), for up to 1024 CTAs, so
+// the flags sit at the same place whatever the SM count a later call uses),
+// then one partial slot of 256 x block_n floats per CTA.
+constexpr int kStreamKMaxCtas = 1024;
+constexpr uint64_t kStreamKFlagBytes = (uint64_t)kStreamKMaxCtas * 8 * 4;
+uint64_t stream_k_workspace_bytes(int sms, int block_n) {
+  return kStreamKFlagBytes + (uint64_t)sms * (uint64_t)(2 * kBlockM) * (uint64_t)block_n * 4;
+}
+
+// Stream-K split of T tiles of kb K blocks over P CTAs: whole waves but the
+// last are walked tile by tile; the last full wave and the partial one
+// (P + r tiles, or all T when T < P) have their K blocks shared evenly, so
+// every CTA ends at the same time.  False when the waves are already whole,
+// or when some CTA would get no K block.
+bool stream_k_split(int64_t tiles, int64_t kb, int sms, int32_t* dp_tiles, int64_t* units) {
+  if (sms < 2 || sms > kStreamKMaxCtas || tiles <= 0) return false;
+  const int64_t q = tiles / sms, r = tiles % sms;
+  if (r == 0) return false;
+  const int64_t dp = q >= 1 ? (q - 1) * sms : 0;
+  const int64_t u = (tiles - dp) * kb;
+  if (u < sms) return false;
+  if (u * (sms + 1) >= ((int64_t)1 << 32)) return false;  // the kernel's unit arithmetic is 32-bit
+  *dp_tiles = (int32_t)dp;
+  *units = u;
+  return true;
+}
+
+
+DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int sms, bool ws = false) {
   DensePlan p;
   const int64_t kb = k / kBlockK;
   const int64_t m_blocks = (m + kBlockM - 1) / kBlockM;
@@ -461,6 +493,42 @@ DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int
     int bm = kBlockM;
     choose_dense_nt_tile(m, n, kb, sms, with_c, &bm, &p.block_n);
     p.tall = bm == 2 * kBlockM;
+    // With a workspace, 256-row tiles in stream-K order where the estimate
+    // beats the tile-by-tile walk by 10%: the same cost table for each CTA's
+    // share of K blocks and of the tiles' final epilogues, plus the fixed cost
+    // of the partial sums measured on GB300 (M = 4096, N = 2112, K = 7168,
+    // 160 tiles of 256 x 224 on 152 SMs, traced per CTA): ~4.8 us while the
+    // contributor writes its 224 KB partial and the MMA waits, ~8 us for the
+    // owner's flag wait, partial reads and stores; ~22 K blocks in all.
+    // DG_STREAM_K = 0 / 1 disables / forces it where it applies.
+    const int forced_sk = env_int("DG_STREAM_K", -1);
+    const int forced_m = env_int("DG_BLOCK_M", 0), forced_n = env_int("DG_BLOCK_N", 0);
+    if (ws && forced_sk != 0 && env_int("DG_TALL_EPI8", 1) != 0 && forced_m != 128 && sms >= 2) {
+      double cost_dp = 1e300;
+      for (const DenseTileCost& t : kDenseTiles)
+        if (t.block_m == bm && t.block_n == p.block_n) cost_dp = dense_nt_cost(t, m, n, kb, sms, with_c);
+      double best = forced_sk == 1 ? 1e300 : 0.9 * cost_dp;
+      for (const DenseTileCost& t : kDenseTiles) {
+        if (t.block_m != 2 * kBlockM || gemm_tall_stages(t.block_n) == 0) continue;
+        if (forced_n != 0 && forced_n != t.block_n) continue;
+        const int64_t tiles = ((m + t.block_m - 1) / t.block_m) * ((n + t.block_n - 1) / t.block_n);
+        int32_t dp = 0;
+        int64_t units = 0;
+        if (!stream_k_split(tiles, kb, sms, &dp, &units)) continue;
+        const double e = with_c ? t.epi_kb_c : t.epi_kb;
+        const double cost = ((double)dp / sms * ((double)kb + e) + (double)units / sms +
+                             (double)(tiles - dp) / sms * e + 22.0) *
+                            (with_c ? t.us_per_kb_c : t.us_per_kb);
+        if (cost < best) {
+          best = cost;
+          p.stream_k = true;
+          p.tall = true;
+          p.block_n = t.block_n;
+          p.sk_dp_tiles = dp;
+          p.sk_units = units;
+        }
+      }
+    }
   } else {
     p.block_n = choose_block_n(m_blocks, n, kb, sms, with_c, false, mode != kDense);
   }
@@ -536,7 +604,8 @@ extern "C" {
 static dg_status dense_gemm(int mode, const char* name, const void* a, const int32_t* sfa,
                             const void* b, const int32_t* sfb, const void* c, void* d, int64_t m,
                             int64_t n, int64_t k, int64_t lda, int64_t ldb, int64_t ldc,
-                            int64_t ldd, void* stream) {
+                            int64_t ldd, void* stream, void* workspace = nullptr,
+                            uint64_t workspace_bytes = 0) {
   if (m < 0) return DG_ERR_INVALID_ARG;
   dg_status s = check_common_k_n(n, k);
   if (s != DG_OK) return s;
@@ -547,14 +616,16 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     return DG_ERR_INVALID_ARG;
   if (lda % 16 || ldb % 16 || ldd % 8 || (c && ldc % 8)) return DG_ERR_ALIGNMENT;
   if (!aligned16(a) || !aligned16(b) || !aligned16(sfa) || !aligned16(sfb) || !aligned16(d) ||
-      (c && !aligned16(c)))
+      (c && !aligned16(c)) || (workspace && !aligned16(workspace)))
     return DG_ERR_ALIGNMENT;
   if (m >= kMaxCoord) return DG_ERR_TOO_LARGE;
   int sms = 0;
   if ((s = current_device(&sms)) != DG_OK) return s;
   if ((s = get_encoder()) != DG_OK) return s;
 
-  const DensePlan plan = plan_dense(mode, m, n, k, c != nullptr, sms);
+  DensePlan plan = plan_dense(mode, m, n, k, c != nullptr, sms, workspace != nullptr);
+  if (plan.stream_k && workspace_bytes < stream_k_workspace_bytes(sms, plan.block_n))
+    plan = plan_dense(mode, m, n, k, c != nullptr, sms, false);  // too small: tile by tile
   const int ksplit = plan.ksplit;
   GemmArgs args = {};
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
@@ -636,13 +707,22 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     return from_cuda(gemm2_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, clusters,
                                   static_cast<cudaStream_t>(stream)));
   }
-  const int grid = (int)(tiles < sms ? tiles : sms);
+  const int grid = plan.stream_k ? sms : (int)(tiles < sms ? tiles : sms);
   args.debug_drop_load = g_debug_drop_load.load(std::memory_order_relaxed);
-  print_config(tall ? "fp8_gemm_nt (256-row tiles)" : plan.short_a ? "fp8_gemm_nt (64-row A slots)" : name,
+  if (plan.stream_k) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    args.sk_flags = reinterpret_cast<uint32_t*>(ws);
+    args.sk_part = reinterpret_cast<float*>(ws + kStreamKFlagBytes);
+    args.sk_units = plan.sk_units;
+    args.sk_dp_tiles = plan.sk_dp_tiles;
+  }
+  print_config(plan.stream_k ? "fp8_gemm_nt (256-row tiles, stream-K)"
+               : tall        ? "fp8_gemm_nt (256-row tiles)"
+               : plan.short_a ? "fp8_gemm_nt (64-row A slots)" : name,
                m, n, k, 1, tall ? 2 * kBlockM : plan.short_a ? kBlockM / 2 : kBlockM, block_n,
                tall ? gemm_tall_stages(block_n) : plan.short_a ? gemm_short_stages(block_n) : gemm_stages(block_n),
                grid, args.band);
-  args.epi8 = env_int("DG_TALL_EPI8", 1) != 0 ? 1 : 0;
+  args.epi8 = (plan.stream_k || env_int("DG_TALL_EPI8", 1) != 0) ? 1 : 0;
   if (tall)
     return from_cuda(gemm_tall_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                       static_cast<cudaStream_t>(stream)));
@@ -658,6 +738,47 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
                          int64_t ldb, int64_t ldc, int64_t ldd, void* stream) {
   return dense_gemm(kDense, "fp8_gemm_nt", a, sfa, b, sfb, c, d, m, n, k, lda, ldb, ldc, ldd,
                     stream);
+}
+
+dg_status dg_fp8_gemm_nt_ws(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                            const void* c, void* d, int64_t m, int64_t n, int64_t k, int64_t lda,
+                            int64_t ldb, int64_t ldc, int64_t ldd, void* workspace,
+                            uint64_t workspace_bytes, void* stream) {
+  return dense_gemm(kDense, "fp8_gemm_nt", a, sfa, b, sfb, c, d, m, n, k, lda, ldb, ldc, ldd, stream,
+                    workspace, workspace_bytes);
+}
+
+dg_status dg_fp8_gemm_nt_workspace_size(int64_t m, int64_t n, int64_t k, int32_t has_c,
+                                        int32_t num_sms, uint64_t* bytes) {
+  if (!bytes) return DG_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (m < 0 || num_sms < 1) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (m >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  if (m == 0 || n == 0) return DG_OK;
+  const DensePlan p = plan_dense(kDense, m, n, k, has_c != 0, num_sms, true);
+  if (p.stream_k) *bytes = stream_k_workspace_bytes(num_sms, p.block_n);
+  return DG_OK;
+}
+
+dg_status dg_plan_fp8_gemm_nt_ws(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,
+                                 int32_t* block_m, int32_t* block_n, int32_t* split_k,
+                                 int32_t* cta_pair, int32_t* stream_k) {
+  if (!block_m || !block_n || !split_k || !cta_pair || !stream_k) return DG_ERR_INVALID_ARG;
+  *block_m = *block_n = *split_k = *cta_pair = *stream_k = 0;
+  if (m < 0 || num_sms < 1) return DG_ERR_INVALID_ARG;
+  dg_status s = check_common_k_n(n, k);
+  if (s != DG_OK) return s;
+  if (m >= kMaxCoord) return DG_ERR_TOO_LARGE;
+  if (m == 0 || n == 0) return DG_OK;
+  const DensePlan p = plan_dense(kDense, m, n, k, has_c != 0, num_sms, true);
+  *block_m = (p.pair || p.tall) ? 2 * kBlockM : p.short_a ? kBlockM / 2 : kBlockM;
+  *block_n = p.block_n;
+  *split_k = p.ksplit;
+  *cta_pair = p.pair ? 1 : 0;
+  *stream_k = p.stream_k ? 1 : 0;
+  return DG_OK;
 }
 
 dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,

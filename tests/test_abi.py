@@ -80,6 +80,25 @@ def test_dense_host_checks(L):
     assert gemm(L, m=1 << 31) == TOO_LARGE
 
 
+def test_workspace_entry_points_host_checks(L):
+    """dg_fp8_gemm_nt_ws: the same checks, plus a 16-byte aligned workspace;
+    the size and plan queries are pure host arithmetic."""
+    def gemm_ws(ws, nbytes, **kw):
+        a = dict(a=P, sfa=P, b=P, sfb=P, c=None, d=P, m=128, n=256, k=512, lda=512, ldb=512,
+                 ldc=0, ldd=256)
+        a.update(kw)
+        return L.dg_fp8_gemm_nt_ws(a["a"], a["sfa"], a["b"], a["sfb"], a["c"], a["d"], a["m"], a["n"],
+                                   a["k"], a["lda"], a["ldb"], a["ldc"], a["ldd"], ws, nbytes, None)
+    assert gemm_ws(C.c_void_p(0x1008), 1 << 20) == ALIGN     # unaligned workspace
+    assert gemm_ws(P, 1 << 20, k=100, lda=112, ldb=112) == ALIGN
+    assert gemm_ws(P, 1 << 20, m=0) == DG_OK
+    out = C.c_uint64(7)
+    assert L.dg_fp8_gemm_nt_workspace_size(128, 256, 100, 0, 152, C.byref(out)) == ALIGN
+    assert L.dg_fp8_gemm_nt_workspace_size(128, 256, 512, 0, 0, C.byref(out)) == INVALID
+    assert L.dg_fp8_gemm_nt_workspace_size(128, 256, 512, 0, 152, None) == INVALID
+    assert L.dg_fp8_gemm_nt_workspace_size(0, 256, 512, 0, 152, C.byref(out)) == DG_OK and out.value == 0
+
+
 def test_grouped_host_checks(L):
     cont = L.dg_m_grouped_fp8_gemm_nt_contiguous
     assert cont(P, P, P, P, P, P, 130, 256, 512, 4, None) == ALIGN      # m_sum % 128

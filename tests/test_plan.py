@@ -14,7 +14,7 @@ import moe_grouped_gemm_fp8_gb300 as dg
 from moe_grouped_gemm_fp8_gb300 import _lib, workloads
 
 SMS = 152
-OVERRIDES = ("DG_BLOCK_M", "DG_BLOCK_N", "DG_SPLIT_K", "DG_CTA_PAIR")
+OVERRIDES = ("DG_BLOCK_M", "DG_BLOCK_N", "DG_SPLIT_K", "DG_CTA_PAIR", "DG_STREAM_K")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -195,3 +195,46 @@ def test_grouped_argument_checks():
     assert L.dg_plan_m_grouped_fp8_gemm_nt_masked(100000, 16, 7168, 2048, 0, SMS, *r) == 7       # groups
     assert L.dg_plan_m_grouped_fp8_gemm_nt_masked(0, 256, 7168, 2048, 0, SMS, *r) == 0
     assert [x.value for x in o] == [0, 0, 0]
+
+
+# ------------------------------------------------------------------ stream-K
+
+
+def plan_ws(m, n, k, has_c=False, sms=SMS):
+    p = dg.plan_fp8_gemm_nt_ws(m, n, k, has_c, sms)
+    return p["block_m"], p["block_n"], p["split_k"], p["cta_pair"], p["stream_k"]
+
+
+@pytest.mark.parametrize("has_c", [False, True])
+def test_stream_k_needs_its_fixed_cost_repaid(has_c):
+    """With a workspace the plan is dg_fp8_gemm_nt's unless stream-K's
+    estimate, which carries the measured cost of the partial sums (~22 K
+    blocks per CTA), wins by 10%: on 152 SMs no prefill or decode shape does
+    (M = 4096, (N, K) = (2112, 7168), whose last wave is mostly empty, measured
+    slower with stream-K than with 128 x 256 tiles); 17 long tiles on 16 SMs
+    (a second wave of one tile) do."""
+    with env():
+        for cfg in workloads.PREFILL + workloads.DECODE:
+            m, n, k = cfg["m"], cfg["n"], cfg["k"]
+            assert plan_ws(m, n, k, has_c) == plan(m, n, k, has_c) + (False,)
+            assert dg.fp8_gemm_nt_workspace_size(m, n, k, has_c, SMS) == 0
+        got = plan_ws(4352, 192, 16384, has_c, sms=16)  # 17 tiles of 256 x 192 on 16 SMs
+        assert got[0] == 256 and got[4], got
+        assert dg.fp8_gemm_nt_workspace_size(4352, 192, 16384, has_c, 16) == 32 * 1024 + 16 * 256 * got[1] * 4
+
+
+def test_stream_k_overrides():
+    with env():
+        os.environ["DG_STREAM_K"] = "0"
+        try:
+            assert not plan_ws(4352, 192, 16384, sms=16)[4]
+            assert dg.fp8_gemm_nt_workspace_size(4352, 192, 16384, False, 16) == 0
+            os.environ["DG_STREAM_K"] = "1"
+            assert plan_ws(512, 384, 128)[4] is False     # 4 K blocks for 152 SMs: nothing to share
+            assert plan_ws(4096, 7168, 2048)[:2] == (256, 224)  # 512 tiles: the 192-wide ones fill 4 waves
+            assert plan_ws(512, 384, 2048, sms=8)[4]      # 4 tiles over 8 SMs
+            os.environ["DG_BLOCK_N"] = "224"
+            assert plan_ws(512, 384, 2048, sms=8)[:2] == (256, 224)
+        finally:
+            os.environ.pop("DG_STREAM_K", None)
+            os.environ.pop("DG_BLOCK_N", None)
