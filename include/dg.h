@@ -119,6 +119,36 @@ dg_status dg_fp8_gemm_nt_ws(const void* a, const int32_t* sfa, const void* b, co
                             int64_t ldb, int64_t ldc, int64_t ldd, void* workspace,
                             uint64_t workspace_bytes, void* stream);
 
+/* dg_fp8_gemm_nt_ws for callers that cannot allocate device memory: a
+ * runtime that reserves all its memory at start-up and forbids allocation
+ * afterwards, a plugin whose host hands it no scratch buffer, or code that
+ * must not call cudaMalloc because it would synchronise the device or is not
+ * allowed where it runs.  The workspace is a 32 MiB array of this library in
+ * device memory, present on every device from the moment libdg.so is loaded
+ * until the process exits (whether or not this function is ever called).
+ * Nothing is allocated or freed: no cudaMalloc, cudaFree or other allocating
+ * routine is called.  Same operation, arguments, layouts and checks as
+ * dg_fp8_gemm_nt; the tile plan is dg_fp8_gemm_nt_ws's for a 32 MiB
+ * workspace.
+ *   - A problem whose plan needs more scratch than the array holds (see
+ *     dg_fp8_gemm_nt_workspace_size; e.g. stream-K with 224-column tiles on
+ *     more than 145 SMs) is rejected with DG_ERR_TOO_LARGE before anything
+ *     is enqueued; dg_fp8_gemm_nt needs no scratch at all.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and leaves its last
+ *     contents in it; each call clears the part that must start at zero (the
+ *     flags) on its stream before its kernel.  Calls whose execution can
+ *     overlap on the device (other streams, other host threads) race on it:
+ *     serialise them.
+ * No counterpart on the pages: this entry point exists for callers of this
+ * library that cannot provide a workspace. */
+dg_status dg_fp8_gemm_nt_static_ws(const void* a, const int32_t* sfa, const void* b,
+                                   const int32_t* sfb, const void* c, void* d, int64_t m,
+                                   int64_t n, int64_t k, int64_t lda, int64_t ldb, int64_t ldc,
+                                   int64_t ldd, void* stream);
+
 /* Bytes of workspace dg_fp8_gemm_nt_ws needs to use stream-K for an
  * M x N x K problem (with C when has_c != 0) on num_sms SMs (the device's
  * count, or the dg_set_num_sms limit); 0 when it would not use stream-K.
