@@ -58,11 +58,11 @@ def _ptr(t: Optional[torch.Tensor]):
 def _need(t: torch.Tensor, name: str, dtypes, ndim: int) -> None:
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
-    if t.dtype not in dtypes:
-        raise TypeError("%s: dtype %s not in %s" % (name, t.dtype, dtypes))
-    if not t.is_cuda:
-        raise ValueError("%s must be a CUDA tensor" % name)
-    if t.dim() != ndim:
+    if t.dtype not in dtypes or not t.is_cuda or t.dim() != ndim:
+        if t.dtype not in dtypes:
+            raise TypeError("%s: dtype %s not in %s" % (name, t.dtype, dtypes))
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
         raise ValueError("%s must have %d dims, got %s" % (name, ndim, tuple(t.shape)))
 
 
@@ -163,7 +163,7 @@ def get_device_error(stream=None) -> Tuple[int, int]:
 
 def sf_packed_shape(mn: int, k: int, groups: Optional[int] = None):
     kp = (k // 128 + 3) // 4
-    shape = (kp, get_tma_aligned_size(mn, 4))
+    shape = (kp, (mn + 3) // 4 * 4)  # rows padded to 16 bytes (dg_get_tma_aligned_size(mn, 4))
     return shape if groups is None else (groups,) + shape
 
 
@@ -280,15 +280,14 @@ def _new_workspace(nbytes: int, device) -> torch.Tensor:
     return ws
 
 
-def _cached_workspace(nbytes: int, stream, device) -> torch.Tensor:
-    """The binding's workspace for this device and stream, grown to nbytes.
-    While a CUDA graph is being captured a fresh one is taken from the
-    graph's memory pool instead (its flag words are zeroed by a captured
-    memset, so every replay starts from zero flags)."""
+def _cached_workspace(nbytes: int, stream_handle, device) -> torch.Tensor:
+    """The binding's workspace for this device and stream (its handle),
+    grown to nbytes.  While a CUDA graph is being captured a fresh one is
+    taken from the graph's memory pool instead (its flag words are zeroed by
+    a captured memset, so every replay starts from zero flags)."""
     if torch.cuda.is_current_stream_capturing():
         return _new_workspace(nbytes, device)
-    s = stream if stream is not None else torch.cuda.current_stream()
-    key = (device.index, s.cuda_stream if isinstance(s, torch.cuda.Stream) else int(s))
+    key = (device.index, stream_handle or 0)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = _new_workspace(nbytes, device)
@@ -329,26 +328,27 @@ def fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.
         if tuple(c.shape) != (m, n) or c.stride(1) != 1:
             raise ValueError("c must be [M, N] with unit column stride")
     _on_current_device(stream, a, sfa, b, sfb, c, d)
+    st = _stream(stream)
     ws = None
     if workspace is None:
         need = fp8_gemm_nt_workspace_size(m, n, k, c is not None)
         if need:
-            ws = _cached_workspace(need, stream, d.device)
+            ws = _cached_workspace(need, st.value, d.device)
     elif workspace is not False:
         _need(workspace, "workspace", (torch.uint8,), 1)
         _on_current_device(stream, workspace)
         ws = workspace
     if ws is None:
-        st = _lib.lib().dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+        rc = _lib.lib().dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                                        m, n, k, a.stride(0), b.stride(0),
-                                       c.stride(0) if c is not None else 0, d.stride(0), _stream(stream))
-        _check(st, "dg_fp8_gemm_nt")
+                                       c.stride(0) if c is not None else 0, d.stride(0), st)
+        _check(rc, "dg_fp8_gemm_nt")
     else:
-        st = _lib.lib().dg_fp8_gemm_nt_ws(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
+        rc = _lib.lib().dg_fp8_gemm_nt_ws(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
                                           m, n, k, a.stride(0), b.stride(0),
                                           c.stride(0) if c is not None else 0, d.stride(0), _ptr(ws),
-                                          ws.numel(), _stream(stream))
-        _check(st, "dg_fp8_gemm_nt_ws")
+                                          ws.numel(), st)
+        _check(rc, "dg_fp8_gemm_nt_ws")
     return d
 
 

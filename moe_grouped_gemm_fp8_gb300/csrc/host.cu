@@ -8,6 +8,7 @@
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
+#include <unistd.h>
 
 #include <algorithm>
 #include <atomic>
@@ -45,6 +46,45 @@ bool env_flag(const char* name) {
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   return (v && *v) ? atoi(v) : dflt;
+}
+
+// The DG_* overrides, read with getenv only when the process environment may
+// have changed since this thread last read them: setenv / putenv / unsetenv
+// (os.environ in Python) replace or move entries of `environ`, so a
+// fingerprint of the entry pointers (a few tens of loads) stands in for the
+// eight getenv scans a call would otherwise make.
+struct EnvConfig {
+  uintptr_t fingerprint = 0;
+  bool valid = false;
+  int block_m = 0, block_n = 0, split_k = 0, cta_pair = 0, stream_k = -1, tall_epi8 = 1,
+      raster_band = 16;
+  bool print_configs = false;
+};
+
+uintptr_t environ_fingerprint() {
+  char** const env = ::environ;  // the process environment (POSIX, unistd.h)
+  uintptr_t h = reinterpret_cast<uintptr_t>(env);
+  uintptr_t n = 0;
+  for (char** e = env; e && *e; ++e, ++n) h = h * 1099511628211ull + reinterpret_cast<uintptr_t>(*e);
+  return h ^ (n << 48);
+}
+
+const EnvConfig& env() {
+  thread_local EnvConfig c;
+  const uintptr_t f = environ_fingerprint();
+  if (!c.valid || c.fingerprint != f) {
+    c.block_m = env_int("DG_BLOCK_M", 0);
+    c.block_n = env_int("DG_BLOCK_N", 0);
+    c.split_k = env_int("DG_SPLIT_K", 0);
+    c.cta_pair = env_int("DG_CTA_PAIR", 0);
+    c.stream_k = env_int("DG_STREAM_K", -1);
+    c.tall_epi8 = env_int("DG_TALL_EPI8", 1);
+    c.raster_band = env_int("DG_RASTER_BAND", 16);
+    c.print_configs = env_flag("DG_PRINT_CONFIGS");
+    c.fingerprint = f;
+    c.valid = true;
+  }
+  return c;
 }
 
 dg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
@@ -235,7 +275,7 @@ dg_status encode_b_mn(Operands& o, const void* b, const int32_t* sfb, int64_t n,
 // whole_boxes: only the widths 128 and 256 (MN-major B tiles, other layouts).
 int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, bool with_c,
                    bool pair, bool whole_boxes = false) {
-  const int forced = env_int("DG_BLOCK_N", 0);
+  const int forced = env().block_n;
   if (whole_boxes ? (forced == 128 || forced == 256)
                   : (pair ? gemm2_block_n_supported(forced) : gemm_block_n_supported(forced)))
     return forced;
@@ -270,9 +310,9 @@ int choose_block_n(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots, boo
 // 128-row estimate) by 3%.
 int choose_tall_block_n(int64_t m, int64_t n, int64_t k_blocks, int slots, bool with_c,
                         double best_cost) {
-  const int forced_m = env_int("DG_BLOCK_M", 0);
+  const int forced_m = env().block_m;
   if (forced_m == 128) return 0;
-  const int forced_n = env_int("DG_BLOCK_N", 0);
+  const int forced_n = env().block_n;
   if (forced_m == 256) return (forced_n == 192 || forced_n == 224) ? forced_n : 192;
   if (forced_n != 0) return 0;  // a forced width means 128-row tiles
   static const int widths[2] = {192, 224};
@@ -317,7 +357,7 @@ double dense_tile_cost(int64_t m_blocks, int64_t n, int64_t k_blocks, int slots,
 // device), so the number of 128-row blocks is estimated from the expected
 // count per group: ceil(m / 128) is on average m / 128 + 1/2.
 int choose_block_n_masked_streaming(int64_t groups, int64_t expected_m, int64_t n, int slots) {
-  const int forced = env_int("DG_BLOCK_N", 0);
+  const int forced = env().block_n;
   if (gemm_block_n_supported(forced)) return forced;
   static const int widths[4] = {128, 192, 224, 256};
   const double blocks = (double)groups * ((double)expected_m / kBlockM + 0.5);
@@ -367,8 +407,8 @@ double dense_nt_cost(const DenseTileCost& t, int64_t m, int64_t n, int64_t k_blo
 // single M block takes 128-row tiles.
 void choose_dense_nt_tile(int64_t m, int64_t n, int64_t k_blocks, int slots, bool with_c, int* block_m,
                           int* block_n) {
-  int forced_m = env_int("DG_BLOCK_M", 0);
-  int forced_n = env_int("DG_BLOCK_N", 0);
+  int forced_m = env().block_m;
+  int forced_n = env().block_n;
   if (forced_m == 256 && gemm_tall_stages(forced_n) == 0) forced_n = 0;  // no such 256-row width
   if (forced_n != 0 && forced_m != 256 && gemm_block_n_supported(forced_n)) forced_m = 128;
   const int sms = slots > 0 ? slots : 1;
@@ -398,13 +438,13 @@ void choose_dense_nt_tile(int64_t m, int64_t n, int64_t k_blocks, int slots, boo
 // DG_RASTER_BAND (in 128-row blocks) overrides.
 int raster_band(int64_t m_blocks, int block_m, int64_t k) {
   (void)k;
-  const int band128 = std::max(1, env_int("DG_RASTER_BAND", 16));
+  const int band128 = std::max(1, env().raster_band);
   return (int)std::max<int64_t>(1, std::min<int64_t>(m_blocks, (int64_t)band128 * kBlockM / block_m));
 }
 
 void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups, int block_m,
                   int block_n, int stages, int grid, int band) {
-  if (!env_flag("DG_PRINT_CONFIGS")) return;
+  if (!env().print_configs) return;
   fprintf(stderr, "dg: %s m=%lld n=%lld k=%lld groups=%d block_m=%d block_n=%d stages=%d grid=%d band=%d\n",
           what, (long long)m, (long long)n, (long long)k, groups, block_m, block_n, stages, grid, band);
 }
@@ -463,7 +503,7 @@ DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int
   // Every CTA's K slice (ceil(K blocks / factor) blocks) must be non-empty.
   {
     const int64_t tiles128 = m_blocks * ((n + 127) / 128);
-    const int forced = env_int("DG_SPLIT_K", 0);
+    const int forced = env().split_k;
     if (mode != kDense) p.ksplit = 1;
     else if (forced == 1 || forced == 2 || forced == 4) p.ksplit = forced;
     else if (tiles128 * 4 <= sms && kb >= 16) p.ksplit = 4;
@@ -481,7 +521,7 @@ DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int
   }
   // CTA pairs (256-row tiles) only on request (DG_CTA_PAIR=1): on the
   // measured shapes they match, not beat, single-CTA tiles.
-  p.pair = mode == kDense && sms >= 2 && m_blocks >= 2 && env_int("DG_CTA_PAIR", 0) == 1;
+  p.pair = mode == kDense && sms >= 2 && m_blocks >= 2 && env().cta_pair == 1;
   if (p.pair) {
     const int64_t p_blocks = (m + 2 * kBlockM - 1) / (2 * kBlockM);
     p.block_n = choose_block_n(p_blocks, n, kb, sms / 2, with_c, true);
@@ -501,9 +541,9 @@ DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int
     // contributor writes its 224 KB partial and the MMA waits, ~8 us for the
     // owner's flag wait, partial reads and stores; ~22 K blocks in all.
     // DG_STREAM_K = 0 / 1 disables / forces it where it applies.
-    const int forced_sk = env_int("DG_STREAM_K", -1);
-    const int forced_m = env_int("DG_BLOCK_M", 0), forced_n = env_int("DG_BLOCK_N", 0);
-    if (ws && forced_sk != 0 && env_int("DG_TALL_EPI8", 1) != 0 && forced_m != 128 && sms >= 2) {
+    const int forced_sk = env().stream_k;
+    const int forced_m = env().block_m, forced_n = env().block_n;
+    if (ws && forced_sk != 0 && env().tall_epi8 != 0 && forced_m != 128 && sms >= 2) {
       double cost_dp = 1e300;
       for (const DenseTileCost& t : kDenseTiles)
         if (t.block_m == bm && t.block_n == p.block_n) cost_dp = dense_nt_cost(t, m, n, kb, sms, with_c);
@@ -570,7 +610,7 @@ GroupedPlan plan_masked(int32_t num_groups, int64_t max_m, int64_t n, int64_t k,
   GroupedPlan p;
   // CTA pairs only on request (DG_CTA_PAIR=1); with few valid rows per group
   // the peer's half of the tile is mostly empty.
-  p.pair = sms >= 2 && max_m > kBlockM && env_int("DG_CTA_PAIR", 0) == 1;
+  p.pair = sms >= 2 && max_m > kBlockM && env().cta_pair == 1;
   const int64_t m_est = expected_m > 0 ? expected_m : max_m;
   if (p.pair)
     p.block_n = choose_block_n(((m_est + 2 * kBlockM - 1) / (2 * kBlockM)) * num_groups, n,
@@ -649,7 +689,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
     args.num_groups = 1;
     args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
     args.k_blocks = (int32_t)(k / kBlockK);
-    args.band = env_int("DG_RASTER_BAND", 16);
+    args.band = env().raster_band;
     if (args.band < 1) args.band = 1;
     args.timeout_ns = g_timeout_ns.load();
     args.pdl = g_pdl.load();
@@ -722,7 +762,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
                m, n, k, 1, tall ? 2 * kBlockM : plan.short_a ? kBlockM / 2 : kBlockM, block_n,
                tall ? gemm_tall_stages(block_n) : plan.short_a ? gemm_short_stages(block_n) : gemm_stages(block_n),
                grid, args.band);
-  args.epi8 = (plan.stream_k || env_int("DG_TALL_EPI8", 1) != 0) ? 1 : 0;
+  args.epi8 = (plan.stream_k || env().tall_epi8 != 0) ? 1 : 0;
   if (tall)
     return from_cuda(gemm_tall_launch(kDense, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid,
                                       static_cast<cudaStream_t>(stream)));
@@ -880,7 +920,7 @@ dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b,
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
   args.n_blocks = (int32_t)((n + 127) / 128);
   args.k_blocks = (int32_t)(k / kBlockK);
-  args.band = env_int("DG_RASTER_BAND", 16);
+  args.band = env().raster_band;
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
   args.pdl = g_pdl.load();
@@ -951,7 +991,7 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
   args.num_groups = num_groups;
   args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
   args.k_blocks = (int32_t)(k / kBlockK);
-  args.band = env_int("DG_RASTER_BAND", 16) / (tall ? 2 : 1);
+  args.band = env().raster_band / (tall ? 2 : 1);
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
   args.pdl = g_pdl.load();
@@ -1003,7 +1043,7 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa,
   const int64_t kb_avg = std::max<int64_t>(1, sum_k / kBlockK / num_groups);
   int block_n = 256;
   {
-    const int forced = env_int("DG_BLOCK_N", 0);
+    const int forced = env().block_n;
     if (forced == 128 || forced == 256) {
       block_n = forced;
     } else {
@@ -1041,7 +1081,7 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa,
   args.num_groups = num_groups;
   args.n_blocks = (int32_t)((n + block_n - 1) / block_n);
   args.k_blocks = (int32_t)(sum_k / kBlockK);
-  args.band = env_int("DG_RASTER_BAND", 16);
+  args.band = env().raster_band;
   if (args.band < 1) args.band = 1;
   args.timeout_ns = g_timeout_ns.load();
   args.pdl = g_pdl.load();
