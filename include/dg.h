@@ -64,7 +64,8 @@ typedef enum dg_status {
   DG_ERR_DEVICE_BAD_INDEX = 6,  /* device: m_indices >= num_groups, masked_m outside [0, max_m],
                                    or a contiguous 128-row block mixing experts */
   DG_ERR_TOO_LARGE = 7,         /* a size beyond the supported range */
-  DG_ERR_DEVICE_BAD_SCALE = 8   /* device: an FP32 scale that is not a positive power of two */
+  DG_ERR_DEVICE_BAD_SCALE = 8,  /* device: an FP32 scale that is not a positive power of two */
+  DG_ERR_DEVICE_CHECK = 9       /* device: a bound checked by the debug library failed */
 } dg_status;
 
 typedef enum dg_sf_format {
@@ -397,6 +398,8 @@ dg_status dg_set_wait_timeout_ns(uint64_t ns);
  * current device.  Returns DG_OK or the first recorded DG_ERR_DEVICE_* code.
  * If detail is not NULL it receives the raw word (code in bits 0-7, the
  * recording site in bits 8-23, block index in bits 32-63).  Debug/test use.
+ * Sites 40-45 belong to the debug library's checks (A load, B load, scale
+ * load, TMEM columns, output rows and columns, stream-K slot and K range).
  * The words are one per device and per process, shared by every launch on
  * every stream: the result is only meaningful when no other work of this
  * library is in flight on the device (a kernel still running on another
@@ -413,6 +416,17 @@ dg_status dg_get_device_error(void* stream, uint64_t* detail);
  * DG_ERR_INVALID_ARG.  No counterpart on the pages: it exists to test the
  * library's own bounded waits. */
 dg_status dg_debug_set_drop_load(int32_t k);
+
+/* Test hook for the device checks of the debug build (libdg_debug.so, built
+ * with DG_DEBUG_CHECKS=1), process-wide, off (0) by default.  With on != 0
+ * the next single-CTA dense NT launches (no split-K, no CTA pair) evaluate
+ * the MMA issuer's TMEM-column check as violated: each records
+ * DG_ERR_DEVICE_CHECK at that check's site in the error word (no access
+ * changes, D is still computed), which dg_get_device_error then returns.
+ * The release library has no checks: there on != 0 gives DG_ERR_INVALID_ARG
+ * and on == 0 DG_OK.  No counterpart on the pages: it exists to show that
+ * a failed check reaches the caller. */
+dg_status dg_debug_plant_check(int32_t on);
 
 /* Static description of a status code. */
 const char* dg_status_string(dg_status s);

@@ -8,6 +8,7 @@ weight gradients (FP32 output).  The kernels live in libdg.so
 """
 from .api import (  # noqa: F401
     DGError,
+    debug_plant_check,
     debug_set_drop_load,
     fp8_gemm_nn,
     fp8_gemm_nt,

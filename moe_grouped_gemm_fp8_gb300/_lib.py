@@ -1,14 +1,17 @@
 """ctypes loader for libdg.so (argument marshalling only).
 
 The library is built in-tree by ``moe_grouped_gemm_fp8_gb300.build``; if it
-is missing this module raises instead of falling back to anything else.
+is missing this module raises instead of falling back to anything else.  With
+``DG_DEBUG_LIBRARY=1`` in the environment when the library is first loaded,
+the build with device-side checks (``libdg_debug.so``) is loaded instead.
 """
 import ctypes as C
 import os
 import re
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libdg.so")
+DEBUG = os.environ.get("DG_DEBUG_LIBRARY", "0") not in ("", "0")
+LIB_PATH = os.path.join(HERE, "libdg_debug.so" if DEBUG else "libdg.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "dg.h")
 
 _LIB = None
@@ -17,7 +20,7 @@ DG_OK = 0
 STATUS_NAMES = {
     0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_ALIGNMENT", 3: "DG_ERR_UNSUPPORTED_ARCH",
     4: "DG_ERR_CUDA", 5: "DG_ERR_DEVICE_TIMEOUT", 6: "DG_ERR_DEVICE_BAD_INDEX",
-    7: "DG_ERR_TOO_LARGE", 8: "DG_ERR_DEVICE_BAD_SCALE",
+    7: "DG_ERR_TOO_LARGE", 8: "DG_ERR_DEVICE_BAD_SCALE", 9: "DG_ERR_DEVICE_CHECK",
 }
 DG_SF_FP32 = 0
 DG_SF_UE8M0_PACKED = 1
@@ -56,6 +59,7 @@ SIGNATURES = {
     "dg_set_wait_timeout_ns": (_st, [C.c_uint64]),
     "dg_get_device_error": (_st, [_p, C.POINTER(C.c_uint64)]),
     "dg_debug_set_drop_load": (_st, [_i32]),
+    "dg_debug_plant_check": (_st, [_i32]),
     "dg_status_string": (C.c_char_p, [_st]),
     "dg_version": (_i32, []),
 }
@@ -73,7 +77,7 @@ def lib():
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(
-                "libdg.so is not built (expected at %s); build it with "
+                "%s is not built; build it with "
                 "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
         L = C.CDLL(LIB_PATH)
         for name, (res, args) in SIGNATURES.items():

@@ -148,6 +148,13 @@ def debug_set_drop_load(k: int) -> None:
     _check(_lib.lib().dg_debug_set_drop_load(int(k)), "dg_debug_set_drop_load")
 
 
+def debug_plant_check(on: bool) -> None:
+    """Test hook of the debug library (DG_DEBUG_LIBRARY=1): the next dense NT
+    launches record DG_ERR_DEVICE_CHECK from the MMA issuer's TMEM check.  The
+    release library refuses on=True (it carries no checks)."""
+    _check(_lib.lib().dg_debug_plant_check(1 if on else 0), "dg_debug_plant_check")
+
+
 def get_device_error(stream=None) -> Tuple[int, int]:
     """Synchronises the stream; returns (status, raw word) and clears the word.
     After a timeout the binding's own workspaces are zero-filled again (an

@@ -3,6 +3,12 @@
 Each translation unit is compiled by nvcc for sm_103a in parallel, then
 linked into one shared library next to this file.  No CMake, no torch
 extension machinery: the library has a plain C ABI.
+
+``build(debug=True)`` builds ``libdg_debug.so`` beside it from the same
+sources with ``-DDG_DEBUG_CHECKS=1``: the kernels check their load
+coordinates, TMEM columns, store rows and stream-K slots, and record
+DG_ERR_DEVICE_CHECK with the site in the error word instead of trapping.
+The binding loads it when ``DG_DEBUG_LIBRARY=1``.
 """
 import os
 import subprocess
@@ -14,6 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libdg.so")
+DEBUG_LIB = os.path.join(HERE, "libdg_debug.so")
 
 SOURCES = ["gemm_bn128.cu", "gemm_bn192.cu", "gemm_bn224.cu", "gemm_bn256.cu",
            "gemm2_bn192.cu", "gemm2_bn224.cu", "gemm2_bn256.cu", "gemm_splitk.cu", "gemm_tall.cu", "gemm_promote.cu", "gemm.cu",
@@ -41,13 +48,17 @@ def _stale(lib: str) -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, lineinfo: bool = True) -> str:
-    if not force and not _stale(LIB):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, lineinfo: bool = True, debug: bool = False) -> str:
+    lib = DEBUG_LIB if debug else LIB
+    if not force and not _stale(lib):
+        return lib
+    build_dir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     flags = ARCH + ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                     "--expt-relaxed-constexpr"]
+    if debug:
+        flags.append("-DDG_DEBUG_CHECKS=1")
     if lineinfo:
         flags.append("-lineinfo")
     if verbose:
@@ -55,7 +66,7 @@ def build(force: bool = False, verbose: bool = False, lineinfo: bool = True) -> 
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         objs.append(obj)
         cmd = [nvcc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -70,11 +81,11 @@ def build(force: bool = False, verbose: bool = False, lineinfo: bool = True) -> 
     if failed:
         msg = "\n".join(" ".join(c) + "\n" + t for c, t in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose="-v" in sys.argv))
+    print(build(force=True, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -31,6 +31,19 @@ __device__ __forceinline__ void record_error(unsigned long long* word, uint32_t 
   atomicCAS(word, 0ull, v);
 }
 
+// Device checks of the debug build (compiled with DG_DEBUG_CHECKS=1, the
+// library libdg_debug.so): a violated bound records DG_ERR_DEVICE_CHECK with
+// its site in the error word and never traps.  TMA loads outside a tensor
+// zero-fill and TMA stores clip, so those accesses still happen; row stores
+// the check rejects are skipped.  Compiled out of the release library.
+#ifndef DG_DEBUG_CHECKS
+#define DG_DEBUG_CHECKS 0
+#endif
+#define DG_CHECK(err, cond, site)                                             \
+  do {                                                                        \
+    if (DG_DEBUG_CHECKS && !(cond)) ::dg::record_error((err), DG_ERR_DEVICE_CHECK, (site)); \
+  } while (0)
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -52,6 +52,13 @@ enum ErrorSite : uint32_t {
   kSiteSplitFree = 10,
   kSiteSplitFull = 11,
   kSiteStreamKPartial = 12,
+  // debug-build checks (DG_DEBUG_CHECKS)
+  kSiteCheckLoadA = 40,
+  kSiteCheckLoadB = 41,
+  kSiteCheckScale = 42,
+  kSiteCheckTmem = 43,
+  kSiteCheckStore = 44,
+  kSiteCheckStreamK = 45,
   kSiteContiguousIndex = 16,
   kSiteMaskedCount = 17,
   kSiteKGroupSize = 18,
@@ -83,6 +90,9 @@ struct GemmArgs {
   // skips on its first tile, so that stage's barrier never completes and the
   // bounded waits must end the launch with DG_ERR_DEVICE_TIMEOUT; 0 = off.
   int32_t debug_drop_load;
+  // Test hook (dg_debug_plant_check, debug library only): nonzero makes the
+  // MMA issuer's TMEM check fail on purpose; no access changes.
+  int32_t debug_plant_check;
   // 256-row dense tiles: drain the accumulator with eight epilogue warps
   int32_t epi8;
   // Stream-K (256-row dense tiles with eight epilogue warps; 0 units = off):

@@ -886,6 +886,18 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
             }
             // MN-major tiles ([K, M] / [K, N] storage): 128 K rows of 128 bytes
             // per box; a 256-column B tile is two boxes 16 KB apart
+            if constexpr (DG_DEBUG_CHECKS) {
+              // K block in range; innermost coordinates on 16-byte boundaries;
+              // rows, column tiles and groups inside their tensors
+              DG_CHECK(err, kb >= 0 && kb < args.k_blocks && (kx & 15) == 0, kSiteCheckLoadA);
+              if constexpr (a_mn_major(MODE)) DG_CHECK(err, (my & 15) == 0 && my < args.m, kSiteCheckLoadA);
+              else if (MODE == kContiguous && BM == 2 * kBlockM)
+                DG_CHECK(err, tile.b0 >= 0 && tile.b0 < args.m_blocks && tile.b1 < args.m_blocks, kSiteCheckLoadA);
+              else DG_CHECK(err, my >= 0 && my < args.m, kSiteCheckLoadA);
+              DG_CHECK(err, tile.nb >= 0 && tile.nb * BN < args.n && ((tile.nb * BN) & 7) == 0 &&
+                                (MODE == kKGrouped || (tile.g >= 0 && tile.g < args.num_groups)),
+                       kSiteCheckLoadB);
+            }
             if constexpr (a_mn_major(MODE)) tma_load_2d(sb, &tm_a, fb, my, kx);
             else if (MODE == kMasked) tma_load_3d(sb, &tm_a, fb, kx, my, tile.g);
             else if (MODE == kContiguous && BM == 2 * kBlockM) {
@@ -954,6 +966,9 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
               tc_fence_after();
               sf_tmem = tmem_base + (uint32_t)(P::kSfBase + slot * L::kSfCols);
             }
+            DG_CHECK(err, args.debug_plant_check == 0 && sf_tmem - tmem_base + (uint32_t)L::kSfCols <= 512u &&
+                              d_tmem - tmem_base + (uint32_t)(MH * BN) <= (uint32_t)P::kSfBase,
+                     kSiteCheckTmem);
             const uint32_t sel = (uint32_t)(kb & 3);
             const uint32_t idesc = idesc0 | (sel << 4) | (sel << 29);
             // K-major operands advance 32 bytes per 32-deep K step; MN-major
@@ -1018,6 +1033,9 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
               const uint32_t bar = sffull(slot);
               const int my = ld.tile.mb * BM, kp = ld.kp;
               mbar_arrive_expect_tx(bar, L::kTxSF);
+              DG_CHECK(err, kp >= 0 && kp < (args.k_blocks + 3) / 4 && my >= 0 &&
+                                (MODE == kContiguous && BM == 2 * kBlockM ? ld.tile.b0 < args.m_blocks : my < args.m),
+                       kSiteCheckScale);
               if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
               else if (MODE == kContiguous && BM == 2 * kBlockM) {
                 tma_load_2d(buf + L::kRawA, &tm_sfa, bar, ld.tile.b0 * kBlockM, kp);
@@ -1113,6 +1131,14 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
           const int row0 = tile.mb * BM + hh * kBlockM + quarter * 32;
           const int row = row0 + lane;
           const bool part = SK && tile.kind == kItemPart;  // stream-K: a partial sum for another CTA
+          // the tile's columns start inside N on an 8-column boundary; a
+          // stream-K CTA's slot and flags lie inside the workspace (1024 CTAs
+          // at most) and its K blocks inside the tile's
+          DG_CHECK(err, tile.nb >= 0 && tile.nb * BN < args.n && ((tile.nb * BN) & 7) == 0 && tile.mb >= 0,
+                   kSiteCheckStore);
+          if constexpr (SK)
+            DG_CHECK(err, gridDim.x <= 1024u && tkb0 >= 0 && tkb0 < tkb1 && tkb1 <= args.k_blocks,
+                     kSiteCheckStreamK);
           // stream-K slot of CTA c for this warp's rows: 32 lanes x BN columns,
           // 16 bytes (4 columns) of a lane at ((col / 4) * 32 + lane) * 4 floats
           auto slot = [&](int c) {
@@ -1343,6 +1369,18 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
         } else {
           row_ok = row < group_valid[tile.g];
           out_row0 = (int64_t)tile.g * args.m + row0;
+        }
+        if constexpr (DG_DEBUG_CHECKS) {
+          // rows written lie inside D (G x M rows when grouped); the tile's
+          // columns start inside N on an 8-column boundary
+          const int64_t rows = (MODE == kMasked || MODE == kKGrouped) ? (int64_t)args.num_groups * args.m
+                                                                      : (int64_t)args.m;
+          const bool ok = tile.nb >= 0 && tile.nb * BN < args.n && ((tile.nb * BN) & 7) == 0 &&
+                          (!row_ok || (out_row0 + lane >= 0 && out_row0 + lane < rows));
+          if (!ok) {
+            DG_CHECK(err, false, kSiteCheckStore);
+            row_ok = false;
+          }
         }
         // The TMA store clips at M and N, so dense quarters always use it; a
         // grouped quarter uses it only when every one of its rows is written.

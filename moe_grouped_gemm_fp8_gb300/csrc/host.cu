@@ -27,6 +27,7 @@ std::atomic<int32_t> g_num_sms_limit{0};
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_pdl{0};
 std::atomic<int32_t> g_debug_drop_load{0};  // test hook, see dg_debug_set_drop_load
+std::atomic<int32_t> g_debug_plant_check{0};  // test hook, see dg_debug_plant_check
 
 struct DeviceInfo {
   std::once_flag once;
@@ -749,6 +750,7 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   }
   const int grid = plan.stream_k ? sms : (int)(tiles < sms ? tiles : sms);
   args.debug_drop_load = g_debug_drop_load.load(std::memory_order_relaxed);
+  args.debug_plant_check = g_debug_plant_check.load(std::memory_order_relaxed);
   if (plan.stream_k) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     args.sk_flags = reinterpret_cast<uint32_t*>(ws);
@@ -1242,6 +1244,16 @@ dg_status dg_debug_set_drop_load(int32_t k) {
   return DG_OK;
 }
 
+dg_status dg_debug_plant_check(int32_t on) {
+#if defined(DG_DEBUG_CHECKS) && DG_DEBUG_CHECKS
+  g_debug_plant_check.store(on != 0 ? 1 : 0);
+  return DG_OK;
+#else
+  if (on != 0) return DG_ERR_INVALID_ARG;  // the release kernels carry no checks
+  return DG_OK;
+#endif
+}
+
 dg_status dg_get_device_error(void* stream, uint64_t* detail) {
   if (detail) *detail = 0;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DG_ERR_CUDA;
@@ -1264,6 +1276,7 @@ const char* dg_status_string(dg_status s) {
     case DG_ERR_DEVICE_BAD_INDEX: return "device: group index or masked count out of range";
     case DG_ERR_TOO_LARGE: return "size beyond the supported range";
     case DG_ERR_DEVICE_BAD_SCALE: return "device: scale is not a positive power of two";
+    case DG_ERR_DEVICE_CHECK: return "device: a bound checked by the debug library failed";
   }
   return "unknown status";
 }

@@ -1,6 +1,8 @@
 import os
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -8,6 +10,23 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (sm_103a) and the built CUDA library")
+
+
+DG_ERR_DEVICE_CHECK = 9
+
+
+@pytest.fixture(autouse=True)
+def _device_checks_clean(request):
+    """Under the debug library (DG_DEBUG_LIBRARY=1, kernels built with
+    DG_DEBUG_CHECKS=1) every GPU test also ends with no failed device check:
+    in-range load coordinates, TMEM columns, output rows and stream-K slots."""
+    yield
+    if os.environ.get("DG_DEBUG_LIBRARY", "0") in ("", "0") or request.node.get_closest_marker("gpu") is None:
+        return
+    import moe_grouped_gemm_fp8_gb300 as dg
+    st, word = dg.get_device_error()
+    assert st != DG_ERR_DEVICE_CHECK, "device check failed at site %d in block %d" % (
+        (word >> 8) & 0xFFFF, word >> 32)
 
 
 def pytest_terminal_summary(terminalreporter, exitstatus, config):
