@@ -337,11 +337,17 @@ int32_t dg_get_mk_alignment_for_contiguous_layout(void);
  * with C (has_c != 0) or without, on a device with num_sms SMs (pass the
  * device's SM count, or the dg_set_num_sms limit when one is set).  Pure host
  * arithmetic: no device, no CUDA call.  The DG_BLOCK_M, DG_BLOCK_N, DG_SPLIT_K
- * and DG_CTA_PAIR environment overrides apply as they do to the call.
+ * and DG_CTA_PAIR environment overrides apply as they do to the call, and
+ * DG_DECODE = 0 turns off the decode kernel below.
  * Writes block_m (rows of A per output tile: 64 for the 64-row A slots of a
  * single short M block, 128, or 256), block_n (columns per tile), split_k
  * (CTAs of one cluster sharing each tile's K blocks: 1, 2 or 4) and cta_pair
- * (1 when a 256-row tile spans two CTAs).  All four are 0 for an empty
+ * (1 when a 256-row tile spans two CTAs).  For M <= 128 the call normally
+ * runs the decode kernel, which swaps the operands' roles: 128 rows of B
+ * fill the MMA's 128 lanes and A's rows are its N side; then block_m is the
+ * MMA's token width (32, 64 or 128, at least M), block_n 128 and split_k the
+ * CTAs of a cluster sharing each 128-column strip's K blocks (1, 2, 4 or 8).
+ * All four are 0 for an empty
  * problem.  Errors as dg_fp8_gemm_nt's shape checks; num_sms < 1 or a NULL
  * output gives DG_ERR_INVALID_ARG.  Cited: same page, section "Utilitários e
  * variáveis de ambiente" (DG_PRINT_CONFIGS prints the configuration chosen
@@ -352,10 +358,12 @@ dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, in
 
 /* The tile configuration dg_fp8_gemm_nt_ws chooses when its workspace is
  * large enough: the outputs of dg_plan_fp8_gemm_nt plus stream_k (1 when the
- * K blocks of the last waves are split between SMs).  Same checks. */
+ * K blocks of the last waves are split between SMs) and swap_ab (1 when the
+ * decode kernel with swapped operand roles runs; dg_fp8_gemm_nt makes the
+ * same choice).  Same checks. */
 dg_status dg_plan_fp8_gemm_nt_ws(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,
                                  int32_t* block_m, int32_t* block_n, int32_t* split_k,
-                                 int32_t* cta_pair, int32_t* stream_k);
+                                 int32_t* cta_pair, int32_t* stream_k, int32_t* swap_ab);
 
 /* The same query for the two M-grouped forms: the tile configuration
  * dg_m_grouped_fp8_gemm_nt_contiguous / _masked chooses (block_m 256 when a

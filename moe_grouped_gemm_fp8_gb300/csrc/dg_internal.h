@@ -111,6 +111,31 @@ struct GemmArgs {
   int32_t sfa_ld;          // align(m, 4)
 };
 
+// Arguments of the decode-sized dense NT kernel (gemm_decode.cu): M <= 128
+// rows of A against 128-row strips of B, the strip's K blocks split over a
+// cluster of `split` CTAs.
+struct DecodeArgs {
+  const __nv_bfloat16* c;  // nullable, [m, ldc]
+  __nv_bfloat16* d;        // [m, ldd]
+  int64_t ldc, ldd;        // elements
+  int32_t m, n;
+  int32_t k_blocks;
+  int32_t n_strips;        // ceil(n / 128)
+  uint64_t timeout_ns;
+  unsigned long long* err; // device error word
+  int32_t pdl;             // launched with programmatic stream serialisation
+  int32_t debug_plant_check;  // test hook of the debug library (dg_debug_plant_check)
+  int32_t debug_drop_load;    // test hook (dg_debug_set_drop_load): 1 + the K block CTA 0 leaves unfilled
+};
+
+// gemm_decode.cu: tn = token columns per MMA (32, 64 or 128, >= M), split =
+// CTAs per cluster (1, 2, 4 or 8); each CTA's K range spans at most
+// gemm_decode_max_packs() scale words of 4 K blocks
+cudaError_t gemm_decode_launch(int tn, int split, const CUtensorMap& a, const CUtensorMap& b,
+                               const CUtensorMap& sfa, const CUtensorMap& sfb, DecodeArgs args,
+                               cudaStream_t stream);
+int gemm_decode_max_packs();
+
 // gemm.cu: dispatch over the tile widths compiled in gemm_bn*.cu (single CTA)
 // and gemm2_bn*.cu (CTA pairs, 256-row tiles)
 int gemm_stages(int block_n);

@@ -58,7 +58,7 @@ struct EnvConfig {
   uintptr_t fingerprint = 0;
   bool valid = false;
   int block_m = 0, block_n = 0, split_k = 0, cta_pair = 0, stream_k = -1, tall_epi8 = 1,
-      raster_band = 16;
+      raster_band = 16, decode = 1;
   bool print_configs = false;
 };
 
@@ -81,6 +81,7 @@ const EnvConfig& env() {
     c.stream_k = env_int("DG_STREAM_K", -1);
     c.tall_epi8 = env_int("DG_TALL_EPI8", 1);
     c.raster_band = env_int("DG_RASTER_BAND", 16);
+    c.decode = env_int("DG_DECODE", 1);
     c.print_configs = env_flag("DG_PRINT_CONFIGS");
     c.fingerprint = f;
     c.valid = true;
@@ -454,7 +455,7 @@ void print_config(const char* what, int64_t m, int64_t n, int64_t k, int groups,
 // the SM count (the DG_* overrides apply), shared by the launch and by
 // dg_plan_fp8_gemm_nt.
 struct DensePlan {
-  int ksplit = 1;        // CTAs of a cluster sharing each tile's K blocks (1, 2, 4)
+  int ksplit = 1;        // CTAs of a cluster sharing each tile's K blocks (1, 2, 4; 1-8 for decode)
   int block_n = 128;     // output columns per tile
   bool pair = false;     // 256-row tiles on a pair of CTAs (only on request)
   bool tall = false;     // 256-row tiles on one CTA
@@ -464,7 +465,39 @@ struct DensePlan {
   bool stream_k = false;
   int32_t sk_dp_tiles = 0;
   int64_t sk_units = 0;
+  // decode-sized M: the swapped-operand kernel (tokens on the MMA's N side,
+  // decode_tn of them per MMA; 128-column strips, K split over ksplit CTAs)
+  bool decode = false;
+  int decode_tn = 0;
 };
+
+// Cluster size of the decode kernel for T strips of kb K blocks on `sms` SMs,
+// 0 when none applies.  The kernel runs one CTA per SM (its pipeline takes
+// the SM's shared memory), so the clusters must fit in one wave: T x S <=
+// sms; every CTA's K range must span at most gemm_decode_max_packs() scale
+// words.  Among those, the largest S (the fewest K blocks per CTA: the
+// kernel is bound by how fast each SM streams its part of B).
+// DG_SPLIT_K = 1, 2, 4 or 8 forces a size where it applies.
+// A cluster's CTAs share one GPC (19 SMs on GB300: 152 SMs in 8 GPCs), so
+// at most floor(19 / S) clusters of S CTAs run per GPC at once (measured:
+// 17 clusters of 8 CTAs take two waves on 152 SMs, 17 of 4 one).
+int decode_split(int64_t strips, int64_t kb, int sms) {
+  constexpr int kGpcSms = 19;
+  const int gpcs = sms / kGpcSms > 0 ? sms / kGpcSms : 1;
+  const int forced = env().split_k;
+  int best = 0;
+  for (int s : {1, 2, 4, 8}) {
+    if (s > kb || strips * s > sms || (s > 1 && strips > (int64_t)gpcs * (kGpcSms / s))) break;
+    if (forced != 0 && forced != s) continue;
+    bool fits = true;
+    for (int r = 0; r < s && fits; ++r) {
+      const int64_t k0 = kb * r / s, k1 = kb * (r + 1) / s;
+      fits = ((k1 - 1) >> 2) - (k0 >> 2) + 1 <= gemm_decode_max_packs();
+    }
+    if (fits) best = s;
+  }
+  return best;
+}
 
 // Workspace of a stream-K launch on `sms` CTAs with block_n columns: a fixed
 // 32 KiB of flag words (one per (CTA, epilogue warp), for up to 1024 CTAs, so
@@ -499,6 +532,24 @@ DensePlan plan_dense(int mode, int64_t m, int64_t n, int64_t k, bool with_c, int
   DensePlan p;
   const int64_t kb = k / kBlockK;
   const int64_t m_blocks = (m + kBlockM - 1) / kBlockM;
+  // at most 128 rows of A (NT): the swapped-operand decode kernel unless
+  // DG_DECODE = 0 (or a DG_BLOCK_* override asks for the tiled kernels)
+  if (mode == kDense && m <= kBlockM && env().decode != 0 && env().block_m == 0 && env().block_n == 0) {
+    // Measured on GB300 (M = 64 and 128, the five (N, K) pairs, graph
+    // replays over copies larger than L2): with clusters of 4 or 8 CTAs it
+    // matches or beats the tiled split-K kernels (N = 4096, K = 7168: 12.8 /
+    // 14.9 us against 13.8 / 15.2); with 1 or 2 (many strips) it does not
+    // (N = 7168, K = 2048, M = 128: 11.6 us against 10.9), so those shapes
+    // keep the tiled kernels.  DG_SPLIT_K forces a size.
+    const int s = decode_split((n + 127) / 128, kb, sms);
+    if (s >= 4 || (s > 0 && env().split_k != 0)) {
+      p.decode = true;
+      p.decode_tn = m <= 32 ? 32 : m <= 64 ? 64 : 128;
+      p.ksplit = s;
+      p.block_n = 128;
+      return p;
+    }
+  }
   // Split-K over a cluster of 2 or 4 CTAs when 128-column tiles would leave
   // most SMs idle (decode-sized M); DG_SPLIT_K = 1, 2 or 4 forces a factor.
   // Every CTA's K slice (ceil(K blocks / factor) blocks) must be non-empty.
@@ -667,6 +718,63 @@ static dg_status dense_gemm(int mode, const char* name, const void* a, const int
   DensePlan plan = plan_dense(mode, m, n, k, c != nullptr, sms, workspace != nullptr);
   if (plan.stream_k && workspace_bytes < stream_k_workspace_bytes(sms, plan.block_n))
     plan = plan_dense(mode, m, n, k, c != nullptr, sms, false);  // too small: tile by tile
+  if (plan.decode) {
+    // A [m, k] and B [n, k] K-major; scale words [kp, align4(rows)], boxes of
+    // 8 packs (the most a CTA's K range spans)
+    const int tn = plan.decode_tn;
+    const int64_t kp = (k / kBlockK + 3) / 4;
+    const int packs = gemm_decode_max_packs();
+    Operands o;
+    {
+      uint64_t dims[2] = {(uint64_t)k, (uint64_t)m};
+      uint64_t strides[1] = {(uint64_t)lda};
+      uint32_t box[2] = {(uint32_t)kBlockK, (uint32_t)tn};
+      if ((s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
+        return s;
+    }
+    {
+      uint64_t dims[2] = {(uint64_t)k, (uint64_t)n};
+      uint64_t strides[1] = {(uint64_t)ldb};
+      uint32_t box[2] = {(uint32_t)kBlockK, 128};
+      if ((s = encode(&o.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
+        return s;
+    }
+    {
+      uint64_t dims[2] = {(uint64_t)align4(m), (uint64_t)kp};
+      uint64_t strides[1] = {(uint64_t)(align4(m) * 4)};
+      uint32_t box[2] = {(uint32_t)tn, (uint32_t)packs};
+      if ((s = encode(&o.sfa, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfa, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) != DG_OK)
+        return s;
+    }
+    {
+      uint64_t dims[2] = {(uint64_t)align4(n), (uint64_t)kp};
+      uint64_t strides[1] = {(uint64_t)(align4(n) * 4)};
+      uint32_t box[2] = {128, (uint32_t)packs};
+      if ((s = encode(&o.sfb, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, sfb, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) != DG_OK)
+        return s;
+    }
+    DecodeArgs da = {};
+    da.c = static_cast<const __nv_bfloat16*>(c);
+    da.d = static_cast<__nv_bfloat16*>(d);
+    da.ldc = c ? ldc : 0;
+    da.ldd = ldd;
+    da.m = (int32_t)m;
+    da.n = (int32_t)n;
+    da.k_blocks = (int32_t)(k / kBlockK);
+    da.n_strips = (int32_t)((n + 127) / 128);
+    da.timeout_ns = g_timeout_ns.load();
+    da.pdl = g_pdl.load();
+    da.debug_plant_check = g_debug_plant_check.load(std::memory_order_relaxed);
+    da.debug_drop_load = g_debug_drop_load.load(std::memory_order_relaxed);
+    print_config("fp8_gemm_nt (decode, swapped operands)", m, n, k, 1, tn, 128, tn == 128 ? 3 : 4,
+                 da.n_strips * plan.ksplit, plan.ksplit);
+    return from_cuda(gemm_decode_launch(tn, plan.ksplit, o.a, o.b, o.sfa, o.sfb, da,
+                                        static_cast<cudaStream_t>(stream)));
+  }
   const int ksplit = plan.ksplit;
   GemmArgs args = {};
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
@@ -806,20 +914,21 @@ dg_status dg_fp8_gemm_nt_workspace_size(int64_t m, int64_t n, int64_t k, int32_t
 
 dg_status dg_plan_fp8_gemm_nt_ws(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,
                                  int32_t* block_m, int32_t* block_n, int32_t* split_k,
-                                 int32_t* cta_pair, int32_t* stream_k) {
-  if (!block_m || !block_n || !split_k || !cta_pair || !stream_k) return DG_ERR_INVALID_ARG;
-  *block_m = *block_n = *split_k = *cta_pair = *stream_k = 0;
+                                 int32_t* cta_pair, int32_t* stream_k, int32_t* swap_ab) {
+  if (!block_m || !block_n || !split_k || !cta_pair || !stream_k || !swap_ab) return DG_ERR_INVALID_ARG;
+  *block_m = *block_n = *split_k = *cta_pair = *stream_k = *swap_ab = 0;
   if (m < 0 || num_sms < 1) return DG_ERR_INVALID_ARG;
   dg_status s = check_common_k_n(n, k);
   if (s != DG_OK) return s;
   if (m >= kMaxCoord) return DG_ERR_TOO_LARGE;
   if (m == 0 || n == 0) return DG_OK;
   const DensePlan p = plan_dense(kDense, m, n, k, has_c != 0, num_sms, true);
-  *block_m = (p.pair || p.tall) ? 2 * kBlockM : p.short_a ? kBlockM / 2 : kBlockM;
+  *block_m = p.decode ? p.decode_tn : (p.pair || p.tall) ? 2 * kBlockM : p.short_a ? kBlockM / 2 : kBlockM;
   *block_n = p.block_n;
   *split_k = p.ksplit;
   *cta_pair = p.pair ? 1 : 0;
   *stream_k = p.stream_k ? 1 : 0;
+  *swap_ab = p.decode ? 1 : 0;
   return DG_OK;
 }
 
@@ -834,7 +943,7 @@ dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, in
   if (m >= kMaxCoord) return DG_ERR_TOO_LARGE;
   if (m == 0 || n == 0) return DG_OK;  // nothing is launched
   const DensePlan p = plan_dense(kDense, m, n, k, has_c != 0, num_sms);
-  *block_m = (p.pair || p.tall) ? 2 * kBlockM : p.short_a ? kBlockM / 2 : kBlockM;
+  *block_m = p.decode ? p.decode_tn : (p.pair || p.tall) ? 2 * kBlockM : p.short_a ? kBlockM / 2 : kBlockM;
   *block_n = p.block_n;
   *split_k = p.ksplit;
   *cta_pair = p.pair ? 1 : 0;

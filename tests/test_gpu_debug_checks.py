@@ -21,7 +21,7 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SUITES = ["tests/test_gpu_gemm.py", "tests/test_gpu_stream_k.py", "tests/test_gpu_kgrouped.py",
+SUITES = ["tests/test_gpu_gemm.py", "tests/test_gpu_decode.py", "tests/test_gpu_stream_k.py", "tests/test_gpu_kgrouped.py",
           "tests/test_gpu_layouts.py", "tests/test_gpu_fp32_scales.py", "tests/test_gpu_fault.py"]
 
 PLANTED = r"""

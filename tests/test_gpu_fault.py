@@ -50,8 +50,10 @@ def test_dropped_stage_times_out_and_context_survives():
     P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "after the injected timeout")
 
 
-def test_dropped_stage_in_a_split_k_cluster_times_out_everywhere():
-    """The same hook in a 4-CTA split-K cluster: CTA 0 never finishes its K
+@pytest.mark.parametrize("decode", ["0", "1"], ids=["tiled", "swapped"])
+def test_dropped_stage_in_a_split_k_cluster_times_out_everywhere(decode):
+    """The same hook in a 4-CTA split-K cluster (the tiled kernel, and the
+    decode kernel with swapped operand roles): CTA 0 never finishes its K
     slice, so the other CTAs' waits for its partials expire too; every CTA
     ends by itself, the error word holds a timeout, and the context stays
     usable."""
@@ -65,7 +67,9 @@ def test_dropped_stage_in_a_split_k_cluster_times_out_everywhere():
     dg.set_wait_timeout_ns(2_000_000)  # 2 ms
     dg.debug_set_drop_load(2)
     os.environ["DG_SPLIT_K"] = "4"
+    os.environ["DG_DECODE"] = decode
     try:
+        assert dg.plan_fp8_gemm_nt_ws(M, N, K)["swap_ab"] == (decode == "1")
         dg.fp8_gemm_nt(*dev)
         st, word = dg.get_device_error()
     finally:
@@ -79,5 +83,6 @@ def test_dropped_stage_in_a_split_k_cluster_times_out_everywhere():
         d = dg.fp8_gemm_nt(*dev)
     finally:
         os.environ.pop("DG_SPLIT_K", None)
+        os.environ.pop("DG_DECODE", None)
     assert dg.get_device_error()[0] == 0
     P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "after the injected split-K timeout")

@@ -64,23 +64,54 @@ def test_prefill_shapes_take_the_measured_tiles(has_c):
             assert plan(cfg["m"], cfg["n"], cfg["k"], has_c) == want + (1, False), cfg
 
 
-# decode: split-K over clusters of 4 or 2 where 128-column tiles leave SMs idle,
-# none where they already fill the GPU (N = 24576); 64-row A slots for M = 64
+# decode (M = 64, 128): the swapped-operand kernel where its strips' K blocks
+# split over clusters of 4 (measured faster on GB300), the tiled kernels
+# elsewhere: split-K over 2 where 128-column tiles leave SMs idle, none where
+# they fill the GPU (N = 24576); 64-row A slots for M = 64.
+# (N, K) -> (block_n, split_k, swap_ab)
 DECODE_CHOICE = {
-    (2112, 7168): (128, 4),
-    (24576, 1536): (192, 1),
-    (7168, 16384): (128, 2),
-    (4096, 7168): (128, 4),
-    (7168, 2048): (128, 2),
+    (2112, 7168): (128, 4, True),
+    (24576, 1536): (192, 1, False),
+    (7168, 16384): (128, 2, False),
+    (4096, 7168): (128, 4, True),
+    (7168, 2048): (128, 2, False),
 }
 
 
+def plan_swap(m, n, k, has_c=False, sms=SMS):
+    p = dg.plan_fp8_gemm_nt_ws(m, n, k, has_c, sms)
+    return p["block_m"], p["block_n"], p["split_k"], p["cta_pair"], p["swap_ab"]
+
+
 @pytest.mark.parametrize("m", [64, 128])
-def test_decode_shapes_split_k(m):
+def test_decode_shapes(m):
     with env():
         for cfg in workloads.PREFILL:
-            bn, ks = DECODE_CHOICE[(cfg["n"], cfg["k"])]
+            bn, ks, swap = DECODE_CHOICE[(cfg["n"], cfg["k"])]
+            assert plan_swap(m, cfg["n"], cfg["k"]) == (m if m == 64 else 128, bn, ks, False, swap), cfg
             assert plan(m, cfg["n"], cfg["k"]) == (m if m == 64 else 128, bn, ks, False), cfg
+
+
+def test_decode_split_rules():
+    """The swapped-operand kernel runs one wave of clusters: S CTAs per
+    strip, at most 152 CTAs, at most floor(19 / S) clusters per 19-SM GPC,
+    every CTA's K range within 8 scale words (29 K blocks)."""
+    with env():
+        # 17 strips: 17 clusters of 8 would take two waves, so 4
+        assert plan_swap(64, 2112, 7168)[2:] == (4, False, True)
+        # 8 strips of 7 K blocks: clusters of 8 (each CTA one K block or more)
+        assert plan_swap(32, 1000, 1024)[2:] == (8, False, True) and plan_swap(32, 1000, 1024)[0] == 32
+        # K of 2 blocks: at most 2 CTAs per strip: clusters of 2 are left to the tiled kernels
+        assert plan_swap(64, 1024, 256)[4] is False
+        # 17 strips of 132 K blocks: 4 CTAs would take 33 blocks (9 scale words)
+        # each, 8 would not fit in one wave: the tiled kernels
+        assert plan_swap(64, 2112, 132 * 128)[4] is False
+        # 16 strips of 128 K blocks: clusters of 8, 16 blocks (4 scale words) each
+        assert plan_swap(64, 2048, 16384)[2:] == (8, False, True)
+    with env(DG_SPLIT_K=2):
+        assert plan_swap(64, 7168, 2048)[2:] == (2, False, True)
+    with env(DG_SPLIT_K=8):  # 17 clusters of 8 do not fit in one wave: tiled kernels
+        assert plan_swap(64, 2112, 7168)[4] is False
 
 
 def test_invariants_over_random_shapes():
@@ -91,9 +122,20 @@ def test_invariants_over_random_shapes():
             n = 8 * int(rng.integers(1, 4000))
             k = 128 * int(rng.integers(1, 130))
             sms = int(rng.choice([1, 2, 8, 66, 132, 152]))
-            bm, bn, ks, pair = plan(m, n, k, bool(rng.integers(0, 2)), sms)
+            bm, bn, ks, pair, swap = plan_swap(m, n, k, bool(rng.integers(0, 2)), sms)
             kb = k // 128
             m_blocks = -(-m // 128)
+            if swap:
+                # decode kernel: one wave of clusters of 4 or 8 CTAs, each CTA
+                # at least one K block and at most 8 scale words of them
+                strips = -(-n // 128)
+                assert m <= 128 and bn == 128 and bm == (32 if m <= 32 else 64 if m <= 64 else 128)
+                assert ks in (4, 8) and strips * ks <= sms and ks <= kb and not pair
+                assert strips <= max(1, sms // 19) * (19 // ks)
+                for r in range(ks):
+                    k0, k1 = kb * r // ks, kb * (r + 1) // ks
+                    assert k1 > k0 and ((k1 - 1) >> 2) - (k0 >> 2) + 1 <= 8
+                continue
             assert bn in (128, 192, 224, 256)
             assert ks in (1, 2, 4) and not pair
             if ks > 1:
