@@ -242,6 +242,9 @@ def step_flops(shapes):
 # block_n, split_k, cta_pair).  A launch whose configuration is not listed has
 # no traffic figure (the counters would be stale).
 CAPTURED_TRAFFIC = {
+    # 256 x 192 tiles, eight epilogue warps, 2048-row raster band:
+    # 367.7 MB read + 47.2 MB written
+    (4096, 7168, 16384, False, 256, 192, 1, 0): 367697152 + 47152128,
 }
 
 
@@ -654,6 +657,23 @@ def _time_graph(fns, replays):
     return statistics.median(ts)
 
 
+def _stream_floor_us(nbytes, dev, replays):
+    """Per-launch device time (us) of a plain streaming read of nbytes (a
+    torch sum over an FP32 buffer), timed like the GEMMs: one launch per
+    buffer copy, copies totalling > 2.5x L2, in one CUDA graph.  The per-launch
+    floor of any kernel that reads that many bytes from HBM once (launch gap,
+    ramp-up and drain included), reported next to the memory-bound GEMMs."""
+    n = max(1, nbytes // 4)
+    bufs = [torch.ones(n, dtype=torch.float32, device=dev) for _ in range(_copies_for(nbytes))]
+    outs = [torch.empty((), dtype=torch.float32, device=dev) for _ in bufs]
+    fns = [(lambda b=b, o=o: torch.sum(b, dim=(0,), out=o)) for b, o in zip(bufs, outs)]
+    for f in fns:
+        f()
+    t = _time_graph(fns, replays)
+    del bufs, outs, fns
+    return t * 1e3
+
+
 def build_cases(name, dg, workloads, dev):
     """GEMM-only launch closures of one workload.  Each case owns enough
     copies of its inputs and outputs that the copies together exceed L2
@@ -785,12 +805,17 @@ def measure_config(name, args, dg, workloads, dev, peaks, peak_src, flush):
     for c in cases:
         t = _time_graph(c["fns"], replays)
         t1 = _time_gemm(c["fns"][0], max(3, replays // 3), flush)
-        res.append({"case": c["name"], "us": t * 1e3, "copies": len(c["fns"]),
-                    "tflops": c["flops"] / (t * 1e-3) / 1e12,
-                    "gbs": c["bytes"] / (t * 1e-3) / 1e9,
-                    "frac_fp8_peak": c["flops"] / (t * 1e-3) / 1e12 / fp8_peak,
-                    "frac_hbm": c["bytes"] / (t * 1e-3) / 1e9 / hbm,
-                    "us_isolated_after_flush": t1 * 1e3})
+        r = {"case": c["name"], "us": t * 1e3, "copies": len(c["fns"]),
+             "tflops": c["flops"] / (t * 1e-3) / 1e12,
+             "gbs": c["bytes"] / (t * 1e-3) / 1e9,
+             "frac_fp8_peak": c["flops"] / (t * 1e-3) / 1e12 / fp8_peak,
+             "frac_hbm": c["bytes"] / (t * 1e-3) / 1e9 / hbm,
+             "us_isolated_after_flush": t1 * 1e3}
+        if CONFIG_BOUND[name] == "hbm":
+            fl = _stream_floor_us(c["bytes"], dev, replays)
+            r["stream_floor_us"] = fl
+            r["floor_over_gemm"] = fl / r["us"]
+        res.append(r)
     st, word = dg.get_device_error()
     if st != 0:
         raise RuntimeError("device error: 0x%x" % word)
@@ -813,9 +838,13 @@ def measure_config(name, args, dg, workloads, dev, peaks, peak_src, flush):
                              + len(cases) * max(3, replays // 3),
              "timing": "CUDA-graph replays of one launch per input copy (copies totalling > 2.5x L2), "
                        "median replay time / launches; us_isolated_after_flush: one launch after an L2 flush"}
+    if CONFIG_BOUND[name] == "hbm":
+        entry["stream_floor"] = ("stream_floor_us: a torch sum reading the case's algorithmic bytes, timed the "
+                                 "same way (one launch per copy in a CUDA graph); floor_over_gemm > 1: the GEMM "
+                                 "takes less time than a plain read of its bytes")
     if name == "decode":
-        entry["plans"] = [dict(shape=list(c["shape"]), **dg.plan_fp8_gemm_nt(*c["shape"],
-                                                                                num_sms=torch.cuda.get_device_properties(dev).multi_processor_count))
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        entry["plans"] = [dict(shape=list(c["shape"]), **dg.plan_fp8_gemm_nt_ws(*c["shape"], num_sms=sms))
                           for c in cases]
     del cases
     torch.cuda.empty_cache()
