@@ -95,6 +95,9 @@ struct GemmArgs {
   int32_t debug_plant_check;
   // 256-row dense tiles: drain the accumulator with eight epilogue warps
   int32_t epi8;
+  // C's base and row stride are multiples of 32 bytes: rows of C may be read
+  // with 32-byte loads
+  int32_t c_v8;
   // Stream-K (256-row dense tiles with eight epilogue warps; 0 units = off):
   // tiles [0, sk_dp_tiles) are walked one per CTA per wave, the K blocks of
   // the remaining tiles (sk_units = their count x k_blocks) are shared out

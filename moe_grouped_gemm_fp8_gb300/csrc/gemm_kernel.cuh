@@ -577,6 +577,47 @@ __device__ __forceinline__ void emit_packed_tma(const uint32_t (&p)[16], uint8_t
   }
 }
 
+// 32 columns of row `crow` of C from col0, as BF16 pairs (dst[i] holds
+// columns 2i, 2i + 1); 0 past M or N.  The register-held epilogues fetch C
+// row by row (a lane's own row), so a warp load touches 32 rows: where C's
+// base and row stride are multiples of 32 bytes (args.c_v8) each lane reads
+// a whole 32-byte sector per load, halving the loads of the 16-byte form.
+__device__ __forceinline__ void load_c_row32(uint32_t (&dst)[16], const GemmArgs& args, int crow, int col0) {
+  const __nv_bfloat16* src = args.c + (int64_t)crow * args.ldc + col0;
+  const bool row_ok = crow < args.m;
+  if (args.c_v8) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t* o = dst + 8 * h;
+      if (row_ok && col0 + 16 * h + 16 <= args.n) {
+        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]), "=r"(o[4]), "=r"(o[5]), "=r"(o[6]),
+                       "=r"(o[7])
+                     : "l"(src + 16 * h));
+      } else {
+        // the last 8 columns of a row ending inside this 16-column piece (N % 16 == 8)
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row_ok && col0 + 16 * h < args.n) v = __ldg(reinterpret_cast<const uint4*>(src + 16 * h));
+        o[0] = v.x;
+        o[1] = v.y;
+        o[2] = v.z;
+        o[3] = v.w;
+        o[4] = o[5] = o[6] = o[7] = 0u;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (row_ok && col0 + 8 * q < args.n) v = __ldg(reinterpret_cast<const uint4*>(src + 8 * q));
+      dst[4 * q] = v.x;
+      dst[4 * q + 1] = v.y;
+      dst[4 * q + 2] = v.z;
+      dst[4 * q + 3] = v.w;
+    }
+  }
+}
+
 // C of one 32 x 32 chunk, fetched coalesced (lane l: 16 bytes of rows l/4 + 8i,
 // piece l % 4) into registers, ahead of the chunk's turn; zero past M and N.
 __device__ __forceinline__ void load_c_chunk(uint4 (&cv)[4], const GemmArgs& args, int col0,
@@ -1122,6 +1163,9 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
         uint32_t pk[NCH][16];
         int acc = 0;
         uint32_t acc_phase = 0;
+        // 32 columns of C of one row (this lane's) as BF16 pairs, 0 past M or N
+        auto load_c = [&](uint32_t(&dst)[16], int crow, int col0) { load_c_row32(dst, args, crow, col0); };
+        int c_ready_it = -1;  // the item whose C pk already holds (fetched during the stores before it)
         for (int it = 0;; ++it) {
           Tile tile;
           int tkb0, tkb1;
@@ -1145,21 +1189,9 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
             return args.sk_part + (size_t)c * (size_t)(2 * 4 * BN * 32) + (size_t)(hh * 4 + quarter) * (BN * 32);
           };
           uint32_t* const my_flags = args.sk_flags;  // [grid][8]
-          if (args.c != nullptr && !part) {
+          if (args.c != nullptr && !part && c_ready_it != it) {
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-              const int col0 = tile.nb * BN + ch * 32;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (row < args.m && col0 + 8 * q < args.n)
-                  v = __ldg(reinterpret_cast<const uint4*>(args.c + (int64_t)row * args.ldc + col0 + 8 * q));
-                pk[ch][4 * q] = v.x;
-                pk[ch][4 * q + 1] = v.y;
-                pk[ch][4 * q + 2] = v.z;
-                pk[ch][4 * q + 3] = v.w;
-              }
-            }
+            for (int ch = 0; ch < NCH; ++ch) load_c(pk[ch], row, tile.nb * BN + ch * 32);
           }
           if (!warp_wait<kSuspendHintNs, EPI8>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
           tc_fence_after();
@@ -1261,20 +1293,33 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty(acc));
+          // The next item's C is fetched chunk by chunk into the registers
+          // each chunk of this tile leaves once staged, so its loads run
+          // under the next tile's MMAs instead of after this tile's stores.
+          Tile nt;
+          int nit = it + 1, nkb0, nkb1, nst = -1;
+          if (args.c != nullptr)
+            for (;; ++nit)
+              if ((nst = sched.item(nit, nt, nkb0, nkb1)) != 0) break;
+          const bool prefetch = nst > 0 && !(SK && nt.kind == kItemPart);
+          const int nrow = prefetch ? nt.mb * BM + hh * kBlockM + quarter * 32 + lane : 0;
           if (live) {
             // the contributors' flags go back to zero for the next launch
             if constexpr (SK)
               if (lane == 0)
                 for (int c = (int)blockIdx.x + 1; c < c_end; ++c) st_relaxed_gpu(my_flags + c * 8 + (warp - 4), 0u);
+          }
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) {
-              const int col0 = tile.nb * BN + ch * 32;
-              if (col0 >= args.n) continue;
+          for (int ch = 0; ch < NCH; ++ch) {
+            const int col0 = tile.nb * BN + ch * 32;
+            if (live && col0 < args.n) {
               if (lane == 0) bulk_wait_group_read<0>();  // the staging chunk's previous store has read it
               __syncwarp();
               emit_packed_tma(pk[ch], ebuf, &tm_d, col0, row0, lane);
             }
+            if (prefetch) load_c(pk[ch], nrow, nt.nb * BN + ch * 32);
           }
+          if (prefetch) c_ready_it = nit;
           if (++acc == NUM_ACC) {
             acc = 0;
             acc_phase ^= 1u;
@@ -1294,6 +1339,17 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t n_xchg = 0;  // split-K exchanges of this quarter so far (barrier phases)
+    // C of the tile being drained (see below); with 128 x 256 dense tiles
+    // (one accumulator) the next tile's C is fetched into these registers
+    // chunk by chunk as this tile's chunks are staged, so it lands under the
+    // next tile's MMAs.  (With two accumulators the MMA already runs a tile
+    // ahead; fetching the next C during the stores there measured slower:
+    // 128 x 224 with C on N = 24576, K = 1536, 151 -> 182 us.)
+    constexpr bool kRegHeld = MH == 2 || (NUM_ACC == 1 && MODE != kKGrouped && KSPLIT == 1);
+    constexpr int kPreHalves = (MODE == kDense && MH == 2 && BN == 192) ? 2 : 1;
+    uint4 cpre[BN / 32][4];
+    uint32_t cpk[kPreHalves][BN / 32][16];
+    int c_ready_it = -1;  // the item whose C is already in cpre / cpk
     for (int it = 0;; ++it) {
       Tile tile;
       int tkb0, tkb1;
@@ -1309,33 +1365,33 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
       // epilogue adds the accumulator in place.
       const bool c_ahead =
           is_dense_mode(MODE) && MH == 1 && KSPLIT == 1 && NUM_ACC == 2 && args.c != nullptr;
-      uint4 cpre[BN / 32][4];
-      if (c_ahead) {
+      if (c_ahead && c_ready_it != it) {
         const int crow0 = tile.mb * BM + quarter * 32;
 #pragma unroll
         for (int ch = 0; ch < BN / 32; ++ch) load_c_chunk(cpre[ch], args, tile.nb * BN + ch * 32, crow0, crow0, lane);
       }
-      constexpr bool kRegHeld = MH == 2 || (NUM_ACC == 1 && MODE != kKGrouped && KSPLIT == 1);
-      constexpr int kPreHalves = (MODE == kDense && MH == 2 && BN == 192) ? 2 : 1;
-      uint32_t cpk[kPreHalves][BN / 32][16];
-      if (kRegHeld && is_dense_mode(MODE) && args.c != nullptr) {
+      // the next item, whose C the 128 x 256 dense epilogue fetches during
+      // this tile's stores (into cpk[0][ch] once chunk ch is staged)
+      const bool c_next = is_dense_mode(MODE) && MH == 1 && KSPLIT == 1 && args.c != nullptr && kRegHeld;
+      Tile nt;
+      int nit = it + 1, nst = -1;
+      if (c_next) {
+        int nkb0, nkb1;
+        for (;; ++nit)
+          if ((nst = sched.item(nit, nt, nkb0, nkb1)) != 0) break;
+      }
+      const bool prefetch = c_next && nst > 0;
+      const int nrow0 = prefetch ? nt.mb * BM + quarter * 32 : 0;
+      auto prefetch_c = [&](int ch) {
+        if (!prefetch) return;
+        load_c_row32(cpk[0][ch], args, nrow0 + lane, nt.nb * BN + ch * 32);
+      };
+      if (kRegHeld && is_dense_mode(MODE) && args.c != nullptr && c_ready_it != it) {
 #pragma unroll
         for (int hh = 0; hh < kPreHalves; ++hh) {
           const int crow = tile.mb * BM + hh * kBlockM + quarter * 32 + lane;
 #pragma unroll
-          for (int ch = 0; ch < BN / 32; ++ch) {
-            const int col0 = tile.nb * BN + ch * 32;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v = make_uint4(0u, 0u, 0u, 0u);
-              if (crow < args.m && col0 + 8 * q < args.n)
-                v = __ldg(reinterpret_cast<const uint4*>(args.c + (int64_t)crow * args.ldc + col0 + 8 * q));
-              cpk[hh][ch][4 * q] = v.x;
-              cpk[hh][ch][4 * q + 1] = v.y;
-              cpk[hh][ch][4 * q + 2] = v.z;
-              cpk[hh][ch][4 * q + 3] = v.w;
-            }
-          }
+          for (int ch = 0; ch < BN / 32; ++ch) load_c_row32(cpk[hh][ch], args, crow, tile.nb * BN + ch * 32);
         }
       }
       if (!warp_wait<kSuspendHintNs, EPI8>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull)) break;
@@ -1406,6 +1462,8 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(acc));
           }
+#pragma unroll
+          for (int ch = 0; ch < BN / 32; ++ch) prefetch_c(ch);
           continue;
         }
         const uint32_t taddr =
@@ -1605,7 +1663,10 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) {
               const int col0 = tile.nb * BN + ch * 32;
-              if (col0 >= args.n) continue;
+              if (col0 >= args.n) {
+                prefetch_c(ch);
+                continue;
+              }
               if (!use_tma) {
                 // a contiguous quarter with rows of other groups or padding
                 if (row_ok) store_packed_row(pk[ch], drow + col0, args.n - col0);
@@ -1616,6 +1677,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
               __syncwarp();
               emit_packed_tma(pk[ch], buf, &tm_d, col0, out_row0, lane);
               ++nchunk;
+              prefetch_c(ch);
               if (is_dense_mode(MODE) && MH == 2 && h == 0 && args.c) {
                 // the second half's C of these columns, into the registers just staged
                 const int row1 = row + kBlockM;
@@ -1700,7 +1762,10 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
             if (lane == 0) mbar_arrive(tempty(acc));
           }
           const int col0 = tile.nb * BN + ch * 32;
-          if (col0 >= args.n) continue;
+          if (col0 >= args.n) {
+            prefetch_c(ch);
+            continue;
+          }
           if (MODE == kKGrouped) {
             kgrouped_chunk(cur, col0);
             continue;
@@ -1715,12 +1780,14 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
             if (c_ahead) emit_chunk_tma_c(f, cpre[ch], buf, &tm_d, col0, out_row0, lane);
             else emit_chunk_tma(f, buf, &tm_d, args, col0, out_row0, row0, is_dense_mode(MODE), lane);
             ++nchunk;
+            prefetch_c(ch);
           } else if (row_ok) {
             store_row_chunk(cur, drow + col0, crow ? crow + col0 : nullptr, args.n - col0);
           }
         }
       }  // halves
       if (stop) break;
+      if (prefetch) c_ready_it = nit;
       if (++acc == NUM_ACC) {
         acc = 0;
         acc_phase ^= 1u;

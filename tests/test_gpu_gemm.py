@@ -549,3 +549,41 @@ def test_dense_split_k_exact_and_deterministic(ks):
     assert np.array_equal(first, want)
     assert np.array_equal(first, again)
     _no_device_error()
+
+
+@pytest.mark.parametrize("tile", [(128, 256), (256, 192), (256, 224)], ids=["128x256", "256x192", "256x224"])
+@pytest.mark.parametrize("c_layout", ["sector_aligned", "offset_16_bytes"])
+@pytest.mark.parametrize("M,N,K", [(300, 392, 512), (520, 1000, 1024)])
+def test_c_row_loads(tile, c_layout, M, N, K):
+    """The register-held epilogues read C row by row, with 32-byte loads when
+    C's base and row stride are multiples of 32 bytes and 16-byte ones
+    otherwise; N % 16 == 8 leaves a last 8-column piece per row.  Both forms,
+    several tiles per CTA (the next tile's C is fetched during the current
+    tile's stores), against the oracle."""
+    w = workloads.dense(M, N, K, seed=3 * M + N, with_c=True)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    o = oracle.gemm_nt(qa, sa, qb, sb, P.bf16_bits(w.c))
+    if c_layout == "sector_aligned":
+        cbuf = torch.zeros(M, N + 8, dtype=torch.bfloat16, device="cuda")  # row stride a multiple of 32 bytes
+        c = cbuf[:, :N]
+    else:
+        cbuf = torch.zeros(M, N + 24, dtype=torch.bfloat16, device="cuda")
+        c = cbuf[:, 8:8 + N]  # base 16 bytes past a 32-byte boundary
+    c.copy_(w.c.cuda())
+    old = {k: os.environ.get(k) for k in ("DG_BLOCK_M", "DG_BLOCK_N")}
+    os.environ["DG_BLOCK_M"], os.environ["DG_BLOCK_N"] = str(tile[0]), str(tile[1])
+    dg.set_num_sms(2)  # several tiles per CTA
+    try:
+        assert (dg.plan_fp8_gemm_nt(M, N, K, True, 2)["block_m"], dg.plan_fp8_gemm_nt(M, N, K, True, 2)["block_n"]) == tile
+        d = dg.fp8_gemm_nt(P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb),
+                           P.dev_packed_sf(sb, N, K, 128), c=c)
+        _no_device_error()
+    finally:
+        dg.set_num_sms(0)
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    P.assert_close(P.bf16_to_f64(d), o, "C row loads %s %s %dx%dx%d" % (tile, c_layout, M, N, K))

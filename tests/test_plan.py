@@ -49,7 +49,7 @@ def plan(m, n, k, has_c=False, sms=SMS):
 # in turn; 256-row tiles drain their accumulator with eight epilogue warps
 PREFILL_CHOICE = {
     (2112, 7168, False): (128, 256), (2112, 7168, True): (128, 256),
-    (24576, 1536, False): (256, 224), (24576, 1536, True): (128, 224),
+    (24576, 1536, False): (256, 224), (24576, 1536, True): (256, 224),
     (7168, 16384, False): (256, 192), (7168, 16384, True): (256, 192),
     (4096, 7168, False): (256, 224), (4096, 7168, True): (256, 224),
     (7168, 2048, False): (256, 192), (7168, 2048, True): (256, 192),
