@@ -1015,9 +1015,10 @@ dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b,
     if ((s = encode(&o.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a, dims_a, str_a, box,
                     CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
       return s;
+    // B tiles of 256 rows (the promotion kernel's 128 x 256 output tiles)
     uint64_t dims_b[3] = {(uint64_t)k, (uint64_t)n, 1};
     uint64_t str_b[2] = {(uint64_t)ldb, (uint64_t)(n * ldb)};
-    uint32_t box_b[3] = {(uint32_t)kBlockK, 128, 1};
+    uint32_t box_b[3] = {(uint32_t)kBlockK, 256, 1};
     if ((s = encode(&o.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, b, dims_b, str_b, box_b,
                     CU_TENSOR_MAP_SWIZZLE_128B)) != DG_OK)
       return s;
@@ -1033,7 +1034,7 @@ dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b,
   args.k = (int32_t)k;
   args.num_groups = 1;
   args.m_blocks = (int32_t)((m + kBlockM - 1) / kBlockM);
-  args.n_blocks = (int32_t)((n + 127) / 128);
+  args.n_blocks = (int32_t)((n + 255) / 256);
   args.k_blocks = (int32_t)(k / kBlockK);
   args.band = env().raster_band;
   if (args.band < 1) args.band = 1;
@@ -1045,7 +1046,7 @@ dg_status dg_fp8_gemm_nt_fp32_sf(const void* a, const float* sfa, const void* b,
   const int64_t tiles = (int64_t)args.m_blocks * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  print_config("fp8_gemm_nt_fp32_sf (promotion)", m, n, k, 1, kBlockM, 128, gemm_promote_stages(), grid,
+  print_config("fp8_gemm_nt_fp32_sf (promotion)", m, n, k, 1, kBlockM, 256, gemm_promote_stages(), grid,
                args.band);
   return from_cuda(gemm_promote_launch(o.a, o.b, o.d, args, grid, static_cast<cudaStream_t>(stream)));
 }
