@@ -30,8 +30,15 @@ def _check(status: int, what: str) -> None:
         raise DGError(status, what)
 
 
+# The current stream's raw handle without building a torch.cuda.Stream object
+# (which costs ~3 us per call on the Grace host).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> C.c_void_p:
     if stream is None:
+        if _raw_stream is not None:
+            return C.c_void_p(_raw_stream(torch.cuda.current_device()))
         stream = torch.cuda.current_stream()
     if isinstance(stream, torch.cuda.Stream):
         return C.c_void_p(stream.cuda_stream)
@@ -124,6 +131,9 @@ def plan_m_grouped_fp8_gemm_nt_masked(num_groups: int, max_m: int, n: int, k: in
 
 def set_num_sms(n: int) -> None:
     _check(_lib.lib().dg_set_num_sms(int(n)), "dg_set_num_sms")
+    # the binding's workspaces are sized for the SM count (a fresh one has
+    # its flags zeroed; the old ones are released stream-ordered)
+    _WORKSPACES.clear()
 
 
 def get_num_sms() -> int:
@@ -289,18 +299,22 @@ def _new_workspace(nbytes: int, device) -> torch.Tensor:
     return ws
 
 
-def _cached_workspace(nbytes: int, stream_handle, device) -> torch.Tensor:
-    """The binding's workspace for this device and stream (its handle),
-    grown to nbytes.  While a CUDA graph is being captured a fresh one is
-    taken from the graph's memory pool instead (its flag words are zeroed by
-    a captured memset, so every replay starts from zero flags)."""
-    if torch.cuda.is_current_stream_capturing():
-        return _new_workspace(nbytes, device)
+# The widest 256-row tile the stream-K form uses; the binding's own workspace
+# holds a partial slot of 256 x this many floats per SM, the most any call
+# can ask for, so a call needs no query to decide (dg_fp8_gemm_nt_ws plans
+# with it and takes stream-K only where that is faster).
+_WS_MAX_BLOCK_N = 224
+
+
+def _stream_workspace(stream_handle, device) -> torch.Tensor:
+    """The binding's workspace for this device and stream (its handle), of
+    the largest size a stream-K launch on the current SM count can use
+    (about 35 MB on 152 SMs); created with zeroed flags on first use."""
     key = (device.index, stream_handle or 0)
     ws = _WORKSPACES.get(key)
-    if ws is None or ws.numel() < nbytes:
-        ws = _new_workspace(nbytes, device)
-        _WORKSPACES[key] = ws
+    if ws is None:
+        nbytes = WORKSPACE_FLAG_BYTES + get_num_sms() * 2 * 128 * _WS_MAX_BLOCK_N * 4
+        ws = _WORKSPACES[key] = _new_workspace(nbytes, device)
     return ws
 
 
@@ -340,24 +354,32 @@ def fp8_gemm_nt(a: torch.Tensor, sfa: torch.Tensor, b: torch.Tensor, sfb: torch.
     st = _stream(stream)
     ws = None
     if workspace is None:
-        need = fp8_gemm_nt_workspace_size(m, n, k, c is not None)
-        if need:
-            ws = _cached_workspace(need, st.value, d.device)
+        if torch.cuda.is_current_stream_capturing():
+            # a captured call gets its own workspace from the graph's pool,
+            # only when its plan uses one
+            need = fp8_gemm_nt_workspace_size(m, n, k, c is not None)
+            if need:
+                ws = _new_workspace(need, d.device)
+        else:
+            ws = _stream_workspace(st.value, d.device)
     elif workspace is not False:
         _need(workspace, "workspace", (torch.uint8,), 1)
         _on_current_device(stream, workspace)
         ws = workspace
+    # pointers go to ctypes as plain ints (the argtypes are void*)
+    cp = c.data_ptr() if c is not None else None
+    ldc = c.stride(0) if c is not None else 0
     if ws is None:
-        rc = _lib.lib().dg_fp8_gemm_nt(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
-                                       m, n, k, a.stride(0), b.stride(0),
-                                       c.stride(0) if c is not None else 0, d.stride(0), st)
-        _check(rc, "dg_fp8_gemm_nt")
+        rc = _lib.lib().dg_fp8_gemm_nt(a.data_ptr(), sfa.data_ptr(), b.data_ptr(), sfb.data_ptr(), cp,
+                                       d.data_ptr(), m, n, k, a.stride(0), b.stride(0), ldc, d.stride(0), st)
+        if rc:
+            _check(rc, "dg_fp8_gemm_nt")
     else:
-        rc = _lib.lib().dg_fp8_gemm_nt_ws(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(d),
-                                          m, n, k, a.stride(0), b.stride(0),
-                                          c.stride(0) if c is not None else 0, d.stride(0), _ptr(ws),
-                                          ws.numel(), st)
-        _check(rc, "dg_fp8_gemm_nt_ws")
+        rc = _lib.lib().dg_fp8_gemm_nt_ws(a.data_ptr(), sfa.data_ptr(), b.data_ptr(), sfb.data_ptr(), cp,
+                                          d.data_ptr(), m, n, k, a.stride(0), b.stride(0), ldc, d.stride(0),
+                                          ws.data_ptr(), ws.numel(), st)
+        if rc:
+            _check(rc, "dg_fp8_gemm_nt_ws")
     return d
 
 
