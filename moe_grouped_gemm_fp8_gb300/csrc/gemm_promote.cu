@@ -254,25 +254,31 @@ __global__ void __launch_bounds__(kPromoteThreads, 1)
           tc_fence_after();
           const uint32_t taddr =
               tmem_base + (pk % NB) * BN + colh * HC + ((uint32_t)(quarter * 32) << 16);
-          // 128 columns in two rounds of 64 (two loads in flight, one wait)
+          // 128 columns as four 32-column loads through two register sets:
+          // the third and fourth loads are issued while the first two
+          // chunks are being added, so the buffer goes back after two load
+          // latencies and half the FMAs
+          uint32_t ra[32], rb[32];
+          tc_ld_32x32b_x32(taddr, ra);
+          tc_ld_32x32b_x32(taddr + 32, rb);
+          tc_wait_ld_regs(ra);
+          tc_wait_ld_regs(rb);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t ra[32], rb[32];
-            tc_ld_32x32b_x32(taddr + h * 64, ra);
-            tc_ld_32x32b_x32(taddr + h * 64 + 32, rb);
-            tc_wait_ld_regs(ra);
-            tc_wait_ld_regs(rb);
-            if (h == 1) {
-              // the partial is in registers: hand the buffer back
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(pempty(pk % NB));
-            }
+          for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(ra[i]), s, acc[i]);
+          tc_ld_32x32b_x32(taddr + 64, ra);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[h * 64 + i] = fmaf(__uint_as_float(ra[i]), s, acc[h * 64 + i]);
+          for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(__uint_as_float(rb[i]), s, acc[32 + i]);
+          tc_ld_32x32b_x32(taddr + 96, rb);
+          tc_wait_ld_regs(ra);
+          tc_wait_ld_regs(rb);
+          // the partial is in registers: hand the buffer back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(pempty(pk % NB));
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[h * 64 + 32 + i] = fmaf(__uint_as_float(rb[i]), s, acc[h * 64 + 32 + i]);
-          }
+          for (int i = 0; i < 32; ++i) acc[64 + i] = fmaf(__uint_as_float(ra[i]), s, acc[64 + i]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[96 + i] = fmaf(__uint_as_float(rb[i]), s, acc[96 + i]);
           ++pk;
         }
       }
