@@ -197,3 +197,26 @@ def test_tensors_must_be_on_the_current_device(monkeypatch):
     api._on_current_device(None, On(1), None, On(1))           # all on cuda:1: accepted
     with pytest.raises(ValueError, match="current CUDA device is cuda:1"):
         api._on_current_device(None, On(1), On(0))
+
+
+def test_debug_library_exports_the_same_abi(L):
+    """libdg_debug.so (the same sources with device-side checks) exports the
+    same functions; its check hook is accepted, the release library's
+    refuses to be switched on (it has no checks to plant into)."""
+    import shutil
+    import subprocess
+    from moe_grouped_gemm_fp8_gb300 import build
+    path = build.build(debug=True)
+    D = C.CDLL(path)
+    for n in _lib.header_functions():
+        assert hasattr(D, n), n
+    nm = shutil.which("nm")
+    if nm is not None:
+        out = subprocess.run([nm, "-D", "--defined-only", path], capture_output=True, text=True,
+                             check=True).stdout
+        exported = sorted({line.split()[-1] for line in out.splitlines()
+                           if line.split() and line.split()[-1].startswith("dg_")})
+        assert exported == _lib.header_functions()
+    D.dg_debug_plant_check.argtypes = [C.c_int32]
+    assert D.dg_debug_plant_check(1) == DG_OK and D.dg_debug_plant_check(0) == DG_OK
+    assert L.dg_debug_plant_check(1) == INVALID and L.dg_debug_plant_check(0) == DG_OK
