@@ -330,8 +330,17 @@ dg_status dg_transform_sf(const float* sf, int32_t* packed, int64_t groups, int6
 /* x rounded up so that x * element_size is a multiple of 16 bytes. */
 int64_t dg_get_tma_aligned_size(int64_t x, int32_t element_size);
 
-/* Row alignment of each expert segment in the contiguous layout: 128. */
+/* Row alignment of each expert segment in the contiguous layouts (the
+ * M-grouped contiguous form along M, the K-grouped form along K): 128 unless
+ * set.  dg_set_mk_alignment_for_contiguous_layout sets the value the getter
+ * returns, process-wide, for callers that lay their segments out by it: a
+ * positive multiple of 128 up to 4096 (the kernels work on 128-row blocks,
+ * so they accept any such multiple; 256, for instance, lets the contiguous
+ * form's 256-row tiles pair every block with one of the same expert),
+ * anything else gives DG_ERR_INVALID_ARG and changes nothing.  Cited: same
+ * section (get / set_mk_alignment_for_contiguous_layout). */
 int32_t dg_get_mk_alignment_for_contiguous_layout(void);
+dg_status dg_set_mk_alignment_for_contiguous_layout(int32_t alignment);
 
 /* The tile configuration dg_fp8_gemm_nt chooses for an M x N x K problem,
  * with C (has_c != 0) or without, on a device with num_sms SMs (pass the

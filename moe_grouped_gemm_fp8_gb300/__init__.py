@@ -18,6 +18,7 @@ from .api import (  # noqa: F401
     fp8_gemm_tt,
     get_device_error,
     get_mk_alignment_for_contiguous_layout,
+    set_mk_alignment_for_contiguous_layout,
     get_num_sms,
     get_pdl,
     get_tma_aligned_size,

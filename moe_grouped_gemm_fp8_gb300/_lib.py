@@ -49,6 +49,7 @@ SIGNATURES = {
     "dg_transform_sf": (_st, [_p, _p, _i64, _i64, _i64, _i32, _p]),
     "dg_get_tma_aligned_size": (_i64, [_i64, _i32]),
     "dg_get_mk_alignment_for_contiguous_layout": (_i32, []),
+    "dg_set_mk_alignment_for_contiguous_layout": (_st, [_i32]),
     "dg_plan_fp8_gemm_nt": (_st, [_i64, _i64, _i64, _i32, _i32, _p, _p, _p, _p]),
     "dg_plan_m_grouped_fp8_gemm_nt_contiguous": (_st, [_i64, _i64, _i64, _i32, _i32, _p, _p]),
     "dg_plan_m_grouped_fp8_gemm_nt_masked": (_st, [_i32, _i64, _i64, _i64, _i64, _i32, _p, _p, _p]),

@@ -81,6 +81,12 @@ def get_mk_alignment_for_contiguous_layout() -> int:
     return int(_lib.lib().dg_get_mk_alignment_for_contiguous_layout())
 
 
+def set_mk_alignment_for_contiguous_layout(alignment: int) -> None:
+    """A positive multiple of 128 up to 4096 (the value the getter returns)."""
+    _check(_lib.lib().dg_set_mk_alignment_for_contiguous_layout(int(alignment)),
+           "dg_set_mk_alignment_for_contiguous_layout")
+
+
 def plan_fp8_gemm_nt(m: int, n: int, k: int, has_c: bool = False, num_sms: int = 152) -> dict:
     """The tile configuration fp8_gemm_nt chooses for an M x N x K problem on
     a device with num_sms SMs, computed on the host (no GPU needed):

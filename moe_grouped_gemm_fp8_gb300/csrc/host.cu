@@ -28,6 +28,7 @@ std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_pdl{0};
 std::atomic<int32_t> g_debug_drop_load{0};  // test hook, see dg_debug_set_drop_load
 std::atomic<int32_t> g_debug_plant_check{0};  // test hook, see dg_debug_plant_check
+std::atomic<int32_t> g_mk_alignment{kBlockM};  // dg_set_mk_alignment_for_contiguous_layout
 
 struct DeviceInfo {
   std::once_flag once;
@@ -1321,7 +1322,13 @@ int64_t dg_get_tma_aligned_size(int64_t x, int32_t element_size) {
   return (x + unit - 1) / unit * unit;
 }
 
-int32_t dg_get_mk_alignment_for_contiguous_layout(void) { return kBlockM; }
+int32_t dg_get_mk_alignment_for_contiguous_layout(void) { return g_mk_alignment.load(); }
+
+dg_status dg_set_mk_alignment_for_contiguous_layout(int32_t alignment) {
+  if (alignment <= 0 || alignment % kBlockM != 0 || alignment > 4096) return DG_ERR_INVALID_ARG;
+  g_mk_alignment.store(alignment);
+  return DG_OK;
+}
 
 dg_status dg_set_num_sms(int32_t n) {
   if (n < 0) return DG_ERR_INVALID_ARG;

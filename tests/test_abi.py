@@ -220,3 +220,19 @@ def test_debug_library_exports_the_same_abi(L):
     D.dg_debug_plant_check.argtypes = [C.c_int32]
     assert D.dg_debug_plant_check(1) == DG_OK and D.dg_debug_plant_check(0) == DG_OK
     assert L.dg_debug_plant_check(1) == INVALID and L.dg_debug_plant_check(0) == DG_OK
+
+
+def test_mk_alignment_setter(L):
+    """set_mk_alignment_for_contiguous_layout: positive multiples of 128 up to
+    4096; anything else is refused and leaves the value unchanged."""
+    assert L.dg_get_mk_alignment_for_contiguous_layout() == 128
+    try:
+        assert L.dg_set_mk_alignment_for_contiguous_layout(256) == DG_OK
+        assert L.dg_get_mk_alignment_for_contiguous_layout() == 256
+        for bad in (0, -128, 64, 100, 192, 4096 + 128):
+            assert L.dg_set_mk_alignment_for_contiguous_layout(bad) == INVALID, bad
+            assert L.dg_get_mk_alignment_for_contiguous_layout() == 256
+        assert L.dg_set_mk_alignment_for_contiguous_layout(4096) == DG_OK
+    finally:
+        assert L.dg_set_mk_alignment_for_contiguous_layout(128) == DG_OK
+    assert L.dg_get_mk_alignment_for_contiguous_layout() == 128

@@ -587,3 +587,42 @@ def test_c_row_loads(tile, c_layout, M, N, K):
             else:
                 os.environ[k] = v
     P.assert_close(P.bf16_to_f64(d), o, "C row loads %s %s %dx%dx%d" % (tile, c_layout, M, N, K))
+
+
+@pytest.mark.parametrize("bn", [(0, 128), (0, 224)], ids=["cta128", "cta224"])
+@pytest.mark.parametrize("tall", [False, True], ids=["128row", "256row"])
+def test_contiguous_layout_aligned_to_the_set_alignment(bn, tall):
+    """Segments padded to the alignment the setter chose (256 here): the
+    kernels work on 128-row blocks, so any multiple of 128 is a valid
+    contiguous layout; routing and values as with 128."""
+    dg.set_mk_alignment_for_contiguous_layout(256)
+    try:
+        align = dg.get_mk_alignment_for_contiguous_layout()
+        assert align == 256
+        G, N, K = 4, 264, 512
+        w = workloads.contiguous(G, N, K, seed=91, counts=[100, 0, 300, 256], align=align)
+        assert all(int(p) % 256 == 0 for p in w.padded)
+        qa, _, sa = P.quantize(w.a, 1)
+        qb, _, sb = P.quantize(w.b, 128)
+        m_sum = w.a.shape[0]
+        dev = (P.dev_codes(qa), P.dev_packed_sf(sa, m_sum, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+        mi = w.m_indices.numpy()
+        o, written = oracle.gemm_contiguous(qa, sa, qb, sb, mi)
+        d = P.sentinel_like((m_sum, N))
+        old = os.environ.get("DG_BLOCK_M")
+        os.environ["DG_BLOCK_M"] = "256" if tall else "128"
+        try:
+            with block_n(bn if not tall else (None, 224)):
+                dg.m_grouped_fp8_gemm_nt_contiguous(*dev, w.m_indices.cuda(), d=d)
+        finally:
+            if old is None:
+                os.environ.pop("DG_BLOCK_M", None)
+            else:
+                os.environ["DG_BLOCK_M"] = old
+        bits = P.bf16_bits(d)
+        wr = written.astype(bool)
+        assert (bits[~wr] == P.SENTINEL_BITS).all(), "padding rows were written"
+        P.assert_close(P.bf16_to_f64(d)[wr], o[wr], "contiguous, 256-row alignment")
+        _no_device_error()
+    finally:
+        dg.set_mk_alignment_for_contiguous_layout(128)
