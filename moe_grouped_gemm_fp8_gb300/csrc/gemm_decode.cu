@@ -431,7 +431,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int i = issued - STAGES < 0 ? 0 : issued - STAGES; i < issued; ++i)
       dec_drain(full(i % STAGES), (uint32_t)(i / STAGES) & 1u, tmo, err, kSiteProducerDrain);
   }
-  if constexpr (S > 1) cluster_wait_acquire();
+  if constexpr (S > 1) {
+    cluster_wait_acquire();
+    // Normally this CTA has received every partial sent to it (its recv wait
+    // completed).  After an abort it may not have: the other CTAs issued
+    // their st.async before arriving at the barrier just passed, but nothing
+    // orders their landing before it.  Wait for them, briefly: a peer that
+    // sent lands within microseconds, one that did not send never will.
+    if (threadIdx.x == 0 && *abort_flag)
+      dec_drain(recv_full, 0, tmo < 1000000u ? tmo : 1000000u, err, kSiteSplitFull);
+  }
 }
 
 template <int TN, int S>
