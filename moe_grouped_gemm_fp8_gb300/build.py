@@ -23,7 +23,7 @@ LIB = os.path.join(HERE, "libdg.so")
 DEBUG_LIB = os.path.join(HERE, "libdg_debug.so")
 
 SOURCES = ["gemm_bn128.cu", "gemm_bn192.cu", "gemm_bn224.cu", "gemm_bn256.cu",
-           "gemm2_bn192.cu", "gemm2_bn224.cu", "gemm2_bn256.cu", "gemm_splitk.cu", "gemm_tall.cu", "gemm_promote.cu", "gemm_decode.cu", "gemm.cu",
+           "gemm2_bn192.cu", "gemm2_bn224.cu", "gemm2_bn256.cu", "gemm_splitk.cu", "gemm_tall.cu", "gemm_promote.cu", "gemm_decode.cu", "gemm_kgrouped.cu", "gemm.cu",
            "quant.cu", "host.cu", "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

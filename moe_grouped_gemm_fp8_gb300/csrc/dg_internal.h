@@ -213,6 +213,12 @@ DG_DECLARE_GEMM_BN(224)
 DG_DECLARE_GEMM_BN(256)
 #undef DG_DECLARE_GEMM_BN
 
+// gemm_kgrouped.cu: K-grouped 128 x 256 tiles with eight epilogue warps
+// (args.err must already be set)
+cudaError_t gemm_kgrouped_epi8_launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sfa,
+                                      const CUtensorMap& sfb, const CUtensorMap& d, const GemmArgs& args,
+                                      int grid, cudaStream_t stream);
+
 // quant.cu
 cudaError_t quantize_launch(const float* x, void* q, void* sf, int64_t groups, int64_t rows,
                             int64_t cols, int block_rows, int sf_format, bool pdl,

@@ -51,6 +51,8 @@ cudaError_t gemm_launch(int mode, int block_n, const CUtensorMap& a, const CUten
   cudaError_t e = error_word_address(&err);
   if (e != cudaSuccess) return e;
   args.err = err;
+  if (mode == kKGrouped && block_n == 256 && args.epi8)
+    return gemm_kgrouped_epi8_launch(a, b, sfa, sfb, d, args, grid, stream);
   switch (block_n) {
     case 128: return gemm_launch_bn128(mode, a, b, sfa, sfb, d, args, grid, stream);
     case 192: return gemm_launch_bn192(mode, a, b, sfa, sfb, d, args, grid, stream);

@@ -686,8 +686,9 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   constexpr int NUM_ACC = P::kNumAcc;
   constexpr int MH = L::kMH;  // 128-row halves of a tile
   static_assert(KSPLIT == 1 || MODE == kDense, "split-K is for the dense form");
-  static_assert(!EPI8 || (BM == 2 * kBlockM && MODE == kDense && NUM_ACC == 1),
-                "eight epilogue warps: 256-row dense tiles with one accumulator");
+  static_assert(!EPI8 || (NUM_ACC == 1 && ((BM == 2 * kBlockM && MODE == kDense) ||
+                                            (BM == kBlockM && MODE == kKGrouped && BN == 256))),
+                "eight epilogue warps: 256-row dense tiles, or 128 x 256 K-grouped tiles, with one accumulator");
   static_assert(!SK || EPI8, "stream-K: 256-row dense tiles with eight epilogue warps");
   static_assert(BM == kBlockM || (BM == 2 * kBlockM && (MODE == kDense || MODE == kContiguous) && KSPLIT == 1) ||
                     (BM == kBlockM / 2 && MODE == kDense),
@@ -1154,7 +1155,106 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     // before the accumulator is ready) added and the sum rounded to BF16 in
     // registers; TMEM goes back to the MMA as soon as all eight warps have
     // read their rows, and only then are the chunks staged and TMA-stored.
-    {
+    if constexpr (MODE == kKGrouped) {
+      // K-grouped 128 x 256 FP32 tiles: warp w drains lane quarter (w & 3),
+      // columns [(w - 4) / 4 * 128, +128): four TMEM loads into 128 registers,
+      // TMEM goes back to the MMA, then the columns (+ C) are stored, each
+      // 16 x 32 box through the warp's staging chunk.  A quarter whose rows
+      // cross M (into the next expert's rows) is stored row by row.
+      if (warp >= 4) {
+        const int quarter = warp & 3;
+        const int chalf = (warp - 4) >> 2;
+        uint8_t* ebuf = epi_smem + (warp - 4) * kEpiBuf;
+        const uint32_t my_row_off = (uint32_t)lane * 64u;
+        const uint32_t my_swz = ((uint32_t)lane >> 1) & 3u;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int it = 0;; ++it) {
+          Tile tile;
+          int tkb0, tkb1;
+          const int st_it = sched.item(it, tile, tkb0, tkb1);
+          if (st_it < 0) break;
+          if (st_it == 0) continue;
+          const int row0 = tile.mb * kBlockM + quarter * 32;
+          const int row = row0 + lane;
+          const bool row_ok = row < args.m;
+          const int64_t out_row0 = (int64_t)tile.g * args.m + row0;
+          const bool k_empty = tkb0 >= tkb1;
+          const int ncol0 = tile.nb * BN + chalf * 128;
+          const bool live = row0 < args.m && ncol0 < args.n;
+          DG_CHECK(err, tile.nb >= 0 && tile.nb * BN < args.n && tile.g >= 0 && tile.g < args.num_groups,
+                   kSiteCheckStore);
+          if (!warp_wait<kSuspendHintNs, EPI8>(tfull(acc), acc_phase, abort_flag, tmo, err, kSiteEpilogueTmemFull))
+            break;
+          tc_fence_after();
+          uint32_t hv[4][32];
+          if (live && !k_empty) {
+            const uint32_t taddr =
+                tmem_base + (uint32_t)(acc * BN + chalf * 128) + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(taddr + c * 32, hv[c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc_wait_ld_regs(hv[c]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty(acc));
+          if (++acc == NUM_ACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          if (!live) continue;
+          float* const drow32 = args.d_f32 + (out_row0 + lane) * args.n;
+          const float* const crow32 = args.c_f32 ? args.c_f32 + (out_row0 + lane) * args.n : nullptr;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col0 = ncol0 + c * 32;
+            if (col0 >= args.n) break;
+            if (row0 + 32 <= args.m) {
+              uint32_t(&f)[32] = hv[c];  // FP32 bits, + C in place
+              if (k_empty) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) f[i] = 0u;
+              }
+              if (crow32) {
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                  if (col0 + 4 * p < args.n) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(crow32 + col0 + 4 * p);
+                    f[4 * p] = __float_as_uint(__uint_as_float(f[4 * p]) + c4.x);
+                    f[4 * p + 1] = __float_as_uint(__uint_as_float(f[4 * p + 1]) + c4.y);
+                    f[4 * p + 2] = __float_as_uint(__uint_as_float(f[4 * p + 2]) + c4.z);
+                    f[4 * p + 3] = __float_as_uint(__uint_as_float(f[4 * p + 3]) + c4.w);
+                  }
+                }
+              }
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                if (col0 + 16 * h >= args.n) break;
+                if (lane == 0) bulk_wait_group_read<0>();  // the staging chunk's previous store has read it
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  *reinterpret_cast<uint4*>(ebuf + my_row_off + 16u * ((uint32_t)j ^ my_swz)) =
+                      make_uint4(f[16 * h + 4 * j], f[16 * h + 4 * j + 1], f[16 * h + 4 * j + 2],
+                                 f[16 * h + 4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_2d(&tm_d, smem_u32(ebuf), col0 + 16 * h, (int32_t)out_row0);
+                  bulk_commit_group();
+                }
+              }
+            } else if (row_ok) {
+              store_row_chunk_f32(hv[c], drow32 + col0, crow32 ? crow32 + col0 : nullptr, args.n - col0,
+                                  k_empty);
+            }
+          }
+        }
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+      }
+    } else {
       if (warp >= 4) {
         const int quarter = warp & 3;
         const int hh = (warp - 4) >> 2;

@@ -1205,8 +1205,12 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa,
   const int64_t tiles = (int64_t)num_groups * args.m_blocks * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
   const int grid = (int)(tiles < sms ? tiles : sms);
-  print_config("k_grouped_fp8_gemm_tn_contiguous", m, n, sum_k, num_groups, kBlockM, block_n,
-               gemm_stages(block_n), grid, args.band);
+  // 256-column tiles drain their accumulator with eight epilogue warps
+  // (DG_TALL_EPI8 = 0: four, each reading its 256 columns in two halves)
+  args.epi8 = (block_n == 256 && env().tall_epi8 != 0) ? 1 : 0;
+  print_config(args.epi8 ? "k_grouped_fp8_gemm_tn_contiguous (eight epilogue warps)"
+                         : "k_grouped_fp8_gemm_tn_contiguous",
+               m, n, sum_k, num_groups, kBlockM, block_n, gemm_stages(block_n), grid, args.band);
   return from_cuda(gemm_launch(kKGrouped, block_n, o.a, o.b, o.sfa, o.sfb, o.d, args, grid, st));
 }
 
