@@ -690,6 +690,14 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
                                             (BM == kBlockM && MODE == kKGrouped && BN == 256))),
                 "eight epilogue warps: 256-row dense tiles, or 128 x 256 K-grouped tiles, with one accumulator");
   static_assert(!SK || EPI8, "stream-K: 256-row dense tiles with eight epilogue warps");
+  // setmaxnreg split of the eight-epilogue-warp layout: the K-grouped role
+  // warps (MN-major loads, per-expert K ranges) need more than 56 registers,
+  // its epilogue (128 FP32 columns per thread) fewer than 224
+  constexpr int kRolesRegs = MODE == kKGrouped ? 72 : kRegsRoles;
+  constexpr int kEpiRegs = MODE == kKGrouped ? 208 : kRegsEpi;
+  static_assert(128 * kRolesRegs + 256 * kEpiRegs <= kGemmThreadsEpi8 * 168 && kRolesRegs % 8 == 0 &&
+                    kEpiRegs % 8 == 0,
+                "setmaxnreg split within the launch's registers");
   static_assert(BM == kBlockM || (BM == 2 * kBlockM && (MODE == kDense || MODE == kContiguous) && KSPLIT == 1) ||
                     (BM == kBlockM / 2 && MODE == kDense),
                 "256-row tiles are for the dense NT and contiguous forms without split-K; "
@@ -888,7 +896,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   // and an idle warp) hands registers to the two epilogue warpgroups at the
   // start of each warpgroup's branch.
   if (EPI8 ? warp < 4 : warp < 3) {
-    if constexpr (EPI8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRoles) : "memory");
+    if constexpr (EPI8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRolesRegs) : "memory");
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       // A single M block of fewer than 128 rows is loaded as a box of
@@ -1148,7 +1156,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
       __syncwarp();
     }
   } else if constexpr (EPI8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi) : "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs) : "memory");
     // ------------------------------------------------------------ epilogue, eight warps
     // Warp w >= 4 drains lane quarter (w & 3) of 128-row half (w - 4) / 4:
     // the lane's whole row of BN columns is read from TMEM, C (fetched
