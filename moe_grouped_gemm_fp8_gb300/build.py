@@ -9,6 +9,10 @@ sources with ``-DDG_DEBUG_CHECKS=1``: the kernels check their load
 coordinates, TMEM columns, store rows and stream-K slots, and record
 DG_ERR_DEVICE_CHECK with the site in the error word instead of trapping.
 The binding loads it when ``DG_DEBUG_LIBRARY=1``.
+
+``build_floor()`` builds ``libdg_floor.so``, a measurement aid for the
+benchmark (the per-launch time of a plain streaming read from HBM), apart
+from the GEMM library.
 """
 import os
 import subprocess
@@ -21,6 +25,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libdg.so")
 DEBUG_LIB = os.path.join(HERE, "libdg_debug.so")
+FLOOR_LIB = os.path.join(HERE, "libdg_floor.so")
+FLOOR_SRC = os.path.join(CSRC, "hbm_floor.cu")
 
 SOURCES = ["gemm_bn128.cu", "gemm_bn192.cu", "gemm_bn224.cu", "gemm_bn256.cu",
            "gemm2_bn192.cu", "gemm2_bn224.cu", "gemm2_bn256.cu", "gemm_splitk.cu", "gemm_tall.cu", "gemm_promote.cu", "gemm_decode.cu", "gemm_kgrouped.cu", "gemm.cu",
@@ -85,6 +91,17 @@ def build(force: bool = False, verbose: bool = False, lineinfo: bool = True, deb
     subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs, check=True)
     os.replace(tmp, lib)
     return lib
+
+
+def build_floor(force: bool = False) -> str:
+    """libdg_floor.so: the streaming-read floor kernel the benchmark times."""
+    if not force and os.path.exists(FLOOR_LIB) and os.path.getmtime(FLOOR_LIB) >= max(
+            os.path.getmtime(FLOOR_SRC), os.path.getmtime(os.path.abspath(__file__))):
+        return FLOOR_LIB
+    tmp = FLOOR_LIB + ".tmp%d" % os.getpid()
+    subprocess.run([_nvcc()] + ARCH + ["-O3", "-Xcompiler", "-fPIC", "-shared", "-o", tmp, FLOOR_SRC], check=True)
+    os.replace(tmp, FLOOR_LIB)
+    return FLOOR_LIB
 
 
 if __name__ == "__main__":
