@@ -236,3 +236,27 @@ def test_mk_alignment_setter(L):
     finally:
         assert L.dg_set_mk_alignment_for_contiguous_layout(128) == DG_OK
     assert L.dg_get_mk_alignment_for_contiguous_layout() == 128
+
+
+def test_floor_library_is_separate_and_checks_its_arguments():
+    """libdg_floor.so (the benchmark's streaming-read floor) exports its one
+    function and nothing of the GEMM library; it refuses a null or unaligned
+    buffer and an empty grid before launching anything."""
+    import shutil
+    import subprocess
+    from moe_grouped_gemm_fp8_gb300 import build
+    path = build.build_floor()
+    F = C.CDLL(path)
+    F.dg_hbm_read_floor.argtypes = [C.c_void_p, C.c_size_t, C.c_void_p, C.c_int, C.c_void_p]
+    F.dg_hbm_read_floor.restype = C.c_int
+    nm = shutil.which("nm")
+    if nm is not None:
+        out = subprocess.run([nm, "-D", "--defined-only", path], capture_output=True, text=True,
+                             check=True).stdout
+        exported = sorted({line.split()[-1] for line in out.splitlines()
+                           if line.split() and line.split()[-1].startswith("dg_")})
+        assert exported == ["dg_hbm_read_floor"]
+    cuda_error_invalid_value = 1
+    assert F.dg_hbm_read_floor(None, 1024, None, 4, None) == cuda_error_invalid_value
+    assert F.dg_hbm_read_floor(0x1008, 1024, None, 4, None) == cuda_error_invalid_value
+    assert F.dg_hbm_read_floor(0x1000, 1024, None, 0, None) == cuda_error_invalid_value
