@@ -239,19 +239,22 @@ def step_flops(shapes):
 # DRAM bytes (read + write) of one launch of the step's largest GEMM, from an
 # ncu capture of that launch, keyed by the shape and the tile configuration
 # the library chose for it at capture time: (m, n, k, with C, block_m,
-# block_n, split_k, cta_pair).  A launch whose configuration is not listed has
-# no traffic figure (the counters would be stale).
+# block_n, split_k, cta_pair, multicast).  A launch whose configuration is not
+# listed has no traffic figure (the counters would be stale).
 CAPTURED_TRAFFIC = {
-    # 256 x 192 tiles, eight epilogue warps, 2048-row raster band:
-    # 367.5 MB read + 47.3 MB written (recaptured after the C-prefetch change
-    # to the eight-warp epilogue; 414.8 MB before it too)
-    (4096, 7168, 16384, False, 256, 192, 1, 0): 367509760 + 47258112,
+    # 256 x 192 tiles, eight epilogue warps, 2048-row raster band, one CTA per
+    # tile: 367.5 MB read + 47.3 MB written
+    (4096, 7168, 16384, False, 256, 192, 1, 0, 0): 367509760 + 47258112,
+    # the same tiles in clusters of two sharing B by TMA multicast:
+    # 393.4 MB read + 47.9 MB written
+    (4096, 7168, 16384, False, 256, 192, 1, 0, 1): 393375232 + 47889408,
 }
 
 
 def captured_traffic(dg, m, n, k, with_c, num_sms):
-    plan = dg.plan_fp8_gemm_nt(m, n, k, has_c=with_c, num_sms=num_sms)
-    key = (m, n, k, bool(with_c), plan["block_m"], plan["block_n"], plan["split_k"], int(plan["cta_pair"]))
+    plan = dg.plan_fp8_gemm_nt_ws(m, n, k, has_c=with_c, num_sms=num_sms)
+    key = (m, n, k, bool(with_c), plan["block_m"], plan["block_n"], plan["split_k"], int(plan["cta_pair"]),
+           int(plan["multicast"]))
     return CAPTURED_TRAFFIC.get(key), plan
 
 

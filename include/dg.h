@@ -367,12 +367,16 @@ dg_status dg_plan_fp8_gemm_nt(int64_t m, int64_t n, int64_t k, int32_t has_c, in
 
 /* The tile configuration dg_fp8_gemm_nt_ws chooses when its workspace is
  * large enough: the outputs of dg_plan_fp8_gemm_nt plus stream_k (1 when the
- * K blocks of the last waves are split between SMs) and swap_ab (1 when the
+ * K blocks of the last waves are split between SMs), swap_ab (1 when the
  * decode kernel with swapped operand roles runs; dg_fp8_gemm_nt makes the
- * same choice).  Same checks. */
+ * same choice) and multicast (1 when the 256-row tiles run in clusters of two
+ * CTAs on adjacent M blocks and one column block of B, each CTA loading half
+ * of the B tile into both with TMA multicast; dg_fp8_gemm_nt makes the same
+ * choice; DG_MULTICAST = 0 turns it off).  Same checks. */
 dg_status dg_plan_fp8_gemm_nt_ws(int64_t m, int64_t n, int64_t k, int32_t has_c, int32_t num_sms,
                                  int32_t* block_m, int32_t* block_n, int32_t* split_k,
-                                 int32_t* cta_pair, int32_t* stream_k, int32_t* swap_ab);
+                                 int32_t* cta_pair, int32_t* stream_k, int32_t* swap_ab,
+                                 int32_t* multicast);
 
 /* The same query for the two M-grouped forms: the tile configuration
  * dg_m_grouped_fp8_gemm_nt_contiguous / _masked chooses (block_m 256 when a

@@ -36,7 +36,7 @@ SIGNATURES = {
                                 C.c_uint64, _p]),
     "dg_fp8_gemm_nt_static_ws": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
     "dg_fp8_gemm_nt_workspace_size": (_st, [_i64, _i64, _i64, _i32, _i32, C.POINTER(C.c_uint64)]),
-    "dg_plan_fp8_gemm_nt_ws": (_st, [_i64, _i64, _i64, _i32, _i32, _p, _p, _p, _p, _p, _p]),
+    "dg_plan_fp8_gemm_nt_ws": (_st, [_i64, _i64, _i64, _i32, _i32, _p, _p, _p, _p, _p, _p, _p]),
     "dg_fp8_gemm_nt_fp32_sf": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
     "dg_fp8_gemm_nn": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),
     "dg_fp8_gemm_tn": (_st, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _i64, _i64, _i64, _p]),

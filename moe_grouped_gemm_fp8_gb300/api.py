@@ -102,15 +102,17 @@ def plan_fp8_gemm_nt(m: int, n: int, k: int, has_c: bool = False, num_sms: int =
 
 def plan_fp8_gemm_nt_ws(m: int, n: int, k: int, has_c: bool = False, num_sms: int = 152) -> dict:
     """The tile configuration fp8_gemm_nt chooses with a large enough
-    workspace: plan_fp8_gemm_nt's keys plus "stream_k" and "swap_ab" (the
-    decode kernel, operand roles swapped; fp8_gemm_nt chooses it too)."""
-    out = [C.c_int32(0) for _ in range(6)]
+    workspace: plan_fp8_gemm_nt's keys plus "stream_k", "swap_ab" (the
+    decode kernel, operand roles swapped; fp8_gemm_nt chooses it too) and
+    "multicast" (256-row tiles in clusters of two sharing B by TMA multicast;
+    fp8_gemm_nt chooses it too)."""
+    out = [C.c_int32(0) for _ in range(7)]
     st = _lib.lib().dg_plan_fp8_gemm_nt_ws(int(m), int(n), int(k), 1 if has_c else 0, int(num_sms),
                                            *[C.byref(o) for o in out])
     _check(st, "dg_plan_fp8_gemm_nt_ws")
-    bm, bn, sk, pair, strk, swap = (int(o.value) for o in out)
+    bm, bn, sk, pair, strk, swap, mc = (int(o.value) for o in out)
     return {"block_m": bm, "block_n": bn, "split_k": sk, "cta_pair": bool(pair), "stream_k": bool(strk),
-            "swap_ab": bool(swap)}
+            "swap_ab": bool(swap), "multicast": bool(mc)}
 
 
 def plan_m_grouped_fp8_gemm_nt_contiguous(m_sum: int, n: int, k: int, num_groups: int,

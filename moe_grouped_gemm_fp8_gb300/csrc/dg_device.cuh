@@ -517,6 +517,29 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       : "memory");
 }
 
+// Arrives on the mbarrier at shared offset `bar` of both CTAs of a 2-CTA
+// cluster (single-CTA MMAs) once every tcgen05 operation issued so far by
+// this thread has completed.
+__device__ __forceinline__ void tc_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+// TMA load of a 3-D box into the shared memory of both CTAs of a 2-CTA
+// cluster, at the same offset `dst` in each, counted (complete_tx) on the
+// mbarrier at offset `bar` of each.
+__device__ __forceinline__ void tma_load_3d_both(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"((uint16_t)3)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- numerics
 
 // Two FP32 values -> two E4M3 codes (round to nearest even, saturating to the

@@ -98,6 +98,9 @@ struct GemmArgs {
   // C's base and row stride are multiples of 32 bytes: rows of C may be read
   // with 32-byte loads
   int32_t c_v8;
+  // 256-row dense tiles: clusters of two CTAs on adjacent M blocks share each
+  // B tile through TMA multicast (the grid is even)
+  int32_t mc;
   // Stream-K (256-row dense tiles with eight epilogue warps; 0 units = off):
   // tiles [0, sk_dp_tiles) are walked one per CTA per wave, the K blocks of
   // the remaining tiles (sk_units = their count x k_blocks) are shared out

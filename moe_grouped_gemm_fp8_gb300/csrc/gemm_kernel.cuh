@@ -186,6 +186,7 @@ struct Scheduler {
   int cursor;              // masked: current group (tile indices only increase)
   int kb_lo, kb_hi;        // K blocks of every tile (not K-grouped)
   int first, stride;       // this CTA's first tile and the stride of its tile walk
+  int pair_rank = -1;      // dense multicast pairs: this CTA's rank (tiles are pairs of M blocks), else -1
   const uint32_t* sk_ctl;  // stream-K kernels: this CTA's units [sk_ctl[0], sk_ctl[1])
 
   __device__ void k_range(const Tile& tile, int& kb0, int& kb1) const {
@@ -292,9 +293,13 @@ struct Scheduler {
     const int per_band = args->band * args->n_blocks;
     const int b = t / per_band;
     const int rem = t - b * per_band;
-    const int rows = min(args->band, args->m_blocks - b * args->band);
+    const int mbs = pair_rank >= 0 ? (args->m_blocks + 1) >> 1 : args->m_blocks;
+    const int rows = min(args->band, mbs - b * args->band);
     tile.nb = rem / rows;
     tile.mb = b * args->band + rem % rows;
+    // a pair's second M block may lie past M (odd count): its loads read
+    // zeros and its epilogue stores nothing
+    if (pair_rank >= 0) tile.mb = 2 * tile.mb + pair_rank;
     tile.g = 0;
     if (MODE == kContiguous) {
       const int g = __ldg(args->m_indices + (int64_t)tile.mb * kBlockM);
@@ -674,7 +679,8 @@ __device__ __forceinline__ void emit_chunk_tma(float (&f)[32], uint8_t* buf,
   }
 }
 
-template <int BN, int STAGES, int MODE, int KSPLIT, int BM = kBlockM, bool EPI8 = false, bool SK = false>
+template <int BN, int STAGES, int MODE, int KSPLIT, int BM = kBlockM, bool EPI8 = false, bool SK = false,
+          bool MC = false>
 __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
@@ -683,6 +689,12 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
                     const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
   using L = GemmLayout<BN, BM>;
   using P = GemmPlan<BN, STAGES, KSPLIT, BM>;
+  // MC: clusters of two CTAs on the same column block of B and adjacent
+  // 256-row blocks of A; each loads half of the B tile into both CTAs' stage
+  // (TMA multicast), so L2 serves B once per pair
+  static_assert(!MC || (MODE == kDense && BM == 2 * kBlockM && EPI8 && !SK && KSPLIT == 1),
+                "multicast pairs: dense 256-row tiles with eight epilogue warps");
+  constexpr int CL = MC ? 2 : KSPLIT;  // CTAs per cluster
   constexpr int NUM_ACC = P::kNumAcc;
   constexpr int MH = L::kMH;  // 128-row halves of a tile
   static_assert(KSPLIT == 1 || MODE == kDense, "split-K is for the dense form");
@@ -740,7 +752,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
+      mbar_init(empty(s), MC ? 2 : 1);  // MC: a stage is free once both CTAs' MMAs are done with it
     }
     for (int p = 0; p < kSfSlots; ++p) {
       mbar_init(sffull(p), 1);
@@ -861,15 +873,15 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     }
   }
   __syncthreads();
-  if (KSPLIT > 1) cluster_sync_all();  // every CTA's barriers exist before remote arrivals
+  if (CL > 1) cluster_sync_all();  // every CTA's barriers exist before remote arrivals
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (threadIdx.x == 0) griddep_launch_dependents();
 
   // tile loop of this CTA (of this cluster, with split-K) and its K slice
-  const uint32_t krank = KSPLIT > 1 ? cluster_ctarank() : 0u;
-  const int first_tile = (int)blockIdx.x / KSPLIT;
-  const int tile_stride = (int)gridDim.x / KSPLIT;
+  const uint32_t krank = CL > 1 ? cluster_ctarank() : 0u;
+  const int first_tile = (int)blockIdx.x / CL;
+  const int tile_stride = (int)gridDim.x / CL;
   const int kb_per = (args.k_blocks + KSPLIT - 1) / KSPLIT;
   const int kb_begin = KSPLIT > 1 ? min(args.k_blocks, (int)krank * kb_per) : 0;
   const int kb_end = KSPLIT > 1 ? min(args.k_blocks, kb_begin + kb_per) : args.k_blocks;
@@ -885,9 +897,11 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   sched.kb_hi = kb_end;
   sched.first = first_tile;
   sched.stride = tile_stride;
+  sched.pair_rank = MC ? (int)krank : -1;
   sched.total = MODE == kMasked      ? tile_start[args.num_groups]
                 : MODE == kKGrouped ? args.num_groups * args.m_blocks * args.n_blocks
                 : (MODE == kContiguous && BM == 2 * kBlockM) ? tile_start[args.num_groups] * args.n_blocks
+                : MC                ? ((args.m_blocks + 1) >> 1) * args.n_blocks
                                     : args.m_blocks * args.n_blocks;
   const uint64_t tmo = args.timeout_ns;
 
@@ -943,7 +957,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
               if constexpr (a_mn_major(MODE)) DG_CHECK(err, (my & 15) == 0 && my < args.m, kSiteCheckLoadA);
               else if (MODE == kContiguous && BM == 2 * kBlockM)
                 DG_CHECK(err, tile.b0 >= 0 && tile.b0 < args.m_blocks && tile.b1 < args.m_blocks, kSiteCheckLoadA);
-              else DG_CHECK(err, my >= 0 && my < args.m, kSiteCheckLoadA);
+              else DG_CHECK(err, my >= 0 && my < (MC ? args.m + BM : args.m), kSiteCheckLoadA);
               DG_CHECK(err, tile.nb >= 0 && tile.nb * BN < args.n && ((tile.nb * BN) & 7) == 0 &&
                                 (MODE == kKGrouped || (tile.g >= 0 && tile.g < args.num_groups)),
                        kSiteCheckLoadB);
@@ -959,6 +973,10 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   #pragma unroll
               for (int h = 0; h < BN / 128; ++h)
                 tma_load_2d(sb + L::kOffB + h * 16384, &tm_b, fb, tile.nb * BN + h * 128, kx);
+            } else if constexpr (MC) {
+              // this CTA's half of the B tile, into the same place in both CTAs
+              tma_load_3d_both(sb + L::kOffB + krank * (uint32_t)(BN / 2 * kBlockK), &tm_b, fb, kx,
+                               tile.nb * BN + (int)krank * (BN / 2), tile.g);
             } else {
               tma_load_3d(sb + L::kOffB, &tm_b, fb, kx, tile.nb * BN, tile.g);
             }
@@ -1040,7 +1058,9 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
                 tc_mma_mxf8(d_tmem + h * BN, adesc + 1024u * h + a_step * j, bdesc + b_step * j,
                             idesc | major_bits, sf_tmem + 4 * h, sf_tmem + 4 * MH,
                             (kb != kb0 || j != 0) ? 1u : 0u);
-            tc_commit(empty(stage));
+            // MC: the other CTA writes half of this stage too, so both are told
+            if constexpr (MC) tc_commit_both(empty(stage));
+            else tc_commit(empty(stage));
             if ((kb & 3) == 3 || kb == kb1 - 1) {
               tc_commit(sfempty(slot));  // the pack's buffer and TMEM slot are free
               ++pack;
@@ -1084,7 +1104,8 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
               const int my = ld.tile.mb * BM, kp = ld.kp;
               mbar_arrive_expect_tx(bar, L::kTxSF);
               DG_CHECK(err, kp >= 0 && kp < (args.k_blocks + 3) / 4 && my >= 0 &&
-                                (MODE == kContiguous && BM == 2 * kBlockM ? ld.tile.b0 < args.m_blocks : my < args.m),
+                                (MODE == kContiguous && BM == 2 * kBlockM ? ld.tile.b0 < args.m_blocks
+                                                                          : my < (MC ? args.m + BM : args.m)),
                        kSiteCheckScale);
               if (MODE == kMasked) tma_load_3d(buf + L::kRawA, &tm_sfa, bar, my, kp, ld.tile.g);
               else if (MODE == kContiguous && BM == 2 * kBlockM) {
@@ -1909,7 +1930,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
 
   __syncthreads();
   // No CTA leaves while others may still reach its shared memory.
-  if constexpr (KSPLIT > 1) {
+  if constexpr (CL > 1) {
     // Clean path: every exchange into this CTA has completed (its mbarrier
     // waits acquired it), so the barrier needs no release (a release would
     // also wait for this CTA's outstanding global writes).  After an abort
@@ -1924,7 +1945,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
     // in every CTA.
     if (*abort_flag) {
       if (threadIdx.x == 0)
-        for (uint32_t r = 0; r < (uint32_t)KSPLIT; ++r)
+        for (uint32_t r = 0; r < (uint32_t)CL; ++r)
           if (r != krank) st_shared_cluster_u32(mapa_shared(smem_u32((const void*)peer_abort), r), 1u);
       fence_acq_rel_cluster();
     }
@@ -1957,17 +1978,20 @@ static cudaError_t set_smem_once(Kern kern, size_t smem) {
   return e;
 }
 
-template <int BN, int STAGES, int MODE, int KSPLIT = 1, int BM = kBlockM, bool EPI8 = false, bool SK = false>
+template <int BN, int STAGES, int MODE, int KSPLIT = 1, int BM = kBlockM, bool EPI8 = false, bool SK = false,
+          bool MC = false>
 static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
                                     const CUtensorMap& sfa, const CUtensorMap& sfb,
                                     const CUtensorMap& d, const GemmArgs& args, int grid,
                                     cudaStream_t stream) {
   using Plan = GemmPlan<BN, STAGES, KSPLIT, BM>;
   static_assert(Plan::smem_bytes(MODE) <= (size_t)kSmemLimit, "shared memory over the per-CTA limit");
-  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT, BM, EPI8, SK>;
+  auto kern = fp8_gemm_kernel<BN, STAGES, MODE, KSPLIT, BM, EPI8, SK, MC>;
   const size_t smem = Plan::smem_bytes(MODE);
+  constexpr int CL = MC ? 2 : KSPLIT;
   cudaError_t e = set_smem_once<
-      KernelTag<BN, STAGES, MODE, KSPLIT, SK ? 6 : EPI8 ? 5 : (BM == kBlockM ? 1 : (BM > kBlockM ? 3 : 4))>>(kern, smem);
+      KernelTag<BN, STAGES, MODE, KSPLIT, MC ? 7 : SK ? 6 : EPI8 ? 5 : (BM == kBlockM ? 1 : (BM > kBlockM ? 3 : 4))>>(
+      kern, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[3];
   unsigned n_attr = 0;
@@ -1977,9 +2001,9 @@ static cudaError_t gemm_launch_impl(const CUtensorMap& a, const CUtensorMap& b,
     attr[n_attr].val.cooperative = 1;
     ++n_attr;
   }
-  if (KSPLIT > 1) {
+  if (CL > 1) {
     attr[n_attr].id = cudaLaunchAttributeClusterDimension;
-    attr[n_attr].val.clusterDim.x = KSPLIT;
+    attr[n_attr].val.clusterDim.x = CL;
     attr[n_attr].val.clusterDim.y = 1;
     attr[n_attr].val.clusterDim.z = 1;
     ++n_attr;

@@ -39,6 +39,11 @@ cudaError_t gemm_tall_launch_impl(int mode, int block_n, const CUtensorMap& a, c
       case 192: return gemm_launch_impl<192, 3, kDense, 1, BM, true, true>(a, b, sfa, sfb, d, args, grid, stream);
       case 224: return gemm_launch_impl<224, 3, kDense, 1, BM, true, true>(a, b, sfa, sfb, d, args, grid, stream);
     }
+  } else if (mode == kDense && args.epi8 && args.mc) {
+    switch (block_n) {
+      case 192: return gemm_launch_impl<192, 3, kDense, 1, BM, true, false, true>(a, b, sfa, sfb, d, args, grid, stream);
+      case 224: return gemm_launch_impl<224, 3, kDense, 1, BM, true, false, true>(a, b, sfa, sfb, d, args, grid, stream);
+    }
   } else if (mode == kDense && args.epi8) {
     switch (block_n) {
       case 192: return gemm_launch_impl<192, 3, kDense, 1, BM, true>(a, b, sfa, sfb, d, args, grid, stream);

@@ -41,19 +41,21 @@ class _FakePlanner:
     def __init__(self, plan):
         self.plan = plan
 
-    def plan_fp8_gemm_nt(self, m, n, k, has_c=False, num_sms=152):
+    def plan_fp8_gemm_nt_ws(self, m, n, k, has_c=False, num_sms=152):
         return dict(self.plan)
 
 
 def test_traffic_only_for_the_captured_tile_configuration(monkeypatch):
-    key = (4096, 7168, 16384, False, 256, 192, 1, 0)
+    key = (4096, 7168, 16384, False, 256, 192, 1, 0, 1)
     monkeypatch.setitem(bench.CAPTURED_TRAFFIC, key, 4.0e8)
-    m, n, k, c, bm, bn, sk, pair = key
-    same = _FakePlanner(dict(block_m=bm, block_n=bn, split_k=sk, cta_pair=bool(pair)))
+    m, n, k, c, bm, bn, sk, pair, mc = key
+    same = _FakePlanner(dict(block_m=bm, block_n=bn, split_k=sk, cta_pair=bool(pair), multicast=bool(mc)))
     t, plan = bench.captured_traffic(same, m, n, k, c, 152)
     assert t == bench.CAPTURED_TRAFFIC[key] and plan["block_n"] == bn
-    other = _FakePlanner(dict(block_m=bm, block_n=bn + 32, split_k=sk, cta_pair=bool(pair)))
+    other = _FakePlanner(dict(block_m=bm, block_n=bn + 32, split_k=sk, cta_pair=bool(pair), multicast=bool(mc)))
     assert bench.captured_traffic(other, m, n, k, c, 152)[0] is None  # a changed tile: stale counters
+    single = _FakePlanner(dict(block_m=bm, block_n=bn, split_k=sk, cta_pair=bool(pair), multicast=False))
+    assert bench.captured_traffic(single, m, n, k, c, 152)[0] != 4.0e8  # the other kernel's counters
     assert bench.captured_traffic(same, m, n + 128, k, c, 152)[0] is None  # another shape
 
 

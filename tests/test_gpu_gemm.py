@@ -148,10 +148,13 @@ def test_short_m_block_ignores_stale_shared_memory(ks, M):
 
 @contextmanager
 def tall_tiles(bn):
-    old = {k: os.environ.get(k) for k in ("DG_BLOCK_M", "DG_BLOCK_N", "DG_CTA_PAIR")}
+    """256-row tiles of width bn on one CTA each (no CTA pair, no split-K,
+    which the plan would otherwise take for the smaller shapes)."""
+    old = {k: os.environ.get(k) for k in ("DG_BLOCK_M", "DG_BLOCK_N", "DG_CTA_PAIR", "DG_SPLIT_K")}
     os.environ["DG_BLOCK_M"] = "256"
     os.environ["DG_BLOCK_N"] = str(bn)
     os.environ["DG_CTA_PAIR"] = "0"
+    os.environ["DG_SPLIT_K"] = "1"
     try:
         yield
     finally:
@@ -202,6 +205,50 @@ def test_dense_256_row_tiles_exact_many_tiles_per_sm(bn):
     finally:
         dg.set_num_sms(0)
     assert np.array_equal(got, want)
+    _no_device_error()
+
+
+@pytest.mark.parametrize("bn", [192, 224])
+@pytest.mark.parametrize("sms", [0, 5])
+@pytest.mark.parametrize("M,N,K", [(600, 520, 1024), (1024, 1000, 640), (257, 448, 2048)])
+def test_dense_multicast_pairs_match_single_ctas_bitwise(bn, sms, M, N, K):
+    """256-row tiles in clusters of two CTAs that load half of each B tile
+    into both (TMA multicast) compute what one CTA per tile computes, bit for
+    bit, with and without C; with an odd number of 256-row blocks the last
+    pair's second tile lies past M and writes nothing (sentinel columns and
+    rows stay untouched)."""
+    w = workloads.dense(M, N, K, seed=M + N + K + bn, with_c=True)
+    qa, _, sa = P.quantize(w.a, 1)
+    qb, _, sb = P.quantize(w.b, 128)
+    args = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    c = w.c.cuda()
+    out = {}
+    old = {k: os.environ.get(k) for k in ("DG_MULTICAST", "DG_STREAM_K")}
+    os.environ["DG_STREAM_K"] = "0"  # tile by tile (stream-K tiles are never paired)
+    dg.set_num_sms(sms)
+    try:
+        for mc in ("1", "0"):
+            os.environ["DG_MULTICAST"] = mc
+            with tall_tiles(bn):
+                assert dg.plan_fp8_gemm_nt_ws(M, N, K, True, sms or 152)["multicast"] == (mc == "1")
+                for with_c in (False, True):
+                    buf = P.sentinel_like((M, N + 24))
+                    dg.fp8_gemm_nt(*args, d=buf[:, :N], c=c if with_c else None)
+                    assert (P.bf16_bits(buf[:, N:]) == P.SENTINEL_BITS).all()
+                    out[mc, with_c] = P.bf16_bits(buf[:, :N])
+                    if mc == "1" and with_c:
+                        d_mc = buf[:, :N].clone()
+    finally:
+        dg.set_num_sms(0)
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    for with_c in (False, True):
+        assert np.array_equal(out["1", with_c], out["0", with_c])
+    o = oracle.gemm_nt(qa, sa, qb, sb, P.bf16_bits(w.c))
+    P.assert_close(P.bf16_to_f64(d_mc), o, "multicast pairs BN=%d %dx%dx%d" % (bn, M, N, K))
     _no_device_error()
 
 

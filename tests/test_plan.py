@@ -14,7 +14,8 @@ import moe_grouped_gemm_fp8_gb300 as dg
 from moe_grouped_gemm_fp8_gb300 import _lib, workloads
 
 SMS = 152
-OVERRIDES = ("DG_BLOCK_M", "DG_BLOCK_N", "DG_SPLIT_K", "DG_CTA_PAIR", "DG_STREAM_K")
+OVERRIDES = ("DG_BLOCK_M", "DG_BLOCK_N", "DG_SPLIT_K", "DG_CTA_PAIR", "DG_STREAM_K", "DG_MULTICAST",
+             "DG_TALL_EPI8")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -280,3 +281,35 @@ def test_stream_k_overrides():
         finally:
             os.environ.pop("DG_STREAM_K", None)
             os.environ.pop("DG_BLOCK_N", None)
+
+
+# ------------------------------------------------------------------ multicast
+
+
+def test_multicast_pairs_go_with_256_row_tiles_walked_tile_by_tile():
+    """Clusters of two CTAs sharing B by TMA multicast are used exactly when
+    the dense plan takes 256-row tiles with eight epilogue warps, tile by
+    tile: never with 128-row tiles, stream-K, CTA pairs, split-K or the
+    decode kernel; DG_MULTICAST = 0 (or the four-warp epilogue) turns them
+    off."""
+    with env():
+        seen = 0
+        for cfg in workloads.PREFILL + workloads.DECODE:
+            for has_c in (False, True):
+                p = dg.plan_fp8_gemm_nt_ws(cfg["m"], cfg["n"], cfg["k"], has_c, SMS)
+                tall = p["block_m"] == 256 and not p["cta_pair"] and not p["swap_ab"]
+                assert p["multicast"] == (tall and not p["stream_k"]), (cfg, has_c, p)
+                seen += p["multicast"]
+        assert seen >= 4  # the prefill shapes that take 256-row tiles
+        assert not dg.plan_fp8_gemm_nt_ws(4352, 192, 16384, False, 16)["multicast"]  # stream-K
+    with env(DG_BLOCK_M=128):
+        assert not dg.plan_fp8_gemm_nt_ws(4096, 7168, 16384, False, SMS)["multicast"]
+    with env(DG_MULTICAST=0):
+        assert not dg.plan_fp8_gemm_nt_ws(4096, 7168, 16384, False, SMS)["multicast"]
+    with env(DG_TALL_EPI8=0):
+        assert not dg.plan_fp8_gemm_nt_ws(4096, 7168, 16384, False, SMS)["multicast"]
+    with env(DG_CTA_PAIR=1):
+        p = dg.plan_fp8_gemm_nt_ws(4096, 7168, 16384, False, SMS)
+        assert p["cta_pair"] and not p["multicast"]
+    with env():
+        assert dg.plan_fp8_gemm_nt_ws(4096, 7168, 16384, False, SMS)["multicast"]
