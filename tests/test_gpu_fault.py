@@ -86,3 +86,43 @@ def test_dropped_stage_in_a_split_k_cluster_times_out_everywhere(decode):
         os.environ.pop("DG_DECODE", None)
     assert dg.get_device_error()[0] == 0
     P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "after the injected split-K timeout")
+
+
+def test_dropped_stage_in_a_multicast_pair_times_out_everywhere():
+    """The same hook in a 2-CTA cluster of 256-row tiles that share each B
+    tile by TMA multicast: CTA 0 never fills one stage, so its peer's copy of
+    that stage (which waits for CTA 0's half of B) never fills either; both
+    CTAs' waits expire, both end by themselves (the abort marks the peer and
+    both take the release/acquire cluster barrier), the error word holds a
+    timeout, and the context stays usable."""
+    M, N, K = 512, 384, 2048
+    g = torch.Generator().manual_seed(115)
+    a = torch.randn(M, K, generator=g); b = torch.randn(N, K, generator=g)
+    qa, _, sa = oracle.quantize(a.numpy(), 1)
+    qb, _, sb = oracle.quantize(b.numpy(), 128)
+    dev = (P.dev_codes(qa), P.dev_packed_sf(sa, M, K, 1), P.dev_codes(qb), P.dev_packed_sf(sb, N, K, 128))
+    env = {"DG_SPLIT_K": "1", "DG_BLOCK_M": "256", "DG_BLOCK_N": "192", "DG_STREAM_K": "0", "DG_MULTICAST": "1"}
+    old = {k: os.environ.get(k) for k in env}
+    os.environ.update(env)
+    try:
+        assert dg.plan_fp8_gemm_nt_ws(M, N, K)["multicast"]
+        assert dg.get_device_error()[0] == 0
+        dg.set_wait_timeout_ns(2_000_000)  # 2 ms
+        dg.debug_set_drop_load(2)
+        try:
+            dg.fp8_gemm_nt(*dev)
+            st, word = dg.get_device_error()
+        finally:
+            dg.debug_set_drop_load(0)
+            dg.set_wait_timeout_ns(2_000_000_000)
+        assert st == DG_ERR_DEVICE_TIMEOUT, (st, hex(word))
+        assert word & 0xFF == DG_ERR_DEVICE_TIMEOUT, hex(word)
+        d = dg.fp8_gemm_nt(*dev)
+        assert dg.get_device_error()[0] == 0
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    P.assert_close(P.bf16_to_f64(d), oracle.gemm_nt(qa, sa, qb, sb), "after the injected multicast-pair timeout")
