@@ -1932,8 +1932,11 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   // No CTA leaves while others may still reach its shared memory.
   if constexpr (CL > 1) {
     // Clean path: every exchange into this CTA has completed (its mbarrier
-    // waits acquired it), so the barrier needs no release (a release would
-    // also wait for this CTA's outstanding global writes).  After an abort
+    // waits acquired it: split-K partials, and with multicast pairs the
+    // peer's halves of B), and the peer's MMA commits that arrive on this
+    // CTA's barriers completed before the peer's MMA thread finished its
+    // drain, so the barrier needs no release (a release would also wait for
+    // this CTA's outstanding global writes).  After an abort
     // that no longer holds: a CTA that gave up on a wait never acquired what
     // its peers sent it, and their remote stores and arrivals may still be in
     // flight.  An aborted CTA therefore marks every peer before the barrier
