@@ -2,7 +2,9 @@
 // M-grouped contiguous forms: two 128-row MMAs per K step share the B tile,
 // so each K block moves 32 KB of A and BN x 128 bytes of B for twice the work
 // of a 128-row tile (3-stage pipeline, one TMEM accumulator of 2 x BN
-// columns).  Contiguous tiles pair two 128-row blocks of one group.
+// columns).  Contiguous tiles pair two 128-row blocks of one group.  Dense
+// tiles walked tile by tile run in clusters of two CTAs on adjacent 256-row
+// blocks that share each B tile through TMA multicast.
 #include "gemm_kernel.cuh"
 
 namespace dg {
