@@ -327,6 +327,24 @@ dg_status dg_transform_sf(const float* sf, int32_t* packed, int64_t groups, int6
 /* Utilities (same page, section "Utilitários e variáveis de ambiente")      */
 /* ------------------------------------------------------------------------ */
 
+/* Environment variables read by the library (when the process environment
+ * changes, not on every call), all optional, for tuning and diagnosis:
+ *   DG_PRINT_CONFIGS=1   print each launch's configuration to stderr;
+ *   DG_BLOCK_M=128|256, DG_BLOCK_N=128|192|224|256   force the tile size;
+ *   DG_SPLIT_K=1|2|4|8   force the split-K cluster size (8: decode kernel);
+ *   DG_CTA_PAIR=1        256-row tiles on 2-CTA pairs (cta_group::2 MMAs);
+ *   DG_STREAM_K=0|1      forbid / force stream-K where a workspace allows it;
+ *   DG_MULTICAST=0       256-row dense tiles one CTA each instead of 2-CTA
+ *                        clusters sharing B by TMA multicast;
+ *   DG_TALL_EPI8=0       four epilogue warps for 256-row tiles instead of eight;
+ *   DG_DECODE=0          tiled kernels instead of the decode kernel for M <= 128;
+ *   DG_RASTER_BAND=n     M blocks per raster band (default 16).
+ * Tile sizes, CTA pairs and multicast clusters give the same bits: each output
+ * element accumulates its K blocks in the same order.  Configurations that
+ * split K between CTAs (split-K, stream-K, decode clusters) add the partial
+ * sums in a fixed order, so their bits are reproducible but may differ from
+ * an unsplit launch's within FP32 rounding. */
+
 /* x rounded up so that x * element_size is a multiple of 16 bytes. */
 int64_t dg_get_tma_aligned_size(int64_t x, int32_t element_size);
 
