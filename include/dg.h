@@ -339,8 +339,9 @@ dg_status dg_transform_sf(const float* sf, int32_t* packed, int64_t groups, int6
  *   DG_TALL_EPI8=0       four epilogue warps for 256-row tiles instead of eight;
  *   DG_DECODE=0          tiled kernels instead of the decode kernel for M <= 128;
  *   DG_RASTER_BAND=n     M blocks per raster band (default 16).
- * Tile sizes and multicast clusters give the same bits (tested): each output
- * element accumulates its K blocks in the same order.  Configurations that
+ * Tile sizes and multicast clusters give the same bits: each output element
+ * accumulates its K blocks in the same order (tested for 128- against
+ * 256-row tiles and for multicast on against off).  Configurations that
  * split K between CTAs (split-K, stream-K, decode clusters) add the partial
  * sums in a fixed order, so their bits are reproducible but may differ from
  * an unsplit launch's within FP32 rounding. */
