@@ -528,6 +528,18 @@ __device__ __forceinline__ void tc_commit_both(uint32_t bar) {
       : "memory");
 }
 
+// TMA load of a 2-D box into the shared memory of both CTAs of a 2-CTA
+// cluster, at the same offset `dst` in each, counted (complete_tx) on the
+// mbarrier at offset `bar` of each.
+__device__ __forceinline__ void tma_load_2d_both(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"((uint16_t)3)
+      : "memory");
+}
+
 // TMA load of a 3-D box into the shared memory of both CTAs of a 2-CTA
 // cluster, at the same offset `dst` in each, counted (complete_tx) on the
 // mbarrier at offset `bar` of each.

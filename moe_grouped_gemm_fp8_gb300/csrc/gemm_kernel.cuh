@@ -270,15 +270,18 @@ struct Scheduler {
       return true;
     }
     if (MODE == kKGrouped) {
-      const int per_group = args->m_blocks * args->n_blocks;
+      // multicast pairs: the walk covers pairs of M blocks, a CTA takes one
+      const int mbs = pair_rank >= 0 ? (args->m_blocks + 1) >> 1 : args->m_blocks;
+      const int per_group = mbs * args->n_blocks;
       tile.g = t / per_group;
       const int r = t - tile.g * per_group;
       const int per_band = args->band * args->n_blocks;
       const int b = r / per_band;
       const int rem = r - b * per_band;
-      const int rows = min(args->band, args->m_blocks - b * args->band);
+      const int rows = min(args->band, mbs - b * args->band);
       tile.nb = rem / rows;
       tile.mb = b * args->band + rem % rows;
+      if (pair_rank >= 0) tile.mb = 2 * tile.mb + pair_rank;
       return true;
     }
     if (MODE == kMasked) {
@@ -689,11 +692,14 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
                     const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
   using L = GemmLayout<BN, BM>;
   using P = GemmPlan<BN, STAGES, KSPLIT, BM>;
-  // MC: clusters of two CTAs on the same column block of B and adjacent
-  // 256-row blocks of A; each loads half of the B tile into both CTAs' stage
-  // (TMA multicast), so L2 serves B once per pair
-  static_assert(!MC || (MODE == kDense && BM == 2 * kBlockM && EPI8 && !SK && KSPLIT == 1),
-                "multicast pairs: dense 256-row tiles with eight epilogue warps");
+  // MC: clusters of two CTAs on the same column block of B (of the same
+  // expert, K-grouped) and adjacent row blocks of A; each loads half of the B
+  // tile into both CTAs' stage (TMA multicast: half the rows of a K-major
+  // tile, one of the two 128-column boxes of an MN-major one), so L2 serves B
+  // once per pair
+  static_assert(!MC || (!SK && KSPLIT == 1 && EPI8 &&
+                        ((MODE == kDense && BM == 2 * kBlockM) || (MODE == kKGrouped && BM == kBlockM && BN == 256))),
+                "multicast pairs: dense 256-row tiles or K-grouped 128 x 256 tiles, eight epilogue warps");
   constexpr int CL = MC ? 2 : KSPLIT;  // CTAs per cluster
   constexpr int NUM_ACC = P::kNumAcc;
   constexpr int MH = L::kMH;  // 128-row halves of a tile
@@ -705,8 +711,8 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   // setmaxnreg split of the eight-epilogue-warp layout: the K-grouped role
   // warps (MN-major loads, per-expert K ranges) need more than 56 registers,
   // its epilogue (128 FP32 columns per thread) fewer than 224
-  constexpr int kRolesRegs = MODE == kKGrouped ? 72 : kRegsRoles;
-  constexpr int kEpiRegs = MODE == kKGrouped ? 208 : kRegsEpi;
+  constexpr int kRolesRegs = MODE == kKGrouped ? (MC ? 104 : 72) : kRegsRoles;
+  constexpr int kEpiRegs = MODE == kKGrouped ? (MC ? 192 : 208) : kRegsEpi;
   static_assert(128 * kRolesRegs + 256 * kEpiRegs <= kGemmThreadsEpi8 * 168 && kRolesRegs % 8 == 0 &&
                     kEpiRegs % 8 == 0,
                 "setmaxnreg split within the launch's registers");
@@ -899,7 +905,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   sched.stride = tile_stride;
   sched.pair_rank = MC ? (int)krank : -1;
   sched.total = MODE == kMasked      ? tile_start[args.num_groups]
-                : MODE == kKGrouped ? args.num_groups * args.m_blocks * args.n_blocks
+                : MODE == kKGrouped ? args.num_groups * (MC ? (args.m_blocks + 1) >> 1 : args.m_blocks) * args.n_blocks
                 : (MODE == kContiguous && BM == 2 * kBlockM) ? tile_start[args.num_groups] * args.n_blocks
                 : MC                ? ((args.m_blocks + 1) >> 1) * args.n_blocks
                                     : args.m_blocks * args.n_blocks;
@@ -954,7 +960,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
               // K block in range; innermost coordinates on 16-byte boundaries;
               // rows, column tiles and groups inside their tensors
               DG_CHECK(err, kb >= 0 && kb < args.k_blocks && (kx & 15) == 0, kSiteCheckLoadA);
-              if constexpr (a_mn_major(MODE)) DG_CHECK(err, (my & 15) == 0 && my < args.m, kSiteCheckLoadA);
+              if constexpr (a_mn_major(MODE)) DG_CHECK(err, (my & 15) == 0 && my < (MC ? args.m + BM : args.m), kSiteCheckLoadA);
               else if (MODE == kContiguous && BM == 2 * kBlockM)
                 DG_CHECK(err, tile.b0 >= 0 && tile.b0 < args.m_blocks && tile.b1 < args.m_blocks, kSiteCheckLoadA);
               else DG_CHECK(err, my >= 0 && my < (MC ? args.m + BM : args.m), kSiteCheckLoadA);
@@ -969,7 +975,10 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
               tma_load_2d(sb, &tm_a, fb, kx, tile.b0 * kBlockM);
               tma_load_2d(sb + kBlockM * kBlockK, &tm_a, fb, kx, (tile.b1 >= 0 ? tile.b1 : tile.b0) * kBlockM);
             } else tma_load_2d(sb, &tm_a, fb, kx, my);
-            if constexpr (b_mn_major(MODE)) {
+            if constexpr (b_mn_major(MODE) && MC) {
+              // this CTA's 128-column box of the B tile, into the same place in both CTAs
+              tma_load_2d_both(sb + L::kOffB + krank * 16384u, &tm_b, fb, tile.nb * BN + (int)krank * 128, kx);
+            } else if constexpr (b_mn_major(MODE)) {
   #pragma unroll
               for (int h = 0; h < BN / 128; ++h)
                 tma_load_2d(sb + L::kOffB + h * 16384, &tm_b, fb, tile.nb * BN + h * 128, kx);

@@ -9,6 +9,7 @@ namespace dg {
 cudaError_t gemm_kgrouped_epi8_launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& sfa,
                                       const CUtensorMap& sfb, const CUtensorMap& d, const GemmArgs& args,
                                       int grid, cudaStream_t stream) {
+  if (args.mc) return gemm_launch_impl<256, 4, kKGrouped, 1, kBlockM, true, false, true>(a, b, sfa, sfb, d, args, grid, stream);
   return gemm_launch_impl<256, 4, kKGrouped, 1, kBlockM, true>(a, b, sfa, sfb, d, args, grid, stream);
 }
 

@@ -1222,10 +1222,15 @@ dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa,
   args.pdl = g_pdl.load();
   const int64_t tiles = (int64_t)num_groups * args.m_blocks * args.n_blocks;
   if (tiles >= kMaxCoord) return DG_ERR_TOO_LARGE;
-  const int grid = (int)(tiles < sms ? tiles : sms);
   // 256-column tiles drain their accumulator with eight epilogue warps
-  // (DG_TALL_EPI8 = 0: four, each reading its 256 columns in two halves)
+  // (DG_TALL_EPI8 = 0: four, each reading its 256 columns in two halves);
+  // with them, clusters of two CTAs on adjacent M blocks of one expert share
+  // each B tile by TMA multicast (DG_MULTICAST = 0 turns it off), on an even grid
   args.epi8 = (block_n == 256 && env().tall_epi8 != 0) ? 1 : 0;
+  args.mc = (args.epi8 && env().multicast != 0 && sms >= 2 && args.m_blocks >= 2) ? 1 : 0;
+  const int64_t pair_tiles = (int64_t)num_groups * ((args.m_blocks + 1) / 2) * args.n_blocks;
+  const int grid = args.mc ? 2 * (int)(pair_tiles < sms / 2 ? pair_tiles : sms / 2)
+                           : (int)(tiles < sms ? tiles : sms);
   print_config(args.epi8 ? "k_grouped_fp8_gemm_tn_contiguous (eight epilogue warps)"
                          : "k_grouped_fp8_gemm_tn_contiguous",
                m, n, sum_k, num_groups, kBlockM, block_n, gemm_stages(block_n), grid, args.band);

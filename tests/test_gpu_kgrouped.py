@@ -191,3 +191,41 @@ def test_k_grouped_end_to_end_with_device_quantisation():
             P.assert_close(got[gi], want[gi], "expert %d" % gi)
         else:
             assert not got[gi].any()
+
+
+@pytest.mark.parametrize("sms", [0, 5])
+@pytest.mark.parametrize("M", [272, 512])
+def test_k_grouped_multicast_pairs_match_single_ctas_bitwise(sms, M):
+    """128 x 256 tiles in clusters of two CTAs on adjacent M blocks of one
+    expert, each loading one of the B tile's two 128-column boxes into both
+    (TMA multicast): the same bits as one CTA per tile, with C, an empty
+    expert and (M = 272) an odd number of M blocks, whose last pair's second
+    tile lies past M and writes nothing."""
+    import os
+    rng = np.random.default_rng(M + sms)
+    ks = np.array([384, 0, 128, 640], dtype=np.int32)
+    sum_k, N = int(ks.sum()), 528
+    a = rng.standard_normal((sum_k, M)).astype(np.float32)
+    b = rng.standard_normal((sum_k, N)).astype(np.float32)
+    (qa, sa, qb, sb), dev = _prepare(a, b)
+    c = torch.from_numpy(rng.standard_normal((len(ks), M, N)).astype(np.float32)).cuda()
+    kst = torch.from_numpy(ks).cuda()
+    out = {}
+    old = {k: os.environ.get(k) for k in ("DG_MULTICAST", "DG_BLOCK_N")}
+    os.environ["DG_BLOCK_N"] = "256"
+    dg.set_num_sms(sms)
+    try:
+        for mc in ("1", "0"):
+            os.environ["DG_MULTICAST"] = mc
+            out[mc] = dg.k_grouped_fp8_gemm_tn_contiguous(*dev, kst, c=c).cpu()
+            _no_device_error()
+    finally:
+        dg.set_num_sms(0)
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    assert torch.equal(out["1"].view(torch.int32), out["0"].view(torch.int32))
+    want = oracle.gemm_k_grouped(qa, sa, qb, sb, ks, c=c.cpu().numpy())
+    P.assert_close(out["1"].double().numpy(), want, "K-grouped multicast pairs M=%d" % M)
