@@ -711,6 +711,7 @@ __global__ void __launch_bounds__(EPI8 ? kGemmThreadsEpi8 : kGemmThreads, 1)
   // setmaxnreg split of the eight-epilogue-warp layout: the K-grouped role
   // warps (MN-major loads, per-expert K ranges) need more than 56 registers,
   // its epilogue (128 FP32 columns per thread) fewer than 224
+  // (the K-grouped role warps spill at 56, and with multicast pairs below 104)
   constexpr int kRolesRegs = MODE == kKGrouped ? (MC ? 104 : 72) : kRegsRoles;
   constexpr int kEpiRegs = MODE == kKGrouped ? (MC ? 192 : 208) : kRegsEpi;
   static_assert(128 * kRolesRegs + 256 * kEpiRegs <= kGemmThreadsEpi8 * 168 && kRolesRegs % 8 == 0 &&
