@@ -334,14 +334,14 @@ dg_status dg_transform_sf(const float* sf, int32_t* packed, int64_t groups, int6
  *   DG_SPLIT_K=1|2|4|8   force the split-K cluster size (8: decode kernel);
  *   DG_CTA_PAIR=1        256-row tiles on 2-CTA pairs (cta_group::2 MMAs);
  *   DG_STREAM_K=0|1      forbid / force stream-K where a workspace allows it;
- *   DG_MULTICAST=0       256-row dense tiles one CTA each instead of 2-CTA
- *                        clusters sharing B by TMA multicast;
+ *   DG_MULTICAST=0       256-row dense tiles and K-grouped tiles one CTA each
+ *                        instead of 2-CTA clusters sharing B by TMA multicast;
  *   DG_TALL_EPI8=0       four epilogue warps for 256-row tiles instead of eight;
  *   DG_DECODE=0          tiled kernels instead of the decode kernel for M <= 128;
  *   DG_RASTER_BAND=n     M blocks per raster band (default 16).
  * Tile sizes and multicast clusters give the same bits: each output element
  * accumulates its K blocks in the same order (tested for 128- against
- * 256-row tiles and for multicast on against off).  Configurations that
+ * 256-row tiles and for multicast on against off, dense and K-grouped).  Configurations that
  * split K between CTAs (split-K, stream-K, decode clusters) add the partial
  * sums in a fixed order, so their bits are reproducible but may differ from
  * an unsplit launch's within FP32 rounding. */
