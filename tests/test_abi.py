@@ -260,3 +260,18 @@ def test_floor_library_is_separate_and_checks_its_arguments():
     assert F.dg_hbm_read_floor(None, 1024, None, 4, None) == cuda_error_invalid_value
     assert F.dg_hbm_read_floor(0x1008, 1024, None, 4, None) == cuda_error_invalid_value
     assert F.dg_hbm_read_floor(0x1000, 1024, None, 0, None) == cuda_error_invalid_value
+
+
+def test_header_lists_exactly_the_environment_variables_the_library_reads():
+    """dg.h's list of DG_* environment variables matches the names host.cu
+    reads, so the documentation cannot drift from the code."""
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    header = open(os.path.join(root, "include", "dg.h")).read()
+    block = header[header.index("Environment variables read by the library"):]
+    block = block[:block.index("*/")]
+    documented = set(re.findall(r"\b(DG_[A-Z0-9_]+)=", block))
+    host = open(os.path.join(root, "moe_grouped_gemm_fp8_gb300", "csrc", "host.cu")).read()
+    read = set(re.findall(r'env_(?:int|flag)\("(DG_[A-Z0-9_]+)"', host))
+    assert read and documented == read, (sorted(documented ^ read))
