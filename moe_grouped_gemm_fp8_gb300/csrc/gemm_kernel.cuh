@@ -60,6 +60,13 @@
 // timing, so results are deterministic - adds C, rounds to BF16 and stores.
 // All four epilogue warps of every CTA share the exchange and the stores.
 // No global scratch memory is used.
+//
+// Multicast pairs (MC: dense 256-row tiles and K-grouped 128 x 256 tiles,
+// eight epilogue warps): clusters of two CTAs walk the same tiles of B with
+// adjacent row blocks of A; each CTA loads half of the B tile into both
+// CTAs' stage (TMA multicast) and its MMA commit frees the stage in both, so
+// the pair moves through the ring in lockstep and L2 serves B once per pair.
+//
 // Every mbarrier wait is bounded; on expiry the kernel records an error,
 // drains its in-flight copies and MMAs, frees TMEM and exits.
 #pragma once
